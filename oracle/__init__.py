@@ -1,0 +1,388 @@
+"""CPU oracle for the quantized message-passing layer -- TEST INFRASTRUCTURE.
+
+Only the tests, the smoke check and the benchmark's CPU-baseline leg use this
+package.  The CUDA library never imports, links or calls it, and it never
+imports the CUDA library.
+
+The loops live in plain C (gq_oracle.c, built with -ffp-contract=off and
+OpenMP over output rows); dense products use numpy's float64 matmul as the
+library primitive.  All values are float64 except the quantizer, whose fp32
+arithmetic is part of its specification.
+
+Routines follow:
+  AdaQP (arXiv 2306.01381) Sec. 2.1 weighted-sum layer, Sec. 2.3 Eqn 4-6
+      (stochastic integer quantization / de-quantization), Sec. 3.1 (only
+      boundary messages are quantized);
+  Sancus (IJCAI 2023) Sec. 2: normalized adjacency D~^-1/2 (A+I) D~^-1/2;
+  Tango (arXiv 2308.00890) Sec. 2.1, Fig. 1: GAT forward/backward steps.
+
+Parity status: every routine is pinned by tests/test_oracle_*.py against the
+Tango worked example, closed forms, dense brute force or finite differences,
+except the single printed head-2 value of dD in the Tango example, whose
+inputs the page does not print (parity unpinned for that number only).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "gq_oracle.c")
+_BUILD = os.path.join(_HERE, "_build")
+_LIB_PATH = os.path.join(_BUILD, "libgq_oracle.so")
+_lock = threading.Lock()
+_lib = None
+
+COEF_GCN, COEF_SAGE, COEF_ONE = 0, 1, 2
+
+
+def build(force: bool = False) -> str:
+    """Compile the C oracle (gcc, portable C, no target-specific flags)."""
+    os.makedirs(_BUILD, exist_ok=True)
+    if (not force and os.path.exists(_LIB_PATH)
+            and os.path.getmtime(_LIB_PATH) >= os.path.getmtime(_SRC)):
+        return _LIB_PATH
+    tmp = _LIB_PATH + f".tmp{os.getpid()}"
+    cmd = ["gcc", "-O2", "-std=c11", "-ffp-contract=off", "-fno-fast-math", "-fopenmp",
+           "-fPIC", "-shared", _SRC, "-o", tmp, "-lm"]
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+def _L():
+    global _lib
+    with _lock:
+        if _lib is None:
+            lib = ctypes.CDLL(build())
+            P, I64, I, U64, D = (ctypes.c_void_p, ctypes.c_int64, ctypes.c_int,
+                                 ctypes.c_uint64, ctypes.c_double)
+            sig = {
+                "orc_fmix32": ([ctypes.c_uint32], ctypes.c_uint32),
+                "orc_hash": ([U64, ctypes.c_uint32, ctypes.c_uint32], ctypes.c_uint32),
+                "orc_uniform": ([U64, ctypes.c_uint32, ctypes.c_uint32], ctypes.c_float),
+                "orc_payload_bytes": ([I, I], I64),
+                "orc_header_offset": ([I, I], I64),
+                "orc_pitch": ([I, I], I64),
+                "orc_quantize": ([P, I64, I, I64, P, I, U64, P], None),
+                "orc_dequant": ([P, I64, I, I, P, P, I64], None),
+                "orc_codes": ([P, I64, I, I, P], None),
+                "orc_degree_norms": ([I64, P, P, P, P, P], None),
+                "orc_spmm": ([I64, P, P, I, P, I, P], None),
+                "orc_spmm_t": ([I64, P, P, I, P, I, P], None),
+                "orc_head_proj": ([I64, I, I, P, P, P], None),
+                "orc_edge_softmax": ([I64, P, P, P, P, I, D, P, P], None),
+                "orc_edge_spmm": ([I64, P, P, P, I, P, I, P], None),
+                "orc_edge_spmm_t": ([I64, P, P, P, I, P, I, P], None),
+                "orc_sddmm_dot": ([I64, P, P, P, P, I, I, P], None),
+                "orc_edge_softmax_bwd": ([I64, P, P, P, P, I, D, P, P, P], None),
+                "orc_edge_segment_sums": ([I64, P, P, P, I, P, P], None),
+            }
+            for name, (args, res) in sig.items():
+                f = getattr(lib, name)
+                f.argtypes = args
+                f.restype = res
+            _lib = lib
+    return _lib
+
+
+def _p(a):
+    return None if a is None else a.ctypes.data_as(ctypes.c_void_p)
+
+
+def _c(a, dtype):
+    return np.ascontiguousarray(np.asarray(a), dtype=dtype)
+
+
+def num_threads() -> int:
+    """OpenMP threads the oracle's parallel loops use."""
+    n = os.environ.get("OMP_NUM_THREADS")
+    if n:
+        return int(n)
+    return len(os.sched_getaffinity(0))
+
+
+# --------------------------------------------------------------------------
+# quantization (AdaQP Sec. 2.3)
+# --------------------------------------------------------------------------
+
+def pitch(d: int, bits: int) -> int:
+    return int(_L().orc_pitch(d, bits))
+
+
+def header_offset(d: int, bits: int) -> int:
+    return int(_L().orc_header_offset(d, bits))
+
+
+def uniform(seed: int, row: int, col: int) -> float:
+    return float(_L().orc_uniform(seed, row, col))
+
+
+def fmix32(h: int) -> int:
+    return int(_L().orc_fmix32(h))
+
+
+def hash32(seed: int, row: int, col: int) -> int:
+    return int(_L().orc_hash(seed, row, col))
+
+
+def quantize(X, mask, bits: int, seed: int, out: np.ndarray | None = None) -> np.ndarray:
+    """Packed rows (n x pitch bytes).  Rows with mask 0 are left as in `out`
+    (zeros when `out` is None)."""
+    X = _c(X, np.float32)
+    n, d = X.shape
+    m = None if mask is None else _c(mask, np.uint8)
+    if out is None:
+        out = np.zeros((n, pitch(d, bits)), dtype=np.uint8)
+    _L().orc_quantize(_p(X), n, d, d, _p(m), bits, seed & 0xFFFFFFFFFFFFFFFF, _p(out))
+    return out
+
+
+def dequant(packed, d: int, bits: int, mask=None) -> np.ndarray:
+    packed = _c(packed, np.uint8)
+    n = packed.shape[0]
+    m = None if mask is None else _c(mask, np.uint8)
+    Y = np.zeros((n, d), dtype=np.float32)
+    _L().orc_dequant(_p(packed), n, d, bits, _p(m), _p(Y), d)
+    return Y
+
+
+def codes(packed, d: int, bits: int) -> np.ndarray:
+    packed = _c(packed, np.uint8)
+    n = packed.shape[0]
+    Q = np.zeros((n, d), dtype=np.int32)
+    _L().orc_codes(_p(packed), n, d, bits, _p(Q))
+    return Q
+
+
+def header(packed, d: int, bits: int):
+    """(S, mn) per row as float32 arrays."""
+    h = header_offset(d, bits)
+    packed = _c(packed, np.uint8)
+    S = packed[:, h:h + 4].copy().view(np.float32).reshape(-1)
+    mn = packed[:, h + 4:h + 8].copy().view(np.float32).reshape(-1)
+    return S, mn
+
+
+def messages(X, packed, mask, d: int, bits: int) -> np.ndarray:
+    """The message rows an aggregation reads (AdaQP Sec. 3.1): de-quantized
+    rows where the node is marginal, the full-precision row otherwise.
+    bits >= 32 means no quantization.  Returns float64."""
+    M = np.array(X, dtype=np.float32, copy=True)
+    if bits < 32:
+        deq = dequant(packed, d, bits)
+        sel = np.ones(M.shape[0], bool) if mask is None else np.asarray(mask).astype(bool)
+        M[sel] = deq[sel]
+    return M.astype(np.float64)
+
+
+# --------------------------------------------------------------------------
+# graph normalization and aggregation
+# --------------------------------------------------------------------------
+
+def degree_norms(rowptr, col):
+    rowptr = _c(rowptr, np.int32)
+    col = _c(col, np.int32)
+    n = rowptr.shape[0] - 1
+    a, b, c = (np.zeros(n, np.float32) for _ in range(3))
+    _L().orc_degree_norms(n, _p(rowptr), _p(col), _p(a), _p(b), _p(c))
+    return a, b, c
+
+
+def spmm(rowptr, col, coef: int, M, transpose: bool = False) -> np.ndarray:
+    """Y = A^ M (transpose=False) or A^T M (transpose=True), float64."""
+    rowptr = _c(rowptr, np.int32)
+    col = _c(col, np.int32)
+    M = _c(M, np.float64)
+    n = rowptr.shape[0] - 1
+    d = M.shape[1]
+    Y = np.zeros((n, d), dtype=np.float64)
+    f = _L().orc_spmm_t if transpose else _L().orc_spmm
+    f(n, _p(rowptr), _p(col), coef, _p(M), d, _p(Y))
+    return Y
+
+
+# --------------------------------------------------------------------------
+# dense products
+# --------------------------------------------------------------------------
+
+def bf16_round(x) -> np.ndarray:
+    """Round float32 values to bfloat16 (nearest, ties to even), returned as
+    float32.  Inputs are first rounded to float32."""
+    f = np.ascontiguousarray(x, dtype=np.float32)
+    b = f.view(np.uint32).astype(np.uint64)
+    b = ((b + 0x7FFF + ((b >> 16) & 1)) >> 16) << 16
+    return (b & 0xFFFFFFFF).astype(np.uint32).view(np.float32).reshape(f.shape)
+
+
+def gemm(A, B, bf16: bool) -> np.ndarray:
+    """A @ B in float64; with bf16=True both operands are first rounded to
+    bfloat16 (the tensor-core input precision)."""
+    if bf16:
+        A, B = bf16_round(A), bf16_round(B)
+    return np.asarray(A, np.float64) @ np.asarray(B, np.float64)
+
+
+# --------------------------------------------------------------------------
+# GCN / GraphSAGE layer (AdaQP Sec. 2.1; Sancus Sec. 2)
+# --------------------------------------------------------------------------
+
+def gcn_layer_fwd(rowptr, col, coef, H_in, W, mask, bits, seed, relu: bool, bf16: bool = True):
+    """Aggregate first, then update:  A = sum_u a_uv m_u,  Z = A W,
+    H_out = relu(Z).  Messages of marginal rows are quantized (bits < 32)."""
+    H_in = _c(H_in, np.float32)
+    d = H_in.shape[1]
+    packed = quantize(H_in, mask, bits, seed) if bits < 32 else None
+    M = messages(H_in, packed, mask, d, bits)
+    A = spmm(rowptr, col, coef, M)
+    Z = gemm(A, W, bf16)
+    H_out = np.maximum(Z, 0.0) if relu else Z
+    return dict(packed=packed, A=A, Z=Z, H_out=H_out)
+
+
+def gcn_layer_bwd(rowptr, col, coef, dH_out, A, Z, W, mask, bits, seed, relu: bool,
+                  bf16: bool = True, need_dinput: bool = True):
+    """dZ = dH_out * relu'(Z); dW = A^T dZ; dA = dZ W^T; the rows of dA of
+    marginal nodes travel quantized (bits < 32); dH_in = A^T-aggregation of
+    those messages.  The quantizer is the identity in backward (its codes
+    are treated as constants)."""
+    dZ = np.asarray(dH_out, np.float64) * ((np.asarray(Z) > 0) if relu else 1.0)
+    dW = gemm(np.asarray(A).T, dZ, bf16)
+    out = dict(dZ=dZ, dW=dW)
+    if need_dinput:
+        dA = gemm(dZ, np.asarray(W).T, bf16).astype(np.float32)
+        d = dA.shape[1]
+        packed = quantize(dA, mask, bits, seed) if bits < 32 else None
+        M = messages(dA, packed, mask, d, bits)
+        out.update(dA=dA, packed=packed, dH_in=spmm(rowptr, col, coef, M, transpose=True))
+    return out
+
+
+# --------------------------------------------------------------------------
+# GAT (Tango Sec. 2.1, Fig. 1)
+# --------------------------------------------------------------------------
+
+def head_proj(Hp, a, heads: int) -> np.ndarray:
+    Hp = _c(Hp, np.float64)
+    a = _c(a, np.float64)
+    n, d = Hp.shape
+    out = np.zeros((n, heads), np.float64)
+    _L().orc_head_proj(n, heads, d // heads, _p(Hp), _p(a), _p(out))
+    return out
+
+
+def edge_softmax(rowptr, col, S, D, slope: float):
+    rowptr = _c(rowptr, np.int32)
+    col = _c(col, np.int32)
+    S = _c(S, np.float64)
+    D = _c(D, np.float64)
+    n, heads = D.shape
+    E = int(rowptr[-1])
+    Epre = np.zeros((E, heads), np.float64)
+    alpha = np.zeros((E, heads), np.float64)
+    _L().orc_edge_softmax(n, _p(rowptr), _p(col), _p(S), _p(D), heads, slope, _p(Epre), _p(alpha))
+    return Epre, alpha
+
+
+def edge_spmm(rowptr, col, alpha, M, transpose: bool = False) -> np.ndarray:
+    rowptr = _c(rowptr, np.int32)
+    col = _c(col, np.int32)
+    alpha = _c(alpha, np.float64)
+    M = _c(M, np.float64)
+    n = rowptr.shape[0] - 1
+    heads = alpha.shape[1]
+    d = M.shape[1]
+    out = np.zeros((n, d), np.float64)
+    f = _L().orc_edge_spmm_t if transpose else _L().orc_edge_spmm
+    f(n, _p(rowptr), _p(col), _p(alpha), heads, _p(M), d, _p(out))
+    return out
+
+
+def sddmm_dot(rowptr, col, dOut, M, heads: int) -> np.ndarray:
+    rowptr = _c(rowptr, np.int32)
+    col = _c(col, np.int32)
+    dOut = _c(dOut, np.float64)
+    M = _c(M, np.float64)
+    n = rowptr.shape[0] - 1
+    d = M.shape[1]
+    E = int(rowptr[-1])
+    out = np.zeros((E, heads), np.float64)
+    _L().orc_sddmm_dot(n, _p(rowptr), _p(col), _p(dOut), _p(M), heads, d, _p(out))
+    return out
+
+
+def edge_softmax_bwd(rowptr, alpha, dalpha, Epre, slope: float):
+    rowptr = _c(rowptr, np.int32)
+    alpha = _c(alpha, np.float64)
+    dalpha = _c(dalpha, np.float64)
+    Ep = None if Epre is None else _c(Epre, np.float64)
+    n = rowptr.shape[0] - 1
+    E, heads = alpha.shape
+    P = np.zeros((n, heads), np.float64)
+    dE = np.zeros((E, heads), np.float64)
+    dEpre = np.zeros((E, heads), np.float64)
+    _L().orc_edge_softmax_bwd(n, _p(rowptr), _p(alpha), _p(dalpha), _p(Ep), heads, slope,
+                              _p(P), _p(dE), _p(dEpre))
+    return P, dE, dEpre
+
+
+def edge_segment_sums(rowptr, col, X):
+    rowptr = _c(rowptr, np.int32)
+    col = _c(col, np.int32)
+    X = _c(X, np.float64)
+    n = rowptr.shape[0] - 1
+    heads = X.shape[1]
+    dD = np.zeros((n, heads), np.float64)
+    dS = np.zeros((n, heads), np.float64)
+    _L().orc_edge_segment_sums(n, _p(rowptr), _p(col), _p(X), heads, _p(dD), _p(dS))
+    return dD, dS
+
+
+def gat_layer_fwd(rowptr, col, H, W, a_src, a_dst, heads, slope, mask=None, bits=32, seed=0,
+                  bf16: bool = True):
+    """Tango Fig. 1a: H' = H W (step 1); S, D head projections (step 2);
+    SDDMM add + LeakyReLU (step 3); edge softmax (step 4); SpMM (step 5).
+    With bits < 32 the H' rows of marginal nodes are the quantized messages."""
+    Hp = gemm(H, W, bf16)
+    S = head_proj(Hp, a_src, heads)
+    D = head_proj(Hp, a_dst, heads)
+    Epre, alpha = edge_softmax(rowptr, col, S, D, slope)
+    Hp32 = Hp.astype(np.float32)
+    d = Hp.shape[1]
+    packed = quantize(Hp32, mask, bits, seed) if bits < 32 else None
+    M = messages(Hp32, packed, mask, d, bits) if bits < 32 else Hp
+    out = edge_spmm(rowptr, col, alpha, M)
+    return dict(Hp=Hp, S=S, D=D, Epre=Epre, alpha=alpha, packed=packed, M=M, out=out)
+
+
+def gat_layer_bwd(rowptr, col, dOut, H, M, Hp, Epre, alpha, W, a_src, a_dst, heads, slope,
+                  mask=None, bits=32, seed=0, bf16: bool = True):
+    """Tango Fig. 1b.  M = the forward messages (H' rows, de-quantized where
+    marginal).  dalpha by SDDMM dot; softmax derivative; LeakyReLU'; dD by
+    in-edge sums, dS by out-edge sums; dM = transposed edge SpMM of dOut
+    (whose marginal rows travel quantized when bits < 32); then
+    dH' = dM + dS a_src + dD a_dst, da_src/da_dst, dW = H^T dH', dH = dH' W^T."""
+    dOut = np.asarray(dOut, np.float64)
+    n, d = dOut.shape
+    F = d // heads
+    dalpha = sddmm_dot(rowptr, col, dOut, M, heads)
+    P, dE, dEpre = edge_softmax_bwd(rowptr, alpha, dalpha, Epre, slope)
+    dD, dS = edge_segment_sums(rowptr, col, dEpre)
+    dOut32 = dOut.astype(np.float32)
+    packed = quantize(dOut32, mask, bits, seed) if bits < 32 else None
+    Mb = messages(dOut32, packed, mask, d, bits) if bits < 32 else dOut
+    dM = edge_spmm(rowptr, col, alpha, Mb, transpose=True)
+    a_src = np.asarray(a_src, np.float64).reshape(heads, F)
+    a_dst = np.asarray(a_dst, np.float64).reshape(heads, F)
+    dHp = dM + np.repeat(dS, F, axis=1) * a_src.reshape(1, d) + np.repeat(dD, F, axis=1) * a_dst.reshape(1, d)
+    Hp = np.asarray(Hp, np.float64)
+    da_src = (dS[:, :, None] * Hp.reshape(n, heads, F)).sum(axis=0)
+    da_dst = (dD[:, :, None] * Hp.reshape(n, heads, F)).sum(axis=0)
+    dW = gemm(np.asarray(H).T, dHp, bf16)
+    dH = gemm(dHp, np.asarray(W).T, bf16)
+    return dict(dalpha=dalpha, P=P, dE=dE, dEpre=dEpre, dD=dD, dS=dS, dM=dM, dHp=dHp,
+                da_src=da_src, da_dst=da_dst, dW=dW, dH=dH, packed=packed)

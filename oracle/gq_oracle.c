@@ -1,0 +1,332 @@
+/*
+ * gq_oracle.c -- plain, slow CPU restatement of the quantized message-passing
+ * layer.  TEST INFRASTRUCTURE ONLY: it is called by the tests, by the smoke
+ * check and by the benchmark's CPU-baseline leg, never by the product path.
+ * It shares no code with the CUDA library.
+ *
+ * Sources (cited by page title and section):
+ *  - AdaQP, "Adaptive Message Quantization and Parallelization for Distributed
+ *    Full-graph GNN Training" (arXiv 2306.01381):
+ *      Sec. 2.1  message passing as a weighted sum  h_v = sigma(W sum_u a_uv h_u)
+ *      Sec. 2.3  Eqn 4 stochastic integer quantization q = round_st((h-Z)/S),
+ *                Z = min(h), S = (max(h)-min(h))/(2^b-1), b in {2,4,8};
+ *                Eqn 5 de-quantization h^ = q*S + Z;  Eqn 6 unbiasedness
+ *      Sec. 3.1  only messages that cross the boundary are quantized
+ *  - Sancus (IJCAI 2023, extended abstract), Sec. 2 Preliminaries:
+ *      A^ = D~^{-1/2} (A+I) D~^{-1/2},  H' = sigma(A^ H W)
+ *  - Tango, "Rethinking quantization for graph neural network training on
+ *    GPUs" (arXiv 2308.00890), Sec. 2.1 / Fig. 1: GAT as GEMM -> head
+ *    projections -> SDDMM add -> LeakyReLU -> edge softmax -> SpMM, and the
+ *    backward steps (SDDMM dot, softmax derivative, in/out-edge sums).
+ *
+ * Precision: the quantizer works in IEEE fp32 round-to-nearest with no FMA
+ * contraction (build with -ffp-contract=off), because its integer codes must
+ * be reproduced bit for bit.  Everything else takes fp32 inputs widened
+ * exactly to double and accumulates in double, in the order of the CSR.
+ *
+ * Readings where the pages are silent (all listed in the design notes):
+ *  - the stochastic-rounding uniform u comes from a counter hash of
+ *    (seed, row, col): MurmurHash3's published 32-bit finalizer "fmix32";
+ *  - S is computed as an fp32 division, the code as floor((x-mn)*(1/S) + u)
+ *    clamped to 2^b-1; a constant row (S == 0) codes every element as 0;
+ *  - de-quantization is one fused multiply-add fmaf(q, S, mn);
+ *  - packed row: payload LSB-first, then S and mn as fp32 (see orc_pitch);
+ *  - directed graphs: A^[v][u] = 1/sqrt(deg_in(v) deg_out(u)) with degrees
+ *    counted including the self-loop; GraphSAGE-mean a_uv = 1/deg_in(v).
+ *
+ * Pins: every routine here is checked by tests against something other than
+ * itself -- the GAT worked example printed on the Tango page, closed forms,
+ * dense brute force and finite differences (tests/test_oracle_*.py).
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+#define ORC_COEF_GCN 0
+#define ORC_COEF_SAGE 1
+#define ORC_COEF_ONE 2
+
+/* ------------------------------------------------------------------------ */
+/* counter hash: MurmurHash3 fmix32 (Appleby, public domain definition)      */
+/* ------------------------------------------------------------------------ */
+static uint32_t fmix32(uint32_t h) {
+  h ^= h >> 16;
+  h *= 0x85EBCA6Bu;
+  h ^= h >> 13;
+  h *= 0xC2B2AE35u;
+  h ^= h >> 16;
+  return h;
+}
+
+uint32_t orc_fmix32(uint32_t h) { return fmix32(h); }
+
+uint32_t orc_hash(uint64_t seed, uint32_t row, uint32_t col) {
+  uint32_t s32 = (uint32_t)seed ^ (uint32_t)(seed >> 32);
+  uint32_t kr = fmix32(row ^ fmix32(s32));
+  return fmix32(kr + col * 0x9E3779B9u);
+}
+
+/* u in [0, 1 - 2^-24]: the top 24 bits of the hash, exact in fp32 */
+float orc_uniform(uint64_t seed, uint32_t row, uint32_t col) {
+  return (float)(orc_hash(seed, row, col) >> 8) * (1.0f / 16777216.0f);
+}
+
+/* ------------------------------------------------------------------------ */
+/* packed row layout                                                         */
+/* ------------------------------------------------------------------------ */
+int64_t orc_payload_bytes(int d, int bits) { return ((int64_t)d * bits + 7) / 8; }
+int64_t orc_header_offset(int d, int bits) { return (orc_payload_bytes(d, bits) + 7) / 8 * 8; }
+int64_t orc_pitch(int d, int bits) { return (orc_header_offset(d, bits) + 8 + 15) / 16 * 16; }
+
+/* ------------------------------------------------------------------------ */
+/* AdaQP Sec. 2.3, Eqn 4: stochastic integer quantization of message rows    */
+/* ------------------------------------------------------------------------ */
+void orc_quantize(const float* X, int64_t n, int d, int64_t ldx, const uint8_t* mask,
+                  int bits, uint64_t seed, uint8_t* packed) {
+  const int64_t pitch = orc_pitch(d, bits);
+  const int64_t hoff = orc_header_offset(d, bits);
+  const int levels = (1 << bits) - 1;
+  for (int64_t r = 0; r < n; ++r) {
+    if (mask && !mask[r]) continue;
+    const float* x = X + r * ldx;
+    uint8_t* row = packed + r * pitch;
+    /* zero-point Z = min(h), range from max(h) */
+    float mn = x[0], mx = x[0];
+    for (int j = 1; j < d; ++j) {
+      if (x[j] < mn) mn = x[j];
+      if (x[j] > mx) mx = x[j];
+    }
+    float S = (mx - mn) / (float)levels;
+    memset(row, 0, (size_t)pitch);
+    for (int j = 0; j < d; ++j) {
+      int q = 0;
+      if (S != 0.0f) {
+        float inv = 1.0f / S;
+        float t = (x[j] - mn) * inv;                 /* (h - Z) / S          */
+        float v = t + orc_uniform(seed, (uint32_t)r, (uint32_t)j); /* + u    */
+        q = (int)floorf(v);                          /* round_st             */
+        if (q > levels) q = levels;
+      }
+      int64_t bit = (int64_t)j * bits;
+      row[bit / 8] |= (uint8_t)(q << (bit % 8));
+    }
+    memcpy(row + hoff, &S, 4);
+    memcpy(row + hoff + 4, &mn, 4);
+  }
+}
+
+/* Read code j of a packed row. */
+static int packed_code(const uint8_t* row, int j, int bits) {
+  int64_t bit = (int64_t)j * bits;
+  return (row[bit / 8] >> (bit % 8)) & ((1 << bits) - 1);
+}
+
+/* AdaQP Eqn 5: h^ = q * S + Z, one fused multiply-add in fp32. */
+void orc_dequant(const uint8_t* packed, int64_t n, int d, int bits, const uint8_t* mask,
+                 float* Y, int64_t ldy) {
+  const int64_t pitch = orc_pitch(d, bits);
+  const int64_t hoff = orc_header_offset(d, bits);
+  for (int64_t r = 0; r < n; ++r) {
+    if (mask && !mask[r]) continue;
+    const uint8_t* row = packed + r * pitch;
+    float S, mn;
+    memcpy(&S, row + hoff, 4);
+    memcpy(&mn, row + hoff + 4, 4);
+    for (int j = 0; j < d; ++j) Y[r * ldy + j] = fmaf((float)packed_code(row, j, bits), S, mn);
+  }
+}
+
+/* Extract the integer codes (for tests). */
+void orc_codes(const uint8_t* packed, int64_t n, int d, int bits, int32_t* Q) {
+  const int64_t pitch = orc_pitch(d, bits);
+  for (int64_t r = 0; r < n; ++r)
+    for (int j = 0; j < d; ++j) Q[r * d + j] = packed_code(packed + r * pitch, j, bits);
+}
+
+/* ------------------------------------------------------------------------ */
+/* Degrees and normalization (Sancus Sec. 2: D~ = D + I)                    */
+/* ------------------------------------------------------------------------ */
+static void degrees(int64_t n, const int32_t* rowptr, const int32_t* col, int64_t* din,
+                    int64_t* dout) {
+  for (int64_t v = 0; v < n; ++v) {
+    din[v] = rowptr[v + 1] - rowptr[v];
+    dout[v] = 0;
+  }
+  for (int64_t e = 0; e < rowptr[n]; ++e) dout[col[e]] += 1;
+}
+
+/* The fp32 normalization vectors a GPU implementation stores:
+ * dinv_in = 1/sqrt(deg_in), dinv_out = 1/sqrt(deg_out), inv_in = 1/deg_in,
+ * each evaluated in double and rounded once to fp32 (0 for degree 0). */
+void orc_degree_norms(int64_t n, const int32_t* rowptr, const int32_t* col, float* dinv_in,
+                      float* dinv_out, float* inv_in) {
+  int64_t* din = (int64_t*)malloc(sizeof(int64_t) * (size_t)(n + 1));
+  int64_t* dout = (int64_t*)malloc(sizeof(int64_t) * (size_t)(n + 1));
+  degrees(n, rowptr, col, din, dout);
+  for (int64_t v = 0; v < n; ++v) {
+    dinv_in[v] = din[v] ? (float)(1.0 / sqrt((double)din[v])) : 0.0f;
+    dinv_out[v] = dout[v] ? (float)(1.0 / sqrt((double)dout[v])) : 0.0f;
+    inv_in[v] = din[v] ? (float)(1.0 / (double)din[v]) : 0.0f;
+  }
+  free(din);
+  free(dout);
+}
+
+/* Aggregation coefficient a_{u,v} of edge u -> v (AdaQP Sec. 2.1 weighted
+ * sum; GCN: Sancus Sec. 2 normalized adjacency; SAGE: neighbourhood mean). */
+static double coef_of(int mode, int64_t din_v, int64_t dout_u) {
+  if (mode == ORC_COEF_GCN) return (1.0 / sqrt((double)dout_u)) * (1.0 / sqrt((double)din_v));
+  if (mode == ORC_COEF_SAGE) return 1.0 / (double)din_v;
+  return 1.0;
+}
+
+/* Y[v,:] = sum_{e = (u -> v)} a_{u,v} M[u,:]   (rows of the CSR are
+ * destinations).  M holds the message rows (de-quantized or raw), double. */
+void orc_spmm(int64_t n, const int32_t* rowptr, const int32_t* col, int coef, const double* M,
+              int d, double* Y) {
+  int64_t* din = (int64_t*)malloc(sizeof(int64_t) * (size_t)(n + 1));
+  int64_t* dout = (int64_t*)malloc(sizeof(int64_t) * (size_t)(n + 1));
+  degrees(n, rowptr, col, din, dout);
+#pragma omp parallel for schedule(dynamic, 64)
+  for (int64_t v = 0; v < n; ++v) {
+    double* y = Y + v * d;
+    for (int j = 0; j < d; ++j) y[j] = 0.0;
+    for (int64_t e = rowptr[v]; e < rowptr[v + 1]; ++e) {
+      int64_t u = col[e];
+      double a = coef_of(coef, din[v], dout[u]);
+      for (int j = 0; j < d; ++j) y[j] += a * M[u * d + j];
+    }
+  }
+  free(din);
+  free(dout);
+}
+
+/* Transposed aggregation (the backward pass of the SpMM):
+ * Y[u,:] = sum_{e = (u -> v)} a_{u,v} M[v,:], a plain scatter over edges. */
+void orc_spmm_t(int64_t n, const int32_t* rowptr, const int32_t* col, int coef, const double* M,
+                int d, double* Y) {
+  int64_t* din = (int64_t*)malloc(sizeof(int64_t) * (size_t)(n + 1));
+  int64_t* dout = (int64_t*)malloc(sizeof(int64_t) * (size_t)(n + 1));
+  degrees(n, rowptr, col, din, dout);
+  memset(Y, 0, sizeof(double) * (size_t)n * (size_t)d);
+  for (int64_t v = 0; v < n; ++v)
+    for (int64_t e = rowptr[v]; e < rowptr[v + 1]; ++e) {
+      int64_t u = col[e];
+      double a = coef_of(coef, din[v], dout[u]);
+      for (int j = 0; j < d; ++j) Y[u * d + j] += a * M[v * d + j];
+    }
+  free(din);
+  free(dout);
+}
+
+/* ------------------------------------------------------------------------ */
+/* GAT (Tango Sec. 2.1, Fig. 1a)                                            */
+/* ------------------------------------------------------------------------ */
+
+/* Step 2: S[u,k] = sum_f H'[u,kF+f] a_src[k,f] (and D likewise). */
+void orc_head_proj(int64_t n, int heads, int F, const double* Hp, const double* a, double* out) {
+  for (int64_t u = 0; u < n; ++u)
+    for (int k = 0; k < heads; ++k) {
+      double s = 0.0;
+      for (int f = 0; f < F; ++f) s += Hp[u * heads * F + k * F + f] * a[k * F + f];
+      out[u * heads + k] = s;
+    }
+}
+
+/* Steps 3-4: E_pre[e,k] = S[u,k] + D[v,k] (SDDMM add), E = LeakyReLU(E_pre),
+ * alpha[e,k] = exp(E[e,k]) / sum_{e' in in(v)} exp(E[e',k]).  The per-(v,k)
+ * maximum is subtracted before exponentiating, which leaves alpha unchanged. */
+void orc_edge_softmax(int64_t n, const int32_t* rowptr, const int32_t* col, const double* S,
+                      const double* D, int heads, double slope, double* Epre, double* alpha) {
+#pragma omp parallel for schedule(dynamic, 64)
+  for (int64_t v = 0; v < n; ++v) {
+    for (int k = 0; k < heads; ++k) {
+      double mx = -INFINITY;
+      for (int64_t e = rowptr[v]; e < rowptr[v + 1]; ++e) {
+        double ep = S[(int64_t)col[e] * heads + k] + D[v * heads + k];
+        double el = ep > 0.0 ? ep : slope * ep;
+        if (Epre) Epre[e * heads + k] = ep;
+        alpha[e * heads + k] = el;
+        if (el > mx) mx = el;
+      }
+      double sum = 0.0;
+      for (int64_t e = rowptr[v]; e < rowptr[v + 1]; ++e) {
+        double x = exp(alpha[e * heads + k] - mx);
+        alpha[e * heads + k] = x;
+        sum += x;
+      }
+      for (int64_t e = rowptr[v]; e < rowptr[v + 1]; ++e) alpha[e * heads + k] /= sum;
+    }
+  }
+}
+
+/* Step 5: out[v, kF+f] = sum_{e=(u->v)} alpha[e,k] M[u, kF+f]. */
+void orc_edge_spmm(int64_t n, const int32_t* rowptr, const int32_t* col, const double* alpha,
+                   int heads, const double* M, int d, double* out) {
+  const int F = d / heads;
+#pragma omp parallel for schedule(dynamic, 64)
+  for (int64_t v = 0; v < n; ++v) {
+    for (int c = 0; c < d; ++c) out[v * d + c] = 0.0;
+    for (int64_t e = rowptr[v]; e < rowptr[v + 1]; ++e)
+      for (int c = 0; c < d; ++c) out[v * d + c] += alpha[e * heads + c / F] * M[(int64_t)col[e] * d + c];
+  }
+}
+
+/* Transposed: out[u, kF+f] = sum_{e=(u->v)} alpha[e,k] M[v, kF+f]. */
+void orc_edge_spmm_t(int64_t n, const int32_t* rowptr, const int32_t* col, const double* alpha,
+                     int heads, const double* M, int d, double* out) {
+  const int F = d / heads;
+  memset(out, 0, sizeof(double) * (size_t)n * (size_t)d);
+  for (int64_t v = 0; v < n; ++v)
+    for (int64_t e = rowptr[v]; e < rowptr[v + 1]; ++e)
+      for (int c = 0; c < d; ++c) out[(int64_t)col[e] * d + c] += alpha[e * heads + c / F] * M[v * d + c];
+}
+
+/* Fig. 1b SDDMM dot: dalpha[e,k] = sum_f dOut[v,kF+f] M[u,kF+f], e = (u->v). */
+void orc_sddmm_dot(int64_t n, const int32_t* rowptr, const int32_t* col, const double* dOut,
+                   const double* M, int heads, int d, double* dalpha) {
+  const int F = d / heads;
+#pragma omp parallel for schedule(dynamic, 64)
+  for (int64_t v = 0; v < n; ++v)
+    for (int64_t e = rowptr[v]; e < rowptr[v + 1]; ++e)
+      for (int k = 0; k < heads; ++k) {
+        double s = 0.0;
+        for (int f = 0; f < F; ++f) s += dOut[v * d + k * F + f] * M[(int64_t)col[e] * d + k * F + f];
+        dalpha[e * heads + k] = s;
+      }
+}
+
+/* Softmax derivative (Tango Sec. 2.1, backward step on edge features):
+ * P[v,k] = sum_{e in in(v)} dalpha[e,k] alpha[e,k];
+ * dE[e,k] = alpha[e,k] (dalpha[e,k] - P[v,k]);
+ * then through the LeakyReLU: dEpre = dE * (Epre > 0 ? 1 : slope).
+ * P may be NULL; Epre may be NULL (then dEpre = dE). */
+void orc_edge_softmax_bwd(int64_t n, const int32_t* rowptr, const double* alpha,
+                          const double* dalpha, const double* Epre, int heads, double slope,
+                          double* P, double* dE, double* dEpre) {
+  for (int64_t v = 0; v < n; ++v)
+    for (int k = 0; k < heads; ++k) {
+      double p = 0.0;
+      for (int64_t e = rowptr[v]; e < rowptr[v + 1]; ++e) p += dalpha[e * heads + k] * alpha[e * heads + k];
+      if (P) P[v * heads + k] = p;
+      for (int64_t e = rowptr[v]; e < rowptr[v + 1]; ++e) {
+        double g = alpha[e * heads + k] * (dalpha[e * heads + k] - p);
+        if (dE) dE[e * heads + k] = g;
+        if (dEpre) dEpre[e * heads + k] = Epre ? (Epre[e * heads + k] > 0.0 ? g : slope * g) : g;
+      }
+    }
+}
+
+/* dD[v,k] = sum_{e in in(v)} X[e,k];  dS[u,k] = sum_{e in out(u)} X[e,k]. */
+void orc_edge_segment_sums(int64_t n, const int32_t* rowptr, const int32_t* col, const double* X,
+                           int heads, double* dD, double* dS) {
+  memset(dD, 0, sizeof(double) * (size_t)n * (size_t)heads);
+  memset(dS, 0, sizeof(double) * (size_t)n * (size_t)heads);
+  for (int64_t v = 0; v < n; ++v)
+    for (int64_t e = rowptr[v]; e < rowptr[v + 1]; ++e)
+      for (int k = 0; k < heads; ++k) {
+        dD[v * heads + k] += X[e * heads + k];
+        dS[(int64_t)col[e] * heads + k] += X[e * heads + k];
+      }
+}

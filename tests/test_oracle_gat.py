@@ -1,0 +1,158 @@
+"""Pins of the oracle's GAT routines (Tango Sec. 2.1, Fig. 1) against the
+page's worked example, softmax invariants, dense brute force and finite
+differences."""
+import json
+import os
+
+import numpy as np
+import pytest
+
+from test_oracle_graph import small_graph, dense_adj
+
+FX = json.load(open(os.path.join(os.path.dirname(__file__), "golden", "tango_gat_example.json")))
+RP = np.array(FX["rowptr"], np.int32)
+CO = np.array(FX["col"], np.int32)
+
+
+def test_example_head_projection(orc):
+    Hp = np.array([FX["Hp_v0"]])
+    S = orc.head_proj(Hp, np.array(FX["a_src"]), 2)[0]
+    # inputs are printed to 2 decimals, so allow their rounding (<= 0.02)
+    np.testing.assert_allclose(S, FX["S_v0_printed"], atol=0.02)
+
+
+def _example_scores():
+    S = np.zeros((4, 2))
+    D = np.zeros((4, 2))
+    S[0] = FX["S_v0_printed"]
+    D[3] = FX["D_v3_printed"]
+    # choose S[v2] so that e4's score is the printed [0.86, 0.14]
+    S[2] = np.array(FX["E_e4_post_leakyrelu_printed"]) - D[3]
+    return S, D
+
+
+def test_example_sddmm_leakyrelu_softmax(orc):
+    S, D = _example_scores()
+    Epre, alpha = orc.edge_softmax(RP, CO, S, D, slope=0.0)
+    np.testing.assert_allclose(Epre[3], FX["E_e3_pre_printed"], atol=1e-12)
+    np.testing.assert_allclose(alpha[3], FX["alpha_e3_printed"], atol=0.01)
+    np.testing.assert_allclose(alpha[4], FX["alpha_e4_printed"], atol=0.01)
+    # exact values of the page's own formula e^1.40/(e^1.40+e^0.86), e^0/(e^0+e^0.14)
+    np.testing.assert_allclose(alpha[3, 0], np.exp(1.40) / (np.exp(1.40) + np.exp(0.86)), rtol=1e-12)
+    np.testing.assert_allclose(alpha[3, 1], 1.0 / (1.0 + np.exp(0.14)), rtol=1e-12)
+    # single in-edge destinations get attention 1
+    np.testing.assert_allclose(alpha[:3], 1.0)
+
+
+def test_example_softmax_backward(orc):
+    S, D = _example_scores()
+    Epre, alpha = orc.edge_softmax(RP, CO, S, D, slope=0.0)
+    dalpha = np.zeros((5, 2))
+    dalpha[3, 0] = FX["dalpha_head1_printed"]["e3"]
+    dalpha[4, 0] = FX["dalpha_head1_printed"]["e4"]
+    dalpha[:, 1] = [0.3, -0.2, 0.5, 0.9, 0.1]          # head 2 not printed: any values
+    dalpha[:3, 0] = [0.7, -1.1, 0.2]
+    P, dE, dEpre = orc.edge_softmax_bwd(RP, alpha, dalpha, Epre, slope=0.0)
+    assert abs(P[3, 0] - FX["P_v3_head1_printed"]) < 0.005
+    assert abs(dE[3, 0] - FX["dE_e3_head1_printed"]) < 0.005
+    dD, dS = orc.edge_segment_sums(RP, CO, dEpre)
+    # printed dS[v3] = dE[e1] = [0, 0]: e1 is v1's only in-edge, so alpha = 1 and dE = 0
+    np.testing.assert_allclose(dS[3], FX["dS_v3_printed"], atol=1e-12)
+    # printed dD[v3] head 1 = 0: softmax gradients sum to zero over a destination
+    assert abs(dD[3, 0] - FX["dD_v3_printed"][0]) < 1e-12
+    # head 2: e3's score is negative, so with the page's LeakyReLU (negative
+    # side ~ 0) only e4 contributes and dD[v3] head 2 = dE[e4] != 0, as the
+    # printed 0.15 != 0 shows; before the LeakyReLU' it would sum to zero.
+    assert abs(dE[3, 1] + dE[4, 1]) < 1e-12
+    assert abs(dD[3, 1] - dE[4, 1]) < 1e-12 and abs(dD[3, 1]) > 1e-3
+
+
+def test_example_output_consistency(orc):
+    # H'[v2] is not printed: solving the printed output for it gives a vector;
+    # feeding that back through the oracle's SpMM must reproduce the output.
+    S, D = _example_scores()
+    _, alpha = orc.edge_softmax(RP, CO, S, D, slope=0.0)
+    Hp = np.zeros((4, 4))
+    Hp[0] = FX["Hp_v0"]
+    out = np.array(FX["out_v3_printed"])
+    a3 = np.repeat(np.array(FX["alpha_e3_printed"]), 2)
+    a4 = np.repeat(np.array(FX["alpha_e4_printed"]), 2)
+    Hp[2] = (out - a3 * Hp[0]) / a4
+    got = orc.edge_spmm(RP, CO, alpha, Hp)[3]
+    np.testing.assert_allclose(got, out, atol=0.02)
+
+
+def test_softmax_invariants_random(orc):
+    rowptr, col = small_graph(50, 400, seed=11)
+    n = len(rowptr) - 1
+    rng = np.random.default_rng(5)
+    S, D = rng.standard_normal((n, 4)), rng.standard_normal((n, 4))
+    Epre, alpha = orc.edge_softmax(rowptr, col, S, D, slope=0.2)
+    for v in range(n):
+        np.testing.assert_allclose(alpha[rowptr[v]:rowptr[v + 1]].sum(0), 1.0, rtol=1e-12)
+    dalpha = rng.standard_normal(alpha.shape)
+    P, dE, dEpre = orc.edge_softmax_bwd(rowptr, alpha, dalpha, Epre, 0.2)
+    for v in range(n):
+        np.testing.assert_allclose(dE[rowptr[v]:rowptr[v + 1]].sum(0), 0.0, atol=1e-12)
+    np.testing.assert_allclose(dEpre, np.where(Epre > 0, dE, 0.2 * dE), rtol=1e-14)
+
+
+def test_edge_spmm_and_sddmm_dense(orc):
+    rowptr, col = small_graph(30, 200, seed=12)
+    n = len(rowptr) - 1
+    E = len(col)
+    rng = np.random.default_rng(6)
+    heads, F = 4, 3
+    alpha = rng.random((E, heads))
+    M = rng.standard_normal((n, heads * F))
+    dst = np.repeat(np.arange(n), np.diff(rowptr))
+    out = orc.edge_spmm(rowptr, col, alpha, M)
+    outT = orc.edge_spmm(rowptr, col, alpha, M, transpose=True)
+    for k in range(heads):
+        Gk = np.zeros((n, n))
+        Gk[dst, col] = alpha[:, k]
+        np.testing.assert_allclose(out[:, k * F:(k + 1) * F], Gk @ M[:, k * F:(k + 1) * F], atol=1e-12)
+        np.testing.assert_allclose(outT[:, k * F:(k + 1) * F], Gk.T @ M[:, k * F:(k + 1) * F], atol=1e-12)
+    dOut = rng.standard_normal((n, heads * F))
+    da = orc.sddmm_dot(rowptr, col, dOut, M, heads)
+    want = np.einsum("ekf,ekf->ek", dOut[dst].reshape(E, heads, F), M[col].reshape(E, heads, F))
+    np.testing.assert_allclose(da, want, atol=1e-12)
+
+
+def _gat_loss(orc, rowptr, col, H, W, a_s, a_d, heads, G):
+    o = orc.gat_layer_fwd(rowptr, col, H, W, a_s, a_d, heads, 0.2, bf16=False)
+    return np.sum(o["out"] * G), o
+
+
+def test_gat_layer_finite_differences(orc):
+    rowptr, col = small_graph(24, 120, seed=13)
+    n = len(rowptr) - 1
+    rng = np.random.default_rng(7)
+    heads, F, din = 2, 3, 5
+    H = rng.standard_normal((n, din))
+    W = rng.standard_normal((din, heads * F)) * 0.5
+    a_s, a_d = rng.standard_normal((heads, F)), rng.standard_normal((heads, F))
+    G = rng.standard_normal((n, heads * F))
+    L0, o = _gat_loss(orc, rowptr, col, H, W, a_s, a_d, heads, G)
+    b = orc.gat_layer_bwd(rowptr, col, G, H, o["M"], o["Hp"], o["Epre"], o["alpha"], W, a_s, a_d,
+                          heads, 0.2, bf16=False)
+    h = 1e-6
+
+    def fd(arr, idx, which):
+        p, m = arr.copy(), arr.copy()
+        p[idx] += h
+        m[idx] -= h
+        args = dict(H=H, W=W, a_s=a_s, a_d=a_d)
+        args[which] = p
+        lp = _gat_loss(orc, rowptr, col, args["H"], args["W"], args["a_s"], args["a_d"], heads, G)[0]
+        args[which] = m
+        lm = _gat_loss(orc, rowptr, col, args["H"], args["W"], args["a_s"], args["a_d"], heads, G)[0]
+        return (lp - lm) / (2 * h)
+
+    for idx in [(0, 0), (2, 5), (4, 3)]:
+        assert abs(fd(W, idx, "W") - b["dW"][idx]) < 1e-5 * (1 + abs(b["dW"][idx]))
+    for idx in [(0, 0), (1, 2)]:
+        assert abs(fd(a_s, idx, "a_s") - b["da_src"][idx]) < 1e-5 * (1 + abs(b["da_src"][idx]))
+        assert abs(fd(a_d, idx, "a_d") - b["da_dst"][idx]) < 1e-5 * (1 + abs(b["da_dst"][idx]))
+    for idx in [(0, 1), (10, 4), (23, 0)]:
+        assert abs(fd(H, idx, "H") - b["dH"][idx]) < 1e-5 * (1 + abs(b["dH"][idx]))
