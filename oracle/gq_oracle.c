@@ -67,9 +67,9 @@ uint32_t orc_hash(uint64_t seed, uint32_t row, uint32_t col) {
   return fmix32(kr + col * 0x9E3779B9u);
 }
 
-/* u in [0, 1 - 2^-24]: the top 24 bits of the hash, exact in fp32 */
+/* u in [0, 1 - 2^-23]: the top 23 bits of the hash, exact in fp32 */
 float orc_uniform(uint64_t seed, uint32_t row, uint32_t col) {
-  return (float)(orc_hash(seed, row, col) >> 8) * (1.0f / 16777216.0f);
+  return (float)(orc_hash(seed, row, col) >> 9) * (1.0f / 8388608.0f);
 }
 
 /* ------------------------------------------------------------------------ */

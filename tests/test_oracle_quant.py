@@ -25,8 +25,8 @@ def test_fmix32_published_vectors(orc):
 
 def test_uniform_range_and_grid(orc):
     us = np.array([orc.uniform(12345, r, c) for r in range(64) for c in range(64)])
-    assert us.min() >= 0.0 and us.max() <= 1.0 - 2.0 ** -24
-    assert np.all(us * 2 ** 24 == np.floor(us * 2 ** 24))   # on the 2^-24 grid
+    assert us.min() >= 0.0 and us.max() <= 1.0 - 2.0 ** -23
+    assert np.all(us * 2 ** 23 == np.floor(us * 2 ** 23))   # on the 2^-23 grid
     # roughly uniform: mean and variance of U(0,1) within 5 sigma
     assert abs(us.mean() - 0.5) < 5 * math.sqrt(1 / 12 / us.size)
     assert abs(us.var() - 1 / 12) < 0.01
@@ -111,7 +111,7 @@ def test_unbiased_and_variance_bounded(orc, bits):
     var = acc2 / T - mean ** 2
     S, _ = orc.header(orc.quantize(X, None, bits, 0), 64, bits)
     S = S.astype(np.float64)[:, None]
-    assert np.all(np.abs(mean - X) <= 5 * S / (2 * math.sqrt(T)) + 2.0 ** -24 * S + 1e-7)
+    assert np.all(np.abs(mean - X) <= 5 * S / (2 * math.sqrt(T)) + 2.0 ** -23 * S + 1e-7)
     assert np.all(var <= S * S / 4 * 1.1 + 1e-12)
     ratio = (var / (S * S)).mean()
     assert abs(ratio - 1 / 6) < 0.02
