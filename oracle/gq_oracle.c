@@ -28,7 +28,8 @@
  *  - the stochastic-rounding uniform u comes from a counter hash of
  *    (seed, row, col): MurmurHash3's published 32-bit finalizer "fmix32";
  *  - S is computed as an fp32 division, the code as floor((x-mn)*(1/S) + u)
- *    clamped to 2^b-1; a constant row (S == 0) codes every element as 0;
+ *    clamped to 2^b-1; a row whose S is below the smallest normal fp32
+ *    (S == 0: a constant row) codes every element as 0, so 1/S is finite;
  *  - de-quantization is one fused multiply-add fmaf(q, S, mn);
  *  - packed row: payload LSB-first, then S and mn as fp32 (see orc_pitch);
  *  - directed graphs: A^[v][u] = 1/sqrt(deg_in(v) deg_out(u)) with degrees
@@ -38,6 +39,7 @@
  * itself -- the GAT worked example printed on the Tango page, closed forms,
  * dense brute force and finite differences (tests/test_oracle_*.py).
  */
+#include <float.h>
 #include <math.h>
 #include <stdint.h>
 #include <stdlib.h>
@@ -101,7 +103,7 @@ void orc_quantize(const float* X, int64_t n, int d, int64_t ldx, const uint8_t* 
     memset(row, 0, (size_t)pitch);
     for (int j = 0; j < d; ++j) {
       int q = 0;
-      if (S != 0.0f) {
+      if (S >= FLT_MIN) { /* S == 0 or subnormal: the row codes as constant */
         float inv = 1.0f / S;
         float t = (x[j] - mn) * inv;                 /* (h - Z) / S          */
         float v = t + orc_uniform(seed, (uint32_t)r, (uint32_t)j); /* + u    */

@@ -74,6 +74,18 @@ def test_constant_row_exact(orc):
         np.testing.assert_array_equal(orc.dequant(pk, 17, b), X)
 
 
+def test_subnormal_scale_codes_as_constant(orc):
+    # S = range / (2^b - 1) below the smallest normal float: every code is 0,
+    # so de-quantization returns the row minimum (error < 255 * 2^-126).
+    x = (np.float32(1e-40) * np.arange(16, dtype=np.float32))[None, :]
+    for b in (2, 4, 8):
+        S, _ = orc.header(orc.quantize(x, None, b, 1), 16, b)
+        assert 0 < S[0] < np.finfo(np.float32).tiny
+        pk = orc.quantize(x, None, b, 1)
+        assert np.all(orc.codes(pk, 16, b) == 0)
+        np.testing.assert_array_equal(orc.dequant(pk, 16, b), np.zeros_like(x))
+
+
 def test_mask_rows_untouched(orc):
     X = synth.normal_matrix(50, 16, seed=1).numpy()
     mask = synth.bernoulli_mask(50, 0.4, seed=2).numpy()
