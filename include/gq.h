@@ -1,0 +1,222 @@
+/*
+ * gq.h -- C ABI of libgq: quantized message passing for full-graph GNN
+ * training on one NVIDIA GB300 (sm_103a).
+ *
+ * What the library computes (each entry point cites its passage):
+ *   AdaQP, "Adaptive Message Quantization and Parallelization for Distributed
+ *   Full-graph GNN Training" (arXiv 2306.01381):
+ *     Sec. 2.1  a layer is aggregation then update, written as a weighted sum
+ *               h_v = sigma(W * sum_{u in {v} U N(v)} a_{u,v} h_u)
+ *     Sec. 2.3  Eqn 4: b-bit stochastic integer quantization of a message row,
+ *               Z = min(h), S = (max(h) - min(h)) / (2^b - 1),
+ *               q = round_st((h - Z) / S), b in {2, 4, 8};
+ *               Eqn 5: de-quantization h^ = q * S + Z
+ *     Sec. 3.1  only the messages of "marginal" nodes travel quantized; the
+ *               others are aggregated in full precision
+ *   Sancus (IJCAI 2023, extended abstract), Sec. 2 Preliminaries:
+ *               A^ = D~^{-1/2} (A + I) D~^{-1/2},  H' = sigma(A^ H W)
+ *   Tango, "Rethinking quantization for graph neural network training on
+ *   GPUs" (arXiv 2308.00890), Sec. 2.1, Fig. 1: GAT forward as GEMM, head
+ *   projections, SDDMM add, LeakyReLU, edge softmax, SpMM; and its backward.
+ *
+ * Conventions shared by every entry point
+ *   - Pointers are DEVICE pointers owned by the caller unless a parameter
+ *     says "host".  The library allocates no device memory: scratch comes
+ *     from a caller buffer sized by the matching *_workspace_bytes query.
+ *   - Every call is asynchronous on `stream` (a cudaStream_t; NULL is the
+ *     legacy default stream) and performs no host<->device copy and no
+ *     synchronization, except gq_graph_prepare, which synchronizes `stream`
+ *     once (documented there).
+ *   - Matrices are row-major with a leading dimension (row pitch) counted in
+ *     elements.  fp32 matrices read or written with vector accesses must be
+ *     16-byte aligned with a leading dimension that is a multiple of 4.
+ *   - Graphs are CSR by DESTINATION: row v lists the sources u of the edges
+ *     u -> v, in ascending order, int32.  Every node should carry its own
+ *     self-loop (the "+ I" of A + I); the library does not add one.
+ *   - Errors: every call returns a gq_status.  Arguments are checked on the
+ *     host before any launch; a failed check launches nothing.  A CUDA launch
+ *     error is reported as GQ_ERR_CUDA.  No kernel traps or asserts.
+ *   - Thread safety: no global mutable host state; calls on different
+ *     streams may run concurrently if their buffers do not overlap.
+ */
+#ifndef GQ_H
+#define GQ_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define GQ_API __attribute__((visibility("default")))
+#else
+#define GQ_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st* gq_stream; /* == cudaStream_t */
+
+typedef enum {
+  GQ_OK = 0,
+  GQ_ERR_INVALID_ARG = 1,  /* null pointer, bad size, bits, alignment      */
+  GQ_ERR_UNSUPPORTED = 2,  /* valid but not supported (e.g. width too big) */
+  GQ_ERR_BAD_GRAPH = 3,    /* CSR fails validation in gq_graph_prepare     */
+  GQ_ERR_CUDA = 4,         /* a CUDA runtime call or launch failed         */
+  GQ_ERR_TIMEOUT = 5,      /* a bounded device-side wait gave up           */
+  GQ_ERR_WORKSPACE = 6     /* workspace or storage buffer too small        */
+} gq_status;
+
+/* Aggregation coefficient a_{u,v} of an edge u -> v. */
+typedef enum {
+  GQ_COEF_GCN = 0,  /* 1/sqrt(deg_in(v) * deg_out(u)), degrees incl. self-loop
+                       (Sancus Sec. 2; for a symmetric graph this is exactly
+                       D~^{-1/2}(A+I)D~^{-1/2})                               */
+  GQ_COEF_SAGE = 1, /* 1/deg_in(v): mean over {v} U N(v) (AdaQP Sec. 2.1)    */
+  GQ_COEF_ONE = 2   /* 1: plain sum                                          */
+} gq_coef;
+
+typedef enum { GQ_ACT_NONE = 0, GQ_ACT_RELU = 1 } gq_act;
+
+/* Human-readable text of a status code (static storage, never NULL). */
+GQ_API const char* gq_status_string(int status);
+
+/* Library ABI version (major * 10000 + minor * 100 + patch). */
+GQ_API int gq_version(void);
+
+/* ------------------------------------------------------------------------
+ * Packed message rows (AdaQP Sec. 2.3, Eqn 4).  One row of the packed
+ * buffer holds one quantized message vector of width d at b bits:
+ *   bytes [0, ceil(d*b/8))  codes q_j, LSB-first: code j occupies bits
+ *                           [(j*b) mod 8, +b) of byte floor(j*b/8)
+ *   bytes up to H           zero, H = gq_packed_header_offset(d, b)
+ *                           (payload rounded up to a multiple of 8)
+ *   bytes [H, H+4)          S, the scale, little-endian fp32
+ *   bytes [H+4, H+8)        Z = min of the row, little-endian fp32
+ *   bytes up to the pitch   zero; pitch = gq_packed_pitch(d, b), a multiple
+ *                           of 16, so every row starts 16-byte aligned.
+ * Row r of the buffer belongs to node r.  Returns -1 for invalid d / bits.
+ * ---------------------------------------------------------------------- */
+GQ_API int64_t gq_packed_pitch(int d, int bits);
+GQ_API int64_t gq_packed_header_offset(int d, int bits);
+
+/* ------------------------------------------------------------------------
+ * gq_quantize_pack -- AdaQP Sec. 2.3, Eqn 4, for every row r with
+ * mask[r] != 0 (every row when mask == NULL):
+ *   Z = min_j X[r,j];  S = (max_j X[r,j] - Z) / (2^b - 1)   (fp32 division)
+ *   u = (fmix32(fmix32(r ^ fmix32(s)) + j * 0x9E3779B9) >> 9) * 2^-23, with
+ *       s = low32(seed) ^ high32(seed) and fmix32 MurmurHash3's finalizer
+ *   q = min(floor((X[r,j] - Z) * (1/S) + u), 2^b - 1)  (fp32, each op
+ *       rounded to nearest, no fused multiply-add); q = 0 for every
+ *       element when S is below the smallest normal fp32 (a constant row).
+ * Rows must be finite with max - min finite; other rows give unspecified
+ * codes (no fault).
+ * The result is bit-for-bit reproducible.  Rows with mask[r] == 0 are not
+ * written.
+ *   X       n x d fp32, leading dimension ldx >= d
+ *   mask    n bytes or NULL
+ *   bits    2, 4 or 8
+ *   packed  n x gq_packed_pitch(d, bits) bytes, 16-byte aligned
+ * Errors: GQ_ERR_INVALID_ARG for null X/packed, n < 0, d < 1, ldx < d,
+ * bits not in {2,4,8}, a misaligned packed buffer; GQ_ERR_UNSUPPORTED for
+ * d > 16384.
+ * ---------------------------------------------------------------------- */
+GQ_API int gq_quantize_pack(const float* X, int64_t n, int d, int64_t ldx, const uint8_t* mask, int bits,
+                     uint64_t seed, uint8_t* packed, gq_stream stream);
+
+/* gq_dequant_unpack -- AdaQP Sec. 2.3, Eqn 5: Y[r,j] = fmaf(q_j, S, Z) for
+ * every row with mask[r] != 0 (all rows when mask == NULL); other rows of Y
+ * are not written.  Y is n x d fp32 with leading dimension ldy >= d.       */
+GQ_API int gq_dequant_unpack(const uint8_t* packed, int64_t n, int d, int bits, const uint8_t* mask,
+                      float* Y, int64_t ldy, gq_stream stream);
+
+/* ------------------------------------------------------------------------
+ * Prepared graph.  gq_graph_prepare derives from the caller's CSR the
+ * transposed CSR (CSC: row u lists the destinations v of the edges u -> v,
+ * ascending, with tr_perm giving each entry's edge id in the CSR), the
+ * degree normalizations, and the lists of "hub" rows whose degree exceeds
+ * hub_threshold (those are aggregated by a whole thread block).
+ * All arrays live in the caller's `storage` buffer.
+ * ---------------------------------------------------------------------- */
+typedef struct gq_graph {
+  int64_t n;                /* nodes                                      */
+  int64_t nnz;              /* edges, self-loops included                 */
+  const int32_t* rowptr;    /* n+1, caller's CSR (destinations)           */
+  const int32_t* col;       /* nnz                                        */
+  int32_t* tr_rowptr;       /* n+1, CSC (sources)                         */
+  int32_t* tr_col;          /* nnz: destination of each CSC entry         */
+  int32_t* tr_perm;         /* nnz: CSR edge id of each CSC entry         */
+  float* dinv_in;           /* n: 1/sqrt(deg_in)  (0 if deg 0)            */
+  float* dinv_out;          /* n: 1/sqrt(deg_out)                         */
+  float* inv_in;            /* n: 1/deg_in                                */
+  int32_t* hub_rows;        /* CSR rows with degree > hub_threshold       */
+  int32_t* tr_hub_rows;     /* CSC rows with degree > hub_threshold       */
+  int64_t n_hub;            /* entries of hub_rows                        */
+  int64_t tr_n_hub;         /* entries of tr_hub_rows                     */
+  int32_t hub_threshold;
+  int32_t max_deg;          /* largest in-degree                          */
+  int32_t tr_max_deg;       /* largest out-degree                         */
+  int32_t reserved;
+} gq_graph;
+
+/* Bytes of `storage` gq_graph_prepare needs for a graph of n nodes and nnz
+ * edges (all derived arrays, 256-byte aligned sub-buffers).               */
+GQ_API size_t gq_graph_storage_bytes(int64_t n, int64_t nnz);
+/* Bytes of scratch gq_graph_prepare needs (free again when it returns).   */
+GQ_API size_t gq_graph_prepare_workspace_bytes(int64_t n, int64_t nnz);
+
+/* gq_graph_prepare -- validates the CSR (rowptr[0] == 0, non-decreasing,
+ * rowptr[n] == nnz, 0 <= col < n) and fills *g (a HOST struct) with device
+ * pointers into `storage`.  Degrees count every CSR entry, so with the
+ * self-loops present they are the D~ = D + I of Sancus Sec. 2.  The norms
+ * are (float)(1.0 / sqrt((double)deg)) and (float)(1.0 / (double)deg),
+ * each rounded once.  The CSC is the stable transpose: entries of a CSC
+ * row are in increasing destination order.
+ * Synchronizes `stream` once, to read back the hub counts and the
+ * validation flags.  hub_threshold <= 0 selects the default (2048).
+ * Errors: GQ_ERR_INVALID_ARG (null pointers, n < 1, nnz < 0 or nnz >= 2^31),
+ * GQ_ERR_WORKSPACE (storage or ws too small), GQ_ERR_BAD_GRAPH.          */
+GQ_API int gq_graph_prepare(int64_t n, int64_t nnz, const int32_t* rowptr, const int32_t* col,
+                     int hub_threshold, void* storage, size_t storage_bytes, void* ws,
+                     size_t ws_bytes, gq_graph* g, gq_stream stream);
+
+/* ------------------------------------------------------------------------
+ * gq_dequant_spmm -- the aggregation of AdaQP Sec. 2.1 / Sancus Sec. 2 with
+ * de-quantization (AdaQP Eqn 5) fused into the gather, mixing quantized and
+ * full-precision rows as AdaQP Sec. 3.1 does:
+ *   transpose == 0:  Y[v,:] = sum_{e = (u -> v)} a_{u,v} m_u
+ *   transpose == 1:  Y[u,:] = sum_{e = (u -> v)} a_{u,v} m_v     (= A^T M)
+ * where the message row m_x = deq(packed row x) if bits < 32 and
+ * (mask == NULL or mask[x] != 0), and m_x = X[x,:] otherwise.
+ *   coef        gq_coef
+ *   X           n x d fp32 (ldx), may be NULL only when every row is read
+ *               from `packed` (bits < 32 and mask == NULL)
+ *   packed      n x gq_packed_pitch(d, bits) bytes (ignored for bits == 32)
+ *   bits        2, 4, 8, or 32 (no quantization)
+ *   Y           n x d fp32 (ldy); every row is written
+ * Sums run in fp32 in a fixed order (deterministic run to run).
+ * Errors: GQ_ERR_INVALID_ARG (null or misaligned pointers, d % 4 != 0 for
+ * an fp32 operand, bad bits/coef); GQ_ERR_UNSUPPORTED for d > 1024.      */
+GQ_API int gq_dequant_spmm(const gq_graph* g, int transpose, int coef, const float* X, int64_t ldx,
+                    const uint8_t* packed, const uint8_t* mask, int d, int bits, float* Y,
+                    int64_t ldy, gq_stream stream);
+
+/* ------------------------------------------------------------------------
+ * gq_edge_spmm -- multi-head attention aggregation (Tango Sec. 2.1, Fig. 1a
+ * step 5, H^(l) = (G (.) alpha) H'), all heads in one pass, with the same
+ * quantized / full-precision message mix as gq_dequant_spmm:
+ *   transpose == 0:  Y[v, kF+f] = sum_{e=(u->v)} alpha[e,k] m_u[kF+f]
+ *   transpose == 1:  Y[u, kF+f] = sum_{e=(u->v)} alpha[e,k] m_v[kF+f]
+ *                    (the backward pass of step 5, Fig. 1b)
+ * with F = d / heads; edge e is the CSR edge id (alpha is E x heads fp32,
+ * row-major, indexed by CSR edge id in both directions).
+ * Errors: as gq_dequant_spmm, plus GQ_ERR_INVALID_ARG when heads does not
+ * divide d and GQ_ERR_UNSUPPORTED unless F is a power of two >= 8.       */
+GQ_API int gq_edge_spmm(const gq_graph* g, int transpose, const float* alpha, int heads, const float* X,
+                 int64_t ldx, const uint8_t* packed, const uint8_t* mask, int d, int bits,
+                 float* Y, int64_t ldy, gq_stream stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* GQ_H */

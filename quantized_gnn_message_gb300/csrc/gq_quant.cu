@@ -1,0 +1,237 @@
+// gq_quant.cu -- per-row stochastic integer quantization with bit-packing,
+// and the matching de-quantization (AdaQP Sec. 2.3, Eqn 4 and Eqn 5).
+//
+// One warp per message row.  Lane l owns the 8-column chunks c = l + 32 i
+// of the row, so each lane packs its 8 codes into one b-byte word and the
+// warp writes the payload with contiguous 2/4/8-byte stores.  Row min/max
+// are warp-shuffle reductions; the noise is a counter hash of (seed, row,
+// column), so the packed bytes do not depend on the launch shape.
+#include "gq_common.cuh"
+
+namespace gq {
+namespace {
+
+constexpr int kQuantThreads = 256;
+
+// Load the 8 values of chunk c (columns 8c .. 8c+7) of row x; columns >= d
+// read as `fill`.
+__device__ __forceinline__ void load_chunk(const float* __restrict__ x, int c, int d, bool vec,
+                                           float fill, float (&v)[8]) {
+  const int j0 = c * 8;
+  if (vec && j0 + 8 <= d) {
+    const float4 a = ldg_f4(x + j0);
+    const float4 b = ldg_f4(x + j0 + 4);
+    v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
+    v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+  } else {
+#pragma unroll
+    for (int i = 0; i < 8; ++i) v[i] = (j0 + i < d) ? __ldg(x + j0 + i) : fill;
+  }
+}
+
+// Codes of one chunk, packed LSB-first into BITS bytes.
+template <int BITS>
+__device__ __forceinline__ uint64_t quantize_chunk(const float (&v)[8], int j0, int d, float mn,
+                                                   float inv, bool constant, uint32_t kr) {
+  constexpr uint32_t L = (1u << BITS) - 1u;
+  uint64_t word = 0;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    uint32_t q = 0;
+    if (!constant && j0 + i < d) {
+      const float t = __fmul_rn(__fsub_rn(v[i], mn), inv);
+      const float s = __fadd_rn(t, noise_u(kr, (uint32_t)(j0 + i)));
+      // floor(s) for s in [0, 2^23): add 2^23 rounding down, read the mantissa
+      q = __float_as_uint(__fadd_rd(s, 8388608.0f)) - 0x4B000000u;
+      q = min(q, L);
+    }
+    word |= (uint64_t)q << (i * BITS);
+  }
+  return word;
+}
+
+template <int BITS>
+__device__ __forceinline__ void store_word(uint8_t* p, uint64_t w) {
+  if (BITS == 8) {
+    *reinterpret_cast<uint2*>(p) = make_uint2((uint32_t)w, (uint32_t)(w >> 32));
+  } else if (BITS == 4) {
+    *reinterpret_cast<uint32_t*>(p) = (uint32_t)w;
+  } else {
+    *reinterpret_cast<uint16_t*>(p) = (uint16_t)w;
+  }
+}
+
+// CPL > 0: the row stays in registers (d <= 256 * CPL).  CPL == 0: two
+// passes over global memory (second pass hits L1/L2), any d.
+template <int BITS, int CPL>
+__global__ void __launch_bounds__(kQuantThreads) quantize_pack_kernel(
+    const float* __restrict__ X, int64_t n, int d, int64_t ldx, const uint8_t* __restrict__ mask,
+    uint32_t seed_key, uint8_t* __restrict__ packed, int64_t pitch, int hoff, bool vec) {
+  constexpr float L = (float)((1 << BITS) - 1);
+  const int lane = threadIdx.x & 31;
+  const int64_t warp = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
+  const int nchunks = (d + 7) >> 3;
+  const int p8 = nchunks * BITS;  // bytes the chunk stores cover
+
+  for (int64_t r = warp; r < n; r += nwarps) {
+    if (mask != nullptr && mask[r] == 0) continue;  // warp-uniform
+    const float* x = X + r * ldx;
+    uint8_t* row = packed + r * pitch;
+
+    float mn = __int_as_float(0x7f800000), mx = -__int_as_float(0x7f800000);
+    float v[CPL > 0 ? CPL : 1][8];
+    if (CPL > 0) {
+#pragma unroll
+      for (int i = 0; i < (CPL > 0 ? CPL : 1); ++i) {
+        const int c = lane + 32 * i;
+        if (c < nchunks) {
+          load_chunk(x, c, d, vec, x[0], v[i]);
+#pragma unroll
+          for (int k = 0; k < 8; ++k) { mn = fminf(mn, v[i][k]); mx = fmaxf(mx, v[i][k]); }
+        }
+      }
+    } else {
+      for (int c = lane; c < nchunks; c += 32) {
+        float w[8];
+        load_chunk(x, c, d, vec, x[0], w);
+#pragma unroll
+        for (int k = 0; k < 8; ++k) { mn = fminf(mn, w[k]); mx = fmaxf(mx, w[k]); }
+      }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      mn = fminf(mn, __shfl_xor_sync(FULL, mn, o));
+      mx = fmaxf(mx, __shfl_xor_sync(FULL, mx, o));
+    }
+    // Eqn 4: Z = min, S = (max - min) / (2^b - 1)
+    const float S = __fdiv_rn(__fsub_rn(mx, mn), L);
+    const bool constant = !(S >= 1.17549435e-38f);  // S below FLT_MIN: code as constant
+    const float inv = constant ? 0.0f : __frcp_rn(S);
+    const uint32_t kr = row_key(seed_key, (uint32_t)r);
+
+    if (CPL > 0) {
+#pragma unroll
+      for (int i = 0; i < (CPL > 0 ? CPL : 1); ++i) {
+        const int c = lane + 32 * i;
+        if (c < nchunks) store_word<BITS>(row + (int64_t)c * BITS, quantize_chunk<BITS>(v[i], c * 8, d, mn, inv, constant, kr));
+      }
+    } else {
+      for (int c = lane; c < nchunks; c += 32) {
+        float w[8];
+        load_chunk(x, c, d, vec, x[0], w);
+        store_word<BITS>(row + (int64_t)c * BITS, quantize_chunk<BITS>(w, c * 8, d, mn, inv, constant, kr));
+      }
+    }
+    if (lane == 0) *reinterpret_cast<float2*>(row + hoff) = make_float2(S, mn);
+    for (int b = p8 + lane; b < hoff; b += 32) row[b] = 0;
+    for (int b = hoff + 8 + lane; b < pitch; b += 32) row[b] = 0;
+  }
+}
+
+template <int BITS>
+__global__ void __launch_bounds__(kQuantThreads) dequant_unpack_kernel(
+    const uint8_t* __restrict__ packed, int64_t n, int d, int64_t pitch, int hoff,
+    const uint8_t* __restrict__ mask, float* __restrict__ Y, int64_t ldy) {
+  const int lane = threadIdx.x & 31;
+  const int64_t warp = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
+  const int nchunks = (d + 7) >> 3;
+  for (int64_t r = warp; r < n; r += nwarps) {
+    if (mask != nullptr && mask[r] == 0) continue;
+    const uint8_t* row = packed + r * pitch;
+    const float2 h = *reinterpret_cast<const float2*>(row + hoff);
+    for (int c = lane; c < nchunks; c += 32) {
+      uint64_t w;
+      if (BITS == 8) {
+        const uint2 t = *reinterpret_cast<const uint2*>(row + (int64_t)c * 8);
+        w = (uint64_t)t.x | ((uint64_t)t.y << 32);
+      } else if (BITS == 4) {
+        w = *reinterpret_cast<const uint32_t*>(row + (int64_t)c * 4);
+      } else {
+        w = *reinterpret_cast<const uint16_t*>(row + (int64_t)c * 2);
+      }
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const int j = c * 8 + i;
+        if (j < d) {
+          const uint32_t q = (uint32_t)(w >> (i * BITS)) & ((1u << BITS) - 1u);
+          Y[r * ldy + j] = __fmaf_rn(code_to_float(q), h.x, h.y);
+        }
+      }
+    }
+  }
+}
+
+int grid_for_rows(int64_t n) {
+  const int64_t rows_per_block = kQuantThreads / 32;
+  int64_t g = (n + rows_per_block - 1) / rows_per_block;
+  const int64_t cap = (int64_t)sm_count() * 8 * 4;
+  if (g > cap) g = cap;
+  if (g < 1) g = 1;
+  return (int)g;
+}
+
+template <int BITS>
+int launch_quantize(const float* X, int64_t n, int d, int64_t ldx, const uint8_t* mask, uint64_t seed,
+                    uint8_t* packed, cudaStream_t s) {
+  const int64_t pitch = packed_pitch(d, BITS);
+  const int hoff = (int)header_offset(d, BITS);
+  const bool vec = aligned(X, 16) && (ldx % 4 == 0);
+  const uint32_t h = seed_key_host(seed);
+  const int grid = grid_for_rows(n);
+  if (d <= 256)
+    quantize_pack_kernel<BITS, 1><<<grid, kQuantThreads, 0, s>>>(X, n, d, ldx, mask, h, packed, pitch, hoff, vec);
+  else if (d <= 512)
+    quantize_pack_kernel<BITS, 2><<<grid, kQuantThreads, 0, s>>>(X, n, d, ldx, mask, h, packed, pitch, hoff, vec);
+  else if (d <= 1024)
+    quantize_pack_kernel<BITS, 4><<<grid, kQuantThreads, 0, s>>>(X, n, d, ldx, mask, h, packed, pitch, hoff, vec);
+  else
+    quantize_pack_kernel<BITS, 0><<<grid, kQuantThreads, 0, s>>>(X, n, d, ldx, mask, h, packed, pitch, hoff, vec);
+  return launch_status();
+}
+
+template <int BITS>
+int launch_dequant(const uint8_t* packed, int64_t n, int d, const uint8_t* mask, float* Y, int64_t ldy,
+                   cudaStream_t s) {
+  dequant_unpack_kernel<BITS><<<grid_for_rows(n), kQuantThreads, 0, s>>>(
+      packed, n, d, packed_pitch(d, BITS), (int)header_offset(d, BITS), mask, Y, ldy);
+  return launch_status();
+}
+
+}  // namespace
+
+int quantize_pack(const float* X, int64_t n, int d, int64_t ldx, const uint8_t* mask, int bits, uint64_t seed,
+                  uint8_t* packed, cudaStream_t s) {
+  if (n < 0 || d < 1 || ldx < d || !valid_bits(bits)) return GQ_ERR_INVALID_ARG;
+  if (n > 0 && (X == nullptr || packed == nullptr)) return GQ_ERR_INVALID_ARG;
+  if (!aligned(packed, 16)) return GQ_ERR_INVALID_ARG;
+  if (d > 16384) return GQ_ERR_UNSUPPORTED;
+  if (n == 0) return GQ_OK;
+  switch (bits) {
+    case 2: return launch_quantize<2>(X, n, d, ldx, mask, seed, packed, s);
+    case 4: return launch_quantize<4>(X, n, d, ldx, mask, seed, packed, s);
+    default: return launch_quantize<8>(X, n, d, ldx, mask, seed, packed, s);
+  }
+}
+
+}  // namespace gq
+
+extern "C" int gq_quantize_pack(const float* X, int64_t n, int d, int64_t ldx, const uint8_t* mask, int bits,
+                                uint64_t seed, uint8_t* packed, gq_stream stream) {
+  return gq::quantize_pack(X, n, d, ldx, mask, bits, seed, packed, (cudaStream_t)stream);
+}
+
+extern "C" int gq_dequant_unpack(const uint8_t* packed, int64_t n, int d, int bits, const uint8_t* mask, float* Y,
+                                 int64_t ldy, gq_stream stream) {
+  if (n < 0 || d < 1 || ldy < d || !gq::valid_bits(bits)) return GQ_ERR_INVALID_ARG;
+  if (n > 0 && (packed == nullptr || Y == nullptr)) return GQ_ERR_INVALID_ARG;
+  if (!gq::aligned(packed, 16)) return GQ_ERR_INVALID_ARG;
+  if (n == 0) return GQ_OK;
+  cudaStream_t s = (cudaStream_t)stream;
+  switch (bits) {
+    case 2: return gq::launch_dequant<2>(packed, n, d, mask, Y, ldy, s);
+    case 4: return gq::launch_dequant<4>(packed, n, d, mask, Y, ldy, s);
+    default: return gq::launch_dequant<8>(packed, n, d, mask, Y, ldy, s);
+  }
+}

@@ -1,0 +1,41 @@
+"""Shared helpers of the GPU parity tests (no method arithmetic here)."""
+import numpy as np
+import pytest
+import torch
+
+import synth
+
+
+def require_cuda():
+    if not torch.cuda.is_available():
+        pytest.fail("CUDA device required for -m gpu tests")
+
+
+def gq():
+    require_cuda()
+    import quantized_gnn_message_gb300 as q
+    q.lib()
+    return q
+
+
+def close(gpu, ref, rtol=1e-4, what=""):
+    """max |gpu - ref| <= rtol * (1 + |ref|), elementwise."""
+    g = np.asarray(gpu, np.float64)
+    r = np.asarray(ref, np.float64)
+    assert g.shape == r.shape, (g.shape, r.shape)
+    err = np.abs(g - r) - rtol * (1.0 + np.abs(r))
+    if err.size and err.max() > 0:
+        i = np.unravel_index(np.argmax(err), err.shape)
+        raise AssertionError(f"{what}: mismatch at {i}: gpu={g[i]!r} ref={r[i]!r} "
+                             f"({int((err > 0).sum())} of {err.size} elements out of tolerance)")
+
+
+def rmat_small(scale=12, n=3000, deg=12, seed=1):
+    return synth.rmat_graph(scale=scale, n=n, n_draws=n * deg, seed=seed)
+
+
+def hub_graph(n=700, seed=3):
+    """A graph with a few very high in- and out-degree nodes plus a ragged
+    tail (some rows with only the self-loop)."""
+    g = synth.rmat_graph(scale=10, n=n, n_draws=n * 30, a=0.7, b=0.12, c=0.12, seed=seed)
+    return g
