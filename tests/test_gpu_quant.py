@@ -74,7 +74,7 @@ def test_quantize_strided_rows(orc):
 def test_quantize_empty_and_single(orc):
     q = gq()
     X = torch.zeros(0, 16, device="cuda")
-    assert q.quantize_pack(X, None, 8, 0).shape == (0, 16)
+    assert q.quantize_pack(X, None, 8, 0).shape == (0, q.packed_pitch(16, 8))
     _run(orc, np.array([[3.0]], np.float32), None, 2, 1)
 
 
