@@ -216,6 +216,74 @@ GQ_API int gq_edge_spmm(const gq_graph* g, int transpose, const float* alpha, in
                  int64_t ldx, const uint8_t* packed, const uint8_t* mask, int d, int bits,
                  float* Y, int64_t ldy, gq_stream stream);
 
+
+/* ------------------------------------------------------------------------
+ * Dense update GEMMs on the tcgen05 tensor cores (bf16 inputs, fp32
+ * accumulation in tensor memory).  AdaQP Sec. 2.1 (update W h), Tango
+ * Sec. 2.1 step 1 (H' = H W) and their backward products.
+ * bf16 matrices are read with TMA: 16-byte aligned base, leading dimension a
+ * multiple of 8 elements.  `dev_err` (nullable) is a device int that a
+ * kernel sets to a non-zero code if a bounded internal wait gave up; read
+ * it after synchronizing (0 = fine).
+ *
+ * gq_gemm_bf16_nt: C[M x N] = act(A[M x K] * B[N x K]^T), i.e. C = A W with
+ *   B = W^T stored row-major.  K <= 256, N <= 256 (whole B stays in shared
+ *   memory).  C fp32 with leading dimension ldc >= N.
+ * ---------------------------------------------------------------------- */
+GQ_API int gq_gemm_bf16_nt(const uint16_t* A, int64_t M, int K, int64_t lda, const uint16_t* B, int N,
+                    int64_t ldb, int act, float* C, int64_t ldc, int* dev_err, gq_stream stream);
+
+/* gq_gemm_bf16_tn: C[K1 x N1] = X[R x K1]^T * Y[R x N1] (+ C if accumulate;
+ *   R == 0 gives C = 0, X and Y may then be NULL),
+ *   the weight gradient dW = A^T dZ.  K1, N1 <= 256.  Rows are split across
+ *   thread blocks; fp32 partials go to `ws` (size from the query, which
+ *   depends on the current device's SM count) and are summed in a fixed
+ *   order, so the result is deterministic.                                */
+GQ_API size_t gq_gemm_bf16_tn_workspace_bytes(int64_t R, int K1, int N1);
+GQ_API int gq_gemm_bf16_tn(const uint16_t* X, int64_t R, int K1, int64_t ldx, const uint16_t* Y, int N1,
+                    int64_t ldy, float* C, int64_t ldc, int accumulate, void* ws, size_t ws_bytes,
+                    int* dev_err, gq_stream stream);
+
+/* gq_to_bf16: dst[r][c] = bf16(src[r][c]) (round to nearest even) for
+ *   c < cols, and 0 for cols <= c < dcols (padding for TMA strides).       */
+GQ_API int gq_to_bf16(const float* src, int64_t rows, int cols, int64_t lds, uint16_t* dst, int64_t ldd,
+               int dcols, gq_stream stream);
+
+/* ------------------------------------------------------------------------
+ * GCN / GraphSAGE-mean layer (AdaQP Sec. 2.1 weighted sum, Sec. 3.1 mixed
+ * quantized/full-precision messages; Sancus Sec. 2 H' = sigma(A^ H W)).
+ *
+ * gq_gcn_layer_fwd:
+ *   packed = quantize_pack(H_in rows with mask != 0, bits, seed)   (bits<32)
+ *   A      = sum_{u->v} a_{u,v} m_u   -> A_save, bf16, n x d_in (lda)
+ *   H_out  = act(A W)                 -> fp32, n x d_out (ldo)
+ *   W is d_in x d_out fp32 row-major.  d_in % 4 == 0, lda % 8 == 0,
+ *   d_in, d_out <= 256.  A_save is what the backward pass needs.
+ *
+ * gq_gcn_layer_bwd (same arguments read in reverse; the quantizer is the
+ * identity in backward):
+ *   dZ    = dH_out * [H_out > 0]  (act = RELU; dH_out for act = NONE)
+ *   dW    = A^T dZ                -> fp32 d_in x d_out (ld d_out)
+ *   if need_dinput:
+ *     dA    = dZ W^T              -> dA_save if non-NULL (n x d_in, ld d_in)
+ *     packed= quantize_pack(dA rows with mask != 0, bits, seed)
+ *     dH_in = A^T-aggregation of the mixed messages -> n x d_in (ldi)
+ * Both take a workspace of gq_gcn_layer_workspace_bytes(n, d_in, d_out,
+ * bits) bytes (256-byte aligned) and a nullable device error word (see
+ * the GEMMs).  Errors: GQ_ERR_INVALID_ARG, GQ_ERR_UNSUPPORTED,
+ * GQ_ERR_WORKSPACE, GQ_ERR_CUDA.
+ * ---------------------------------------------------------------------- */
+GQ_API size_t gq_gcn_layer_workspace_bytes(int64_t n, int d_in, int d_out, int bits);
+GQ_API int gq_gcn_layer_fwd(const gq_graph* g, int coef, const float* H_in, int64_t ldh, int d_in,
+                     const float* W, int d_out, const uint8_t* mask, int bits, uint64_t seed, int act,
+                     uint16_t* A_save, int64_t lda, float* H_out, int64_t ldo, void* ws,
+                     size_t ws_bytes, int* dev_err, gq_stream stream);
+GQ_API int gq_gcn_layer_bwd(const gq_graph* g, int coef, const float* dH_out, int64_t ldd,
+                     const uint16_t* A_save, int64_t lda, const float* H_out, int64_t ldo,
+                     const float* W, int d_in, int d_out, const uint8_t* mask, int bits, uint64_t seed,
+                     int act, int need_dinput, float* dW, float* dH_in, int64_t ldi, float* dA_save,
+                     void* ws, size_t ws_bytes, int* dev_err, gq_stream stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -80,6 +80,14 @@ def _SIGNATURES(P, I64, I, U64, F, S):
         ("gq_graph_prepare", [I64, I64, P, P, I, P, S, P, S, GP, P], I),
         ("gq_dequant_spmm", [GP, I, I, P, I64, P, P, I, I, P, I64, P], I),
         ("gq_edge_spmm", [GP, I, P, I, P, I64, P, P, I, I, P, I64, P], I),
+        ("gq_gemm_bf16_nt", [P, I64, I, I64, P, I, I64, I, P, I64, P, P], I),
+        ("gq_gemm_bf16_tn_workspace_bytes", [I64, I, I], S),
+        ("gq_gemm_bf16_tn", [P, I64, I, I64, P, I, I64, P, I64, I, P, S, P, P], I),
+        ("gq_to_bf16", [P, I64, I, I64, P, I64, I, P], I),
+        ("gq_gcn_layer_workspace_bytes", [I64, I, I, I], S),
+        ("gq_gcn_layer_fwd", [GP, I, P, I64, I, P, I, P, I, U64, I, P, I64, P, I64, P, S, P, P], I),
+        ("gq_gcn_layer_bwd", [GP, I, P, I64, P, I64, P, I64, P, I, I, P, I, U64, I, I, P, P, I64, P, P, S, P, P],
+         I),
     ]
 
 
@@ -258,3 +266,125 @@ def edge_spmm(g: Graph, alpha: torch.Tensor, X: torch.Tensor | None, packed: tor
     _check(lib().gq_edge_spmm(g.ref, int(transpose), _ptr(alpha), heads, _ptr(X), ldx, _ptr(packed), _ptr(mask),
                               d, bits, _ptr(out), _rows(out), _stream()), "gq_edge_spmm")
     return out
+
+
+# --------------------------------------------------------------------------
+# dense GEMMs
+# --------------------------------------------------------------------------
+
+def _ld_bf16(t):
+    ld = _rows(t)
+    if ld % 8:
+        raise GQError("bf16 operands need a leading dimension that is a multiple of 8")
+    return ld
+
+
+def gemm_nt(A: torch.Tensor, B: torch.Tensor, act: int = ACT_NONE, out: torch.Tensor | None = None,
+            dev_err: torch.Tensor | None = None) -> torch.Tensor:
+    """C = act(A @ B^T) with A [M x K] and B [N x K] bf16 (views may be
+    narrower than their leading dimension)."""
+    _cuda(A, torch.bfloat16, "A")
+    _cuda(B, torch.bfloat16, "B")
+    M, K = A.shape
+    N = B.shape[0]
+    if out is None:
+        out = torch.empty(M, N, dtype=torch.float32, device=A.device)
+    _check(lib().gq_gemm_bf16_nt(_ptr(A), M, K, _ld_bf16(A), _ptr(B), N, _ld_bf16(B), act, _ptr(out), _rows(out),
+                                 _ptr(dev_err), _stream()), "gq_gemm_bf16_nt")
+    return out
+
+
+def gemm_tn(X: torch.Tensor, Y: torch.Tensor, out: torch.Tensor | None = None, accumulate: bool = False,
+            dev_err: torch.Tensor | None = None) -> torch.Tensor:
+    """C = X^T @ Y with X [R x K1] and Y [R x N1] bf16."""
+    _cuda(X, torch.bfloat16, "X")
+    _cuda(Y, torch.bfloat16, "Y")
+    R, K1 = X.shape
+    N1 = Y.shape[1]
+    if out is None:
+        out = torch.zeros(K1, N1, dtype=torch.float32, device=X.device)
+    wb = int(lib().gq_gemm_bf16_tn_workspace_bytes(R, K1, N1))
+    ws = torch.empty(wb, dtype=torch.uint8, device=X.device)
+    _check(lib().gq_gemm_bf16_tn(_ptr(X), R, K1, _ld_bf16(X), _ptr(Y), N1, _ld_bf16(Y), _ptr(out), _rows(out),
+                                 int(accumulate), _ptr(ws), wb, _ptr(dev_err), _stream()), "gq_gemm_bf16_tn")
+    return out
+
+
+def to_bf16(src: torch.Tensor, pad_to: int = 8) -> torch.Tensor:
+    """bf16 copy of a 2-D fp32 tensor, columns zero-padded to a multiple of
+    `pad_to` (returned as a view of the unpadded width)."""
+    _cuda(src, torch.float32, "src")
+    rows, cols = src.shape
+    dcols = (cols + pad_to - 1) // pad_to * pad_to
+    dst = torch.empty(rows, dcols, dtype=torch.bfloat16, device=src.device)
+    _check(lib().gq_to_bf16(_ptr(src), rows, cols, _rows(src), _ptr(dst), dcols, dcols, _stream()), "gq_to_bf16")
+    return dst[:, :cols]
+
+
+# --------------------------------------------------------------------------
+# GCN / GraphSAGE-mean layer
+# --------------------------------------------------------------------------
+
+class Workspace:
+    """A reusable device scratch buffer that grows on demand."""
+
+    def __init__(self, device="cuda"):
+        self.device = device
+        self.buf = torch.empty(0, dtype=torch.uint8, device=device)
+
+    def get(self, nbytes: int) -> torch.Tensor:
+        if self.buf.numel() < nbytes:
+            self.buf = torch.empty(nbytes, dtype=torch.uint8, device=self.device)
+        return self.buf
+
+
+def _round8(x):
+    return (x + 7) // 8 * 8
+
+
+def gcn_layer_fwd(g: Graph, H_in: torch.Tensor, W: torch.Tensor, mask, bits: int, seed: int, act: int,
+                  coef: int = COEF_GCN, ws: Workspace | None = None, A_save=None, H_out=None,
+                  dev_err: torch.Tensor | None = None):
+    """Returns (A_save bf16 [n x d_in] view, H_out fp32 [n x d_out])."""
+    _cuda(H_in, torch.float32, "H_in")
+    _cuda(W, torch.float32, "W")
+    n, d_in = H_in.shape
+    d_out = W.shape[1]
+    dev = H_in.device
+    lda = _round8(d_in)
+    if A_save is None:
+        A_save = torch.empty(n, lda, dtype=torch.bfloat16, device=dev)
+    if H_out is None:
+        H_out = torch.empty(n, d_out, dtype=torch.float32, device=dev)
+    L = lib()
+    wb = int(L.gq_gcn_layer_workspace_bytes(n, d_in, d_out, bits))
+    buf = (ws or Workspace(dev)).get(wb)
+    _check(L.gq_gcn_layer_fwd(g.ref, coef, _ptr(H_in), _rows(H_in), d_in, _ptr(W.contiguous()), d_out, _ptr(mask),
+                              bits, seed & 0xFFFFFFFFFFFFFFFF, act, _ptr(A_save), _rows(A_save), _ptr(H_out),
+                              _rows(H_out), _ptr(buf), buf.numel(), _ptr(dev_err), _stream()), "gq_gcn_layer_fwd")
+    return A_save[:, :d_in], H_out
+
+
+def gcn_layer_bwd(g: Graph, dH_out: torch.Tensor, A_save: torch.Tensor, H_out: torch.Tensor, W: torch.Tensor,
+                  mask, bits: int, seed: int, act: int, need_dinput: bool = True, coef: int = COEF_GCN,
+                  ws: Workspace | None = None, dW=None, dH_in=None, dA_save=None,
+                  dev_err: torch.Tensor | None = None):
+    """Returns (dW [d_in x d_out], dH_in [n x d_in] or None)."""
+    _cuda(dH_out, torch.float32, "dH_out")
+    _cuda(A_save, torch.bfloat16, "A_save")
+    n, d_out = dH_out.shape
+    d_in = W.shape[0]
+    dev = dH_out.device
+    if dW is None:
+        dW = torch.empty(d_in, d_out, dtype=torch.float32, device=dev)
+    if need_dinput and dH_in is None:
+        dH_in = torch.empty(n, d_in, dtype=torch.float32, device=dev)
+    L = lib()
+    wb = int(L.gq_gcn_layer_workspace_bytes(n, d_in, d_out, bits))
+    buf = (ws or Workspace(dev)).get(wb)
+    _check(L.gq_gcn_layer_bwd(g.ref, coef, _ptr(dH_out), _rows(dH_out), _ptr(A_save), _rows(A_save), _ptr(H_out),
+                              _rows(H_out) if H_out is not None else 0, _ptr(W.contiguous()), d_in, d_out,
+                              _ptr(mask), bits, seed & 0xFFFFFFFFFFFFFFFF, act, int(need_dinput), _ptr(dW),
+                              _ptr(dH_in), _rows(dH_in) if dH_in is not None else 0, _ptr(dA_save), _ptr(buf),
+                              buf.numel(), _ptr(dev_err), _stream()), "gq_gcn_layer_bwd")
+    return dW, (dH_in if need_dinput else None)

@@ -1,0 +1,49 @@
+// gq_internal.cuh -- library-internal entry points shared between the
+// translation units (not part of the C ABI).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "gq.h"
+
+namespace gq {
+
+int quantize_pack(const float* X, int64_t n, int d, int64_t ldx, const uint8_t* mask, int bits, uint64_t seed,
+                  uint8_t* packed, cudaStream_t s);
+
+// Aggregation; Yb != nullptr writes the output in bf16 (leading dim ldy).
+int dequant_spmm(const gq_graph* g, int transpose, int coef, const float* X, int64_t ldx, const uint8_t* packed,
+                 const uint8_t* mask, int d, int bits, float* Y, int64_t ldy, cudaStream_t s, void* Yb);
+int edge_spmm(const gq_graph* g, int transpose, const float* alpha, int heads, const float* X, int64_t ldx,
+              const uint8_t* packed, const uint8_t* mask, int d, int bits, float* Y, int64_t ldy, cudaStream_t s);
+
+int row_gemm(const void* A, int64_t M, int K, int64_t lda, const void* B, int N, int64_t ldb, int act, float* C,
+             int64_t ldc, const float* a_src, const float* a_dst, float* S, float* D, int heads, int* err,
+             cudaStream_t s);
+size_t wgrad_workspace(int64_t R, int K1, int N1);
+int wgrad_gemm(const void* X, int64_t R, int K1, int64_t ldx, const void* Y, int N1, int64_t ldy, float* C,
+               int64_t ldc, int accumulate, void* ws, size_t ws_bytes, int* err, cudaStream_t s);
+// dst = bf16(src), columns [cols, dcols) zero; with gate, elements whose
+// gate value is not > 0 become 0 (ReLU derivative taken from the output).
+int to_bf16(const float* src, int64_t rows, int cols, int64_t lds, void* dst, int64_t ldd, int dcols,
+            const float* gate, int64_t ldg, cudaStream_t s);
+// dst[n][k] = bf16(W[k][n]) for k < K, 0 for K <= k < kpad.
+int transpose_bf16(const float* W, int K, int N, int64_t ldw, void* dst, int64_t ldd, int kpad, cudaStream_t s);
+
+// Bump allocator over a caller workspace (256-byte aligned pieces).
+struct Carve {
+  char* base;
+  size_t cap, used = 0;
+  Carve(void* b, size_t c) : base(static_cast<char*>(b)), cap(c) {}
+  void* take(size_t bytes) {
+    const size_t off = (used + 255) & ~(size_t)255;
+    used = off + bytes;
+    return (base == nullptr || used > cap) ? nullptr : base + off;
+  }
+  bool ok() const { return used <= cap; }
+};
+
+inline int64_t round8(int64_t x) { return (x + 7) / 8 * 8; }
+
+}  // namespace gq

@@ -7,6 +7,7 @@
 // are warp-shuffle reductions; the noise is a counter hash of (seed, row,
 // column), so the packed bytes do not depend on the launch shape.
 #include "gq_common.cuh"
+#include "gq_internal.cuh"
 
 namespace gq {
 namespace {

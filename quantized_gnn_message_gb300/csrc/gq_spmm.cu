@@ -20,7 +20,10 @@
 //     warps interleave 32-edge batches and their partial rows are summed in
 //     shared memory in warp order.
 // Every sum runs in a fixed order, so results are identical run to run.
+#include <cuda_bf16.h>
+
 #include "gq_common.cuh"
+#include "gq_internal.cuh"
 
 namespace gq {
 
@@ -39,6 +42,7 @@ struct SpmmParams {
   int hoff;
   const uint8_t* mask;      // null: every row packed (BITS < 32)
   float* Y;
+  __nv_bfloat16* Yb;        // if set, the output is written in bf16 here instead
   int64_t ldy;
   int64_t n_rows;
   int d;
@@ -192,10 +196,25 @@ __device__ __forceinline__ void group_reduce(float (&acc)[CPL][8]) {
       for (int k = 0; k < 8; ++k) acc[i][k] += __shfl_xor_sync(FULL, acc[i][k], o);
 }
 
-template <int CPL>
-__device__ __forceinline__ void store_chunk(float* y, int c, int d, float s, const float (&a)[8]) {
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  const __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<const uint32_t*>(&h);
+}
+
+__device__ __forceinline__ void store_chunk(const SpmmParams& p, int64_t r, int c, float s, const float (&a)[8]) {
+  if (p.Yb != nullptr) {
+    __nv_bfloat16* y = p.Yb + r * p.ldy + c * 8;
+    if (c * 8 + 4 < p.d) {
+      *reinterpret_cast<uint4*>(y) = make_uint4(pack_bf16x2(a[0] * s, a[1] * s), pack_bf16x2(a[2] * s, a[3] * s),
+                                                pack_bf16x2(a[4] * s, a[5] * s), pack_bf16x2(a[6] * s, a[7] * s));
+    } else {
+      *reinterpret_cast<uint2*>(y) = make_uint2(pack_bf16x2(a[0] * s, a[1] * s), pack_bf16x2(a[2] * s, a[3] * s));
+    }
+    return;
+  }
+  float* y = p.Y + r * p.ldy;
   st_f4(y + c * 8, a[0] * s, a[1] * s, a[2] * s, a[3] * s);
-  if (c * 8 + 4 < d) st_f4(y + c * 8 + 4, a[4] * s, a[5] * s, a[6] * s, a[7] * s);
+  if (c * 8 + 4 < p.d) st_f4(y + c * 8 + 4, a[4] * s, a[5] * s, a[6] * s, a[7] * s);
 }
 
 template <int BITS, int G, int CPL, bool EW>
@@ -227,7 +246,10 @@ __global__ void __launch_bounds__(kSpmmThreads) spmm_kernel(const SpmmParams p) 
       float t = 0.0f;
 #pragma unroll
       for (int ww = 0; ww < kSpmmWarps; ++ww) t += part[ww * p.d + j];
-      p.Y[r * p.ldy + j] = t * s;
+      if (p.Yb != nullptr)
+        p.Yb[r * p.ldy + j] = __float2bfloat16_rn(t * s);
+      else
+        p.Y[r * p.ldy + j] = t * s;
     }
     return;
   }
@@ -245,7 +267,7 @@ __global__ void __launch_bounds__(kSpmmThreads) spmm_kernel(const SpmmParams p) 
 #pragma unroll
       for (int i = 0; i < CPL; ++i) {
         const int c = gl + G * i;
-        if (c < nchunks) store_chunk<CPL>(p.Y + r * p.ldy, c, p.d, s, acc[i]);
+        if (c < nchunks) store_chunk(p, r, c, s, acc[i]);
       }
     }
   }
@@ -288,8 +310,8 @@ int launch_any(const SpmmParams& p, int bits, cudaStream_t s) {
 
 // Common argument checks and message-source setup.
 int spmm_setup(const gq_graph* g, int transpose, const float* X, int64_t ldx, const uint8_t* packed,
-               const uint8_t* mask, int d, int bits, float* Y, int64_t ldy, SpmmParams& p) {
-  if (g == nullptr || Y == nullptr || d < 1 || ldy < d) return GQ_ERR_INVALID_ARG;
+               const uint8_t* mask, int d, int bits, float* Y, int64_t ldy, SpmmParams& p, void* Yb = nullptr) {
+  if (g == nullptr || (Y == nullptr && Yb == nullptr) || d < 1 || ldy < d) return GQ_ERR_INVALID_ARG;
   if (!(bits == 32 || valid_bits(bits))) return GQ_ERR_INVALID_ARG;
   if (d > 1024) return GQ_ERR_UNSUPPORTED;
   const bool all_packed = bits < 32 && mask == nullptr;
@@ -297,7 +319,11 @@ int spmm_setup(const gq_graph* g, int transpose, const float* X, int64_t ldx, co
     if (X == nullptr || ldx < d || d % 4 != 0 || ldx % 4 != 0 || !aligned(X, 16)) return GQ_ERR_INVALID_ARG;
   }
   if (bits < 32 && (packed == nullptr || !aligned(packed, 16))) return GQ_ERR_INVALID_ARG;
-  if (d % 4 != 0 || ldy % 4 != 0 || !aligned(Y, 16)) return GQ_ERR_INVALID_ARG;
+  if (Yb != nullptr) {
+    if (d % 4 != 0 || ldy % 8 != 0 || !aligned(Yb, 16)) return GQ_ERR_INVALID_ARG;
+  } else if (d % 4 != 0 || ldy % 4 != 0 || !aligned(Y, 16)) {
+    return GQ_ERR_INVALID_ARG;
+  }
   p = SpmmParams{};
   p.rowptr = transpose ? g->tr_rowptr : g->rowptr;
   p.col = transpose ? g->tr_col : g->col;
@@ -312,15 +338,16 @@ int spmm_setup(const gq_graph* g, int transpose, const float* X, int64_t ldx, co
   p.hoff = bits < 32 ? (int)header_offset(d, bits) : 0;
   p.mask = mask;
   p.Y = Y;
+  p.Yb = static_cast<__nv_bfloat16*>(Yb);
   p.ldy = ldy;
   p.d = d;
   return GQ_OK;
 }
 
 int dequant_spmm(const gq_graph* g, int transpose, int coef, const float* X, int64_t ldx, const uint8_t* packed,
-                 const uint8_t* mask, int d, int bits, float* Y, int64_t ldy, cudaStream_t s) {
+                 const uint8_t* mask, int d, int bits, float* Y, int64_t ldy, cudaStream_t s, void* Yb) {
   SpmmParams p;
-  GQ_TRY(spmm_setup(g, transpose, X, ldx, packed, mask, d, bits, Y, ldy, p));
+  GQ_TRY(spmm_setup(g, transpose, X, ldx, packed, mask, d, bits, Y, ldy, p, Yb));
   if (coef == GQ_COEF_GCN) {
     // a_{u,v} = dinv_out[u] * dinv_in[v]
     p.colscale = transpose ? g->dinv_in : g->dinv_out;
@@ -358,7 +385,7 @@ int edge_spmm(const gq_graph* g, int transpose, const float* alpha, int heads, c
 extern "C" int gq_dequant_spmm(const gq_graph* g, int transpose, int coef, const float* X, int64_t ldx,
                                const uint8_t* packed, const uint8_t* mask, int d, int bits, float* Y, int64_t ldy,
                                gq_stream stream) {
-  return gq::dequant_spmm(g, transpose, coef, X, ldx, packed, mask, d, bits, Y, ldy, (cudaStream_t)stream);
+  return gq::dequant_spmm(g, transpose, coef, X, ldx, packed, mask, d, bits, Y, ldy, (cudaStream_t)stream, nullptr);
 }
 
 extern "C" int gq_edge_spmm(const gq_graph* g, int transpose, const float* alpha, int heads, const float* X,

@@ -1,0 +1,82 @@
+"""GCN / GraphSAGE-mean layer on the GPU vs the oracle, stage by stage on
+the GPU's own stage inputs (AdaQP Sec. 2.1/3.1; Sancus Sec. 2):
+  A      vs oracle aggregation of the same messages  (bf16 output: 5e-3)
+  H_out  vs act(A_gpu W) in float64 on bf16 inputs   (2e-2 bar, 1e-3 check)
+  dW, dA vs float64 products on bf16 inputs          (2e-2 bar, 1e-3 check)
+  dH_in  vs oracle transposed aggregation of dA_gpu's messages (1e-4)
+Quantized bytes of both passes are reproduced bit for bit by the oracle."""
+import numpy as np
+import pytest
+import torch
+
+import synth
+from gpu_helpers import gq, close, rmat_small, hub_graph
+
+pytestmark = pytest.mark.gpu
+
+
+def _case(orc, g, d_in, d_out, bits, act, coef, mask_frac=0.3, seed=0, hub_threshold=0):
+    q = gq()
+    G = q.graph_prepare(g.rowptr.cuda(), g.col.cuda(), hub_threshold)
+    rp, co = g.rowptr.numpy(), g.col.numpy()
+    H = synth.normal_matrix(g.n, d_in, seed=seed + 1)
+    W = synth.glorot(d_in, d_out, seed=seed + 2)
+    mask = synth.bernoulli_mask(g.n, mask_frac, seed=seed + 3)
+    dY = synth.normal_matrix(g.n, d_out, seed=seed + 4, tag=synth.TAG_GRAD)
+    sf, sb = synth.layer_seed(seed, 0, False), synth.layer_seed(seed, 0, True)
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    Hd, Wd, md, dYd = H.cuda(), W.cuda(), mask.cuda(), dY.cuda()
+    A, Hout = q.gcn_layer_fwd(G, Hd, Wd, md, bits, sf, act, coef=coef, dev_err=err)
+    dA = torch.empty(g.n, d_in, device="cuda")
+    dW, dHin = q.gcn_layer_bwd(G, dYd, A, Hout, Wd, md, bits, sb, act, True, coef=coef, dA_save=dA, dev_err=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+
+    Hn, mn = H.numpy(), mask.numpy()
+    pk = orc.quantize(Hn, mn, bits, sf) if bits < 32 else None
+    A_ref = orc.spmm(rp, co, coef, orc.messages(Hn, pk, mn, d_in, bits))
+    A_gpu = A.float().cpu().numpy()
+    close(A_gpu, A_ref, rtol=5e-3, what="A (bf16)")
+    Z = orc.gemm(A_gpu, W.numpy(), bf16=True)
+    H_ref = np.maximum(Z, 0) if act else Z
+    close(Hout.cpu().numpy(), H_ref, rtol=2e-2, what="H_out bar")
+    close(Hout.cpu().numpy(), H_ref, rtol=1e-3, what="H_out")
+
+    Hg = Hout.cpu().numpy()
+    dZ = dY.numpy().astype(np.float64) * ((Hg > 0) if act else 1.0)
+    dW_ref = orc.gemm(A_gpu.T, dZ, bf16=True)
+    close(dW.cpu().numpy(), dW_ref, rtol=2e-2, what="dW bar")
+    close(dW.cpu().numpy(), dW_ref, rtol=1e-3, what="dW")
+    dA_ref = orc.gemm(dZ, W.numpy().T, bf16=True)
+    dAg = dA.cpu().numpy()
+    close(dAg, dA_ref, rtol=1e-3, what="dA")
+    pkb = orc.quantize(dAg, mn, bits, sb) if bits < 32 else None
+    dH_ref = orc.spmm(rp, co, coef, orc.messages(dAg, pkb, mn, d_in, bits), transpose=True)
+    close(dHin.cpu().numpy(), dH_ref, rtol=1e-4, what="dH_in")
+
+
+@pytest.mark.parametrize("bits", [2, 4, 8, 32])
+@pytest.mark.parametrize("act", [0, 1])
+def test_gcn_layer_tiny(orc, bits, act):
+    # the tiny workload: uniform graph, 1,024 nodes, 64 -> 64, 30% marginal
+    _case(orc, synth.uniform_graph(1024, 16384, seed=0), 64, 64, bits, act, coef=0)
+
+
+@pytest.mark.parametrize("d_in,d_out", [(100, 256), (128, 256), (256, 256), (256, 47)])
+@pytest.mark.parametrize("bits", [2, 8])
+def test_gcn_layer_widths(orc, d_in, d_out, bits):
+    _case(orc, rmat_small(), d_in, d_out, bits, act=1 if d_out != 47 else 0, coef=0, mask_frac=0.6)
+
+
+@pytest.mark.parametrize("coef", [1, 2])
+def test_gcn_layer_coefficients(orc, coef):
+    _case(orc, rmat_small(), 64, 64, 4, 1, coef=coef, mask_frac=0.4)
+
+
+def test_gcn_layer_hubs(orc):
+    _case(orc, hub_graph(), 128, 128, 2, 1, coef=0, mask_frac=0.5, hub_threshold=40)
+
+
+def test_gcn_layer_all_central_and_all_marginal(orc):
+    _case(orc, rmat_small(), 64, 32, 8, 1, coef=0, mask_frac=0.0)
+    _case(orc, rmat_small(), 64, 32, 8, 1, coef=0, mask_frac=1.0)
