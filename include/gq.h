@@ -84,6 +84,10 @@ GQ_API const char* gq_status_string(int status);
 /* Library ABI version (major * 10000 + minor * 100 + patch). */
 GQ_API int gq_version(void);
 
+/* sizeof(gq_graph) as compiled into the library (lets bindings that mirror
+ * the struct check their layout). */
+GQ_API size_t gq_graph_struct_bytes(void);
+
 /* ------------------------------------------------------------------------
  * Packed message rows (AdaQP Sec. 2.3, Eqn 4).  One row of the packed
  * buffer holds one quantized message vector of width d at b bits:
@@ -134,10 +138,24 @@ GQ_API int gq_dequant_unpack(const uint8_t* packed, int64_t n, int d, int bits, 
  * Prepared graph.  gq_graph_prepare derives from the caller's CSR the
  * transposed CSR (CSC: row u lists the destinations v of the edges u -> v,
  * ascending, with tr_perm giving each entry's edge id in the CSR), the
- * degree normalizations, and the lists of "hub" rows whose degree exceeds
- * hub_threshold (those are aggregated by a whole thread block).
+ * degree normalizations, and, for each direction, a static schedule of the
+ * "heavy" rows (degree > hub_threshold): each is one thread-block task, or
+ * several tasks of at most split_edges edges whose partial rows are summed
+ * in task order (a split group).  Light rows are one warp each.
  * All arrays live in the caller's `storage` buffer.
  * ---------------------------------------------------------------------- */
+typedef struct gq_sched {
+  const int32_t* tasks;     /* n_tasks x {row, e_begin, e_end, group}; group
+                               = index into groups, or -1 (unsplit row)   */
+  const int32_t* groups;    /* n_groups x {row, first_task, n_tasks,
+                               first_slot}: the group's tasks write their
+                               partial rows to workspace slots
+                               first_slot .. first_slot + n_tasks - 1    */
+  int64_t n_tasks;
+  int64_t n_groups;
+  int64_t n_slots;          /* partial-row slots over all groups          */
+} gq_sched;
+
 typedef struct gq_graph {
   int64_t n;                /* nodes                                      */
   int64_t nnz;              /* edges, self-loops included                 */
@@ -149,14 +167,12 @@ typedef struct gq_graph {
   float* dinv_in;           /* n: 1/sqrt(deg_in)  (0 if deg 0)            */
   float* dinv_out;          /* n: 1/sqrt(deg_out)                         */
   float* inv_in;            /* n: 1/deg_in                                */
-  int32_t* hub_rows;        /* CSR rows with degree > hub_threshold       */
-  int32_t* tr_hub_rows;     /* CSC rows with degree > hub_threshold       */
-  int64_t n_hub;            /* entries of hub_rows                        */
-  int64_t tr_n_hub;         /* entries of tr_hub_rows                     */
-  int32_t hub_threshold;
+  gq_sched sched;           /* heavy rows of the CSR                      */
+  gq_sched tr_sched;        /* heavy rows of the CSC                      */
+  int32_t hub_threshold;    /* rows with more edges are heavy             */
+  int32_t split_edges;      /* heavy rows are cut into tasks of this size */
   int32_t max_deg;          /* largest in-degree                          */
   int32_t tr_max_deg;       /* largest out-degree                         */
-  int32_t reserved;
 } gq_graph;
 
 /* Bytes of `storage` gq_graph_prepare needs for a graph of n nodes and nnz
@@ -172,13 +188,16 @@ GQ_API size_t gq_graph_prepare_workspace_bytes(int64_t n, int64_t nnz);
  * are (float)(1.0 / sqrt((double)deg)) and (float)(1.0 / (double)deg),
  * each rounded once.  The CSC is the stable transpose: entries of a CSC
  * row are in increasing destination order.
- * Synchronizes `stream` once, to read back the hub counts and the
- * validation flags.  hub_threshold <= 0 selects the default (2048).
- * Errors: GQ_ERR_INVALID_ARG (null pointers, n < 1, nnz < 0 or nnz >= 2^31),
- * GQ_ERR_WORKSPACE (storage or ws too small), GQ_ERR_BAD_GRAPH.          */
+ * hub_threshold (>= 32; <= 0 selects 256) and split_edges (>= 256; <= 0
+ * selects 4096) shape the heavy-row schedule; heavier tasks come first.
+ * Synchronizes `stream` and copies the (small) heavy-row lists through
+ * host memory once per direction.
+ * Errors: GQ_ERR_INVALID_ARG (null pointers, n < 1, nnz < 0 or nnz >= 2^31,
+ * hub_threshold or split_edges out of range), GQ_ERR_WORKSPACE (storage or
+ * ws too small), GQ_ERR_BAD_GRAPH, GQ_ERR_CUDA.                           */
 GQ_API int gq_graph_prepare(int64_t n, int64_t nnz, const int32_t* rowptr, const int32_t* col,
-                     int hub_threshold, void* storage, size_t storage_bytes, void* ws,
-                     size_t ws_bytes, gq_graph* g, gq_stream stream);
+                     int hub_threshold, int split_edges, void* storage, size_t storage_bytes,
+                     void* ws, size_t ws_bytes, gq_graph* g, gq_stream stream);
 
 /* ------------------------------------------------------------------------
  * gq_dequant_spmm -- the aggregation of AdaQP Sec. 2.1 / Sancus Sec. 2 with
@@ -194,12 +213,17 @@ GQ_API int gq_graph_prepare(int64_t n, int64_t nnz, const int32_t* rowptr, const
  *   packed      n x gq_packed_pitch(d, bits) bytes (ignored for bits == 32)
  *   bits        2, 4, 8, or 32 (no quantization)
  *   Y           n x d fp32 (ldy); every row is written
+ *   ws          gq_spmm_workspace_bytes(g, transpose, d) bytes of scratch
+ *               (partial rows of split heavy rows); may be NULL when that
+ *               size is 0.  Calls sharing one workspace must not overlap.
  * Sums run in fp32 in a fixed order (deterministic run to run).
  * Errors: GQ_ERR_INVALID_ARG (null or misaligned pointers, d % 4 != 0 for
- * an fp32 operand, bad bits/coef); GQ_ERR_UNSUPPORTED for d > 1024.      */
+ * an fp32 operand, bad bits/coef); GQ_ERR_UNSUPPORTED for d > 1024;
+ * GQ_ERR_WORKSPACE.                                                       */
+GQ_API size_t gq_spmm_workspace_bytes(const gq_graph* g, int transpose, int d);
 GQ_API int gq_dequant_spmm(const gq_graph* g, int transpose, int coef, const float* X, int64_t ldx,
                     const uint8_t* packed, const uint8_t* mask, int d, int bits, float* Y,
-                    int64_t ldy, gq_stream stream);
+                    int64_t ldy, void* ws, size_t ws_bytes, gq_stream stream);
 
 /* ------------------------------------------------------------------------
  * gq_edge_spmm -- multi-head attention aggregation (Tango Sec. 2.1, Fig. 1a
@@ -211,10 +235,11 @@ GQ_API int gq_dequant_spmm(const gq_graph* g, int transpose, int coef, const flo
  * with F = d / heads; edge e is the CSR edge id (alpha is E x heads fp32,
  * row-major, indexed by CSR edge id in both directions).
  * Errors: as gq_dequant_spmm, plus GQ_ERR_INVALID_ARG when heads does not
- * divide d and GQ_ERR_UNSUPPORTED unless F is a power of two >= 8.       */
+ * divide d and GQ_ERR_UNSUPPORTED unless F is a power of two >= 8.
+ * Workspace: as gq_dequant_spmm.                                          */
 GQ_API int gq_edge_spmm(const gq_graph* g, int transpose, const float* alpha, int heads, const float* X,
                  int64_t ldx, const uint8_t* packed, const uint8_t* mask, int d, int bits,
-                 float* Y, int64_t ldy, gq_stream stream);
+                 float* Y, int64_t ldy, void* ws, size_t ws_bytes, gq_stream stream);
 
 
 /* ------------------------------------------------------------------------
@@ -268,21 +293,27 @@ GQ_API int gq_to_bf16(const float* src, int64_t rows, int cols, int64_t lds, uin
  *     dA    = dZ W^T              -> dA_save if non-NULL (n x d_in, ld d_in)
  *     packed= quantize_pack(dA rows with mask != 0, bits, seed)
  *     dH_in = A^T-aggregation of the mixed messages -> n x d_in (ldi)
- * Both take a workspace of gq_gcn_layer_workspace_bytes(n, d_in, d_out,
+ * Both take a workspace of gq_gcn_layer_workspace_bytes(g, d_in, d_out,
  * bits) bytes (256-byte aligned) and a nullable device error word (see
  * the GEMMs).  Errors: GQ_ERR_INVALID_ARG, GQ_ERR_UNSUPPORTED,
  * GQ_ERR_WORKSPACE, GQ_ERR_CUDA.
+ * Tracing: stage_events (nullable) is an array of cudaEvent_t handles,
+ * 2 per stage; events[2k] is recorded on `stream` before stage k and
+ * events[2k+1] after it.  Forward stages: 0 quantize, 1 aggregate,
+ * 2 update GEMM.  Backward stages: 0 dZ, 1 dW, 2 dA, 3 quantize,
+ * 4 transposed aggregate (stages 2-4 only when need_dinput).
  * ---------------------------------------------------------------------- */
-GQ_API size_t gq_gcn_layer_workspace_bytes(int64_t n, int d_in, int d_out, int bits);
+GQ_API size_t gq_gcn_layer_workspace_bytes(const gq_graph* g, int d_in, int d_out, int bits);
 GQ_API int gq_gcn_layer_fwd(const gq_graph* g, int coef, const float* H_in, int64_t ldh, int d_in,
                      const float* W, int d_out, const uint8_t* mask, int bits, uint64_t seed, int act,
                      uint16_t* A_save, int64_t lda, float* H_out, int64_t ldo, void* ws,
-                     size_t ws_bytes, int* dev_err, gq_stream stream);
+                     size_t ws_bytes, int* dev_err, void* const* stage_events, gq_stream stream);
 GQ_API int gq_gcn_layer_bwd(const gq_graph* g, int coef, const float* dH_out, int64_t ldd,
                      const uint16_t* A_save, int64_t lda, const float* H_out, int64_t ldo,
                      const float* W, int d_in, int d_out, const uint8_t* mask, int bits, uint64_t seed,
                      int act, int need_dinput, float* dW, float* dH_in, int64_t ldi, float* dA_save,
-                     void* ws, size_t ws_bytes, int* dev_err, gq_stream stream);
+                     void* ws, size_t ws_bytes, int* dev_err, void* const* stage_events,
+                     gq_stream stream);
 
 #ifdef __cplusplus
 }

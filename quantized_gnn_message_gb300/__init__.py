@@ -30,6 +30,12 @@ class GQError(RuntimeError):
     pass
 
 
+class Sched_t(ctypes.Structure):
+    """Mirror of the C struct gq_sched."""
+    _fields_ = [("tasks", ctypes.c_void_p), ("groups", ctypes.c_void_p), ("n_tasks", ctypes.c_int64),
+                ("n_groups", ctypes.c_int64), ("n_slots", ctypes.c_int64)]
+
+
 class Graph_t(ctypes.Structure):
     """Mirror of the C struct gq_graph."""
     _fields_ = [
@@ -37,10 +43,9 @@ class Graph_t(ctypes.Structure):
         ("rowptr", ctypes.c_void_p), ("col", ctypes.c_void_p),
         ("tr_rowptr", ctypes.c_void_p), ("tr_col", ctypes.c_void_p), ("tr_perm", ctypes.c_void_p),
         ("dinv_in", ctypes.c_void_p), ("dinv_out", ctypes.c_void_p), ("inv_in", ctypes.c_void_p),
-        ("hub_rows", ctypes.c_void_p), ("tr_hub_rows", ctypes.c_void_p),
-        ("n_hub", ctypes.c_int64), ("tr_n_hub", ctypes.c_int64),
-        ("hub_threshold", ctypes.c_int32), ("max_deg", ctypes.c_int32),
-        ("tr_max_deg", ctypes.c_int32), ("reserved", ctypes.c_int32),
+        ("sched", Sched_t), ("tr_sched", Sched_t),
+        ("hub_threshold", ctypes.c_int32), ("split_edges", ctypes.c_int32),
+        ("max_deg", ctypes.c_int32), ("tr_max_deg", ctypes.c_int32),
     ]
 
 
@@ -62,6 +67,8 @@ def lib():
                 fn = getattr(L, name)
                 fn.argtypes = args
                 fn.restype = res
+            if L.gq_graph_struct_bytes() != ctypes.sizeof(Graph_t):
+                raise GQError("gq_graph layout mismatch between libgq and its Python mirror")
             _lib = L
     return _lib
 
@@ -71,23 +78,25 @@ def _SIGNATURES(P, I64, I, U64, F, S):
     return [
         ("gq_status_string", [I], ctypes.c_char_p),
         ("gq_version", [], I),
+        ("gq_graph_struct_bytes", [], S),
         ("gq_packed_pitch", [I, I], I64),
         ("gq_packed_header_offset", [I, I], I64),
         ("gq_quantize_pack", [P, I64, I, I64, P, I, U64, P, P], I),
         ("gq_dequant_unpack", [P, I64, I, I, P, P, I64, P], I),
         ("gq_graph_storage_bytes", [I64, I64], S),
         ("gq_graph_prepare_workspace_bytes", [I64, I64], S),
-        ("gq_graph_prepare", [I64, I64, P, P, I, P, S, P, S, GP, P], I),
-        ("gq_dequant_spmm", [GP, I, I, P, I64, P, P, I, I, P, I64, P], I),
-        ("gq_edge_spmm", [GP, I, P, I, P, I64, P, P, I, I, P, I64, P], I),
+        ("gq_graph_prepare", [I64, I64, P, P, I, I, P, S, P, S, GP, P], I),
+        ("gq_spmm_workspace_bytes", [GP, I, I], S),
+        ("gq_dequant_spmm", [GP, I, I, P, I64, P, P, I, I, P, I64, P, S, P], I),
+        ("gq_edge_spmm", [GP, I, P, I, P, I64, P, P, I, I, P, I64, P, S, P], I),
         ("gq_gemm_bf16_nt", [P, I64, I, I64, P, I, I64, I, P, I64, P, P], I),
         ("gq_gemm_bf16_tn_workspace_bytes", [I64, I, I], S),
         ("gq_gemm_bf16_tn", [P, I64, I, I64, P, I, I64, P, I64, I, P, S, P, P], I),
         ("gq_to_bf16", [P, I64, I, I64, P, I64, I, P], I),
-        ("gq_gcn_layer_workspace_bytes", [I64, I, I, I], S),
-        ("gq_gcn_layer_fwd", [GP, I, P, I64, I, P, I, P, I, U64, I, P, I64, P, I64, P, S, P, P], I),
-        ("gq_gcn_layer_bwd", [GP, I, P, I64, P, I64, P, I64, P, I, I, P, I, U64, I, I, P, P, I64, P, P, S, P, P],
-         I),
+        ("gq_gcn_layer_workspace_bytes", [GP, I, I, I], S),
+        ("gq_gcn_layer_fwd", [GP, I, P, I64, I, P, I, P, I, U64, I, P, I64, P, I64, P, S, P, P, P], I),
+        ("gq_gcn_layer_bwd",
+         [GP, I, P, I64, P, I64, P, I64, P, I, I, P, I, U64, I, I, P, P, I64, P, P, S, P, P, P], I),
     ]
 
 
@@ -210,15 +219,25 @@ class Graph:
         return self._view("inv_in", self.n, torch.float32)
 
     @property
-    def n_hub(self):
-        return int(self.c.n_hub)
+    def n_tasks(self):
+        return int(self.c.sched.n_tasks)
 
     @property
-    def tr_n_hub(self):
-        return int(self.c.tr_n_hub)
+    def tr_n_tasks(self):
+        return int(self.c.tr_sched.n_tasks)
+
+    def sched_arrays(self, transpose: bool = False):
+        """(tasks [n_tasks x 4], groups [n_groups x 4]) as int32 tensors."""
+        sc = self.c.tr_sched if transpose else self.c.sched
+        out = []
+        for ptr, cnt in ((sc.tasks, sc.n_tasks), (sc.groups, sc.n_groups)):
+            off = ptr - self.storage.data_ptr()
+            out.append(self.storage[off:off + cnt * 16].view(torch.int32).view(-1, 4))
+        return out
 
 
-def graph_prepare(rowptr: torch.Tensor, col: torch.Tensor, hub_threshold: int = 0) -> Graph:
+def graph_prepare(rowptr: torch.Tensor, col: torch.Tensor, hub_threshold: int = 0,
+                  split_edges: int = 0) -> Graph:
     _cuda(rowptr, torch.int32, "rowptr")
     _cuda(col, torch.int32, "col")
     n = rowptr.numel() - 1
@@ -229,8 +248,8 @@ def graph_prepare(rowptr: torch.Tensor, col: torch.Tensor, hub_threshold: int = 
     storage = torch.empty(sb, dtype=torch.uint8, device=rowptr.device)
     ws = torch.empty(wb, dtype=torch.uint8, device=rowptr.device)
     g = Graph_t()
-    _check(L.gq_graph_prepare(n, nnz, _ptr(rowptr), _ptr(col), hub_threshold, _ptr(storage), sb, _ptr(ws), wb,
-                              ctypes.byref(g), _stream()), "gq_graph_prepare")
+    _check(L.gq_graph_prepare(n, nnz, _ptr(rowptr), _ptr(col), hub_threshold, split_edges, _ptr(storage), sb,
+                              _ptr(ws), wb, ctypes.byref(g), _stream()), "gq_graph_prepare")
     del ws
     return Graph(n, nnz, rowptr, col, storage, g)
 
@@ -249,8 +268,10 @@ def dequant_spmm(g: Graph, X: torch.Tensor | None, packed: torch.Tensor | None, 
     if out is None:
         out = torch.empty(g.n, d, dtype=torch.float32, device=dev)
     ldx = _rows(X) if X is not None else d
+    wb = int(lib().gq_spmm_workspace_bytes(g.ref, int(transpose), d))
+    ws = torch.empty(max(wb, 1), dtype=torch.uint8, device=dev)
     _check(lib().gq_dequant_spmm(g.ref, int(transpose), coef, _ptr(X), ldx, _ptr(packed), _ptr(mask), d, bits,
-                                 _ptr(out), _rows(out), _stream()), "gq_dequant_spmm")
+                                 _ptr(out), _rows(out), _ptr(ws), wb, _stream()), "gq_dequant_spmm")
     return out
 
 
@@ -263,8 +284,10 @@ def edge_spmm(g: Graph, alpha: torch.Tensor, X: torch.Tensor | None, packed: tor
     if out is None:
         out = torch.empty(g.n, d, dtype=torch.float32, device=alpha.device)
     ldx = _rows(X) if X is not None else d
+    wb = int(lib().gq_spmm_workspace_bytes(g.ref, int(transpose), d))
+    ws = torch.empty(max(wb, 1), dtype=torch.uint8, device=alpha.device)
     _check(lib().gq_edge_spmm(g.ref, int(transpose), _ptr(alpha), heads, _ptr(X), ldx, _ptr(packed), _ptr(mask),
-                              d, bits, _ptr(out), _rows(out), _stream()), "gq_edge_spmm")
+                              d, bits, _ptr(out), _rows(out), _ptr(ws), wb, _stream()), "gq_edge_spmm")
     return out
 
 
@@ -342,9 +365,19 @@ def _round8(x):
     return (x + 7) // 8 * 8
 
 
+def _events(evs):
+    """ctypes array of cudaEvent_t handles (or None) for the stage trace."""
+    if evs is None:
+        return None
+    arr = (ctypes.c_void_p * len(evs))()
+    for i, e in enumerate(evs):
+        arr[i] = e.cuda_event
+    return arr
+
+
 def gcn_layer_fwd(g: Graph, H_in: torch.Tensor, W: torch.Tensor, mask, bits: int, seed: int, act: int,
                   coef: int = COEF_GCN, ws: Workspace | None = None, A_save=None, H_out=None,
-                  dev_err: torch.Tensor | None = None):
+                  dev_err: torch.Tensor | None = None, events=None):
     """Returns (A_save bf16 [n x d_in] view, H_out fp32 [n x d_out])."""
     _cuda(H_in, torch.float32, "H_in")
     _cuda(W, torch.float32, "W")
@@ -357,18 +390,19 @@ def gcn_layer_fwd(g: Graph, H_in: torch.Tensor, W: torch.Tensor, mask, bits: int
     if H_out is None:
         H_out = torch.empty(n, d_out, dtype=torch.float32, device=dev)
     L = lib()
-    wb = int(L.gq_gcn_layer_workspace_bytes(n, d_in, d_out, bits))
+    wb = int(L.gq_gcn_layer_workspace_bytes(g.ref, d_in, d_out, bits))
     buf = (ws or Workspace(dev)).get(wb)
     _check(L.gq_gcn_layer_fwd(g.ref, coef, _ptr(H_in), _rows(H_in), d_in, _ptr(W.contiguous()), d_out, _ptr(mask),
                               bits, seed & 0xFFFFFFFFFFFFFFFF, act, _ptr(A_save), _rows(A_save), _ptr(H_out),
-                              _rows(H_out), _ptr(buf), buf.numel(), _ptr(dev_err), _stream()), "gq_gcn_layer_fwd")
+                              _rows(H_out), _ptr(buf), buf.numel(), _ptr(dev_err), _events(events), _stream()),
+           "gq_gcn_layer_fwd")
     return A_save[:, :d_in], H_out
 
 
 def gcn_layer_bwd(g: Graph, dH_out: torch.Tensor, A_save: torch.Tensor, H_out: torch.Tensor, W: torch.Tensor,
                   mask, bits: int, seed: int, act: int, need_dinput: bool = True, coef: int = COEF_GCN,
                   ws: Workspace | None = None, dW=None, dH_in=None, dA_save=None,
-                  dev_err: torch.Tensor | None = None):
+                  dev_err: torch.Tensor | None = None, events=None):
     """Returns (dW [d_in x d_out], dH_in [n x d_in] or None)."""
     _cuda(dH_out, torch.float32, "dH_out")
     _cuda(A_save, torch.bfloat16, "A_save")
@@ -380,11 +414,11 @@ def gcn_layer_bwd(g: Graph, dH_out: torch.Tensor, A_save: torch.Tensor, H_out: t
     if need_dinput and dH_in is None:
         dH_in = torch.empty(n, d_in, dtype=torch.float32, device=dev)
     L = lib()
-    wb = int(L.gq_gcn_layer_workspace_bytes(n, d_in, d_out, bits))
+    wb = int(L.gq_gcn_layer_workspace_bytes(g.ref, d_in, d_out, bits))
     buf = (ws or Workspace(dev)).get(wb)
     _check(L.gq_gcn_layer_bwd(g.ref, coef, _ptr(dH_out), _rows(dH_out), _ptr(A_save), _rows(A_save), _ptr(H_out),
                               _rows(H_out) if H_out is not None else 0, _ptr(W.contiguous()), d_in, d_out,
                               _ptr(mask), bits, seed & 0xFFFFFFFFFFFFFFFF, act, int(need_dinput), _ptr(dW),
                               _ptr(dH_in), _rows(dH_in) if dH_in is not None else 0, _ptr(dA_save), _ptr(buf),
-                              buf.numel(), _ptr(dev_err), _stream()), "gq_gcn_layer_bwd")
+                              buf.numel(), _ptr(dev_err), _events(events), _stream()), "gq_gcn_layer_bwd")
     return dW, (dH_in if need_dinput else None)

@@ -16,6 +16,8 @@ extern "C" const char* gq_status_string(int status) {
 
 extern "C" int gq_version(void) { return 100; }
 
+extern "C" size_t gq_graph_struct_bytes(void) { return sizeof(gq_graph); }
+
 extern "C" int64_t gq_packed_pitch(int d, int bits) {
   if (d < 1 || !gq::valid_bits(bits)) return -1;
   return gq::packed_pitch(d, bits);

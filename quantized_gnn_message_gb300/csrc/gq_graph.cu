@@ -9,12 +9,18 @@
 // order and results are identical run to run.
 #include <string.h>
 
+#include <algorithm>
+#include <vector>
+
 #include "gq_common.cuh"
 
 namespace gq {
 namespace {
 
-constexpr int kDefaultHub = 2048;
+constexpr int kDefaultHub = 256;
+constexpr int kDefaultSplit = 4096;
+constexpr int kMinHub = 32;
+constexpr int kMinSplit = 256;
 constexpr int kScanThreads = 512;
 constexpr int kScanItems = 8;
 constexpr int kScanTile = kScanThreads * kScanItems;  // 4096
@@ -112,7 +118,7 @@ int scan_exclusive(const int32_t* in, int32_t* out, int64_t n, int32_t* scratch,
 
 // -------------------------------------------------------- degree kernels ---
 __global__ void rows_kernel(int64_t n, int64_t nnz, const int32_t* __restrict__ rowptr, float* dinv_in, float* inv_in,
-                            int32_t* hub_rows, int hub_threshold, Counters* cnt) {
+                            int32_t* hubs, int64_t max_hubs, int hub_threshold, Counters* cnt) {
   const int64_t v = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
   if (v >= n) return;
   const int32_t a = rowptr[v], b = rowptr[v + 1];
@@ -122,7 +128,14 @@ __global__ void rows_kernel(int64_t n, int64_t nnz, const int32_t* __restrict__ 
   const int32_t deg = b - a;
   dinv_in[v] = deg > 0 ? __double2float_rn(1.0 / sqrt((double)deg)) : 0.0f;
   inv_in[v] = deg > 0 ? __double2float_rn(1.0 / (double)deg) : 0.0f;
-  if (deg > hub_threshold) hub_rows[atomicAdd(&cnt->n_hub, 1)] = (int32_t)v;
+  if (deg > hub_threshold) {
+    const int i = atomicAdd(&cnt->n_hub, 1);
+    if (i < max_hubs) {
+      hubs[3 * i] = (int32_t)v;
+      hubs[3 * i + 1] = a;
+      hubs[3 * i + 2] = deg;
+    }
+  }
   atomicMax(&cnt->max_deg, deg);
 }
 
@@ -138,13 +151,21 @@ __global__ void count_cols_kernel(int64_t nnz, int64_t n, const int32_t* __restr
   atomicAdd(&counts[c], 1);
 }
 
-__global__ void out_rows_kernel(int64_t n, const int32_t* __restrict__ tr_rowptr, float* dinv_out,
-                                int32_t* tr_hub_rows, int hub_threshold, Counters* cnt) {
+__global__ void out_rows_kernel(int64_t n, const int32_t* __restrict__ tr_rowptr, float* dinv_out, int32_t* hubs,
+                                int64_t max_hubs, int hub_threshold, Counters* cnt) {
   const int64_t u = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
   if (u >= n) return;
-  const int32_t deg = tr_rowptr[u + 1] - tr_rowptr[u];
+  const int32_t a = tr_rowptr[u];
+  const int32_t deg = tr_rowptr[u + 1] - a;
   dinv_out[u] = deg > 0 ? __double2float_rn(1.0 / sqrt((double)deg)) : 0.0f;
-  if (deg > hub_threshold) tr_hub_rows[atomicAdd(&cnt->tr_n_hub, 1)] = (int32_t)u;
+  if (deg > hub_threshold) {
+    const int i = atomicAdd(&cnt->tr_n_hub, 1);
+    if (i < max_hubs) {
+      hubs[3 * i] = (int32_t)u;
+      hubs[3 * i + 1] = a;
+      hubs[3 * i + 2] = deg;
+    }
+  }
   atomicMax(&cnt->tr_max_deg, deg);
 }
 
@@ -241,8 +262,12 @@ __global__ void gather_rows_kernel(int64_t nnz, const int32_t* __restrict__ perm
   if (i < nnz) tr_col[i] = edge_row[perm[i]];
 }
 
+int64_t max_tasks(int64_t nnz) { return nnz / kMinHub + nnz / kMinSplit + 2; }
+int64_t max_groups(int64_t nnz) { return nnz / kMinSplit + 1; }
+int64_t max_hubs(int64_t nnz) { return nnz / kMinHub + 1; }
+
 struct StorageLayout {
-  size_t tr_rowptr, tr_col, tr_perm, dinv_in, dinv_out, inv_in, hub, tr_hub, total;
+  size_t tr_rowptr, tr_col, tr_perm, dinv_in, dinv_out, inv_in, tasks, groups, tr_tasks, tr_groups, total;
 };
 
 StorageLayout storage_layout(int64_t n, int64_t nnz) {
@@ -254,14 +279,16 @@ StorageLayout storage_layout(int64_t n, int64_t nnz) {
   L.dinv_in = o;   o += align256(sizeof(float) * n);
   L.dinv_out = o;  o += align256(sizeof(float) * n);
   L.inv_in = o;    o += align256(sizeof(float) * n);
-  L.hub = o;       o += align256(sizeof(int32_t) * n);
-  L.tr_hub = o;    o += align256(sizeof(int32_t) * n);
+  L.tasks = o;     o += align256(sizeof(int32_t) * 4 * max_tasks(nnz));
+  L.groups = o;    o += align256(sizeof(int32_t) * 4 * max_groups(nnz));
+  L.tr_tasks = o;  o += align256(sizeof(int32_t) * 4 * max_tasks(nnz));
+  L.tr_groups = o; o += align256(sizeof(int32_t) * 4 * max_groups(nnz));
   L.total = o;
   return L;
 }
 
 struct WsLayout {
-  size_t counters, counts, keys_a, keys_b, vals_a, vals_b, hist, scan, total;
+  size_t counters, counts, keys_a, keys_b, vals_a, vals_b, hist, scan, hubs, tr_hubs, total;
   int64_t tiles;
 };
 
@@ -280,11 +307,53 @@ WsLayout ws_layout(int64_t n, int64_t nnz) {
   L.vals_b = o;   o += align256(sizeof(int32_t) * m);  // also edge_row at the end
   L.hist = o;     o += align256(sizeof(int32_t) * hist_elems);
   L.scan = o;     o += align256(sizeof(int32_t) * (scan_scratch_elems(scan_n) + 64));
+  L.hubs = o;     o += align256(sizeof(int32_t) * 3 * max_hubs(nnz));
+  L.tr_hubs = o;  o += align256(sizeof(int32_t) * 3 * max_hubs(nnz));
   L.total = o;
   return L;
 }
 
 unsigned blocks_for(int64_t n, int t) { return (unsigned)((n + t - 1) / t); }
+
+// Cut the heavy rows {row, e_begin, deg} into block tasks, heaviest first.
+int build_sched(const std::vector<int32_t>& hubs, int split, int32_t* d_tasks, int32_t* d_groups, gq_sched* out,
+                std::vector<int32_t>& tasks, std::vector<int32_t>& groups, cudaStream_t s) {
+  const size_t nh = hubs.size() / 3;
+  std::vector<size_t> order(nh);
+  for (size_t i = 0; i < nh; ++i) order[i] = i;
+  std::sort(order.begin(), order.end(), [&](size_t x, size_t y) {
+    if (hubs[3 * x + 2] != hubs[3 * y + 2]) return hubs[3 * x + 2] > hubs[3 * y + 2];
+    return hubs[3 * x] < hubs[3 * y];
+  });
+  tasks.clear();
+  groups.clear();
+  int32_t slots = 0;
+  for (size_t k = 0; k < nh; ++k) {
+    const int32_t row = hubs[3 * order[k]], e0 = hubs[3 * order[k] + 1], deg = hubs[3 * order[k] + 2];
+    const int32_t nch = (deg + split - 1) / split;
+    int32_t grp = -1;
+    if (nch > 1) {
+      grp = (int32_t)(groups.size() / 4);
+      groups.insert(groups.end(), {row, (int32_t)(tasks.size() / 4), nch, slots});
+      slots += nch;
+    }
+    for (int32_t c = 0; c < nch; ++c) {
+      const int32_t b = e0 + c * split;
+      const int32_t e = (c == nch - 1) ? e0 + deg : b + split;
+      tasks.insert(tasks.end(), {row, b, e, grp});
+    }
+  }
+  out->tasks = d_tasks;
+  out->groups = d_groups;
+  out->n_tasks = (int64_t)(tasks.size() / 4);
+  out->n_groups = (int64_t)(groups.size() / 4);
+  out->n_slots = slots;
+  if (!tasks.empty())
+    GQ_TRY_CUDA(cudaMemcpyAsync(d_tasks, tasks.data(), tasks.size() * 4, cudaMemcpyHostToDevice, s));
+  if (!groups.empty())
+    GQ_TRY_CUDA(cudaMemcpyAsync(d_groups, groups.data(), groups.size() * 4, cudaMemcpyHostToDevice, s));
+  return GQ_OK;
+}
 
 }  // namespace
 }  // namespace gq
@@ -300,8 +369,8 @@ extern "C" size_t gq_graph_prepare_workspace_bytes(int64_t n, int64_t nnz) {
 }
 
 extern "C" int gq_graph_prepare(int64_t n, int64_t nnz, const int32_t* rowptr, const int32_t* col, int hub_threshold,
-                                void* storage, size_t storage_bytes, void* ws, size_t ws_bytes, gq_graph* g,
-                                gq_stream stream) {
+                                int split_edges, void* storage, size_t storage_bytes, void* ws, size_t ws_bytes,
+                                gq_graph* g, gq_stream stream) {
   using namespace gq;
   if (g == nullptr || rowptr == nullptr || storage == nullptr || ws == nullptr) return GQ_ERR_INVALID_ARG;
   if (n < 1 || nnz < 0 || nnz >= (int64_t)0x7fffffff || n >= (int64_t)0x7fffffff) return GQ_ERR_INVALID_ARG;
@@ -311,6 +380,8 @@ extern "C" int gq_graph_prepare(int64_t n, int64_t nnz, const int32_t* rowptr, c
   const WsLayout WL = ws_layout(n, nnz);
   if (storage_bytes < SL.total || ws_bytes < WL.total) return GQ_ERR_WORKSPACE;
   if (hub_threshold <= 0) hub_threshold = kDefaultHub;
+  if (split_edges <= 0) split_edges = kDefaultSplit;
+  if (hub_threshold < kMinHub || split_edges < kMinSplit) return GQ_ERR_INVALID_ARG;
   cudaStream_t s = (cudaStream_t)stream;
 
   char* st = static_cast<char*>(storage);
@@ -327,9 +398,10 @@ extern "C" int gq_graph_prepare(int64_t n, int64_t nnz, const int32_t* rowptr, c
   G.dinv_in = reinterpret_cast<float*>(st + SL.dinv_in);
   G.dinv_out = reinterpret_cast<float*>(st + SL.dinv_out);
   G.inv_in = reinterpret_cast<float*>(st + SL.inv_in);
-  G.hub_rows = reinterpret_cast<int32_t*>(st + SL.hub);
-  G.tr_hub_rows = reinterpret_cast<int32_t*>(st + SL.tr_hub);
   G.hub_threshold = hub_threshold;
+  G.split_edges = split_edges;
+  int32_t* hubs = reinterpret_cast<int32_t*>(wb + WL.hubs);
+  int32_t* tr_hubs = reinterpret_cast<int32_t*>(wb + WL.tr_hubs);
 
   Counters* cnt = reinterpret_cast<Counters*>(wb + WL.counters);
   int32_t* counts = reinterpret_cast<int32_t*>(wb + WL.counts);
@@ -342,14 +414,16 @@ extern "C" int gq_graph_prepare(int64_t n, int64_t nnz, const int32_t* rowptr, c
 
   GQ_TRY_CUDA(cudaMemsetAsync(cnt, 0, sizeof(Counters), s));
   GQ_TRY_CUDA(cudaMemsetAsync(counts, 0, sizeof(int32_t) * (n + 1), s));
-  rows_kernel<<<blocks_for(n, 256), 256, 0, s>>>(n, nnz, rowptr, G.dinv_in, G.inv_in, G.hub_rows, hub_threshold, cnt);
+  rows_kernel<<<blocks_for(n, 256), 256, 0, s>>>(n, nnz, rowptr, G.dinv_in, G.inv_in, hubs, max_hubs(nnz),
+                                                  hub_threshold, cnt);
   GQ_TRY(launch_status());
   if (nnz > 0) {
     count_cols_kernel<<<blocks_for(nnz, 256), 256, 0, s>>>(nnz, n, col, counts, cnt);
     GQ_TRY(launch_status());
   }
   GQ_TRY(scan_exclusive(counts, G.tr_rowptr, n + 1, scan, s));
-  out_rows_kernel<<<blocks_for(n, 256), 256, 0, s>>>(n, G.tr_rowptr, G.dinv_out, G.tr_hub_rows, hub_threshold, cnt);
+  out_rows_kernel<<<blocks_for(n, 256), 256, 0, s>>>(n, G.tr_rowptr, G.dinv_out, tr_hubs, max_hubs(nnz),
+                                                      hub_threshold, cnt);
   GQ_TRY(launch_status());
 
   if (nnz > 0) {
@@ -386,8 +460,16 @@ extern "C" int gq_graph_prepare(int64_t n, int64_t nnz, const int32_t* rowptr, c
   GQ_TRY_CUDA(cudaMemcpyAsync(&h, cnt, sizeof(Counters), cudaMemcpyDeviceToHost, s));
   GQ_TRY_CUDA(cudaStreamSynchronize(s));
   if (h.err != 0) return GQ_ERR_BAD_GRAPH;
-  G.n_hub = h.n_hub;
-  G.tr_n_hub = h.tr_n_hub;
+  if (h.n_hub > max_hubs(nnz) || h.tr_n_hub > max_hubs(nnz)) return GQ_ERR_BAD_GRAPH;
+  std::vector<int32_t> hv((size_t)h.n_hub * 3), thv((size_t)h.tr_n_hub * 3), tasks, groups, tr_tasks, tr_groups;
+  if (h.n_hub > 0) GQ_TRY_CUDA(cudaMemcpyAsync(hv.data(), hubs, hv.size() * 4, cudaMemcpyDeviceToHost, s));
+  if (h.tr_n_hub > 0) GQ_TRY_CUDA(cudaMemcpyAsync(thv.data(), tr_hubs, thv.size() * 4, cudaMemcpyDeviceToHost, s));
+  GQ_TRY_CUDA(cudaStreamSynchronize(s));
+  GQ_TRY(build_sched(hv, split_edges, reinterpret_cast<int32_t*>(st + SL.tasks),
+                     reinterpret_cast<int32_t*>(st + SL.groups), &G.sched, tasks, groups, s));
+  GQ_TRY(build_sched(thv, split_edges, reinterpret_cast<int32_t*>(st + SL.tr_tasks),
+                     reinterpret_cast<int32_t*>(st + SL.tr_groups), &G.tr_sched, tr_tasks, tr_groups, s));
+  GQ_TRY_CUDA(cudaStreamSynchronize(s));  // host task vectors must outlive the copies
   G.max_deg = h.max_deg;
   G.tr_max_deg = h.tr_max_deg;
   *g = G;

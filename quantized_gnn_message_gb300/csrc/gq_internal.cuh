@@ -13,10 +13,13 @@ int quantize_pack(const float* X, int64_t n, int d, int64_t ldx, const uint8_t* 
                   uint8_t* packed, cudaStream_t s);
 
 // Aggregation; Yb != nullptr writes the output in bf16 (leading dim ldy).
+size_t spmm_workspace(const gq_graph* g, int transpose, int d);
 int dequant_spmm(const gq_graph* g, int transpose, int coef, const float* X, int64_t ldx, const uint8_t* packed,
-                 const uint8_t* mask, int d, int bits, float* Y, int64_t ldy, cudaStream_t s, void* Yb);
+                 const uint8_t* mask, int d, int bits, float* Y, int64_t ldy, void* ws, size_t ws_bytes,
+                 cudaStream_t s, void* Yb);
 int edge_spmm(const gq_graph* g, int transpose, const float* alpha, int heads, const float* X, int64_t ldx,
-              const uint8_t* packed, const uint8_t* mask, int d, int bits, float* Y, int64_t ldy, cudaStream_t s);
+              const uint8_t* packed, const uint8_t* mask, int d, int bits, float* Y, int64_t ldy, void* ws,
+              size_t ws_bytes, cudaStream_t s);
 
 int row_gemm(const void* A, int64_t M, int K, int64_t lda, const void* B, int N, int64_t ldb, int act, float* C,
              int64_t ldc, const float* a_src, const float* a_dst, float* S, float* D, int heads, int* err,
@@ -41,7 +44,7 @@ struct Carve {
     used = off + bytes;
     return (base == nullptr || used > cap) ? nullptr : base + off;
   }
-  bool ok() const { return used <= cap; }
+  bool ok() const { return base != nullptr && used <= cap; }
 };
 
 inline int64_t round8(int64_t x) { return (x + 7) / 8 * 8; }

@@ -16,9 +16,12 @@
 //     Edge metadata (column id, coefficient, mask bit) is loaded 32 edges at
 //     a time, one per lane, and broadcast with shuffles; U edges per group
 //     are gathered before any is consumed, to keep loads in flight.
-//   - a hub row (degree > hub_threshold) is one whole block's job: its 8
-//     warps interleave 32-edge batches and their partial rows are summed in
-//     shared memory in warp order.
+//   - a heavy row is one or more thread-block tasks (the graph's static
+//     schedule, heaviest first, so they start before the light rows): the 8
+//     warps of a block interleave 32-edge batches and their partial rows are
+//     summed in shared memory in warp order.  A row cut into several tasks
+//     writes one partial row per task to the workspace; the last task to
+//     finish (arrival ticket) adds them in task order.
 // Every sum runs in a fixed order, so results are identical run to run.
 #include <cuda_bf16.h>
 
@@ -46,9 +49,12 @@ struct SpmmParams {
   int64_t ldy;
   int64_t n_rows;
   int d;
-  const int32_t* hub_rows;
-  int64_t n_hub;
+  const int32_t* tasks;     // heavy-row schedule (see gq_sched)
+  const int32_t* groups;
+  int64_t n_tasks;
   int hub_threshold;
+  float* partial;           // [slot][d] partial rows of split heavy rows
+  int* tickets;             // [group] arrivals, zero at launch
 };
 
 namespace {
@@ -225,10 +231,12 @@ __global__ void __launch_bounds__(kSpmmThreads) spmm_kernel(const SpmmParams p) 
   const int gl = lane % G;
   const int nchunks = (p.d + 7) >> 3;
 
-  if ((int64_t)blockIdx.x < p.n_hub) {
-    const int64_t r = p.hub_rows[blockIdx.x];
+  if ((int64_t)blockIdx.x < p.n_tasks) {
+    __shared__ int last;
+    const int4 task = __ldg(reinterpret_cast<const int4*>(p.tasks) + blockIdx.x);
+    const int64_t r = task.x;
     float acc[CPL][8] = {};
-    accumulate_row<BITS, G, CPL, EW>(p, p.rowptr[r], p.rowptr[r + 1], w, kSpmmWarps, acc);
+    accumulate_row<BITS, G, CPL, EW>(p, task.y, task.z, w, kSpmmWarps, acc);
     group_reduce<G, CPL>(acc);
     if (lane < G) {
 #pragma unroll
@@ -242,10 +250,36 @@ __global__ void __launch_bounds__(kSpmmThreads) spmm_kernel(const SpmmParams p) 
     }
     __syncthreads();
     const float s = p.rowscale ? p.rowscale[r] : 1.0f;
+    if (task.w < 0) {  // the whole row in this task
+      for (int j = threadIdx.x; j < p.d; j += blockDim.x) {
+        float t = 0.0f;
+#pragma unroll
+        for (int ww = 0; ww < kSpmmWarps; ++ww) t += part[ww * p.d + j];
+        if (p.Yb != nullptr)
+          p.Yb[r * p.ldy + j] = __float2bfloat16_rn(t * s);
+        else
+          p.Y[r * p.ldy + j] = t * s;
+      }
+      return;
+    }
+    const int4 grp = __ldg(reinterpret_cast<const int4*>(p.groups) + task.w);
+    float* mine = p.partial + (int64_t)(grp.w + ((int)blockIdx.x - grp.y)) * p.d;
     for (int j = threadIdx.x; j < p.d; j += blockDim.x) {
       float t = 0.0f;
 #pragma unroll
       for (int ww = 0; ww < kSpmmWarps; ++ww) t += part[ww * p.d + j];
+      mine[j] = t;
+    }
+    __threadfence();
+    __syncthreads();
+    if (threadIdx.x == 0) last = (atomicAdd(&p.tickets[task.w], 1) == grp.z - 1);
+    __syncthreads();
+    if (!last) return;
+    __threadfence();
+    const float* base = p.partial + (int64_t)grp.w * p.d;
+    for (int j = threadIdx.x; j < p.d; j += blockDim.x) {
+      float t = 0.0f;
+      for (int k = 0; k < grp.z; ++k) t += __ldcg(base + (int64_t)k * p.d + j);
       if (p.Yb != nullptr)
         p.Yb[r * p.ldy + j] = __float2bfloat16_rn(t * s);
       else
@@ -254,11 +288,11 @@ __global__ void __launch_bounds__(kSpmmThreads) spmm_kernel(const SpmmParams p) 
     return;
   }
 
-  const int64_t gw = ((int64_t)blockIdx.x - p.n_hub) * kSpmmWarps + w;
-  const int64_t nw = ((int64_t)gridDim.x - p.n_hub) * kSpmmWarps;
+  const int64_t gw = ((int64_t)blockIdx.x - p.n_tasks) * kSpmmWarps + w;
+  const int64_t nw = ((int64_t)gridDim.x - p.n_tasks) * kSpmmWarps;
   for (int64_t r = gw; r < p.n_rows; r += nw) {
     const int64_t a = p.rowptr[r], b = p.rowptr[r + 1];
-    if (b - a > p.hub_threshold) continue;  // a block handles it
+    if (b - a > p.hub_threshold) continue;  // a block task handles it
     float acc[CPL][8] = {};
     accumulate_row<BITS, G, CPL, EW>(p, a, b, 0, 1, acc);
     group_reduce<G, CPL>(acc);
@@ -280,7 +314,7 @@ int launch_cfg(const SpmmParams& p, cudaStream_t s) {
   int64_t grid = (int64_t)sm_count() * 8;
   if (grid > rows_blocks) grid = rows_blocks;
   if (grid < 1) grid = 1;
-  grid += p.n_hub;
+  grid += p.n_tasks;
   if (grid > 0x7fffffff) return GQ_ERR_UNSUPPORTED;
   spmm_kernel<BITS, G, CPL, EW><<<(unsigned)grid, kSpmmThreads, smem, s>>>(p);
   return launch_status();
@@ -309,8 +343,14 @@ int launch_any(const SpmmParams& p, int bits, cudaStream_t s) {
 }  // namespace
 
 // Common argument checks and message-source setup.
+size_t ws_bytes_for(const gq_sched& sc, int d) {
+  if (sc.n_groups == 0) return 0;
+  return ((size_t)sc.n_slots * d * sizeof(float) + 255) / 256 * 256 + (size_t)sc.n_groups * sizeof(int) + 256;
+}
+
 int spmm_setup(const gq_graph* g, int transpose, const float* X, int64_t ldx, const uint8_t* packed,
-               const uint8_t* mask, int d, int bits, float* Y, int64_t ldy, SpmmParams& p, void* Yb = nullptr) {
+               const uint8_t* mask, int d, int bits, float* Y, int64_t ldy, void* ws, size_t ws_bytes,
+               cudaStream_t s, SpmmParams& p, void* Yb = nullptr) {
   if (g == nullptr || (Y == nullptr && Yb == nullptr) || d < 1 || ldy < d) return GQ_ERR_INVALID_ARG;
   if (!(bits == 32 || valid_bits(bits))) return GQ_ERR_INVALID_ARG;
   if (d > 1024) return GQ_ERR_UNSUPPORTED;
@@ -327,9 +367,17 @@ int spmm_setup(const gq_graph* g, int transpose, const float* X, int64_t ldx, co
   p = SpmmParams{};
   p.rowptr = transpose ? g->tr_rowptr : g->rowptr;
   p.col = transpose ? g->tr_col : g->col;
-  p.hub_rows = transpose ? g->tr_hub_rows : g->hub_rows;
-  p.n_hub = transpose ? g->tr_n_hub : g->n_hub;
+  const gq_sched& sc = transpose ? g->tr_sched : g->sched;
+  p.tasks = sc.tasks;
+  p.groups = sc.groups;
+  p.n_tasks = sc.n_tasks;
   p.hub_threshold = g->hub_threshold;
+  if (sc.n_groups > 0) {
+    if (ws == nullptr || ws_bytes < ws_bytes_for(sc, d) || !aligned(ws, 256)) return GQ_ERR_WORKSPACE;
+    p.partial = static_cast<float*>(ws);
+    p.tickets = reinterpret_cast<int*>(static_cast<char*>(ws) + ((size_t)sc.n_slots * d * sizeof(float) + 255) / 256 * 256);
+    GQ_TRY_CUDA(cudaMemsetAsync(p.tickets, 0, (size_t)sc.n_groups * sizeof(int), s));
+  }
   p.n_rows = g->n;
   p.X = X;
   p.ldx = ldx;
@@ -344,10 +392,16 @@ int spmm_setup(const gq_graph* g, int transpose, const float* X, int64_t ldx, co
   return GQ_OK;
 }
 
+size_t spmm_workspace(const gq_graph* g, int transpose, int d) {
+  if (g == nullptr || d < 1) return 0;
+  return ws_bytes_for(transpose ? g->tr_sched : g->sched, d);
+}
+
 int dequant_spmm(const gq_graph* g, int transpose, int coef, const float* X, int64_t ldx, const uint8_t* packed,
-                 const uint8_t* mask, int d, int bits, float* Y, int64_t ldy, cudaStream_t s, void* Yb) {
+                 const uint8_t* mask, int d, int bits, float* Y, int64_t ldy, void* ws, size_t ws_bytes,
+                 cudaStream_t s, void* Yb) {
   SpmmParams p;
-  GQ_TRY(spmm_setup(g, transpose, X, ldx, packed, mask, d, bits, Y, ldy, p, Yb));
+  GQ_TRY(spmm_setup(g, transpose, X, ldx, packed, mask, d, bits, Y, ldy, ws, ws_bytes, s, p, Yb));
   if (coef == GQ_COEF_GCN) {
     // a_{u,v} = dinv_out[u] * dinv_in[v]
     p.colscale = transpose ? g->dinv_in : g->dinv_out;
@@ -359,14 +413,14 @@ int dequant_spmm(const gq_graph* g, int transpose, int coef, const float* X, int
   } else if (coef != GQ_COEF_ONE) {
     return GQ_ERR_INVALID_ARG;
   }
-  if (g->n == 0) return GQ_OK;
   return launch_any<false>(p, bits, s);
 }
 
 int edge_spmm(const gq_graph* g, int transpose, const float* alpha, int heads, const float* X, int64_t ldx,
-              const uint8_t* packed, const uint8_t* mask, int d, int bits, float* Y, int64_t ldy, cudaStream_t s) {
+              const uint8_t* packed, const uint8_t* mask, int d, int bits, float* Y, int64_t ldy, void* ws,
+              size_t ws_bytes, cudaStream_t s) {
   SpmmParams p;
-  GQ_TRY(spmm_setup(g, transpose, X, ldx, packed, mask, d, bits, Y, ldy, p));
+  GQ_TRY(spmm_setup(g, transpose, X, ldx, packed, mask, d, bits, Y, ldy, ws, ws_bytes, s, p));
   if (alpha == nullptr || heads < 1 || d % heads != 0) return GQ_ERR_INVALID_ARG;
   const int F = d / heads;
   int fshift = 0;
@@ -376,20 +430,25 @@ int edge_spmm(const gq_graph* g, int transpose, const float* alpha, int heads, c
   p.heads = heads;
   p.fshift = fshift;
   p.eperm = transpose ? g->tr_perm : nullptr;
-  if (g->n == 0) return GQ_OK;
   return launch_any<true>(p, bits, s);
 }
 
 }  // namespace gq
 
+extern "C" size_t gq_spmm_workspace_bytes(const gq_graph* g, int transpose, int d) {
+  return gq::spmm_workspace(g, transpose, d);
+}
+
 extern "C" int gq_dequant_spmm(const gq_graph* g, int transpose, int coef, const float* X, int64_t ldx,
                                const uint8_t* packed, const uint8_t* mask, int d, int bits, float* Y, int64_t ldy,
-                               gq_stream stream) {
-  return gq::dequant_spmm(g, transpose, coef, X, ldx, packed, mask, d, bits, Y, ldy, (cudaStream_t)stream, nullptr);
+                               void* ws, size_t ws_bytes, gq_stream stream) {
+  return gq::dequant_spmm(g, transpose, coef, X, ldx, packed, mask, d, bits, Y, ldy, ws, ws_bytes,
+                          (cudaStream_t)stream, nullptr);
 }
 
 extern "C" int gq_edge_spmm(const gq_graph* g, int transpose, const float* alpha, int heads, const float* X,
                             int64_t ldx, const uint8_t* packed, const uint8_t* mask, int d, int bits, float* Y,
-                            int64_t ldy, gq_stream stream) {
-  return gq::edge_spmm(g, transpose, alpha, heads, X, ldx, packed, mask, d, bits, Y, ldy, (cudaStream_t)stream);
+                            int64_t ldy, void* ws, size_t ws_bytes, gq_stream stream) {
+  return gq::edge_spmm(g, transpose, alpha, heads, X, ldx, packed, mask, d, bits, Y, ldy, ws, ws_bytes,
+                       (cudaStream_t)stream);
 }

@@ -1,0 +1,78 @@
+"""A stack of GCN / GraphSAGE-mean layers over one prepared graph.
+
+Owns the per-layer device buffers (saved activations, gradients, one
+shared workspace) and runs forward / backward through the C ABI layer
+calls; no arithmetic happens here.  Layer l uses ReLU except the last
+(AdaQP Sec. 2.1 layer form with sigma = ReLU on hidden layers).
+"""
+from __future__ import annotations
+
+import torch
+
+from . import (ACT_NONE, ACT_RELU, COEF_GCN, Graph, Workspace, gcn_layer_bwd, gcn_layer_fwd, lib)
+
+# stages traced per call (see gq_gcn_layer_fwd / gq_gcn_layer_bwd)
+FWD_STAGES = ("quantize", "aggregate", "update_gemm")
+BWD_STAGES = ("dz", "dw_gemm", "da_gemm", "quantize_bwd", "aggregate_t")
+
+
+def launches_fwd(bits: int) -> int:
+    """Kernels one gq_gcn_layer_fwd call launches: [quantize] + aggregate
+    + W transpose + GEMM."""
+    return (1 if bits < 32 else 0) + 3
+
+
+def launches_bwd(bits: int, need_dinput: bool) -> int:
+    """dZ + weight GEMM + split reduction [+ W convert + dA GEMM +
+    [quantize] + transposed aggregate]."""
+    n = 3
+    if need_dinput:
+        n += 3 + (1 if bits < 32 else 0)
+    return n
+
+
+class GCNStack:
+    def __init__(self, g: Graph, widths, mask: torch.Tensor | None, coef: int = COEF_GCN,
+                 device="cuda"):
+        self.g = g
+        self.widths = tuple(widths)
+        self.L = len(widths) - 1
+        self.mask = mask
+        self.coef = coef
+        n = g.n
+        self.ws = Workspace(device)
+        r8 = lambda x: (x + 7) // 8 * 8
+        self.A = [torch.empty(n, r8(widths[l]), dtype=torch.bfloat16, device=device) for l in range(self.L)]
+        self.H = [torch.empty(n, widths[l + 1], dtype=torch.float32, device=device) for l in range(self.L)]
+        self.dH = [torch.empty(n, widths[l], dtype=torch.float32, device=device) for l in range(self.L)]
+        self.dW = [torch.empty(widths[l], widths[l + 1], dtype=torch.float32, device=device) for l in range(self.L)]
+        self.err = torch.zeros(1, dtype=torch.int32, device=device)
+        L = lib()
+        self.ws.get(max(int(L.gq_gcn_layer_workspace_bytes(g.ref, widths[l], widths[l + 1], 2))
+                        for l in range(self.L)))
+
+    def act(self, l: int) -> int:
+        return ACT_RELU if l < self.L - 1 else ACT_NONE
+
+    def forward(self, X: torch.Tensor, Ws, bits: int, seeds, events=None):
+        h = X
+        for l in range(self.L):
+            ev = None if events is None else events[l]
+            gcn_layer_fwd(self.g, h, Ws[l], self.mask, bits, seeds[l], self.act(l), coef=self.coef, ws=self.ws,
+                          A_save=self.A[l], H_out=self.H[l], dev_err=self.err, events=ev)
+            h = self.H[l]
+        return h
+
+    def backward(self, dY: torch.Tensor, Ws, bits: int, seeds, need_input_grad: bool = False, events=None):
+        g = dY
+        for l in reversed(range(self.L)):
+            need = need_input_grad or l > 0
+            ev = None if events is None else events[l]
+            gcn_layer_bwd(self.g, g, self.A[l], self.H[l], Ws[l], self.mask, bits, seeds[l], self.act(l), need,
+                          coef=self.coef, ws=self.ws, dW=self.dW[l], dH_in=self.dH[l] if need else None,
+                          dev_err=self.err, events=ev)
+            g = self.dH[l]
+        return self.dW
+
+    def launches(self, bits: int, need_input_grad: bool = False) -> int:
+        return sum(launches_fwd(bits) + launches_bwd(bits, need_input_grad or l > 0) for l in range(self.L))

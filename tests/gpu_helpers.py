@@ -34,8 +34,7 @@ def rmat_small(scale=12, n=3000, deg=12, seed=1):
     return synth.rmat_graph(scale=scale, n=n, n_draws=n * deg, seed=seed)
 
 
-def hub_graph(n=700, seed=3):
-    """A graph with a few very high in- and out-degree nodes plus a ragged
-    tail (some rows with only the self-loop)."""
-    g = synth.rmat_graph(scale=10, n=n, n_draws=n * 30, a=0.7, b=0.12, c=0.12, seed=seed)
-    return g
+def hub_graph(n=3000, seed=3):
+    """A graph with a dozen rows (in and out) above 256 edges, a heavier
+    head up to ~650 edges, and a ragged tail of rows with few edges."""
+    return synth.rmat_graph(scale=12, n=n, n_draws=n * 30, a=0.75, b=0.1, c=0.1, seed=seed)

@@ -40,6 +40,12 @@ def test_library_exports_every_declared_symbol(q):
     assert not missing, missing
 
 
+def test_graph_struct_mirror(q):
+    import ctypes as C
+    assert q.lib().gq_graph_struct_bytes() == C.sizeof(q.Graph_t)
+    assert C.sizeof(q.Sched_t) == 40
+
+
 def test_packed_sizes_match_layout(q, orc):
     for d in (1, 2, 7, 8, 31, 32, 47, 64, 100, 128, 255, 256, 1000):
         for b in (2, 4, 8):
@@ -59,6 +65,6 @@ def test_argument_checks_without_launch(q):
     assert L.gq_quantize_pack(fake, 10, 16, 8, None, 8, 0, fake, None) == 1          # ldx < d
     assert L.gq_quantize_pack(fake, 10, 16, 16, None, 8, 0, ctypes.c_void_p(0x1008), None) == 1  # misaligned
     assert L.gq_quantize_pack(fake, 0, 16, 16, None, 8, 0, fake, None) == 0            # empty: no-op
-    assert L.gq_graph_prepare(0, 0, fake, fake, 0, fake, 0, fake, 0, None, None) == 1
+    assert L.gq_graph_prepare(0, 0, fake, fake, 0, 0, fake, 0, fake, 0, None, None) == 1
     assert L.gq_status_string(3) == b"graph fails CSR validation"
-    assert L.gq_dequant_spmm(None, 0, 0, None, 0, None, None, 16, 8, None, 16, None) == 1
+    assert L.gq_dequant_spmm(None, 0, 0, None, 0, None, None, 16, 8, None, 16, None, 0, None) == 1

@@ -15,9 +15,9 @@ from gpu_helpers import gq, close, rmat_small, hub_graph
 pytestmark = pytest.mark.gpu
 
 
-def _case(orc, g, d_in, d_out, bits, act, coef, mask_frac=0.3, seed=0, hub_threshold=0):
+def _case(orc, g, d_in, d_out, bits, act, coef, mask_frac=0.3, seed=0, hub_threshold=0, split_edges=0):
     q = gq()
-    G = q.graph_prepare(g.rowptr.cuda(), g.col.cuda(), hub_threshold)
+    G = q.graph_prepare(g.rowptr.cuda(), g.col.cuda(), hub_threshold, split_edges)
     rp, co = g.rowptr.numpy(), g.col.numpy()
     H = synth.normal_matrix(g.n, d_in, seed=seed + 1)
     W = synth.glorot(d_in, d_out, seed=seed + 2)
@@ -75,6 +75,7 @@ def test_gcn_layer_coefficients(orc, coef):
 
 def test_gcn_layer_hubs(orc):
     _case(orc, hub_graph(), 128, 128, 2, 1, coef=0, mask_frac=0.5, hub_threshold=40)
+    _case(orc, hub_graph(), 128, 128, 2, 1, coef=0, mask_frac=0.5, hub_threshold=32, split_edges=256)
 
 
 def test_gcn_layer_all_central_and_all_marginal(orc):

@@ -10,10 +10,37 @@ from gpu_helpers import gq, rmat_small, hub_graph
 pytestmark = pytest.mark.gpu
 
 
-def _check(orc, g, hub_threshold=0):
+def _check_sched(tasks, groups, ptr, thr, split):
+    """Tasks cover exactly the edges of the rows heavier than thr, in pieces
+    of at most `split` edges, heaviest rows first; split rows form groups."""
+    deg = np.diff(ptr)
+    heavy = np.nonzero(deg > thr)[0]
+    cover = {}
+    for t, (r, b, e, grp) in enumerate(tasks):
+        assert deg[r] > thr and ptr[r] <= b < e <= ptr[r + 1] and e - b <= split
+        cover.setdefault(r, []).append((b, e, grp, t))
+    assert sorted(cover) == sorted(heavy.tolist())
+    for r, pieces in cover.items():
+        pieces.sort()
+        assert pieces[0][0] == ptr[r] and pieces[-1][1] == ptr[r + 1]
+        assert all(pieces[i][1] == pieces[i + 1][0] for i in range(len(pieces) - 1))
+        if len(pieces) == 1:
+            assert pieces[0][2] == -1
+        else:
+            gi = pieces[0][2]
+            assert all(p[2] == gi for p in pieces)
+            gr, first, cnt, _ = groups[gi]
+            assert gr == r and cnt == len(pieces) and [p[3] for p in pieces] == list(range(first, first + cnt))
+    first_task_deg = [deg[cover_r] for cover_r in [t[0] for t in tasks]]
+    assert all(first_task_deg[i] >= first_task_deg[i + 1] for i in range(len(first_task_deg) - 1))
+    slots = [gr[3] for gr in groups]
+    assert slots == list(np.cumsum([0] + [gr[2] for gr in groups])[:-1])
+
+
+def _check(orc, g, hub_threshold=0, split_edges=0):
     q = gq()
     rp, co = g.rowptr.cuda(), g.col.cuda()
-    G = q.graph_prepare(rp, co, hub_threshold)
+    G = q.graph_prepare(rp, co, hub_threshold, split_edges)
     rowptr, col = g.rowptr.numpy(), g.col.numpy()
     n, nnz = g.n, g.nnz
     di, do, ii = orc.degree_norms(rowptr, col)
@@ -27,9 +54,10 @@ def _check(orc, g, hub_threshold=0):
     np.testing.assert_array_equal(G.tr_rowptr.cpu().numpy(), np.concatenate([[0], np.cumsum(cnt)]))
     np.testing.assert_array_equal(G.tr_perm.cpu().numpy(), perm)
     np.testing.assert_array_equal(G.tr_col.cpu().numpy(), dst[perm])
-    thr = G.c.hub_threshold
-    assert G.n_hub == int((np.diff(rowptr) > thr).sum())
-    assert G.tr_n_hub == int((cnt > thr).sum())
+    thr, split = G.c.hub_threshold, G.c.split_edges
+    for tr, ptr in ((False, rowptr), (True, np.concatenate([[0], np.cumsum(cnt)]))):
+        tasks, groups = (x.cpu().numpy() for x in G.sched_arrays(tr))
+        _check_sched(tasks, groups, ptr, thr, split)
     assert G.c.max_deg == np.diff(rowptr).max() and G.c.tr_max_deg == cnt.max()
     return G
 
@@ -40,7 +68,18 @@ def test_prepare_uniform(orc):
 
 def test_prepare_rmat_hubs(orc):
     G = _check(orc, hub_graph(), hub_threshold=64)
-    assert G.n_hub > 0 and G.tr_n_hub > 0
+    assert G.n_tasks > 0 and G.tr_n_tasks > 0
+    G = _check(orc, hub_graph(), hub_threshold=32, split_edges=256)
+    assert G.c.sched.n_groups > 0 and G.c.tr_sched.n_groups > 0
+
+
+def test_prepare_rejects_bad_schedule_args():
+    q = gq()
+    g = synth.uniform_graph(64, 256, seed=1)
+    with pytest.raises(q.GQError, match="invalid"):
+        q.graph_prepare(g.rowptr.cuda(), g.col.cuda(), 16, 0)
+    with pytest.raises(q.GQError, match="invalid"):
+        q.graph_prepare(g.rowptr.cuda(), g.col.cuda(), 64, 100)
 
 
 def test_prepare_rmat_medium(orc):

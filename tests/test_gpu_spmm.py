@@ -14,9 +14,9 @@ from gpu_helpers import gq, close, rmat_small, hub_graph
 pytestmark = pytest.mark.gpu
 
 
-def _spmm_case(orc, g, d, bits, coef, transpose, mask_frac, hub_threshold=0, seed=0):
+def _spmm_case(orc, g, d, bits, coef, transpose, mask_frac, hub_threshold=0, seed=0, split_edges=0):
     q = gq()
-    G = q.graph_prepare(g.rowptr.cuda(), g.col.cuda(), hub_threshold)
+    G = q.graph_prepare(g.rowptr.cuda(), g.col.cuda(), hub_threshold, split_edges)
     X = synth.normal_matrix(g.n, d, seed=seed + d).numpy()
     mask = None if mask_frac is None else synth.bernoulli_mask(g.n, mask_frac, seed=seed + 1).numpy()
     Xd = torch.from_numpy(X).cuda()
@@ -49,9 +49,13 @@ def test_spmm_widths(orc, d, bits):
 @pytest.mark.parametrize("transpose", [False, True])
 @pytest.mark.parametrize("bits", [4, 32])
 @pytest.mark.parametrize("d", [32, 256, 512])
-def test_spmm_hub_block_path(orc, transpose, bits, d):
-    G = _spmm_case(orc, hub_graph(), d, bits, 0, transpose, 0.4, hub_threshold=48)
-    assert (G.tr_n_hub if transpose else G.n_hub) > 0
+@pytest.mark.parametrize("split", [0, 256])
+def test_spmm_heavy_rows(orc, transpose, bits, d, split):
+    G = _spmm_case(orc, hub_graph(), d, bits, 0, transpose, 0.4, hub_threshold=48, split_edges=split)
+    sc = G.c.tr_sched if transpose else G.c.sched
+    assert sc.n_tasks > 0
+    if split:
+        assert sc.n_groups > 0
 
 
 @pytest.mark.parametrize("bits", [2, 8])
@@ -71,7 +75,7 @@ def test_spmm_all_marginal_no_X(orc, bits):
 def test_spmm_deterministic(orc):
     q = gq()
     g = hub_graph()
-    G = q.graph_prepare(g.rowptr.cuda(), g.col.cuda(), 32)
+    G = q.graph_prepare(g.rowptr.cuda(), g.col.cuda(), 32, 256)
     X = synth.normal_matrix(g.n, 128, seed=1, device="cuda")
     pk = q.quantize_pack(X, None, 4, 1)
     a = q.dequant_spmm(G, X, pk, None, 128, 4)
@@ -86,7 +90,7 @@ def test_edge_spmm(orc, transpose, bits):
     g = hub_graph()
     heads, F = 4, 16
     d = heads * F
-    G = q.graph_prepare(g.rowptr.cuda(), g.col.cuda(), 40)
+    G = q.graph_prepare(g.rowptr.cuda(), g.col.cuda(), 40, 256)
     alpha = np.random.default_rng(2).random((g.nnz, heads)).astype(np.float32)
     X = synth.normal_matrix(g.n, d, seed=2).numpy()
     mask = synth.bernoulli_mask(g.n, 0.5, seed=3).numpy()
