@@ -64,7 +64,9 @@ typedef enum {
   GQ_ERR_BAD_GRAPH = 3,    /* CSR fails validation in gq_graph_prepare     */
   GQ_ERR_CUDA = 4,         /* a CUDA runtime call or launch failed         */
   GQ_ERR_TIMEOUT = 5,      /* a bounded device-side wait gave up           */
-  GQ_ERR_WORKSPACE = 6     /* workspace or storage buffer too small        */
+  GQ_ERR_WORKSPACE = 6,    /* workspace or storage buffer too small        */
+  GQ_ERR_SCRATCH_LIMIT = 7 /* request exceeds the fixed scratch of
+                              gq_dequant_spmm_noalloc                      */
 } gq_status;
 
 /* Aggregation coefficient a_{u,v} of an edge u -> v. */
@@ -314,6 +316,28 @@ GQ_API int gq_gcn_layer_bwd(const gq_graph* g, int coef, const float* dH_out, in
                      int act, int need_dinput, float* dW, float* dH_in, int64_t ldi, float* dA_save,
                      void* ws, size_t ws_bytes, int* dev_err, void* const* stage_events,
                      gq_stream stream);
+
+/* ------------------------------------------------------------------------
+ * gq_dequant_spmm_noalloc -- no counterpart on the pages: a convenience of
+ * this library.  Same arguments and result as gq_dequant_spmm, minus the
+ * workspace, for callers that may not allocate device memory where they
+ * aggregate (a memory-pool hook, a plug-in that is only lent its input and
+ * output buffers, a path that must not block on or fail in an allocator).
+ * Its scratch is one fixed array of gq_noalloc_scratch_bytes() bytes (8 MiB)
+ * compiled into the library, held on every GPU that loads the library until
+ * the process exits.  The call allocates nothing.
+ *   - The first call on a device looks up the array's address with that
+ *     device current; make it before any stream capture.
+ *   - All calls on a device share the array and find the previous call's
+ *     contents in it; each call clears what must start at zero.  Calls that
+ *     overlap on the GPU race on the array.
+ *   - A graph and width whose scratch need (gq_spmm_workspace_bytes)
+ *     exceeds the array return GQ_ERR_SCRATCH_LIMIT; nothing is launched.
+ * ---------------------------------------------------------------------- */
+GQ_API size_t gq_noalloc_scratch_bytes(void);
+GQ_API int gq_dequant_spmm_noalloc(const gq_graph* g, int transpose, int coef, const float* X,
+                                   int64_t ldx, const uint8_t* packed, const uint8_t* mask, int d,
+                                   int bits, float* Y, int64_t ldy, gq_stream stream);
 
 #ifdef __cplusplus
 }

@@ -79,6 +79,7 @@ def _SIGNATURES(P, I64, I, U64, F, S):
         ("gq_status_string", [I], ctypes.c_char_p),
         ("gq_version", [], I),
         ("gq_graph_struct_bytes", [], S),
+        ("gq_noalloc_scratch_bytes", [], S),
         ("gq_packed_pitch", [I, I], I64),
         ("gq_packed_header_offset", [I, I], I64),
         ("gq_quantize_pack", [P, I64, I, I64, P, I, U64, P, P], I),

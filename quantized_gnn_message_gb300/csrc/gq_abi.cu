@@ -10,6 +10,7 @@ extern "C" const char* gq_status_string(int status) {
     case GQ_ERR_CUDA: return "CUDA runtime error";
     case GQ_ERR_TIMEOUT: return "device-side wait timed out";
     case GQ_ERR_WORKSPACE: return "workspace or storage too small";
+    case GQ_ERR_SCRATCH_LIMIT: return "request exceeds the fixed scratch of the no-allocation entry point";
     default: return "unknown status";
   }
 }
