@@ -318,6 +318,60 @@ GQ_API int gq_gcn_layer_bwd(const gq_graph* g, int coef, const float* dH_out, in
                      gq_stream stream);
 
 /* ------------------------------------------------------------------------
+ * gq_sddmm_edge_softmax -- Tango Sec. 2.1, Fig. 1a steps 3-4, per
+ * destination v and head k (heads contiguous, S and D n x heads fp32):
+ *   E_pre[e,k] = S[u,k] + D[v,k]                  (SDDMM add, e = u -> v)
+ *   E[e,k]     = E_pre if E_pre > 0, else slope * E_pre      (LeakyReLU)
+ *   alpha[e,k] = exp(E[e,k]) / sum_{e' in in(v)} exp(E[e',k])
+ * computed with the per-(v,k) maximum subtracted (same value), in fp32
+ * (Tango Sec. 3.2 keeps the layer before softmax in full precision).
+ * alpha and E_pre (nullable) are E x heads, indexed by CSR edge id.
+ * heads in {1, 2, 4, 8}; S, D, alpha 16-byte aligned.  Workspace:
+ * gq_edge_softmax_workspace_bytes (split heavy rows only; may be 0).
+ * ---------------------------------------------------------------------- */
+GQ_API size_t gq_edge_softmax_workspace_bytes(const gq_graph* g, int heads);
+GQ_API int gq_sddmm_edge_softmax(const gq_graph* g, const float* S, const float* D, int heads, float slope,
+                          float* E_pre, float* alpha, void* ws, size_t ws_bytes, gq_stream stream);
+
+/* ------------------------------------------------------------------------
+ * GAT layer (Tango Sec. 2.1, Fig. 1a / 1b), F = f features per head,
+ * d = heads * f, W is d_in x d fp32, a_src / a_dst are heads x f fp32.
+ *
+ * gq_gat_layer_fwd:
+ *   H'    = H W          (tcgen05 bf16 GEMM)                 -> Hp_save n x d
+ *   S, D  = H' a_src, H' a_dst per head (GEMM epilogue)      -> n x heads
+ *   [bits < 32: the H' rows of marginal nodes are quantized  -> packed_save]
+ *   alpha = edge softmax of LeakyReLU(S[u] + D[v])           -> E x heads
+ *   out   = sum_{u->v} alpha[e,k] m_u[kF+f]                  -> n x d
+ *   packed_save (n x gq_packed_pitch(d, bits), nullable) keeps the
+ *   forward's quantized messages for the backward pass (required there
+ *   when bits < 32).
+ * gq_gat_layer_bwd (the quantizer is the identity in backward):
+ *   dalpha = SDDMM dot of dOut[v] with the forward messages m_u;
+ *   dE_pre = alpha (dalpha - P) LeakyReLU'; dD = in-edge sums, dS =
+ *   out-edge sums; dM = transposed multi-head SpMM of dOut (rows of
+ *   marginal nodes quantized when bits < 32, seed);
+ *   dH' = dM + dS a_src + dD a_dst; da_src = sum_u dS[u] H'[u],
+ *   da_dst likewise; dW = H^T dH'; dH = dH' W^T.
+ *   dEpre_save (E x heads) and dHp_save (n x d fp32) are optional copies.
+ * Limits: heads in {1,2,4,8}, f a power of two >= 16, d_in, d <= 256.
+ * Workspace: gq_gat_layer_workspace_bytes(g, d_in, heads, f, bits).
+ * ---------------------------------------------------------------------- */
+GQ_API size_t gq_gat_layer_workspace_bytes(const gq_graph* g, int d_in, int heads, int f, int bits);
+GQ_API int gq_gat_layer_fwd(const gq_graph* g, const float* H, int64_t ldh, int d_in, const float* W,
+                     const float* a_src, const float* a_dst, int heads, int f, float slope,
+                     const uint8_t* mask, int bits, uint64_t seed, float* Hp_save, float* S_save,
+                     float* D_save, float* alpha_save, uint8_t* packed_save, float* out, void* ws,
+                     size_t ws_bytes, int* dev_err, gq_stream stream);
+GQ_API int gq_gat_layer_bwd(const gq_graph* g, const float* dOut, const float* H, int64_t ldh,
+                     const float* Hp_save, const float* S_save, const float* D_save,
+                     const float* alpha_save, const uint8_t* packed_save, const float* W,
+                     const float* a_src, const float* a_dst, int d_in, int heads, int f, float slope,
+                     const uint8_t* mask, int bits, uint64_t seed, float* dW, float* da_src,
+                     float* da_dst, float* dH, float* dEpre_save, float* dHp_save, void* ws,
+                     size_t ws_bytes, int* dev_err, gq_stream stream);
+
+/* ------------------------------------------------------------------------
  * gq_dequant_spmm_noalloc -- no counterpart on the pages: a convenience of
  * this library.  Same arguments and result as gq_dequant_spmm, minus the
  * workspace, for callers that may not allocate device memory where they

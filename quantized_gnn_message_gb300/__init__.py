@@ -95,6 +95,12 @@ def _SIGNATURES(P, I64, I, U64, F, S):
         ("gq_gemm_bf16_tn", [P, I64, I, I64, P, I, I64, P, I64, I, P, S, P, P], I),
         ("gq_to_bf16", [P, I64, I, I64, P, I64, I, P], I),
         ("gq_gcn_layer_workspace_bytes", [GP, I, I, I], S),
+        ("gq_edge_softmax_workspace_bytes", [GP, I], S),
+        ("gq_sddmm_edge_softmax", [GP, P, P, I, F, P, P, P, S, P], I),
+        ("gq_gat_layer_workspace_bytes", [GP, I, I, I, I], S),
+        ("gq_gat_layer_fwd", [GP, P, I64, I, P, P, P, I, I, F, P, I, U64, P, P, P, P, P, P, P, S, P, P], I),
+        ("gq_gat_layer_bwd", [GP, P, P, I64, P, P, P, P, P, P, P, P, I, I, I, F, P, I, U64, P, P, P, P, P, P, P, S,
+                              P, P], I),
         ("gq_gcn_layer_fwd", [GP, I, P, I64, I, P, I, P, I, U64, I, P, I64, P, I64, P, S, P, P, P], I),
         ("gq_gcn_layer_bwd",
          [GP, I, P, I64, P, I64, P, I64, P, I, I, P, I, U64, I, I, P, P, I64, P, P, S, P, P, P], I),
@@ -423,3 +429,64 @@ def gcn_layer_bwd(g: Graph, dH_out: torch.Tensor, A_save: torch.Tensor, H_out: t
                               _ptr(dH_in), _rows(dH_in) if dH_in is not None else 0, _ptr(dA_save), _ptr(buf),
                               buf.numel(), _ptr(dev_err), _events(events), _stream()), "gq_gcn_layer_bwd")
     return dW, (dH_in if need_dinput else None)
+
+
+# --------------------------------------------------------------------------
+# GAT
+# --------------------------------------------------------------------------
+
+def sddmm_edge_softmax(g: Graph, S: torch.Tensor, D: torch.Tensor, slope: float = 0.2, with_epre: bool = False):
+    """alpha (E x heads) [, E_pre] of Tango Fig. 1a steps 3-4."""
+    _cuda(S, torch.float32, "S")
+    _cuda(D, torch.float32, "D")
+    heads = S.shape[1]
+    alpha = torch.empty(g.nnz, heads, dtype=torch.float32, device=S.device)
+    Epre = torch.empty_like(alpha) if with_epre else None
+    wb = int(lib().gq_edge_softmax_workspace_bytes(g.ref, heads))
+    ws = torch.empty(max(wb, 1), dtype=torch.uint8, device=S.device)
+    _check(lib().gq_sddmm_edge_softmax(g.ref, _ptr(S.contiguous()), _ptr(D.contiguous()), heads, slope, _ptr(Epre),
+                                       _ptr(alpha), _ptr(ws), wb, _stream()), "gq_sddmm_edge_softmax")
+    return (alpha, Epre) if with_epre else alpha
+
+
+class GATLayer:
+    """Buffers and calls of one GAT layer (heads x f, LeakyReLU slope)."""
+
+    def __init__(self, g: Graph, d_in: int, heads: int, f: int, slope: float = 0.2, bits: int = 32,
+                 mask=None, device="cuda"):
+        self.g, self.d_in, self.heads, self.f, self.slope, self.bits, self.mask = g, d_in, heads, f, slope, bits, mask
+        d = heads * f
+        n = g.n
+        self.Hp = torch.empty(n, d, dtype=torch.float32, device=device)
+        self.S = torch.empty(n, heads, dtype=torch.float32, device=device)
+        self.D = torch.empty(n, heads, dtype=torch.float32, device=device)
+        self.alpha = torch.empty(g.nnz, heads, dtype=torch.float32, device=device)
+        self.packed = (torch.empty(n, packed_pitch(d, bits), dtype=torch.uint8, device=device)
+                       if bits < 32 else None)
+        self.out = torch.empty(n, d, dtype=torch.float32, device=device)
+        self.dW = torch.empty(d_in, d, dtype=torch.float32, device=device)
+        self.da_src = torch.empty(heads, f, dtype=torch.float32, device=device)
+        self.da_dst = torch.empty(heads, f, dtype=torch.float32, device=device)
+        self.dH = torch.empty(n, d_in, dtype=torch.float32, device=device)
+        self.err = torch.zeros(1, dtype=torch.int32, device=device)
+        self.ws = Workspace(device)
+        self.ws.get(int(lib().gq_gat_layer_workspace_bytes(g.ref, d_in, heads, f, bits)))
+
+    def forward(self, H, W, a_src, a_dst, seed: int = 0):
+        buf = self.ws.buf
+        _check(lib().gq_gat_layer_fwd(self.g.ref, _ptr(H), _rows(H), self.d_in, _ptr(W), _ptr(a_src), _ptr(a_dst),
+                                      self.heads, self.f, self.slope, _ptr(self.mask), self.bits,
+                                      seed & 0xFFFFFFFFFFFFFFFF, _ptr(self.Hp), _ptr(self.S), _ptr(self.D),
+                                      _ptr(self.alpha), _ptr(self.packed), _ptr(self.out), _ptr(buf), buf.numel(),
+                                      _ptr(self.err), _stream()), "gq_gat_layer_fwd")
+        return self.out
+
+    def backward(self, dOut, H, W, a_src, a_dst, seed: int = 0, dEpre=None, dHp=None):
+        buf = self.ws.buf
+        _check(lib().gq_gat_layer_bwd(self.g.ref, _ptr(dOut), _ptr(H), _rows(H), _ptr(self.Hp), _ptr(self.S),
+                                      _ptr(self.D), _ptr(self.alpha), _ptr(self.packed), _ptr(W), _ptr(a_src),
+                                      _ptr(a_dst), self.d_in, self.heads, self.f, self.slope, _ptr(self.mask),
+                                      self.bits, seed & 0xFFFFFFFFFFFFFFFF, _ptr(self.dW), _ptr(self.da_src),
+                                      _ptr(self.da_dst), _ptr(self.dH), _ptr(dEpre), _ptr(dHp), _ptr(buf),
+                                      buf.numel(), _ptr(self.err), _stream()), "gq_gat_layer_bwd")
+        return self.dW, self.da_src, self.da_dst, self.dH

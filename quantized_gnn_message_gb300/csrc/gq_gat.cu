@@ -1,0 +1,679 @@
+// gq_gat.cu -- the edge kernels of the GAT layer (Tango Sec. 2.1, Fig. 1).
+//
+// edge_softmax_kernel  (Fig. 1a steps 3-4), per destination row v:
+//     E_pre[e,k] = S[u,k] + D[v,k]            (SDDMM add, e = u -> v)
+//     E[e,k]     = LeakyReLU(E_pre[e,k])
+//     alpha[e,k] = exp(E[e,k] - max_v) / sum_{e' in in(v)} exp(E[e',k] - max_v)
+//   one pass keeps an online (max, sum) per head, a second writes alpha.
+// gat_edge_bwd_kernel  (Fig. 1b), per destination row v:
+//     dalpha[e,k] = sum_f dOut[v,kF+f] m_u[kF+f]          (SDDMM dot)
+//     P[v,k]      = sum_e alpha[e,k] dalpha[e,k]
+//     dE_pre[e,k] = alpha (dalpha - P) * (E_pre > 0 ? 1 : slope)
+//     dD[v,k]     = sum_e dE_pre[e,k]                      (in-edge sum)
+// gat_node_bwd_kernel  per source row u (transposed CSR):
+//     dS[u,k]     = sum_{e in out(u)} dE_pre[e,k]          (out-edge sum)
+//     dH'[u,c]    = dM[u,c] + dS[u,k] a_src[k,f] + dD[u,k] a_dst[k,f]
+//     partial sums of da_src = sum_u dS[u,k] H'[u,:], da_dst likewise.
+// Heavy rows follow the graph's static schedule (block tasks; split rows
+// combine per-task partials in task order in the last block to finish).
+// Scores, attention and their gradients stay fp32 (Tango Sec. 3.2: full
+// precision before the softmax).
+#include <cuda_bf16.h>
+
+#include "gq_common.cuh"
+#include "gq_internal.cuh"
+#include "gq_msg.cuh"
+
+namespace gq {
+namespace {
+
+constexpr int kGatThreads = 256;
+constexpr int kGatWarps = kGatThreads / 32;
+constexpr float kNegInf = -__builtin_huge_valf();
+
+// ------------------------------------------------------------ helpers ---
+template <int K>
+__device__ __forceinline__ void load_k(const float* __restrict__ p, float (&v)[K]) {
+  if constexpr (K == 4) {
+    const float4 a = __ldg(reinterpret_cast<const float4*>(p));
+    v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
+  } else if constexpr (K == 8) {
+    const float4 a = __ldg(reinterpret_cast<const float4*>(p));
+    const float4 b = __ldg(reinterpret_cast<const float4*>(p + 4));
+    v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
+    v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+  } else {
+#pragma unroll
+    for (int k = 0; k < K; ++k) v[k] = __ldg(p + k);
+  }
+}
+
+__device__ __forceinline__ float lrelu(float x, float slope) { return x > 0.0f ? x : slope * x; }
+
+// online softmax state: fold value x into (m, l)
+__device__ __forceinline__ void online_add(float& m, float& l, float x) {
+  if (x > m) {
+    l = l * expf(m - x) + 1.0f;
+    m = x;
+  } else {
+    l += expf(x - m);
+  }
+}
+
+__device__ __forceinline__ void online_merge(float& m, float& l, float m2, float l2) {
+  const float M = fmaxf(m, m2);
+  if (M == kNegInf) return;  // both empty
+  l = l * expf(m - M) + l2 * expf(m2 - M);
+  m = M;
+}
+
+struct Sched {
+  const int32_t* tasks;
+  const int32_t* groups;
+  int64_t n_tasks;
+  int hub_threshold;
+  float* partial;  // [slot][...]
+  int* tickets;    // [group]
+};
+
+// Block-wide: publish this task's partial (n floats at `mine`), take a
+// ticket; returns true in the last block of the group (after a fence).
+__device__ __forceinline__ bool last_of_group(const Sched& sc, int group, int n_in_group) {
+  __shared__ int last;
+  __threadfence();
+  __syncthreads();
+  if (threadIdx.x == 0) last = (atomicAdd(&sc.tickets[group], 1) == n_in_group - 1);
+  __syncthreads();
+  if (last) __threadfence();
+  return last;
+}
+
+// ------------------------------------------------------- edge softmax ---
+struct SoftmaxParams {
+  const int32_t* rowptr;
+  const int32_t* col;
+  const float* S;
+  const float* D;
+  float slope;
+  float* alpha;
+  float* Epre;
+  int64_t n_rows;
+  Sched sc;
+};
+
+template <int K>
+__device__ __forceinline__ void sm_scores(const SoftmaxParams& p, int64_t e, const float (&dv)[K], float (&ep)[K]) {
+  float s[K];
+  load_k<K>(p.S + (int64_t)__ldg(p.col + e) * K, s);
+#pragma unroll
+  for (int k = 0; k < K; ++k) ep[k] = s[k] + dv[k];
+}
+
+// (max, sum) of this thread's edges e = first, first + stride, ...
+template <int K>
+__device__ __forceinline__ void sm_pass1(const SoftmaxParams& p, int64_t first, int64_t end, int64_t stride,
+                                         const float (&dv)[K], float (&m)[K], float (&l)[K]) {
+#pragma unroll
+  for (int k = 0; k < K; ++k) {
+    m[k] = kNegInf;
+    l[k] = 0.0f;
+  }
+  for (int64_t e = first; e < end; e += stride) {
+    float ep[K];
+    sm_scores<K>(p, e, dv, ep);
+#pragma unroll
+    for (int k = 0; k < K; ++k) online_add(m[k], l[k], lrelu(ep[k], p.slope));
+  }
+}
+
+template <int K>
+__device__ __forceinline__ void sm_pass2(const SoftmaxParams& p, int64_t first, int64_t end, int64_t stride,
+                                         const float (&dv)[K], const float (&M)[K], const float (&L)[K]) {
+  for (int64_t e = first; e < end; e += stride) {
+    float ep[K];
+    sm_scores<K>(p, e, dv, ep);
+#pragma unroll
+    for (int k = 0; k < K; ++k) {
+      p.alpha[e * K + k] = expf(lrelu(ep[k], p.slope) - M[k]) / L[k];
+      if (p.Epre != nullptr) p.Epre[e * K + k] = ep[k];
+    }
+  }
+}
+
+template <int K>
+__device__ __forceinline__ void warp_merge(float (&m)[K], float (&l)[K]) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1)
+#pragma unroll
+    for (int k = 0; k < K; ++k) {
+      const float m2 = __shfl_xor_sync(FULL, m[k], o);
+      const float l2 = __shfl_xor_sync(FULL, l[k], o);
+      online_merge(m[k], l[k], m2, l2);
+    }
+}
+
+template <int K>
+__global__ void __launch_bounds__(kGatThreads) edge_softmax_kernel(const SoftmaxParams p) {
+  __shared__ float red[kGatWarps][2 * K];
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  if ((int64_t)blockIdx.x < p.sc.n_tasks) {
+    const int4 task = __ldg(reinterpret_cast<const int4*>(p.sc.tasks) + blockIdx.x);
+    const int64_t v = task.x;
+    float dv[K];
+    load_k<K>(p.D + v * K, dv);
+    float m[K], l[K];
+    sm_pass1<K>(p, (int64_t)task.y + threadIdx.x, task.z, kGatThreads, dv, m, l);
+    warp_merge<K>(m, l);
+    if (lane == 0)
+#pragma unroll
+      for (int k = 0; k < K; ++k) {
+        red[w][2 * k] = m[k];
+        red[w][2 * k + 1] = l[k];
+      }
+    __syncthreads();
+#pragma unroll
+    for (int k = 0; k < K; ++k) {  // every thread merges the warps in order
+      m[k] = red[0][2 * k];
+      l[k] = red[0][2 * k + 1];
+      for (int ww = 1; ww < kGatWarps; ++ww) online_merge(m[k], l[k], red[ww][2 * k], red[ww][2 * k + 1]);
+    }
+    if (task.w < 0) {
+      sm_pass2<K>(p, (int64_t)task.y + threadIdx.x, task.z, kGatThreads, dv, m, l);
+      return;
+    }
+    const int4 grp = __ldg(reinterpret_cast<const int4*>(p.sc.groups) + task.w);
+    float* mine = p.sc.partial + (int64_t)(grp.w + ((int)blockIdx.x - grp.y)) * 2 * K;
+    if (threadIdx.x < K) {
+      mine[2 * threadIdx.x] = m[threadIdx.x];
+      mine[2 * threadIdx.x + 1] = l[threadIdx.x];
+    }
+    if (!last_of_group(p.sc, task.w, grp.z)) return;
+    const float* base = p.sc.partial + (int64_t)grp.w * 2 * K;
+#pragma unroll
+    for (int k = 0; k < K; ++k) {
+      m[k] = __ldcg(base + 2 * k);
+      l[k] = __ldcg(base + 2 * k + 1);
+      for (int t = 1; t < grp.z; ++t) online_merge(m[k], l[k], __ldcg(base + t * 2 * K + 2 * k), __ldcg(base + t * 2 * K + 2 * k + 1));
+    }
+    sm_pass2<K>(p, (int64_t)p.rowptr[v] + threadIdx.x, p.rowptr[v + 1], kGatThreads, dv, m, l);
+    return;
+  }
+  const int64_t gw = ((int64_t)blockIdx.x - p.sc.n_tasks) * kGatWarps + w;
+  const int64_t nw = ((int64_t)gridDim.x - p.sc.n_tasks) * kGatWarps;
+  for (int64_t v = gw; v < p.n_rows; v += nw) {
+    const int64_t a = p.rowptr[v], b = p.rowptr[v + 1];
+    if (b - a > p.sc.hub_threshold) continue;
+    float dv[K];
+    load_k<K>(p.D + v * K, dv);
+    float m[K], l[K];
+    sm_pass1<K>(p, a + lane, b, 32, dv, m, l);
+    warp_merge<K>(m, l);
+    sm_pass2<K>(p, a + lane, b, 32, dv, m, l);
+  }
+}
+
+// --------------------------------------------------- GAT edge backward ---
+struct EdgeBwdParams {
+  const int32_t* rowptr;
+  const int32_t* col;
+  const float* dOut;   // n x d, ld = d
+  MsgSrc msg;          // forward messages m_u (H' or its de-quantized rows)
+  const float* alpha;  // E x K
+  const float* S;
+  const float* D;      // n x K
+  float slope;
+  float* dEpre;        // E x K (holds dalpha between the passes)
+  float* dD;           // n x K
+  int64_t n_rows;
+  int d, gshift;       // lanes per head = 1 << gshift (F / 8)
+  Sched sc;
+};
+
+// Pass 1 over edges [first batch ...): dalpha for each edge (all lanes of
+// the warp on one edge, lane l owning columns 8l..8l+7), stored to dEpre;
+// returns this warp's partial P for the lane's head (meaningful on the
+// head's first lane).
+template <int BITS, int K>
+__device__ __forceinline__ float eb_pass1(const EdgeBwdParams& p, int64_t beg, int64_t end, int first, int stride,
+                                          const float (&g)[8]) {
+  constexpr int U = 4;
+  const int lane = threadIdx.x & 31;
+  const int nchunks = p.d >> 3;
+  const bool live = lane < nchunks;
+  const int head = lane >> p.gshift;
+  const bool leader = live && (lane & ((1 << p.gshift) - 1)) == 0;
+  float P = 0.0f;
+  for (int64_t base = beg + 32 * (int64_t)first; base < end; base += 32 * (int64_t)stride) {
+    const int64_t e = base + lane;
+    int32_t x = 0;
+    bool qx = false;
+    if (e < end) {
+      x = __ldg(p.col + e);
+      qx = is_quant<BITS>(p.msg, x);
+    }
+    const int cnt = (int)min((int64_t)32, end - base);
+    for (int jj = 0; jj < cnt; jj += U) {
+      RawChunk<BITS> r[U];
+#pragma unroll
+      for (int t = 0; t < U; ++t) {
+        const int j = jj + t < cnt ? jj + t : 0;
+        const int32_t xj = __shfl_sync(FULL, x, j);
+        const bool qj = __shfl_sync(FULL, (int)qx, j) != 0;
+        if (live && jj + t < cnt) load_raw<BITS>(p.msg, xj, qj, lane, r[t]);
+      }
+#pragma unroll
+      for (int t = 0; t < U; ++t) {
+        float dot = 0.0f;
+        if (live && jj + t < cnt) {
+          float v[8];
+          decode<BITS>(r[t], v);
+#pragma unroll
+          for (int i = 0; i < 8; ++i) dot = __fmaf_rn(g[i], v[i], dot);
+        }
+        for (int o = 1; o < (1 << p.gshift); o <<= 1) dot += __shfl_xor_sync(FULL, dot, o);
+        if (leader && jj + t < cnt) {
+          const int64_t ej = base + jj + t;
+          const float a = __ldg(p.alpha + ej * K + head);
+          p.dEpre[ej * K + head] = dot;
+          P = __fmaf_rn(a, dot, P);
+        }
+      }
+    }
+  }
+  return P;
+}
+
+// Pass 2 (thread per edge): dE_pre from dalpha, P; returns the thread's
+// partial dD per head.
+template <int K>
+__device__ __forceinline__ void eb_pass2(const EdgeBwdParams& p, int64_t v, int64_t first, int64_t end,
+                                         int64_t stride, const float (&P)[K], float (&dd)[K]) {
+  float dv[K];
+  load_k<K>(p.D + v * K, dv);
+#pragma unroll
+  for (int k = 0; k < K; ++k) dd[k] = 0.0f;
+  for (int64_t e = first; e < end; e += stride) {
+    float s[K], a[K];
+    load_k<K>(p.S + (int64_t)__ldg(p.col + e) * K, s);
+    load_k<K>(p.alpha + e * K, a);
+#pragma unroll
+    for (int k = 0; k < K; ++k) {
+      const float da = __ldcg(p.dEpre + e * K + k);
+      const float dE = a[k] * (da - P[k]);
+      const float g = (s[k] + dv[k]) > 0.0f ? dE : p.slope * dE;
+      p.dEpre[e * K + k] = g;
+      dd[k] += g;
+    }
+  }
+}
+
+template <int K>
+__device__ __forceinline__ void warp_sum(float (&x)[K]) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1)
+#pragma unroll
+    for (int k = 0; k < K; ++k) x[k] += __shfl_xor_sync(FULL, x[k], o);
+}
+
+template <int BITS, int K>
+__global__ void __launch_bounds__(kGatThreads) gat_edge_bwd_kernel(const EdgeBwdParams p) {
+  __shared__ float red[kGatWarps][K];
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  const int nchunks = p.d >> 3;
+  if ((int64_t)blockIdx.x < p.sc.n_tasks) {
+    const int4 task = __ldg(reinterpret_cast<const int4*>(p.sc.tasks) + blockIdx.x);
+    const int64_t v = task.x;
+    float g[8] = {};
+    if (lane < nchunks) {
+      const float4 a = ldg_f4(p.dOut + v * p.d + lane * 8), b = ldg_f4(p.dOut + v * p.d + lane * 8 + 4);
+      g[0] = a.x; g[1] = a.y; g[2] = a.z; g[3] = a.w; g[4] = b.x; g[5] = b.y; g[6] = b.z; g[7] = b.w;
+    }
+    const float Pw = eb_pass1<BITS, K>(p, task.y, task.z, w, kGatWarps, g);
+    // P per head from each warp's head leaders, summed in warp order
+    if (lane < nchunks && (lane & ((1 << p.gshift) - 1)) == 0) red[w][lane >> p.gshift] = Pw;
+    __syncthreads();
+    float P[K];
+#pragma unroll
+    for (int k = 0; k < K; ++k) {
+      P[k] = 0.0f;
+      for (int ww = 0; ww < kGatWarps; ++ww) P[k] += red[ww][k];
+    }
+    __syncthreads();
+    int64_t e0 = task.y, e1 = task.z;
+    if (task.w >= 0) {
+      const int4 grp = __ldg(reinterpret_cast<const int4*>(p.sc.groups) + task.w);
+      float* mine = p.sc.partial + (int64_t)(grp.w + ((int)blockIdx.x - grp.y)) * K;
+      if (threadIdx.x < K) mine[threadIdx.x] = P[threadIdx.x];
+      if (!last_of_group(p.sc, task.w, grp.z)) return;
+      const float* base = p.sc.partial + (int64_t)grp.w * K;
+#pragma unroll
+      for (int k = 0; k < K; ++k) {
+        P[k] = 0.0f;
+        for (int t = 0; t < grp.z; ++t) P[k] += __ldcg(base + t * K + k);
+      }
+      e0 = p.rowptr[v];
+      e1 = p.rowptr[v + 1];
+    }
+    float dd[K];
+    eb_pass2<K>(p, v, e0 + threadIdx.x, e1, kGatThreads, P, dd);
+    warp_sum<K>(dd);
+    if (lane == 0)
+#pragma unroll
+      for (int k = 0; k < K; ++k) red[w][k] = dd[k];
+    __syncthreads();
+    if (threadIdx.x < K) {
+      float t = 0.0f;
+      for (int ww = 0; ww < kGatWarps; ++ww) t += red[ww][threadIdx.x];
+      p.dD[v * K + threadIdx.x] = t;
+    }
+    return;
+  }
+  const int64_t gw = ((int64_t)blockIdx.x - p.sc.n_tasks) * kGatWarps + w;
+  const int64_t nw = ((int64_t)gridDim.x - p.sc.n_tasks) * kGatWarps;
+  for (int64_t v = gw; v < p.n_rows; v += nw) {
+    const int64_t a = p.rowptr[v], b = p.rowptr[v + 1];
+    if (b - a > p.sc.hub_threshold) continue;
+    float g[8] = {};
+    if (lane < nchunks) {
+      const float4 x = ldg_f4(p.dOut + v * p.d + lane * 8), y = ldg_f4(p.dOut + v * p.d + lane * 8 + 4);
+      g[0] = x.x; g[1] = x.y; g[2] = x.z; g[3] = x.w; g[4] = y.x; g[5] = y.y; g[6] = y.z; g[7] = y.w;
+    }
+    const float Pw = eb_pass1<BITS, K>(p, a, b, 0, 1, g);
+    float P[K];
+#pragma unroll
+    for (int k = 0; k < K; ++k) P[k] = __shfl_sync(FULL, Pw, k << p.gshift);
+    __syncwarp();
+    float dd[K];
+    eb_pass2<K>(p, v, a + lane, b, 32, P, dd);
+    warp_sum<K>(dd);
+    if (lane < K) {
+      float t = dd[0];
+#pragma unroll
+      for (int k = 1; k < K; ++k)
+        if (lane == k) t = dd[k];
+      p.dD[v * K + lane] = t;
+    }
+  }
+}
+
+// --------------------------------------------------- GAT node backward ---
+struct NodeBwdParams {
+  const int32_t* tr_rowptr;
+  const int32_t* tr_perm;
+  const float* dEpre;   // E x K (by CSR edge id)
+  const float* dD;      // n x K
+  const float* dM;      // n x d
+  const float* Hp;      // n x d
+  const float* a_src;   // d
+  const float* a_dst;   // d
+  __nv_bfloat16* dHp;   // n x ldb (bf16, for the GEMMs)
+  int64_t ldb;
+  float* dHp32;         // optional n x d fp32 copy
+  float* dS;            // optional n x K
+  float* part;          // [block][2 d] partial da_src | da_dst
+  int64_t n_rows;
+  int d, fshift;
+};
+
+__device__ __forceinline__ uint32_t bf2(float lo, float hi) {
+  const __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<const uint32_t*>(&h);
+}
+
+template <int K>
+__global__ void __launch_bounds__(kGatThreads) gat_node_bwd_kernel(const NodeBwdParams p) {
+  extern __shared__ float sm[];  // [kGatWarps][2 d]
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  const int nchunks = p.d >> 3;
+  const bool live = lane < nchunks;
+  const int head = (lane * 8) >> p.fshift;
+  float as[8] = {}, ad[8] = {};
+  if (live) {
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      as[i] = __ldg(p.a_src + lane * 8 + i);
+      ad[i] = __ldg(p.a_dst + lane * 8 + i);
+    }
+  }
+  float acc_s[8] = {}, acc_d[8] = {};
+  const int64_t gw = (int64_t)blockIdx.x * kGatWarps + w;
+  const int64_t nw = (int64_t)gridDim.x * kGatWarps;
+  for (int64_t u = gw; u < p.n_rows; u += nw) {
+    const int64_t a = p.tr_rowptr[u], b = p.tr_rowptr[u + 1];
+    float ds[K];
+#pragma unroll
+    for (int k = 0; k < K; ++k) ds[k] = 0.0f;
+    for (int64_t e = a + lane; e < b; e += 32) {
+      float x[K];
+      load_k<K>(p.dEpre + (int64_t)__ldg(p.tr_perm + e) * K, x);
+#pragma unroll
+      for (int k = 0; k < K; ++k) ds[k] += x[k];
+    }
+    warp_sum<K>(ds);
+    float dsh = ds[0], ddh;
+#pragma unroll
+    for (int k = 1; k < K; ++k)
+      if (head == k) dsh = ds[k];
+    if (p.dS != nullptr && lane < K) {
+      float t = ds[0];
+#pragma unroll
+      for (int k = 1; k < K; ++k)
+        if (lane == k) t = ds[k];
+      p.dS[u * K + lane] = t;
+    }
+    if (!live) continue;
+    ddh = __ldg(p.dD + u * K + head);
+    const float4 m0 = ldg_f4(p.dM + u * p.d + lane * 8), m1 = ldg_f4(p.dM + u * p.d + lane * 8 + 4);
+    const float4 h0 = ldg_f4(p.Hp + u * p.d + lane * 8), h1 = ldg_f4(p.Hp + u * p.d + lane * 8 + 4);
+    const float mv[8] = {m0.x, m0.y, m0.z, m0.w, m1.x, m1.y, m1.z, m1.w};
+    const float hv[8] = {h0.x, h0.y, h0.z, h0.w, h1.x, h1.y, h1.z, h1.w};
+    float o[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      o[i] = mv[i] + dsh * as[i] + ddh * ad[i];
+      acc_s[i] = __fmaf_rn(dsh, hv[i], acc_s[i]);
+      acc_d[i] = __fmaf_rn(ddh, hv[i], acc_d[i]);
+    }
+    *reinterpret_cast<uint4*>(p.dHp + u * p.ldb + lane * 8) =
+        make_uint4(bf2(o[0], o[1]), bf2(o[2], o[3]), bf2(o[4], o[5]), bf2(o[6], o[7]));
+    if (p.dHp32 != nullptr) {
+      st_f4(p.dHp32 + u * p.d + lane * 8, o[0], o[1], o[2], o[3]);
+      st_f4(p.dHp32 + u * p.d + lane * 8 + 4, o[4], o[5], o[6], o[7]);
+    }
+  }
+  if (live)
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      sm[w * 2 * p.d + lane * 8 + i] = acc_s[i];
+      sm[w * 2 * p.d + p.d + lane * 8 + i] = acc_d[i];
+    }
+  __syncthreads();
+  for (int j = threadIdx.x; j < 2 * p.d; j += blockDim.x) {
+    float t = 0.0f;
+    for (int ww = 0; ww < kGatWarps; ++ww) t += sm[ww * 2 * p.d + j];
+    p.part[(int64_t)blockIdx.x * 2 * p.d + j] = t;
+  }
+}
+
+__global__ void sum_blocks_kernel(const float* __restrict__ part, int blocks, int n, float* out_a, float* out_b,
+                                  int split) {
+  const int j = blockIdx.x * blockDim.x + threadIdx.x;
+  if (j >= n) return;
+  float t = 0.0f;
+  for (int b = 0; b < blocks; ++b) t += part[(int64_t)b * n + j];
+  if (j < split)
+    out_a[j] = t;
+  else
+    out_b[j - split] = t;
+}
+
+Sched make_sched(const gq_sched& s, int hub_threshold, void* ws, int per_slot_floats) {
+  Sched r{};
+  r.tasks = s.tasks;
+  r.groups = s.groups;
+  r.n_tasks = s.n_tasks;
+  r.hub_threshold = hub_threshold;
+  if (s.n_groups > 0) {
+    r.partial = static_cast<float*>(ws);
+    r.tickets = reinterpret_cast<int*>(static_cast<char*>(ws) +
+                                       ((size_t)s.n_slots * per_slot_floats * sizeof(float) + 255) / 256 * 256);
+  }
+  return r;
+}
+
+size_t sched_ws(const gq_sched& s, int per_slot_floats) {
+  if (s.n_groups == 0) return 0;
+  return ((size_t)s.n_slots * per_slot_floats * sizeof(float) + 255) / 256 * 256 + (size_t)s.n_groups * 4 + 256;
+}
+
+int light_grid(int64_t n_rows, int64_t n_tasks) {
+  int64_t blocks = (n_rows + kGatWarps - 1) / kGatWarps;
+  const int64_t cap = (int64_t)sm_count() * 8;
+  if (blocks > cap) blocks = cap;
+  if (blocks < 1) blocks = 1;
+  return (int)(blocks + n_tasks);
+}
+
+template <int K>
+int launch_softmax(const SoftmaxParams& p, cudaStream_t s) {
+  edge_softmax_kernel<K><<<light_grid(p.n_rows, p.sc.n_tasks), kGatThreads, 0, s>>>(p);
+  return launch_status();
+}
+
+template <int BITS, int K>
+int launch_edge_bwd(const EdgeBwdParams& p, cudaStream_t s) {
+  gat_edge_bwd_kernel<BITS, K><<<light_grid(p.n_rows, p.sc.n_tasks), kGatThreads, 0, s>>>(p);
+  return launch_status();
+}
+
+}  // namespace
+
+// ---------------------------------------------------------------- API ---
+size_t edge_softmax_workspace(const gq_graph* g, int heads) { return sched_ws(g->sched, 2 * heads); }
+size_t edge_bwd_workspace(const gq_graph* g, int heads) { return sched_ws(g->sched, heads); }
+
+int edge_softmax(const gq_graph* g, const float* S, const float* D, int heads, float slope, float* Epre,
+                 float* alpha, void* ws, size_t ws_bytes, cudaStream_t s) {
+  if (g == nullptr || S == nullptr || D == nullptr || alpha == nullptr) return GQ_ERR_INVALID_ARG;
+  if (!(heads == 1 || heads == 2 || heads == 4 || heads == 8)) return GQ_ERR_UNSUPPORTED;
+  if (!aligned(S, 16) || !aligned(D, 16)) return GQ_ERR_INVALID_ARG;
+  SoftmaxParams p{};
+  p.rowptr = g->rowptr;
+  p.col = g->col;
+  p.S = S;
+  p.D = D;
+  p.slope = slope;
+  p.alpha = alpha;
+  p.Epre = Epre;
+  p.n_rows = g->n;
+  const size_t need = edge_softmax_workspace(g, heads);
+  if (need > 0 && (ws == nullptr || ws_bytes < need || !aligned(ws, 256))) return GQ_ERR_WORKSPACE;
+  p.sc = make_sched(g->sched, g->hub_threshold, ws, 2 * heads);
+  if (g->sched.n_groups > 0) GQ_TRY_CUDA(cudaMemsetAsync(p.sc.tickets, 0, g->sched.n_groups * sizeof(int), s));
+  switch (heads) {
+    case 1: return launch_softmax<1>(p, s);
+    case 2: return launch_softmax<2>(p, s);
+    case 4: return launch_softmax<4>(p, s);
+    default: return launch_softmax<8>(p, s);
+  }
+}
+
+int gat_edge_bwd(const gq_graph* g, const float* dOut, const float* Hp, const uint8_t* packed, const uint8_t* mask,
+                 int bits, const float* alpha, const float* S, const float* D, int heads, int d, float slope,
+                 float* dEpre, float* dD, void* ws, size_t ws_bytes, cudaStream_t s) {
+  if (!(heads == 1 || heads == 2 || heads == 4 || heads == 8)) return GQ_ERR_UNSUPPORTED;
+  if (d < 8 || d > 256 || d % heads) return GQ_ERR_UNSUPPORTED;
+  const int F = d / heads;
+  int gshift = 0;
+  while ((8 << gshift) < F) ++gshift;
+  if ((8 << gshift) != F) return GQ_ERR_UNSUPPORTED;  // head width: 8 * power of two
+  EdgeBwdParams p{};
+  p.rowptr = g->rowptr;
+  p.col = g->col;
+  p.dOut = dOut;
+  p.msg = MsgSrc{Hp, d, packed, bits < 32 ? packed_pitch(d, bits) : 0, bits < 32 ? (int)header_offset(d, bits) : 0,
+                 mask, d};
+  p.alpha = alpha;
+  p.S = S;
+  p.D = D;
+  p.slope = slope;
+  p.dEpre = dEpre;
+  p.dD = dD;
+  p.n_rows = g->n;
+  p.d = d;
+  p.gshift = gshift;
+  const size_t need = edge_bwd_workspace(g, heads);
+  if (need > 0 && (ws == nullptr || ws_bytes < need || !aligned(ws, 256))) return GQ_ERR_WORKSPACE;
+  p.sc = make_sched(g->sched, g->hub_threshold, ws, heads);
+  if (g->sched.n_groups > 0) GQ_TRY_CUDA(cudaMemsetAsync(p.sc.tickets, 0, g->sched.n_groups * sizeof(int), s));
+#define GQ_EB(B)                                       \
+  switch (heads) {                                     \
+    case 1: return launch_edge_bwd<B, 1>(p, s);        \
+    case 2: return launch_edge_bwd<B, 2>(p, s);        \
+    case 4: return launch_edge_bwd<B, 4>(p, s);        \
+    default: return launch_edge_bwd<B, 8>(p, s);       \
+  }
+  switch (bits) {
+    case 2: GQ_EB(2)
+    case 4: GQ_EB(4)
+    case 8: GQ_EB(8)
+    default: GQ_EB(32)
+  }
+#undef GQ_EB
+}
+
+int node_bwd_blocks() { return sm_count() * 2; }
+
+size_t node_bwd_workspace(int d) { return (size_t)node_bwd_blocks() * 2 * d * sizeof(float) + 256; }
+
+int gat_node_bwd(const gq_graph* g, const float* dEpre, const float* dD, const float* dM, const float* Hp,
+                 const float* a_src, const float* a_dst, int heads, int d, void* dHp_bf16, int64_t ldb, float* dHp32,
+                 float* dS, float* da_src, float* da_dst, void* ws, size_t ws_bytes, cudaStream_t s) {
+  if (d < 8 || d > 256 || d % 8 || d % heads) return GQ_ERR_UNSUPPORTED;
+  const int F = d / heads;
+  int fshift = 0;
+  while ((1 << fshift) < F) ++fshift;
+  if ((1 << fshift) != F || F < 8) return GQ_ERR_UNSUPPORTED;
+  if (ws == nullptr || ws_bytes < node_bwd_workspace(d)) return GQ_ERR_WORKSPACE;
+  NodeBwdParams p{};
+  p.tr_rowptr = g->tr_rowptr;
+  p.tr_perm = g->tr_perm;
+  p.dEpre = dEpre;
+  p.dD = dD;
+  p.dM = dM;
+  p.Hp = Hp;
+  p.a_src = a_src;
+  p.a_dst = a_dst;
+  p.dHp = static_cast<__nv_bfloat16*>(dHp_bf16);
+  p.ldb = ldb;
+  p.dHp32 = dHp32;
+  p.dS = dS;
+  p.part = static_cast<float*>(ws);
+  p.n_rows = g->n;
+  p.d = d;
+  p.fshift = fshift;
+  const int blocks = node_bwd_blocks();
+  const size_t smem = sizeof(float) * kGatWarps * 2 * d;
+  switch (heads) {
+    case 1: gat_node_bwd_kernel<1><<<blocks, kGatThreads, smem, s>>>(p); break;
+    case 2: gat_node_bwd_kernel<2><<<blocks, kGatThreads, smem, s>>>(p); break;
+    case 4: gat_node_bwd_kernel<4><<<blocks, kGatThreads, smem, s>>>(p); break;
+    case 8: gat_node_bwd_kernel<8><<<blocks, kGatThreads, smem, s>>>(p); break;
+    default: return GQ_ERR_UNSUPPORTED;
+  }
+  GQ_TRY(launch_status());
+  sum_blocks_kernel<<<(2 * d + 255) / 256, 256, 0, s>>>(p.part, blocks, 2 * d, da_src, da_dst, d);
+  return launch_status();
+}
+
+}  // namespace gq
+
+extern "C" size_t gq_edge_softmax_workspace_bytes(const gq_graph* g, int heads) {
+  if (g == nullptr || heads < 1) return 0;
+  return gq::edge_softmax_workspace(g, heads);
+}
+
+extern "C" int gq_sddmm_edge_softmax(const gq_graph* g, const float* S, const float* D, int heads, float slope,
+                                     float* E_pre, float* alpha, void* ws, size_t ws_bytes, gq_stream stream) {
+  return gq::edge_softmax(g, S, D, heads, slope, E_pre, alpha, ws, ws_bytes, (cudaStream_t)stream);
+}

@@ -50,3 +50,20 @@ struct Carve {
 inline int64_t round8(int64_t x) { return (x + 7) / 8 * 8; }
 
 }  // namespace gq
+
+namespace gq {
+
+// GAT edge kernels (gq_gat.cu)
+size_t edge_softmax_workspace(const gq_graph* g, int heads);
+size_t edge_bwd_workspace(const gq_graph* g, int heads);
+size_t node_bwd_workspace(int d);
+int edge_softmax(const gq_graph* g, const float* S, const float* D, int heads, float slope, float* Epre,
+                 float* alpha, void* ws, size_t ws_bytes, cudaStream_t s);
+int gat_edge_bwd(const gq_graph* g, const float* dOut, const float* Hp, const uint8_t* packed, const uint8_t* mask,
+                 int bits, const float* alpha, const float* S, const float* D, int heads, int d, float slope,
+                 float* dEpre, float* dD, void* ws, size_t ws_bytes, cudaStream_t s);
+int gat_node_bwd(const gq_graph* g, const float* dEpre, const float* dD, const float* dM, const float* Hp,
+                 const float* a_src, const float* a_dst, int heads, int d, void* dHp_bf16, int64_t ldb, float* dHp32,
+                 float* dS, float* da_src, float* da_dst, void* ws, size_t ws_bytes, cudaStream_t s);
+
+}  // namespace gq

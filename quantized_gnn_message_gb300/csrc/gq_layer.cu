@@ -142,3 +142,138 @@ extern "C" int gq_gcn_layer_bwd(const gq_graph* g, int coef, const float* dH_out
   GQ_TRY(dequant_spmm(g, 1, coef, dA, d_in, w.packed, mask, d_in, bits, dH_in, ldi, w.sp, w.sp_bytes, s, nullptr));
   return tr.end(4);
 }
+
+// ---------------------------------------------------------------------------
+// GAT layer (Tango Sec. 2.1, Fig. 1a forward, Fig. 1b backward)
+// ---------------------------------------------------------------------------
+namespace gq {
+namespace {
+
+struct GatWs {
+  void* hb;          // H in bf16 [n][round8(d_in)]
+  void* wb;          // W^T (fwd) or W (bwd) in bf16
+  uint8_t* packed;   // quantized H' (fwd, if the caller keeps none) / quantized dOut (bwd)
+  void* sx;          // softmax / edge-backward split scratch
+  size_t sx_bytes;
+  void* sp;          // edge SpMM scratch
+  size_t sp_bytes;
+  float* dEpre;      // E x heads
+  float* dD;         // n x heads
+  float* dM;         // n x d
+  void* dhb;         // dH' bf16 [n][d]
+  void* nb;          // node-kernel partials
+  size_t nb_bytes;
+  void* wg;          // weight-GEMM partials
+  size_t wg_bytes;
+};
+
+Carve carve_gat(const gq_graph* g, void* ws, size_t ws_bytes, int d_in, int heads, int d, int bits, GatWs& w) {
+  const int64_t n = g->n;
+  Carve c(ws, ws_bytes);
+  w.hb = c.take((size_t)n * round8(d_in) * 2);
+  const int64_t a = (int64_t)d * round8(d_in), b = (int64_t)d_in * round8(d);
+  w.wb = c.take((size_t)(a > b ? a : b) * 2);
+  w.packed = bits < 32 ? static_cast<uint8_t*>(c.take((size_t)n * packed_pitch(d, bits))) : nullptr;
+  const size_t s1 = edge_softmax_workspace(g, heads), s2 = edge_bwd_workspace(g, heads);
+  w.sx_bytes = s1 > s2 ? s1 : s2;
+  w.sx = w.sx_bytes ? c.take(w.sx_bytes) : nullptr;
+  const size_t p0 = spmm_workspace(g, 0, d), p1 = spmm_workspace(g, 1, d);
+  w.sp_bytes = p0 > p1 ? p0 : p1;
+  w.sp = w.sp_bytes ? c.take(w.sp_bytes) : nullptr;
+  w.dEpre = static_cast<float*>(c.take((size_t)g->nnz * heads * sizeof(float)));
+  w.dD = static_cast<float*>(c.take((size_t)n * heads * sizeof(float)));
+  w.dM = static_cast<float*>(c.take((size_t)n * d * sizeof(float)));
+  w.dhb = c.take((size_t)n * d * 2);
+  w.nb_bytes = node_bwd_workspace(d);
+  w.nb = c.take(w.nb_bytes);
+  w.wg_bytes = wgrad_workspace(n, d_in, d);
+  w.wg = c.take(w.wg_bytes);
+  return c;
+}
+
+int gat_check(const gq_graph* g, int d_in, int heads, int f, int bits) {
+  if (g == nullptr || d_in < 1 || heads < 1 || f < 1) return GQ_ERR_INVALID_ARG;
+  if (!(bits == 32 || valid_bits(bits))) return GQ_ERR_INVALID_ARG;
+  const int d = heads * f;
+  if (d_in > 256 || d > 256 || d % 8 || !(heads == 1 || heads == 2 || heads == 4 || heads == 8) || f < 16 ||
+      (f & (f - 1)))
+    return GQ_ERR_UNSUPPORTED;
+  return GQ_OK;
+}
+
+}  // namespace
+}  // namespace gq
+
+extern "C" size_t gq_gat_layer_workspace_bytes(const gq_graph* g, int d_in, int heads, int f, int bits) {
+  if (g == nullptr || d_in < 1 || heads < 1 || f < 1) return 0;
+  gq::GatWs w;
+  return gq::carve_gat(g, nullptr, 0, d_in, heads, heads * f, bits, w).used + 256;
+}
+
+extern "C" int gq_gat_layer_fwd(const gq_graph* g, const float* H, int64_t ldh, int d_in, const float* W,
+                                const float* a_src, const float* a_dst, int heads, int f, float slope,
+                                const uint8_t* mask, int bits, uint64_t seed, float* Hp_save, float* S_save,
+                                float* D_save, float* alpha_save, uint8_t* packed_save, float* out, void* ws,
+                                size_t ws_bytes, int* dev_err, gq_stream stream) {
+  using namespace gq;
+  GQ_TRY(gat_check(g, d_in, heads, f, bits));
+  if (H == nullptr || W == nullptr || a_src == nullptr || a_dst == nullptr || Hp_save == nullptr ||
+      S_save == nullptr || D_save == nullptr || alpha_save == nullptr || out == nullptr || ldh < d_in)
+    return GQ_ERR_INVALID_ARG;
+  cudaStream_t s = (cudaStream_t)stream;
+  const int d = heads * f;
+  GatWs w;
+  if (ws == nullptr || !carve_gat(g, ws, ws_bytes, d_in, heads, d, bits, w).ok()) return GQ_ERR_WORKSPACE;
+  const int64_t ldhb = round8(d_in);
+  // step 1: H' = H W ; step 2: S = H' a_src, D = H' a_dst (GEMM epilogue)
+  GQ_TRY(to_bf16(H, g->n, d_in, ldh, w.hb, ldhb, (int)ldhb, nullptr, 0, s));
+  GQ_TRY(transpose_bf16(W, d_in, d, d, w.wb, ldhb, (int)ldhb, s));
+  GQ_TRY(row_gemm(w.hb, g->n, d_in, ldhb, w.wb, d, ldhb, GQ_ACT_NONE, Hp_save, d, a_src, a_dst, S_save, D_save,
+                  heads, dev_err, s));
+  // optional quantization of the messages H' of marginal nodes
+  uint8_t* packed = nullptr;
+  if (bits < 32) {
+    packed = packed_save != nullptr ? packed_save : w.packed;
+    GQ_TRY(quantize_pack(Hp_save, g->n, d, d, mask, bits, seed, packed, s));
+  }
+  // steps 3-4: SDDMM add + LeakyReLU + edge softmax ; step 5: SpMM
+  GQ_TRY(edge_softmax(g, S_save, D_save, heads, slope, nullptr, alpha_save, w.sx, w.sx_bytes, s));
+  return edge_spmm(g, 0, alpha_save, heads, Hp_save, d, packed, mask, d, bits, out, d, w.sp, w.sp_bytes, s);
+}
+
+extern "C" int gq_gat_layer_bwd(const gq_graph* g, const float* dOut, const float* H, int64_t ldh,
+                                const float* Hp_save, const float* S_save, const float* D_save,
+                                const float* alpha_save, const uint8_t* packed_save, const float* W,
+                                const float* a_src, const float* a_dst, int d_in, int heads, int f, float slope,
+                                const uint8_t* mask, int bits, uint64_t seed, float* dW, float* da_src,
+                                float* da_dst, float* dH, float* dEpre_save, float* dHp_save, void* ws,
+                                size_t ws_bytes, int* dev_err, gq_stream stream) {
+  using namespace gq;
+  GQ_TRY(gat_check(g, d_in, heads, f, bits));
+  if (dOut == nullptr || H == nullptr || Hp_save == nullptr || S_save == nullptr || D_save == nullptr ||
+      alpha_save == nullptr || W == nullptr || a_src == nullptr || a_dst == nullptr || dW == nullptr ||
+      da_src == nullptr || da_dst == nullptr || dH == nullptr || ldh < d_in)
+    return GQ_ERR_INVALID_ARG;
+  if (bits < 32 && packed_save == nullptr) return GQ_ERR_INVALID_ARG;
+  cudaStream_t s = (cudaStream_t)stream;
+  const int d = heads * f;
+  GatWs w;
+  if (ws == nullptr || !carve_gat(g, ws, ws_bytes, d_in, heads, d, bits, w).ok()) return GQ_ERR_WORKSPACE;
+  float* dEpre = dEpre_save != nullptr ? dEpre_save : w.dEpre;
+  // SDDMM dot -> dalpha; softmax derivative; LeakyReLU'; dD = in-edge sums
+  GQ_TRY(gat_edge_bwd(g, dOut, Hp_save, packed_save, mask, bits, alpha_save, S_save, D_save, heads, d, slope, dEpre,
+                      w.dD, w.sx, w.sx_bytes, s));
+  // dM = transposed multi-head SpMM of dOut (marginal rows travel quantized)
+  if (bits < 32) GQ_TRY(quantize_pack(dOut, g->n, d, d, mask, bits, seed, w.packed, s));
+  GQ_TRY(edge_spmm(g, 1, alpha_save, heads, dOut, d, w.packed, mask, d, bits, w.dM, d, w.sp, w.sp_bytes, s));
+  // dS = out-edge sums; dH' = dM + dS a_src + dD a_dst; da_src, da_dst
+  GQ_TRY(gat_node_bwd(g, dEpre, w.dD, w.dM, Hp_save, a_src, a_dst, heads, d, w.dhb, d, dHp_save, nullptr, da_src,
+                      da_dst, w.nb, w.nb_bytes, s));
+  // dW = H^T dH' ; dH = dH' W^T
+  const int64_t ldhb = round8(d_in);
+  GQ_TRY(to_bf16(H, g->n, d_in, ldh, w.hb, ldhb, (int)ldhb, nullptr, 0, s));
+  GQ_TRY(wgrad_gemm(w.hb, g->n, d_in, ldhb, w.dhb, d, d, dW, d, 0, w.wg, w.wg_bytes, dev_err, s));
+  GQ_TRY(to_bf16(W, d_in, d, d, w.wb, round8(d), (int)round8(d), nullptr, 0, s));
+  return row_gemm(w.dhb, g->n, d, d, w.wb, d_in, round8(d), GQ_ACT_NONE, dH, d_in, nullptr, nullptr, nullptr,
+                  nullptr, 0, dev_err, s);
+}
