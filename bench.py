@@ -395,6 +395,152 @@ def run_ours(args, w):
         torch.distributed.destroy_process_group()
 
 
+def _timed(fn, iters, flush):
+    """Average device ms of fn() over `iters` calls, L2 flushed before each."""
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(iters)]
+    for a, b in evs:
+        flush.fill_(1)
+        a.record()
+        fn()
+        b.record()
+    torch.cuda.synchronize()
+    return sum(a.elapsed_time(b) for a, b in evs) / iters
+
+
+def run_gat(args, w):
+    """GAT layer forward+backward (Tango Fig. 1a/1b) on one GPU."""
+    import quantized_gnn_message_gb300 as q
+    from quantized_gnn_message_gb300.build import build
+    build()
+    q.lib()
+    dev = torch.device("cuda", 0)
+    g = w.make_graph(device=dev)
+    d_in, heads, f = w.widths
+    d = heads * f
+    G = q.graph_prepare(g.rowptr, g.col)
+    H = synth.normal_matrix(g.n, d_in, seed=w.seed, device=dev)
+    Wt = synth.glorot(d_in, d, seed=w.seed + 1, device=dev)
+    a_s = synth.glorot(heads, f, seed=w.seed + 2, device=dev)
+    a_d = synth.glorot(heads, f, seed=w.seed + 3, device=dev)
+    dOut = synth.normal_matrix(g.n, d, seed=w.seed, tag=synth.TAG_GRAD, device=dev)
+    bits = w.bits[0]
+    L = q.GATLayer(G, d_in, heads, f, 0.2, bits, None)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    fwd = lambda: L.forward(H, Wt, a_s, a_d, 1)
+    bwd = lambda: L.backward(dOut, H, Wt, a_s, a_d, 2)
+    for _ in range(args.warmup):
+        fwd()
+        bwd()
+    with ClockSampler(0) as clocks:
+        t_f = _timed(fwd, args.steps, flush)
+        t_b = _timed(bwd, args.steps, flush)
+    # dominant edge kernels alone, same inputs
+    t_sm = _timed(lambda: q.sddmm_edge_softmax(G, L.S, L.D), args.steps, flush)
+    out = torch.empty(g.n, d, device=dev)
+    t_sp = _timed(lambda: q.edge_spmm(G, L.alpha, L.Hp, None, None, d, 32, out=out), args.steps, flush)
+    E, n = g.nnz, g.n
+    sm_bytes = (n + 1) * 4 + E * 4 + 2 * n * heads * 4 + E * heads * 4
+    sp_bytes = (n + 1) * 4 + E * 4 + E * heads * 4 + n * d * 4 * 2
+    peaks, kind = measured_peaks()
+    peak = float(peaks.get("hbm_gbs", FALLBACK_HBM_GBS))
+    step_ms = t_f + t_b
+    line = {"metric": METRIC, "value": E / (step_ms / 1e3), "unit": UNIT, "n_gpus": 1, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": step_ms, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f32 accumulate; bf16 tensor-core GEMM inputs", "data": "synthetic",
+            "config": {"workload": w.name, "nodes": n, "edges": E, "d_in": d_in, "heads": heads, "f": f,
+                       "bits": bits, "l2": "flushed before every timed call"},
+            "stages_ms": {"layer_fwd": t_f, "layer_bwd": t_b, "edge_softmax": t_sm, "edge_spmm": t_sp},
+            "kernels_gbs": {"edge_softmax": sm_bytes / (t_sm / 1e3) / 1e9,
+                            "edge_spmm": sp_bytes / (t_sp / 1e3) / 1e9},
+            "roofline": {"kernel": "edge_spmm_kernel (multi-head aggregation)", "bound": "hbm",
+                         "achieved": sp_bytes / (t_sp / 1e3) / 1e9, "peak": peak, "unit": "GB/s",
+                         "frac": sp_bytes / (t_sp / 1e3) / 1e9 / peak, "peak_source": f"hbm_gbs of {kind}",
+                         "traffic": None, "algorithmic_bytes_per_launch": sp_bytes, "avg_launch_ms": t_sp}}
+    cs = clocks.summary()
+    if cs is not None:
+        line["clocks"] = cs
+    print(json.dumps(line), flush=True)
+
+
+def run_aggregate(args, w):
+    """Quantize + de-quantizing aggregation forward + transposed, alone, over
+    a sweep of widths and bit-widths (all nodes marginal)."""
+    import quantized_gnn_message_gb300 as q
+    from quantized_gnn_message_gb300.build import build
+    build()
+    q.lib()
+    dev = torch.device("cuda", 0)
+    if args.graph_scale is not None:
+        import dataclasses
+        S = args.graph_scale
+        w = dataclasses.replace(w, name=f"aggregate-rmat{S}",
+                                graph=dict(kind="rmat", scale=S, n=1 << S, n_draws=32 << S))
+    t0 = time.perf_counter()
+    g = w.make_graph(device=dev)
+    t_gen = time.perf_counter() - t0
+    t0 = time.perf_counter()
+    G = q.graph_prepare(g.rowptr, g.col)
+    torch.cuda.synchronize()
+    t_prep = time.perf_counter() - t0
+    ds = [int(x) for x in args.sweep_d.split(",")] if args.sweep_d else list(w.sweep_d)
+    bl = [int(x) for x in args.sweep_bits.split(",")] if args.sweep_bits else list(w.bits)
+    dmax = max(ds)
+    X = synth.normal_matrix(g.n, dmax, seed=w.seed, device=dev)
+    Y = torch.empty(g.n * dmax, dtype=torch.float32, device=dev)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    E, n = g.nnz, g.n
+    peaks, kind = measured_peaks()
+    peak = float(peaks.get("hbm_gbs", FALLBACK_HBM_GBS))
+    L = q.lib()
+    rows = []
+    tot_edges, tot_ms = 0, 0.0
+    best = None
+    with ClockSampler(0) as clocks:
+        for d in ds:
+            Xd = X[:, :d]
+            Yd = Y[:n * d].view(n, d)
+            for b in bl:
+                pk = torch.empty(n, q.packed_pitch(d, b), dtype=torch.uint8, device=dev)
+                qz = lambda: q.quantize_pack(Xd, None, b, 7, out=pk)
+                fw = lambda: q.dequant_spmm(G, None, pk, None, d, b, out=Yd)
+                bw = lambda: q.dequant_spmm(G, None, pk, None, d, b, transpose=True, out=Yd)
+                for _ in range(args.warmup):
+                    qz(); fw(); bw()
+                tq = _timed(qz, args.steps, flush)
+                tf = _timed(fw, args.steps, flush)
+                tb = _timed(bw, args.steps, flush)
+                pitch = q.packed_pitch(d, b)
+                comp = (n + 1) * 4 + E * 4 + 2 * n * 4 + n * pitch + n * d * 4
+                stream = (n + 1) * 4 + E * 8 + n * 4 + E * pitch + n * d * 4
+                qbytes = n * d * 4 + n * pitch
+                r = {"d": d, "bits": b, "quantize_ms": tq, "fwd_ms": tf, "bwd_ms": tb,
+                     "quantize_gbs": qbytes / (tq / 1e3) / 1e9,
+                     "fwd_gbs_compulsory": comp / (tf / 1e3) / 1e9, "bwd_gbs_compulsory": comp / (tb / 1e3) / 1e9,
+                     "fwd_gbs_streaming": stream / (tf / 1e3) / 1e9, "bwd_gbs_streaming": stream / (tb / 1e3) / 1e9,
+                     "edges_per_s_fwd": E / (tf / 1e3)}
+                rows.append(r)
+                tot_edges += 2 * E
+                tot_ms += tf + tb
+                if best is None or r["fwd_gbs_compulsory"] > best["fwd_gbs_compulsory"]:
+                    best = r
+                del pk
+    line = {"metric": METRIC, "value": tot_edges / (tot_ms / 1e3), "unit": UNIT, "n_gpus": 1,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": tot_ms, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f32 accumulate; 2/4/8-bit message codes",
+            "data": "synthetic",
+            "config": {"workload": w.name, "nodes": n, "edges": E, "sweep_d": ds, "bits": bl,
+                       "generation_s": t_gen, "prepare_s": t_prep, "l2": "flushed before every timed call"},
+            "sweep": rows,
+            "roofline": {"kernel": "spmm_kernel forward (best of sweep)", "bound": "hbm",
+                         "achieved": best["fwd_gbs_compulsory"], "peak": peak, "unit": "GB/s",
+                         "frac": best["fwd_gbs_compulsory"] / peak, "peak_source": f"hbm_gbs of {kind}",
+                         "traffic": None, "at": {"d": best["d"], "bits": best["bits"]}}}
+    cs = clocks.summary()
+    if cs is not None:
+        line["clocks"] = cs
+    print(json.dumps(line), flush=True)
+
+
 def load_traffic(workload):
     """DRAM traffic per launch of the aggregation kernel from the committed
     ncu summary, if it was taken on the kernel source as it is now."""
@@ -417,17 +563,28 @@ def main():
     ap.add_argument("--steps", type=int, default=10)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--workload", default=GCN3_RMAT17.name, choices=[k for k, v in BY_NAME.items()
-                                                                      if v.kind == "gcn"])
+    ap.add_argument("--workload", default=GCN3_RMAT17.name, choices=list(BY_NAME))
+    ap.add_argument("--sweep-d", default=None, help="aggregate workload: comma-separated widths")
+    ap.add_argument("--sweep-bits", default=None, help="aggregate workload: comma-separated bit-widths")
+    ap.add_argument("--graph-scale", type=int, default=None,
+                    help="aggregate workload: R-MAT scale S (2^S nodes, 32 draws per node) for smaller cases")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
     w = BY_NAME[args.workload]
     if args.impl == "reference":
         ws, rank, _ = dist_env()
         if rank == 0:
-            run_reference(args, w)
+            if w.kind != "gcn":
+                print(json.dumps({"impl": "reference", "unavailable": "the oracle sample covers the GCN workloads"}))
+            else:
+                run_reference(args, w)
         return
-    run_ours(args, w)
+    if w.kind == "gat":
+        run_gat(args, w)
+    elif w.kind == "aggregate":
+        run_aggregate(args, w)
+    else:
+        run_ours(args, w)
 
 
 if __name__ == "__main__":
