@@ -156,6 +156,11 @@ typedef struct gq_sched {
   int64_t n_tasks;
   int64_t n_groups;
   int64_t n_slots;          /* partial-row slots over all groups          */
+  const int32_t* light;     /* n_light x {row_begin, row_end}: runs of
+                               consecutive light rows with at most
+                               light_edges edges in all (heavy rows never
+                               inside), covering every light row once     */
+  int64_t n_light;
 } gq_sched;
 
 typedef struct gq_graph {
@@ -237,7 +242,7 @@ GQ_API int gq_dequant_spmm(const gq_graph* g, int transpose, int coef, const flo
  * with F = d / heads; edge e is the CSR edge id (alpha is E x heads fp32,
  * row-major, indexed by CSR edge id in both directions).
  * Errors: as gq_dequant_spmm, plus GQ_ERR_INVALID_ARG when heads does not
- * divide d and GQ_ERR_UNSUPPORTED unless F is a power of two >= 8.
+ * divide d and GQ_ERR_UNSUPPORTED unless F is a power of two >= 16.
  * Workspace: as gq_dequant_spmm.                                          */
 GQ_API int gq_edge_spmm(const gq_graph* g, int transpose, const float* alpha, int heads, const float* X,
                  int64_t ldx, const uint8_t* packed, const uint8_t* mask, int d, int bits,

@@ -33,7 +33,8 @@ class GQError(RuntimeError):
 class Sched_t(ctypes.Structure):
     """Mirror of the C struct gq_sched."""
     _fields_ = [("tasks", ctypes.c_void_p), ("groups", ctypes.c_void_p), ("n_tasks", ctypes.c_int64),
-                ("n_groups", ctypes.c_int64), ("n_slots", ctypes.c_int64)]
+                ("n_groups", ctypes.c_int64), ("n_slots", ctypes.c_int64), ("light", ctypes.c_void_p),
+                ("n_light", ctypes.c_int64)]
 
 
 class Graph_t(ctypes.Structure):

@@ -21,6 +21,7 @@ constexpr int kDefaultHub = 256;
 constexpr int kDefaultSplit = 4096;
 constexpr int kMinHub = 32;
 constexpr int kMinSplit = 256;
+constexpr int kLightEdges = 256;  // edge budget of one light-row run
 constexpr int kScanThreads = 512;
 constexpr int kScanItems = 8;
 constexpr int kScanTile = kScanThreads * kScanItems;  // 4096
@@ -265,9 +266,16 @@ __global__ void gather_rows_kernel(int64_t nnz, const int32_t* __restrict__ perm
 int64_t max_tasks(int64_t nnz) { return nnz / kMinHub + nnz / kMinSplit + 2; }
 int64_t max_groups(int64_t nnz) { return nnz / kMinSplit + 1; }
 int64_t max_hubs(int64_t nnz) { return nnz / kMinHub + 1; }
+// runs end at a budget (each run but the last of a stretch holds more than
+// half a budget of edges) or at a heavy row
+int64_t max_light(int64_t n, int64_t nnz) {
+  const int64_t b = 2 * nnz / kLightEdges + max_hubs(nnz) + 2;
+  return b < n + 1 ? b : n + 1;
+}
 
 struct StorageLayout {
-  size_t tr_rowptr, tr_col, tr_perm, dinv_in, dinv_out, inv_in, tasks, groups, tr_tasks, tr_groups, total;
+  size_t tr_rowptr, tr_col, tr_perm, dinv_in, dinv_out, inv_in, tasks, groups, tr_tasks, tr_groups, light, tr_light,
+      total;
 };
 
 StorageLayout storage_layout(int64_t n, int64_t nnz) {
@@ -283,6 +291,8 @@ StorageLayout storage_layout(int64_t n, int64_t nnz) {
   L.groups = o;    o += align256(sizeof(int32_t) * 4 * max_groups(nnz));
   L.tr_tasks = o;  o += align256(sizeof(int32_t) * 4 * max_tasks(nnz));
   L.tr_groups = o; o += align256(sizeof(int32_t) * 4 * max_groups(nnz));
+  L.light = o;     o += align256(sizeof(int32_t) * 2 * max_light(n, nnz));
+  L.tr_light = o;  o += align256(sizeof(int32_t) * 2 * max_light(n, nnz));
   L.total = o;
   return L;
 }
@@ -314,6 +324,38 @@ WsLayout ws_layout(int64_t n, int64_t nnz) {
 }
 
 unsigned blocks_for(int64_t n, int t) { return (unsigned)((n + t - 1) / t); }
+
+// Runs of consecutive light rows (degree <= threshold) with at most
+// kLightEdges edges each (a run holds at least one row); heavy rows end a
+// run and belong to none.
+int build_light(const std::vector<int32_t>& ptr, int64_t n, int thr, int32_t* d_light, gq_sched* out,
+                std::vector<int32_t>& runs, int64_t cap, cudaStream_t s) {
+  runs.clear();
+  int64_t start = -1, edges = 0;
+  for (int64_t r = 0; r < n; ++r) {
+    const int64_t deg = (int64_t)ptr[r + 1] - ptr[r];
+    if (deg > thr) {
+      if (start >= 0) runs.insert(runs.end(), {(int32_t)start, (int32_t)r});
+      start = -1;
+      edges = 0;
+      continue;
+    }
+    if (start >= 0 && edges + deg > kLightEdges) {
+      runs.insert(runs.end(), {(int32_t)start, (int32_t)r});
+      start = -1;
+      edges = 0;
+    }
+    if (start < 0) start = r;
+    edges += deg;
+  }
+  if (start >= 0) runs.insert(runs.end(), {(int32_t)start, (int32_t)n});
+  if ((int64_t)(runs.size() / 2) > cap) return GQ_ERR_BAD_GRAPH;
+  out->light = d_light;
+  out->n_light = (int64_t)(runs.size() / 2);
+  if (!runs.empty())
+    GQ_TRY_CUDA(cudaMemcpyAsync(d_light, runs.data(), runs.size() * 4, cudaMemcpyHostToDevice, s));
+  return GQ_OK;
+}
 
 // Cut the heavy rows {row, e_begin, deg} into block tasks, heaviest first.
 int build_sched(const std::vector<int32_t>& hubs, int split, int32_t* d_tasks, int32_t* d_groups, gq_sched* out,
@@ -469,6 +511,15 @@ extern "C" int gq_graph_prepare(int64_t n, int64_t nnz, const int32_t* rowptr, c
                      reinterpret_cast<int32_t*>(st + SL.groups), &G.sched, tasks, groups, s));
   GQ_TRY(build_sched(thv, split_edges, reinterpret_cast<int32_t*>(st + SL.tr_tasks),
                      reinterpret_cast<int32_t*>(st + SL.tr_groups), &G.tr_sched, tr_tasks, tr_groups, s));
+  // light-row runs of both directions (row pointers read back once)
+  std::vector<int32_t> hptr((size_t)n + 1), htr((size_t)n + 1), runs, tr_runs;
+  GQ_TRY_CUDA(cudaMemcpyAsync(hptr.data(), rowptr, (n + 1) * 4, cudaMemcpyDeviceToHost, s));
+  GQ_TRY_CUDA(cudaMemcpyAsync(htr.data(), G.tr_rowptr, (n + 1) * 4, cudaMemcpyDeviceToHost, s));
+  GQ_TRY_CUDA(cudaStreamSynchronize(s));
+  GQ_TRY(build_light(hptr, n, hub_threshold, reinterpret_cast<int32_t*>(st + SL.light), &G.sched, runs,
+                     max_light(n, nnz), s));
+  GQ_TRY(build_light(htr, n, hub_threshold, reinterpret_cast<int32_t*>(st + SL.tr_light), &G.tr_sched, tr_runs,
+                     max_light(n, nnz), s));
   GQ_TRY_CUDA(cudaStreamSynchronize(s));  // host task vectors must outlive the copies
   G.max_deg = h.max_deg;
   G.tr_max_deg = h.tr_max_deg;

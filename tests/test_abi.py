@@ -43,7 +43,7 @@ def test_library_exports_every_declared_symbol(q):
 def test_graph_struct_mirror(q):
     import ctypes as C
     assert q.lib().gq_graph_struct_bytes() == C.sizeof(q.Graph_t)
-    assert C.sizeof(q.Sched_t) == 40
+    assert C.sizeof(q.Sched_t) == 56
 
 
 def test_packed_sizes_match_layout(q, orc):

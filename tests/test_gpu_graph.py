@@ -10,7 +10,7 @@ from gpu_helpers import gq, rmat_small, hub_graph
 pytestmark = pytest.mark.gpu
 
 
-def _check_sched(tasks, groups, ptr, thr, split):
+def _check_sched(tasks, groups, ptr, thr, split, light=None):
     """Tasks cover exactly the edges of the rows heavier than thr, in pieces
     of at most `split` edges, heaviest rows first; split rows form groups."""
     deg = np.diff(ptr)
@@ -32,6 +32,15 @@ def _check_sched(tasks, groups, ptr, thr, split):
             gr, first, cnt, _ = groups[gi]
             assert gr == r and cnt == len(pieces) and [p[3] for p in pieces] == list(range(first, first + cnt))
     first_task_deg = [deg[cover_r] for cover_r in [t[0] for t in tasks]]
+    # light runs: consecutive light rows, every light row exactly once,
+    # at most 256 edges per run unless the run is a single row
+    if light is not None:
+        seen = np.zeros(len(ptr) - 1, np.int32)
+        for rb, re in light:
+            assert rb < re and np.all(deg[rb:re] <= thr)
+            assert ptr[re] - ptr[rb] <= 256 or re - rb == 1
+            seen[rb:re] += 1
+        np.testing.assert_array_equal(seen, (deg <= thr).astype(np.int32))
     assert all(first_task_deg[i] >= first_task_deg[i + 1] for i in range(len(first_task_deg) - 1))
     slots = [gr[3] for gr in groups]
     assert slots == list(np.cumsum([0] + [gr[2] for gr in groups])[:-1])
@@ -57,7 +66,10 @@ def _check(orc, g, hub_threshold=0, split_edges=0):
     thr, split = G.c.hub_threshold, G.c.split_edges
     for tr, ptr in ((False, rowptr), (True, np.concatenate([[0], np.cumsum(cnt)]))):
         tasks, groups = (x.cpu().numpy() for x in G.sched_arrays(tr))
-        _check_sched(tasks, groups, ptr, thr, split)
+        sc = G.c.tr_sched if tr else G.c.sched
+        off = sc.light - G.storage.data_ptr()
+        light = G.storage[off:off + sc.n_light * 8].view(torch.int32).view(-1, 2).cpu().numpy()
+        _check_sched(tasks, groups, ptr, thr, split, light)
     assert G.c.max_deg == np.diff(rowptr).max() and G.c.tr_max_deg == cnt.max()
     return G
 
