@@ -530,24 +530,63 @@ __global__ void __launch_bounds__(kSpmmThreads) spmm_kernel(const SpmmParams p) 
 
 
 // ---------------------------------------------------------------------------
-// Asynchronous-copy aggregation (coefficient modes, d <= 512).
+// Asynchronous-copy aggregation (coefficient modes, d <= 512, every message
+// row of one kind: all packed, or all fp32).
 //
-// Every message row a group needs is copied into a per-group ring of
-// shared memory with cp.async (16-byte pieces spread over the group's
-// lanes, the coefficient as one 4-byte copy), kAS steps of U edges deep,
-// and consumed kAS - 1 steps later.  In-flight data lives in shared memory,
-// not registers, so each SM keeps ~100 KB of gathers in flight at full
-// occupancy.  Work units: heavy-row block tasks (each group streams a
-// contiguous slice of the row) and runs of light rows (one group each,
-// rows retired edge by edge as they are consumed).
+// A group of LG lanes walks a stream of edges (a slice of a heavy task, or
+// one of the schedule's runs of consecutive light rows).  The message row of
+// each edge is copied into the group's shared-memory ring with cp.async in
+// contiguous 16-byte pieces spread over the lanes (a packed row whole,
+// payload and {S, Z} together; an fp32 row as the pieces each lane will
+// read), kAS - 1 steps of U edges ahead of the step being consumed.  Column
+// ids are loaded two steps ahead and coefficients at issue time, into
+// register rings indexed by the unrolled stage number.
+//
+// Packed rows: lane j owns columns [16 j, 16 j + 16) and reads its payload
+// slice and the (broadcast) header from the slot.  De-quantization is
+// folded into the accumulation:
+//   a (q S + Z) = (a S)(q - c) + a (Z + c S),   c = 2^(b-1),
+// so the per-edge term a (Z + c S) is summed once per lane.  The code q sits
+// in the low mantissa bits of a float with exponent 2^23 (a byte permute for
+// b = 8; a bit mask at offset o for b = 2, 4, giving 2^23 + q 2^o); one
+// subtraction leaves (q - c) 2^o exactly, and the FMA takes a S 2^-o, so
+// the product a S (q - c) is the same exact product as without the offset.
+// fp32 rows: lane j owns the 4-column pieces j, j + LG, j + 2 LG, j + 3 LG.
+// Pairs of columns go through the two-lane fp32 add and FMA of sm_100-class
+// GPUs; each lane of those is an ordinary round-to-nearest fp32 operation.
 // ---------------------------------------------------------------------------
 constexpr int kAS = 4;  // pipeline stages
 
+typedef unsigned long long f32x2;
+
+__device__ __forceinline__ f32x2 f2_pack(float lo, float hi) {
+  f32x2 r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+__device__ __forceinline__ float2 f2_unpack(f32x2 v) {
+  float2 r;
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(r.x), "=f"(r.y) : "l"(v));
+  return r;
+}
+__device__ __forceinline__ f32x2 f2_fma(f32x2 a, f32x2 b, f32x2 c) {
+  f32x2 d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+__device__ __forceinline__ f32x2 f2_add(f32x2 a, f32x2 b) {
+  f32x2 d;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ f32x2 f2_mul(f32x2 a, f32x2 b) {
+  f32x2 d;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+
 __device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
-}
-__device__ __forceinline__ void cp_async4(uint32_t dst, const void* src) {
-  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(dst), "l"(src) : "memory");
 }
 __device__ __forceinline__ void cp_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 template <int N>
@@ -556,124 +595,210 @@ __device__ __forceinline__ void cp_wait() {
 }
 __device__ __forceinline__ uint32_t sm_addr(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
 
-// Bytes of one edge slot and of one group's ring.
-__host__ __device__ inline int async_slot(int d, int bits, bool mixed) {
-  int b = bits < 32 ? (int)packed_pitch(d, bits) : 4 * d;
-  if (mixed && 4 * d > b) b = 4 * d;
-  return (b + 15) / 16 * 16;
-}
-__host__ __device__ inline int async_ring(int slot, int U) { return kAS * U * slot + ((kAS * U * 5 + 15) / 16) * 16; }
+// 16-byte pieces a lane copies per packed row: a row of d <= 16 LG columns
+// has at most LG + 1 pieces at b = 8 and at most LG at b = 2, 4.
+template <int BITS>
+constexpr int kPiecesPerLane = BITS == 8 ? 2 : 1;
 
-template <int BITS, bool MIXED>
-__device__ __forceinline__ void adecode(const SpmmParams& p, const uint8_t* sl, bool quant, float coef, int c0,
-                                        float (&acc)[kLC], float& accz) {
-  if (BITS < 32 && (!MIXED || quant)) {
-    LMsg<BITS, true> m;
-    m.quant = true;
-    m.h = *reinterpret_cast<const float2*>(sl + p.hoff);
-    const uint8_t* pl = sl + c0 * BITS / 8;
+// Bytes of one edge slot: the largest row of the width bucket (d <= 16 LG),
+// a packed row (payload rounded to 8 bytes, {S, Z}, rounded to 16) or an
+// fp32 row.  A compile-time stride keeps every slot address an immediate
+// offset from the group's ring.
+template <int BITS, int LG>
+constexpr int kSlot = BITS < 32 ? ((2 * BITS * LG + 7) / 8 * 8 + 8 + 15) / 16 * 16 : 64 * LG;
+
+constexpr uint32_t kMagicBits = 0x4B000000u;  // 2^23 as fp32
+constexpr float kMagic = 8388608.0f;
+
+// The loop-invariant pair -(2^23 + c), c = 2^(b-1), for the subtraction.
+template <int BITS>
+__device__ __forceinline__ f32x2 a_bias() {
+  constexpr float c = (float)(1 << (BITS < 32 ? BITS - 1 : 0));
+  return f2_pack(-(kMagic + c), -(kMagic + c));
+}
+
+// The lane's place in its group's ring and in the row.
+template <int LG>
+struct ALane {
+  const uint8_t* ring;  // group ring, for reading
+  uint32_t sring;       // the same, shared-space address
+  unsigned gmask;       // lanes of the group
+  int gl;
+  bool has0, has1;      // packed rows: pieces gl and gl + LG exist
+  int c0;               // packed rows: first of the lane's 16 columns
+  bool on;              // the lane owns at least one column
+  int nv;               // fp32 rows: pieces gl + LG k, k < nv, are in range
+  const uint8_t* src;   // the lane's first piece in message row 0
+  uint32_t stride;      // bytes between message rows
+};
+
+// Column of accumulator entry i (acc[i / 2], half i % 2) of this lane.
+template <int BITS, int LG>
+__device__ __forceinline__ int a_col(const ALane<LG>& L, int i) {
+  if constexpr (BITS < 32) return L.c0 + i;
+  else return 4 * (L.gl + LG * (i >> 2)) + (i & 3);
+}
+
+// Accumulate one edge from its slot sl with coefficient cf.
+template <int BITS, int LG>
+__device__ __forceinline__ void a_consume(const SpmmParams& p, const ALane<LG>& L, const uint8_t* sl, float cf,
+                                          f32x2 bias, f32x2 (&acc)[8], float& accz) {
+  if constexpr (BITS < 32) {
+    constexpr float c = (float)(1 << (BITS - 1));
+    const float2 h = *reinterpret_cast<const float2*>(sl + p.hoff);
+    const float cs = cf * h.x;
+    accz = __fmaf_rn(cf, __fmaf_rn(c, h.x, h.y), accz);
+    const f32x2 cs2 = f2_pack(cs, cs);
+    const uint8_t* pl = sl + L.gl * (2 * BITS);
+    // the lane's 16 codes spread one per byte over four words, in column
+    // order: byte a of sp[k] is code 4 a + k (b = 2), byte a of sp[2 h + k]
+    // is code 8 h + 2 a + k (b = 4), byte a of sp[k] is code 4 k + a (b = 8)
+    uint32_t sp[4];
     if constexpr (BITS == 8) {
       const uint4 t = *reinterpret_cast<const uint4*>(pl);
-      m.w[0] = t.x; m.w[1] = t.y; m.w[2] = t.z; m.w[3] = t.w;
+      sp[0] = t.x; sp[1] = t.y; sp[2] = t.z; sp[3] = t.w;
     } else if constexpr (BITS == 4) {
       const uint2 t = *reinterpret_cast<const uint2*>(pl);
-      m.w[0] = t.x; m.w[1] = t.y;
-    } else if constexpr (BITS == 2) {
-      m.w[0] = *reinterpret_cast<const uint32_t*>(pl);
+      sp[0] = t.x & 0x0F0F0F0Fu; sp[1] = (t.x >> 4) & 0x0F0F0F0Fu;
+      sp[2] = t.y & 0x0F0F0F0Fu; sp[3] = (t.y >> 4) & 0x0F0F0F0Fu;
+    } else {
+      const uint32_t t = *reinterpret_cast<const uint32_t*>(pl);
+      sp[0] = t & 0x03030303u; sp[1] = (t >> 2) & 0x03030303u;
+      sp[2] = (t >> 4) & 0x03030303u; sp[3] = (t >> 6) & 0x03030303u;
     }
-    lconsume<BITS, true>(m, coef, acc, accz);
-  } else {
-    const float* xr = reinterpret_cast<const float*>(sl) + c0;
 #pragma unroll
-    for (int k = 0; k < kLC; k += 4) {
-      if (c0 + k < p.d) {
-        const float4 a = *reinterpret_cast<const float4*>(xr + k);
-        acc[k] = __fmaf_rn(coef, a.x, acc[k]);
-        acc[k + 1] = __fmaf_rn(coef, a.y, acc[k + 1]);
-        acc[k + 2] = __fmaf_rn(coef, a.z, acc[k + 2]);
-        acc[k + 3] = __fmaf_rn(coef, a.w, acc[k + 3]);
+    for (int i = 0; i < 8; ++i) {
+      // columns 2i, 2i + 1: (word, byte) of each
+      int w0, b0, w1, b1;
+      if constexpr (BITS == 8) { w0 = i >> 1; b0 = (2 * i) & 3; w1 = w0; b1 = b0 + 1; }
+      else if constexpr (BITS == 4) { w0 = 2 * (i >> 2); b0 = i & 3; w1 = w0 + 1; b1 = b0; }
+      else { w0 = 2 * (i & 1); b0 = i >> 1; w1 = w0 + 1; b1 = b0; }
+      const f32x2 v = f2_pack(__uint_as_float(__byte_perm(sp[w0], kMagicBits, 0x7540u | b0)),
+                              __uint_as_float(__byte_perm(sp[w1], kMagicBits, 0x7540u | b1)));
+      acc[i] = f2_fma(cs2, f2_add(v, bias), acc[i]);
+    }
+  } else {
+    const f32x2 c2 = f2_pack(cf, cf);
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      if (k < L.nv) {
+        const f32x2* xr = reinterpret_cast<const f32x2*>(sl + 16 * (L.gl + LG * k));
+        acc[2 * k] = f2_fma(c2, xr[0], acc[2 * k]);
+        acc[2 * k + 1] = f2_fma(c2, xr[1], acc[2 * k + 1]);
       }
     }
   }
 }
 
-// Stream edges [eb, ee) through the group's ring.  LIGHT: the edges are
-// those of rows [row0, row1) and each row is written when its last edge
-// has been consumed; otherwise they all belong to one row and the sums are
-// left in acc / accz.
-template <int BITS, int LG, bool MIXED, int U, bool LIGHT>
-__device__ __forceinline__ void async_stream(const SpmmParams& p, uint8_t* ring, int slot, unsigned gmask, int gl,
-                                             int c0, int64_t eb, int64_t ee, int64_t row0, int64_t row1,
-                                             float (&acc)[kLC], float& accz) {
-  float* coefs = reinterpret_cast<float*>(ring + kAS * U * slot);
-  uint8_t* flags = reinterpret_cast<uint8_t*>(coefs + kAS * U);
-  const int64_t nsteps = (ee - eb + U - 1) / U;
-  const int chunks_q = (int)(p.pitch / 16);
-  const int chunks_x = p.d / 4;
-  int32_t cx[U], nx[U];
-  bool cq[U];
+// Write the lane's columns of row r: (acc + accz) * rs.
+template <int BITS, int LG>
+__device__ __forceinline__ void a_flush(const SpmmParams& p, const ALane<LG>& L, int64_t r, float rs,
+                                        const f32x2 (&acc)[8], float accz) {
+  float o[16];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const float2 v = f2_unpack(acc[i]);
+    o[2 * i] = (v.x + accz) * rs;
+    o[2 * i + 1] = (v.y + accz) * rs;
+  }
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const int col = a_col<BITS, LG>(L, 4 * k);
+    if (col < p.d) {
+      if (p.Yb != nullptr)
+        *reinterpret_cast<uint2*>(p.Yb + r * p.ldy + col) =
+            make_uint2(pack_bf16x2(o[4 * k], o[4 * k + 1]), pack_bf16x2(o[4 * k + 2], o[4 * k + 3]));
+      else
+        st_f4(p.Y + r * p.ldy + col, o[4 * k], o[4 * k + 1], o[4 * k + 2], o[4 * k + 3]);
+    }
+  }
+}
+
+// Stream the edges [eb, eb + n) through the group's ring.  LIGHT: they are
+// the edges of rows [row0, row1) and each row is written once its last edge
+// has been consumed; otherwise the sums are left in acc / accz.
+template <int BITS, int LG, int U, bool LIGHT>
+__device__ __forceinline__ void a_stream(const SpmmParams& p, const ALane<LG>& L, f32x2 bias, int eb, int n,
+                                         int row0, int row1, f32x2 (&acc)[8], float& accz) {
+  const float* __restrict__ colscale = p.colscale;
+  const int nsteps = (n + U - 1) / U;
+  uint32_t cx[kAS][U];
+  float cf[kAS][U];
+  // column ids two steps ahead: cp points at edge 2 U of the current step,
+  // rem counts the edges from there to the end of the stream
+  const int32_t* __restrict__ cp = p.col + eb;
 #pragma unroll
   for (int t = 0; t < U; ++t) {
-    cx[t] = (eb + t < ee) ? __ldg(p.col + eb + t) : 0;
-    cq[t] = BITS < 32 && (!MIXED || (p.mask == nullptr || __ldg(p.mask + cx[t]) != 0));
-    nx[t] = (eb + U + t < ee) ? __ldg(p.col + eb + U + t) : 0;
+    cx[0][t] = t < n ? (uint32_t)__ldg(cp + t) : 0u;
+    cx[1][t] = U + t < n ? (uint32_t)__ldg(cp + U + t) : 0u;
   }
-  int64_t row = row0, re = LIGHT ? __ldg(p.rowptr + row0 + 1) : 0;
-  for (int64_t s = 0; s < nsteps + kAS - 1; ++s) {
-    __syncwarp(gmask);  // the slots refilled below have been consumed
-    if (s < nsteps) {
-      const int st = (int)(s % kAS);
+  cp += 2 * U;
+  int rem = n - 2 * U;
+  // light rows: end of the current row and of the next (relative to eb),
+  // and their output scales, one row ahead
+  int row = row0;
+  int rend = 0, rnext = 0;
+  float rs = 1.0f, rsn = 1.0f;
+  if (LIGHT) {
+    rend = __ldg(p.rowptr + row0 + 1) - eb;
+    rnext = row0 + 2 <= row1 ? __ldg(p.rowptr + row0 + 2) - eb : 0x7fffffff;
+    if (p.rowscale) {
+      rs = __ldg(p.rowscale + row0);
+      rsn = row0 + 1 < row1 ? __ldg(p.rowscale + row0 + 1) : 1.0f;
+    }
+  }
+  for (int s0 = 0; s0 < nsteps + kAS - 1; s0 += kAS) {
 #pragma unroll
-      for (int t = 0; t < U; ++t) {
-        const int64_t e = eb + s * U + t;
-        if (e < ee) {
-          uint8_t* dst = ring + (st * U + t) * slot;
-          if (BITS < 32 && (!MIXED || cq[t])) {
-            const uint8_t* src = p.packed + (int64_t)cx[t] * p.pitch;
-            for (int k = gl; k < chunks_q; k += LG) cp_async16(sm_addr(dst + 16 * k), src + 16 * k);
-          } else {
-            const float* src = p.X + (int64_t)cx[t] * p.ldx;
-            for (int k = gl; k < chunks_x; k += LG) cp_async16(sm_addr(dst + 16 * k), src + 4 * k);
-          }
-          if (gl == 0) {
-            if (p.colscale != nullptr) cp_async4(sm_addr(coefs + st * U + t), p.colscale + cx[t]);
-            if (MIXED) flags[st * U + t] = cq[t] ? 1 : 0;
+    for (int j = 0; j < kAS; ++j) {
+      const int s = s0 + j;
+      __syncwarp(L.gmask);  // stage j was consumed in the previous step
+      if (s < nsteps) {
+#pragma unroll
+        for (int t = 0; t < U; ++t) cx[(j + 2) % kAS][t] = t < rem ? (uint32_t)__ldg(cp + t) : 0u;
+        cp += U;
+        rem -= U;
+#pragma unroll
+        for (int t = 0; t < U; ++t) {
+          if (U == 1 || t < rem + 3 * U) {  // edge s U + t exists
+            const uint32_t x = cx[j][t];
+            cf[j][t] = colscale != nullptr ? __ldg(colscale + x) : 1.0f;
+            const uint32_t dst = L.sring + (j * U + t) * kSlot<BITS, LG>;
+            const uint8_t* src = L.src + (size_t)x * L.stride;
+            if constexpr (BITS < 32) {
+              if (L.has0) cp_async16(dst + 16 * L.gl, src);
+              if (kPiecesPerLane<BITS> > 1 && L.has1) cp_async16(dst + 16 * (L.gl + LG), src + 16 * LG);
+            } else {
+#pragma unroll
+              for (int k = 0; k < 4; ++k)
+                if (k < L.nv) cp_async16(dst + 16 * (L.gl + LG * k), src + 16 * LG * k);
+            }
           }
         }
       }
-      // column ids (and mask bits) of the next step are ready; fetch the one after
+      cp_commit();
+      const int c = s - (kAS - 1);
+      if (c >= 0 && c < nsteps) {
+        cp_wait<kAS - 1>();
+        __syncwarp(L.gmask);  // every lane's pieces of the slot have landed
+        const int jc = (j + 1) % kAS;
 #pragma unroll
-      for (int t = 0; t < U; ++t) {
-        cx[t] = nx[t];
-        const int64_t e1 = eb + (s + 1) * U + t, e2 = eb + (s + 2) * U + t;
-        cq[t] = BITS < 32 && (!MIXED || (e1 < ee && (p.mask == nullptr || __ldg(p.mask + cx[t]) != 0)));
-        nx[t] = (e2 < ee) ? __ldg(p.col + e2) : 0;
-      }
-    }
-    cp_commit();
-    if (s >= kAS - 1) {
-      const int64_t c = s - (kAS - 1);
-      cp_wait<kAS - 1>();
-      __syncwarp(gmask);
-      const int st = (int)(c % kAS);
+        for (int t = 0; t < U; ++t) {
+          const int e = c * U + t;
+          if (U == 1 || e < n) {
+            if (LIGHT) {
+              while (e >= rend) {
+                if (L.on) a_flush<BITS, LG>(p, L, row, rs, acc, accz);
 #pragma unroll
-      for (int t = 0; t < U; ++t) {
-        const int64_t e = eb + c * U + t;
-        if (e < ee) {
-          if (LIGHT) {
-            while (e >= re) {
-              lflush(p, row, c0, acc, accz);
-#pragma unroll
-              for (int k = 0; k < kLC; ++k) acc[k] = 0.0f;
-              accz = 0.0f;
-              ++row;
-              re = __ldg(p.rowptr + row + 1);
+                for (int i = 0; i < 8; ++i) acc[i] = 0ull;
+                accz = 0.0f;
+                ++row;
+                rend = rnext;
+                rnext = row + 2 <= row1 ? __ldg(p.rowptr + row + 2) - eb : 0x7fffffff;
+                rs = rsn;
+                if (p.rowscale) rsn = row + 1 < row1 ? __ldg(p.rowscale + row + 1) : 1.0f;
+              }
             }
-          }
-          if (c0 < p.d) {
-            const float coef = p.colscale != nullptr ? coefs[st * U + t] : 1.0f;
-            const bool quant = !MIXED || flags[st * U + t] != 0;
-            adecode<BITS, MIXED>(p, ring + (st * U + t) * slot, quant, coef, c0, acc, accz);
+            if (L.on) a_consume<BITS, LG>(p, L, L.ring + (jc * U + t) * kSlot<BITS, LG>, cf[jc][t], bias, acc, accz);
           }
         }
       }
@@ -681,46 +806,75 @@ __device__ __forceinline__ void async_stream(const SpmmParams& p, uint8_t* ring,
   }
   if (LIGHT) {
     for (; row < row1; ++row) {
-      lflush(p, row, c0, acc, accz);
+      if (L.on) a_flush<BITS, LG>(p, L, row, p.rowscale ? __ldg(p.rowscale + row) : 1.0f, acc, accz);
 #pragma unroll
-      for (int k = 0; k < kLC; ++k) acc[k] = 0.0f;
+      for (int i = 0; i < 8; ++i) acc[i] = 0ull;
       accz = 0.0f;
     }
   }
 }
 
-template <int BITS, int LG, bool MIXED, int U>
-__global__ void __launch_bounds__(kSpmmThreads) spmm_async_kernel(const SpmmParams p, int slot, int ring) {
+template <int BITS, int LG, int U>
+__global__ void __launch_bounds__(kSpmmThreads) spmm_async_kernel(const SpmmParams p) {
   extern __shared__ __align__(16) uint8_t asm_[];
   constexpr int NG = 32 / LG;
   const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
-  const int g = lane / LG, gl = lane % LG;
-  const unsigned gmask = (LG == 32 ? 0xffffffffu : ((1u << LG) - 1u)) << (g * LG);
-  uint8_t* myring = asm_ + (size_t)(w * NG + g) * ring;
-  const int c0 = gl * kLC;
-  float acc[kLC] = {};
+  const int g = lane / LG;
+  ALane<LG> L;
+  L.gl = lane % LG;
+  constexpr int SLOT = kSlot<BITS, LG>;
+  L.ring = asm_ + (w * NG + g) * (kAS * U * SLOT);
+  L.sring = sm_addr(L.ring);
+  L.gmask = (LG == 32 ? 0xffffffffu : ((1u << LG) - 1u)) << (g * LG);
+  const int pieces = BITS < 32 ? (int)(p.pitch / 16) : 0;
+  L.has0 = L.gl < pieces;
+  L.has1 = L.gl + LG < pieces;
+  L.c0 = 16 * L.gl;
+  if constexpr (BITS < 32) {
+    L.on = L.c0 < p.d;
+    L.nv = 0;
+    L.src = p.packed + 16 * L.gl;
+    L.stride = (uint32_t)p.pitch;
+  } else {
+    L.src = reinterpret_cast<const uint8_t*>(p.X + 4 * L.gl);
+    L.stride = (uint32_t)(p.ldx * 4);
+    const int nq = p.d / 4;  // 4-column pieces of a row
+    L.nv = L.gl < nq ? min(4, (nq - L.gl + LG - 1) / LG) : 0;
+    L.on = L.nv > 0;
+  }
+  const f32x2 bias = a_bias<BITS>();
+  f32x2 acc[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) acc[i] = 0ull;
   float accz = 0.0f;
   if ((int64_t)blockIdx.x < p.n_tasks) {
     const int4 task = __ldg(reinterpret_cast<const int4*>(p.tasks) + blockIdx.x);
     const int sid = w * NG + g;
-    const int64_t len = task.z - task.y;
-    int64_t chunk = (len + kSpmmWarps * NG - 1) / (kSpmmWarps * NG);
+    const int len = task.z - task.y;
+    int chunk = (len + kSpmmWarps * NG - 1) / (kSpmmWarps * NG);
     chunk = (chunk + U - 1) / U * U;
-    const int64_t b0 = task.y + (int64_t)sid * chunk;
-    const int64_t b1 = min(b0 + chunk, (int64_t)task.z);
-    if (b0 < b1) async_stream<BITS, LG, MIXED, U, false>(p, myring, slot, gmask, gl, c0, b0, b1, 0, 0, acc, accz);
+    const int b0 = task.y + sid * chunk;
+    const int b1 = min(b0 + chunk, task.z);
+    if (b0 < b1) a_stream<BITS, LG, U, false>(p, L, bias, b0, b1 - b0, 0, 0, acc, accz);
+    float o[16];
 #pragma unroll
-    for (int k = 0; k < kLC; ++k) acc[k] += accz;
+    for (int i = 0; i < 8; ++i) {
+      const float2 v = f2_unpack(acc[i]);
+      o[2 * i] = v.x + accz;
+      o[2 * i + 1] = v.y + accz;
+    }
 #pragma unroll
-    for (int o = LG; o < 32; o <<= 1)
+    for (int off = LG; off < 32; off <<= 1)
 #pragma unroll
-      for (int k = 0; k < kLC; ++k) acc[k] += __shfl_xor_sync(FULL, acc[k], o);
+      for (int k = 0; k < 16; ++k) o[k] += __shfl_xor_sync(FULL, o[k], off);
     __syncthreads();  // every ring is drained: reuse the space for the warp partials
     float* part = reinterpret_cast<float*>(asm_);
-    if (lane < LG && c0 < p.d)
+    if (lane < LG && L.on)
 #pragma unroll
-      for (int k = 0; k < kLC; ++k)
-        if (c0 + k < p.d) part[w * p.d + c0 + k] = acc[k];
+      for (int k = 0; k < 16; ++k) {
+        const int col = a_col<BITS, LG>(L, k);
+        if (col < p.d) part[w * p.d + col] = o[k];
+      }
     __syncthreads();
     finish_heavy(p, task, part);
     return;
@@ -729,21 +883,24 @@ __global__ void __launch_bounds__(kSpmmThreads) spmm_async_kernel(const SpmmPara
   const int64_t ngroups = ((int64_t)gridDim.x - p.n_tasks) * kSpmmWarps * NG;
   for (int64_t t = gid; t < p.n_light; t += ngroups) {
     const int2 run = __ldg(reinterpret_cast<const int2*>(p.light) + t);
-    const int64_t eb = __ldg(p.rowptr + run.x), ee = __ldg(p.rowptr + run.y);
-    async_stream<BITS, LG, MIXED, U, true>(p, myring, slot, gmask, gl, c0, eb, ee, run.x, run.y, acc, accz);
+    const int eb = __ldg(p.rowptr + run.x), ee = __ldg(p.rowptr + run.y);
+    a_stream<BITS, LG, U, true>(p, L, bias, eb, ee - eb, run.x, run.y, acc, accz);
   }
 }
 
-template <int BITS, int LG, bool MIXED, int U>
-int launch_async(SpmmParams p, cudaStream_t s) {
-  const int slot = async_slot(p.d, BITS, MIXED);
-  const int ring = async_ring(slot, U);
+template <int BITS, int LG, int U>
+int launch_async(const SpmmParams& p, cudaStream_t s) {
   constexpr int NG = 32 / LG;
-  size_t smem = (size_t)kSpmmWarps * NG * ring;
+  constexpr int SLOT = kSlot<BITS, LG>;
+  static_assert(BITS == 32 || SLOT / 16 <= kPiecesPerLane<BITS> * LG, "row pieces exceed the lanes' share");
+  if (BITS < 32 && p.pitch > SLOT) return GQ_ERR_UNSUPPORTED;
+  if (BITS == 32 && 4 * p.d > SLOT) return GQ_ERR_UNSUPPORTED;
+  size_t smem = (size_t)kSpmmWarps * NG * kAS * U * SLOT;
   const size_t part = sizeof(float) * kSpmmWarps * p.d;
   if (smem < part) smem = part;
-  auto kern = spmm_async_kernel<BITS, LG, MIXED, U>;
-  if (smem > 48 * 1024) GQ_TRY_CUDA(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem));
+  auto kern = spmm_async_kernel<BITS, LG, U>;
+  // (the kernel also holds a few bytes of static shared memory)
+  if (smem > 32 * 1024) GQ_TRY_CUDA(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem));
   int per_sm = 0;
   if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kSpmmThreads, smem) != cudaSuccess || per_sm < 1)
     return GQ_ERR_UNSUPPORTED;
@@ -753,28 +910,28 @@ int launch_async(SpmmParams p, cudaStream_t s) {
   if (light < 1) light = 1;
   const int64_t grid = p.n_tasks + light;
   if (grid > 0x7fffffff) return GQ_ERR_UNSUPPORTED;
-  kern<<<(unsigned)grid, kSpmmThreads, smem, s>>>(p, slot, ring);
+  kern<<<(unsigned)grid, kSpmmThreads, smem, s>>>(p);
   return launch_status();
 }
 
-template <int BITS, bool MIXED, int U>
+template <int BITS, int U>
 int launch_async_d(const SpmmParams& p, cudaStream_t s) {
-  if (p.d <= 16) return launch_async<BITS, 1, MIXED, U>(p, s);
-  if (p.d <= 32) return launch_async<BITS, 2, MIXED, U>(p, s);
-  if (p.d <= 64) return launch_async<BITS, 4, MIXED, U>(p, s);
-  if (p.d <= 128) return launch_async<BITS, 8, MIXED, U>(p, s);
-  if (p.d <= 256) return launch_async<BITS, 16, MIXED, U>(p, s);
-  return launch_async<BITS, 32, MIXED, U>(p, s);
+  if (p.d <= 16) return launch_async<BITS, 1, U>(p, s);
+  if (p.d <= 32) return launch_async<BITS, 2, U>(p, s);
+  if (p.d <= 64) return launch_async<BITS, 4, U>(p, s);
+  if (p.d <= 128) return launch_async<BITS, 8, U>(p, s);
+  if (p.d <= 256) return launch_async<BITS, 16, U>(p, s);
+  return launch_async<BITS, 32, U>(p, s);
 }
 
 // Coefficient-mode aggregation with d <= 512 and one kind of message row
 // (all packed, or all fp32); packed rows keep two edges per stage.
 int launch_async_any(const SpmmParams& p, int bits, cudaStream_t s) {
   switch (bits) {
-    case 2: return launch_async_d<2, false, 2>(p, s);
-    case 4: return launch_async_d<4, false, 2>(p, s);
-    case 8: return launch_async_d<8, false, 2>(p, s);
-    default: return launch_async_d<32, false, 1>(p, s);
+    case 2: return launch_async_d<2, 2>(p, s);
+    case 4: return launch_async_d<4, 2>(p, s);
+    case 8: return launch_async_d<8, 2>(p, s);
+    default: return launch_async_d<32, 1>(p, s);
   }
 }
 
@@ -887,10 +1044,11 @@ int dequant_spmm(const gq_graph* g, int transpose, int coef, const float* X, int
   } else if (coef != GQ_COEF_ONE) {
     return GQ_ERR_INVALID_ARG;
   }
-  // every message row of one kind (all packed, or all fp32): asynchronous
-  // pipeline; a mix of packed and fp32 rows (a mask): warp per light row,
+  // every message row of one kind (all packed, or all fp32; a row stride
+  // under 2^31 bytes): asynchronous pipeline; a mix of packed and fp32 rows (a mask): warp per light row,
   // whose registers hold the 1 KB fp32 rows more cheaply than 1 KB ring slots
-  if (d <= 512 && !(bits < 32 && mask != nullptr)) return launch_async_any(p, bits, s);
+  if (d <= 512 && !(bits < 32 && mask != nullptr) && (bits < 32 || ldx <= (int64_t)1 << 29))
+    return launch_async_any(p, bits, s);
   return launch_any<false>(p, bits, s);
 }
 
