@@ -1,6 +1,7 @@
 // gq_common.cuh -- shared device/host helpers of libgq (CUDA, sm_103a).
 #pragma once
 
+#include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -82,6 +83,12 @@ __device__ __forceinline__ float code_to_float(uint32_t code) {
 template <int K>
 __device__ __forceinline__ float byte_to_float(uint32_t w) {
   return __fsub_rn(__uint_as_float(__byte_perm(w, 0x4B000000u, 0x7540u | K)), 8388608.0f);
+}
+
+// Two floats as one bf16x2 word (round to nearest even), lo in the low half.
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  const __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<const uint32_t*>(&h);
 }
 
 __device__ __forceinline__ float4 ldg_f4(const float* p) { return __ldg(reinterpret_cast<const float4*>(p)); }

@@ -390,20 +390,47 @@ __global__ void wgrad_reduce_kernel(const float* __restrict__ partial, int split
 }
 
 // -------------------------------------------------------- conversions ---
-// dst[r][c] = bf16(src[r][c]) for c < cols, 0 for cols <= c < dcols.
+// dst[r][c] = bf16(src[r][c]) for c < cols, 0 for cols <= c < dcols, and
+// 0 also where gate[r][c] <= 0 (ReLU' taken from the layer output).  A
+// block covers rpb rows, tpr threads a row, each thread 4 columns at a time
+// (VEC: one 16-byte load per operand and one 8-byte store).
+template <bool VEC>
 __global__ void to_bf16_kernel(const float* __restrict__ src, int64_t rows, int cols, int64_t lds,
                                __nv_bfloat16* __restrict__ dst, int64_t ldd, int dcols,
-                               const float* __restrict__ gate, int64_t ldg) {
-  const int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-  const int64_t r = idx / dcols;
-  const int c = (int)(idx % dcols);
-  if (r >= rows) return;
-  float v = 0.0f;
-  if (c < cols) {
-    v = src[r * lds + c];
-    if (gate != nullptr && !(gate[r * ldg + c] > 0.0f)) v = 0.0f;  // ReLU' from the layer output
+                               const float* __restrict__ gate, int64_t ldg, int tpr, int rpb) {
+  const int local = (int)threadIdx.x / tpr;
+  const int64_t r = (int64_t)blockIdx.x * rpb + local;
+  if (local >= rpb || r >= rows) return;
+  for (int c = ((int)threadIdx.x - local * tpr) * 4; c < dcols; c += 4 * tpr) {
+  float v[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+  if (VEC && c + 4 <= cols) {
+    const float4 x = __ldg(reinterpret_cast<const float4*>(src + r * lds + c));
+    v[0] = x.x; v[1] = x.y; v[2] = x.z; v[3] = x.w;
+    if (gate != nullptr) {
+      const float4 gv = __ldg(reinterpret_cast<const float4*>(gate + r * ldg + c));
+      if (!(gv.x > 0.0f)) v[0] = 0.0f;
+      if (!(gv.y > 0.0f)) v[1] = 0.0f;
+      if (!(gv.z > 0.0f)) v[2] = 0.0f;
+      if (!(gv.w > 0.0f)) v[3] = 0.0f;
+    }
+  } else {
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      if (c + k < cols) {
+        v[k] = src[r * lds + c + k];
+        if (gate != nullptr && !(gate[r * ldg + c + k] > 0.0f)) v[k] = 0.0f;
+      }
+    }
   }
-  dst[r * ldd + c] = __float2bfloat16_rn(v);
+  __nv_bfloat16* d = dst + r * ldd + c;
+  if (VEC && c + 4 <= dcols) {
+    *reinterpret_cast<uint2*>(d) = make_uint2(pack_bf16x2(v[0], v[1]), pack_bf16x2(v[2], v[3]));
+  } else {
+#pragma unroll
+    for (int k = 0; k < 4; ++k)
+      if (c + k < dcols) d[k] = __float2bfloat16_rn(v[k]);
+  }
+  }
 }
 
 // dst[n][k] = bf16(W[k][n]) (transpose), zero for k >= K.
@@ -529,11 +556,18 @@ int wgrad_gemm(const void* X, int64_t R, int K1, int64_t ldx, const void* Y, int
 
 int to_bf16(const float* src, int64_t rows, int cols, int64_t lds, void* dst, int64_t ldd, int dcols,
             const float* gate, int64_t ldg, cudaStream_t s) {
-  if (rows == 0) return GQ_OK;
-  const int64_t total = rows * dcols;
-  to_bf16_kernel<<<(unsigned)((total + 255) / 256), 256, 0, s>>>(src, rows, cols, lds,
-                                                                  static_cast<__nv_bfloat16*>(dst), ldd, dcols, gate,
-                                                                  ldg);
+  if (rows == 0 || dcols == 0) return GQ_OK;
+  const int tpr = min((dcols + 3) / 4, 256);  // threads a row; wider rows loop
+  const int rpb = 256 / tpr;
+  const int64_t blocks = (rows + rpb - 1) / rpb;
+  if (blocks > 0x7fffffff) return GQ_ERR_UNSUPPORTED;
+  auto* d = static_cast<__nv_bfloat16*>(dst);
+  const bool vec = lds % 4 == 0 && ldd % 4 == 0 && aligned(src, 16) && aligned(dst, 8) &&
+                   (gate == nullptr || (ldg % 4 == 0 && aligned(gate, 16)));
+  if (vec)
+    to_bf16_kernel<true><<<(unsigned)blocks, 256, 0, s>>>(src, rows, cols, lds, d, ldd, dcols, gate, ldg, tpr, rpb);
+  else
+    to_bf16_kernel<false><<<(unsigned)blocks, 256, 0, s>>>(src, rows, cols, lds, d, ldd, dcols, gate, ldg, tpr, rpb);
   return launch_status();
 }
 

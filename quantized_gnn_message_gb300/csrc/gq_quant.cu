@@ -1,11 +1,13 @@
 // gq_quant.cu -- per-row stochastic integer quantization with bit-packing,
 // and the matching de-quantization (AdaQP Sec. 2.3, Eqn 4 and Eqn 5).
 //
-// One warp per message row.  Lane l owns the 8-column chunks c = l + 32 i
-// of the row, so each lane packs its 8 codes into one b-byte word and the
-// warp writes the payload with contiguous 2/4/8-byte stores.  Row min/max
-// are warp-shuffle reductions; the noise is a counter hash of (seed, row,
-// column), so the packed bytes do not depend on the launch shape.
+// A group of G lanes per message row (G = 32 for d > 128, fewer for
+// narrower rows, so a warp quantizes 32 / G rows at once).  Lane l of the
+// group owns the 8-column chunks c = l + G i of the row, so each lane packs
+// its 8 codes into one b-byte word and the group writes the payload with
+// contiguous 2/4/8-byte stores.  Row min/max are shuffle reductions within
+// the group; the noise is a counter hash of (seed, row, column), so the
+// packed bytes do not depend on the launch shape.
 #include "gq_common.cuh"
 #include "gq_internal.cuh"
 
@@ -62,22 +64,27 @@ __device__ __forceinline__ void store_word(uint8_t* p, uint64_t w) {
   }
 }
 
-// CPL > 0: the row stays in registers (d <= 256 * CPL).  CPL == 0: two
-// passes over global memory (second pass hits L1/L2), any d.
-template <int BITS, int CPL>
+// A row is the job of a group of G lanes (G <= 32, a power of two); a warp
+// takes 32 / G consecutive rows per iteration.  CPL > 0: the row stays in
+// registers (d <= 8 G CPL).  CPL == 0 (G = 32): two passes over global
+// memory (the second hits L1/L2), any d.
+template <int BITS, int CPL, int G>
 __global__ void __launch_bounds__(kQuantThreads) quantize_pack_kernel(
     const float* __restrict__ X, int64_t n, int d, int64_t ldx, const uint8_t* __restrict__ mask,
     uint32_t seed_key, uint8_t* __restrict__ packed, int64_t pitch, int hoff, bool vec) {
   constexpr float L = (float)((1 << BITS) - 1);
+  constexpr int NGR = 32 / G;
   const int lane = threadIdx.x & 31;
+  const int gl = lane % G;
   const int64_t warp = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
   const int nchunks = (d + 7) >> 3;
   const int p8 = nchunks * BITS;  // bytes the chunk stores cover
 
-  for (int64_t r = warp; r < n; r += nwarps) {
-    if (mask != nullptr && mask[r] == 0) continue;  // warp-uniform
-    const float* x = X + r * ldx;
+  for (int64_t r0 = warp * NGR; r0 < n; r0 += nwarps * NGR) {  // warp-uniform
+    const int64_t r = r0 + lane / G;
+    const bool act = r < n && (mask == nullptr || mask[r] != 0);  // group-uniform
+    const float* x = X + (act ? r : 0) * ldx;
     uint8_t* row = packed + r * pitch;
 
     float mn = __int_as_float(0x7f800000), mx = -__int_as_float(0x7f800000);
@@ -85,15 +92,15 @@ __global__ void __launch_bounds__(kQuantThreads) quantize_pack_kernel(
     if (CPL > 0) {
 #pragma unroll
       for (int i = 0; i < (CPL > 0 ? CPL : 1); ++i) {
-        const int c = lane + 32 * i;
-        if (c < nchunks) {
+        const int c = gl + G * i;
+        if (act && c < nchunks) {
           load_chunk(x, c, d, vec, x[0], v[i]);
 #pragma unroll
           for (int k = 0; k < 8; ++k) { mn = fminf(mn, v[i][k]); mx = fmaxf(mx, v[i][k]); }
         }
       }
-    } else {
-      for (int c = lane; c < nchunks; c += 32) {
+    } else if (act) {
+      for (int c = gl; c < nchunks; c += G) {
         float w[8];
         load_chunk(x, c, d, vec, x[0], w);
 #pragma unroll
@@ -101,10 +108,11 @@ __global__ void __launch_bounds__(kQuantThreads) quantize_pack_kernel(
       }
     }
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
+    for (int o = G / 2; o > 0; o >>= 1) {
       mn = fminf(mn, __shfl_xor_sync(FULL, mn, o));
       mx = fmaxf(mx, __shfl_xor_sync(FULL, mx, o));
     }
+    if (!act) continue;
     // Eqn 4: Z = min, S = (max - min) / (2^b - 1)
     const float S = __fdiv_rn(__fsub_rn(mx, mn), L);
     const bool constant = !(S >= 1.17549435e-38f);  // S below FLT_MIN: code as constant
@@ -114,19 +122,19 @@ __global__ void __launch_bounds__(kQuantThreads) quantize_pack_kernel(
     if (CPL > 0) {
 #pragma unroll
       for (int i = 0; i < (CPL > 0 ? CPL : 1); ++i) {
-        const int c = lane + 32 * i;
+        const int c = gl + G * i;
         if (c < nchunks) store_word<BITS>(row + (int64_t)c * BITS, quantize_chunk<BITS>(v[i], c * 8, d, mn, inv, constant, kr));
       }
     } else {
-      for (int c = lane; c < nchunks; c += 32) {
+      for (int c = gl; c < nchunks; c += G) {
         float w[8];
         load_chunk(x, c, d, vec, x[0], w);
         store_word<BITS>(row + (int64_t)c * BITS, quantize_chunk<BITS>(w, c * 8, d, mn, inv, constant, kr));
       }
     }
-    if (lane == 0) *reinterpret_cast<float2*>(row + hoff) = make_float2(S, mn);
-    for (int b = p8 + lane; b < hoff; b += 32) row[b] = 0;
-    for (int b = hoff + 8 + lane; b < pitch; b += 32) row[b] = 0;
+    if (gl == 0) *reinterpret_cast<float2*>(row + hoff) = make_float2(S, mn);
+    for (int b = p8 + gl; b < hoff; b += G) row[b] = 0;
+    for (int b = hoff + 8 + gl; b < pitch; b += G) row[b] = 0;
   }
 }
 
@@ -180,15 +188,26 @@ int launch_quantize(const float* X, int64_t n, int d, int64_t ldx, const uint8_t
   const int hoff = (int)header_offset(d, BITS);
   const bool vec = aligned(X, 16) && (ldx % 4 == 0);
   const uint32_t h = seed_key_host(seed);
-  const int grid = grid_for_rows(n);
-  if (d <= 256)
-    quantize_pack_kernel<BITS, 1><<<grid, kQuantThreads, 0, s>>>(X, n, d, ldx, mask, h, packed, pitch, hoff, vec);
-  else if (d <= 512)
-    quantize_pack_kernel<BITS, 2><<<grid, kQuantThreads, 0, s>>>(X, n, d, ldx, mask, h, packed, pitch, hoff, vec);
-  else if (d <= 1024)
-    quantize_pack_kernel<BITS, 4><<<grid, kQuantThreads, 0, s>>>(X, n, d, ldx, mask, h, packed, pitch, hoff, vec);
-  else
-    quantize_pack_kernel<BITS, 0><<<grid, kQuantThreads, 0, s>>>(X, n, d, ldx, mask, h, packed, pitch, hoff, vec);
+  // lanes per row: enough 8-column chunks for one each, up to a warp
+  const int nch = (d + 7) / 8;
+  const int G = nch <= 1 ? 1 : nch <= 2 ? 2 : nch <= 4 ? 4 : nch <= 8 ? 8 : nch <= 16 ? 16 : 32;
+  const int grid = grid_for_rows((n + 32 / G - 1) / (32 / G));
+  switch (G) {
+    case 1: quantize_pack_kernel<BITS, 1, 1><<<grid, kQuantThreads, 0, s>>>(X, n, d, ldx, mask, h, packed, pitch, hoff, vec); break;
+    case 2: quantize_pack_kernel<BITS, 1, 2><<<grid, kQuantThreads, 0, s>>>(X, n, d, ldx, mask, h, packed, pitch, hoff, vec); break;
+    case 4: quantize_pack_kernel<BITS, 1, 4><<<grid, kQuantThreads, 0, s>>>(X, n, d, ldx, mask, h, packed, pitch, hoff, vec); break;
+    case 8: quantize_pack_kernel<BITS, 1, 8><<<grid, kQuantThreads, 0, s>>>(X, n, d, ldx, mask, h, packed, pitch, hoff, vec); break;
+    case 16: quantize_pack_kernel<BITS, 1, 16><<<grid, kQuantThreads, 0, s>>>(X, n, d, ldx, mask, h, packed, pitch, hoff, vec); break;
+    default:
+      if (d <= 256)
+        quantize_pack_kernel<BITS, 1, 32><<<grid, kQuantThreads, 0, s>>>(X, n, d, ldx, mask, h, packed, pitch, hoff, vec);
+      else if (d <= 512)
+        quantize_pack_kernel<BITS, 2, 32><<<grid, kQuantThreads, 0, s>>>(X, n, d, ldx, mask, h, packed, pitch, hoff, vec);
+      else if (d <= 1024)
+        quantize_pack_kernel<BITS, 4, 32><<<grid, kQuantThreads, 0, s>>>(X, n, d, ldx, mask, h, packed, pitch, hoff, vec);
+      else
+        quantize_pack_kernel<BITS, 0, 32><<<grid, kQuantThreads, 0, s>>>(X, n, d, ldx, mask, h, packed, pitch, hoff, vec);
+  }
   return launch_status();
 }
 

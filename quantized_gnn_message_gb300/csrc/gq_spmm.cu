@@ -210,11 +210,6 @@ __device__ __forceinline__ void group_reduce(float (&acc)[CPL][8]) {
       for (int k = 0; k < 8; ++k) acc[i][k] += __shfl_xor_sync(FULL, acc[i][k], o);
 }
 
-__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
-  const __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
-  return *reinterpret_cast<const uint32_t*>(&h);
-}
-
 __device__ __forceinline__ void store_chunk(const SpmmParams& p, int64_t r, int c, float s, const float (&a)[8]) {
   if (p.Yb != nullptr) {
     __nv_bfloat16* y = p.Yb + r * p.ldy + c * 8;
@@ -602,10 +597,10 @@ constexpr int kPiecesPerLane = BITS == 8 ? 2 : 1;
 
 // Bytes of one edge slot: the largest row of the width bucket (d <= 16 LG),
 // a packed row (payload rounded to 8 bytes, {S, Z}, rounded to 16) or an
-// fp32 row.  A compile-time stride keeps every slot address an immediate
-// offset from the group's ring.
-template <int BITS, int LG>
-constexpr int kSlot = BITS < 32 ? ((2 * BITS * LG + 7) / 8 * 8 + 8 + 15) / 16 * 16 : 64 * LG;
+// fp32 row (also when packed and fp32 rows mix: MX).  A compile-time stride
+// keeps every slot address an immediate offset from the group's ring.
+template <int BITS, int LG, bool MX>
+constexpr int kSlot = BITS < 32 && !MX ? ((2 * BITS * LG + 7) / 8 * 8 + 8 + 15) / 16 * 16 : 64 * LG;
 
 constexpr uint32_t kMagicBits = 0x4B000000u;  // 2^23 as fp32
 constexpr float kMagic = 8388608.0f;
@@ -630,6 +625,12 @@ struct ALane {
   int nv;               // fp32 rows: pieces gl + LG k, k < nv, are in range
   const uint8_t* src;   // the lane's first piece in message row 0
   uint32_t stride;      // bytes between message rows
+  // mixed rows: an fp32 row's columns [c0, c0 + 16) as nvm 16-byte pieces,
+  // piece k stored at 64 gl + 16 (k ^ swz) of the slot so that the pieces
+  // of a quarter-warp fall in distinct banks
+  const uint8_t* srcx;
+  uint32_t stridex;
+  int nvm, swz;
 };
 
 // Column of accumulator entry i (acc[i / 2], half i % 2) of this lane.
@@ -640,10 +641,20 @@ __device__ __forceinline__ int a_col(const ALane<LG>& L, int i) {
 }
 
 // Accumulate one edge from its slot sl with coefficient cf.
-template <int BITS, int LG>
-__device__ __forceinline__ void a_consume(const SpmmParams& p, const ALane<LG>& L, const uint8_t* sl, float cf,
-                                          f32x2 bias, f32x2 (&acc)[8], float& accz) {
-  if constexpr (BITS < 32) {
+template <int BITS, int LG, bool MX>
+__device__ __forceinline__ void a_consume(const SpmmParams& p, const ALane<LG>& L, const uint8_t* sl, bool quant,
+                                          float cf, f32x2 bias, f32x2 (&acc)[8], float& accz) {
+  if (MX && !quant) {
+    const f32x2 c2 = f2_pack(cf, cf);
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      if (k < L.nvm) {
+        const f32x2* xr = reinterpret_cast<const f32x2*>(sl + 64 * L.gl + 16 * (k ^ L.swz));
+        acc[2 * k] = f2_fma(c2, xr[0], acc[2 * k]);
+        acc[2 * k + 1] = f2_fma(c2, xr[1], acc[2 * k + 1]);
+      }
+    }
+  } else if constexpr (BITS < 32) {
     constexpr float c = (float)(1 << (BITS - 1));
     const float2 h = *reinterpret_cast<const float2*>(sl + p.hoff);
     const float cs = cf * h.x;
@@ -717,13 +728,14 @@ __device__ __forceinline__ void a_flush(const SpmmParams& p, const ALane<LG>& L,
 // Stream the edges [eb, eb + n) through the group's ring.  LIGHT: they are
 // the edges of rows [row0, row1) and each row is written once its last edge
 // has been consumed; otherwise the sums are left in acc / accz.
-template <int BITS, int LG, int U, bool LIGHT>
+template <int BITS, int LG, int U, bool LIGHT, bool MX>
 __device__ __forceinline__ void a_stream(const SpmmParams& p, const ALane<LG>& L, f32x2 bias, int eb, int n,
                                          int row0, int row1, f32x2 (&acc)[8], float& accz) {
   const float* __restrict__ colscale = p.colscale;
   const int nsteps = (n + U - 1) / U;
   uint32_t cx[kAS][U];
   float cf[kAS][U];
+  bool mq[kAS][U];  // mixed rows: the gathered row is packed
   // column ids two steps ahead: cp points at edge 2 U of the current step,
   // rem counts the edges from there to the end of the stream
   const int32_t* __restrict__ cp = p.col + eb;
@@ -734,6 +746,10 @@ __device__ __forceinline__ void a_stream(const SpmmParams& p, const ALane<LG>& L
   }
   cp += 2 * U;
   int rem = n - 2 * U;
+  // mixed rows: mask bits of the next step to issue, loaded one step ahead
+  bool mqn[U];
+#pragma unroll
+  for (int t = 0; t < U; ++t) mqn[t] = MX && t < n && __ldg(p.mask + cx[0][t]) != 0;
   // light rows: end of the current row and of the next (relative to eb),
   // and their output scales, one row ahead
   int row = row0;
@@ -755,6 +771,13 @@ __device__ __forceinline__ void a_stream(const SpmmParams& p, const ALane<LG>& L
       if (s < nsteps) {
 #pragma unroll
         for (int t = 0; t < U; ++t) cx[(j + 2) % kAS][t] = t < rem ? (uint32_t)__ldg(cp + t) : 0u;
+        if (MX) {
+#pragma unroll
+          for (int t = 0; t < U; ++t) {
+            mq[j][t] = mqn[t];
+            mqn[t] = t < rem + U && __ldg(p.mask + cx[(j + 1) % kAS][t]) != 0;  // edge (s + 1) U + t
+          }
+        }
         cp += U;
         rem -= U;
 #pragma unroll
@@ -762,9 +785,14 @@ __device__ __forceinline__ void a_stream(const SpmmParams& p, const ALane<LG>& L
           if (U == 1 || t < rem + 3 * U) {  // edge s U + t exists
             const uint32_t x = cx[j][t];
             cf[j][t] = colscale != nullptr ? __ldg(colscale + x) : 1.0f;
-            const uint32_t dst = L.sring + (j * U + t) * kSlot<BITS, LG>;
+            const uint32_t dst = L.sring + (j * U + t) * kSlot<BITS, LG, MX>;
             const uint8_t* src = L.src + (size_t)x * L.stride;
-            if constexpr (BITS < 32) {
+            if (MX && !mq[j][t]) {
+              const uint8_t* sx = L.srcx + (size_t)x * L.stridex;
+#pragma unroll
+              for (int k = 0; k < 4; ++k)
+                if (k < L.nvm) cp_async16(dst + 64 * L.gl + 16 * (k ^ L.swz), sx + 16 * k);
+            } else if constexpr (BITS < 32) {
               if (L.has0) cp_async16(dst + 16 * L.gl, src);
               if (kPiecesPerLane<BITS> > 1 && L.has1) cp_async16(dst + 16 * (L.gl + LG), src + 16 * LG);
             } else {
@@ -798,7 +826,9 @@ __device__ __forceinline__ void a_stream(const SpmmParams& p, const ALane<LG>& L
                 if (p.rowscale) rsn = row + 1 < row1 ? __ldg(p.rowscale + row + 1) : 1.0f;
               }
             }
-            if (L.on) a_consume<BITS, LG>(p, L, L.ring + (jc * U + t) * kSlot<BITS, LG>, cf[jc][t], bias, acc, accz);
+            if (L.on)
+              a_consume<BITS, LG, MX>(p, L, L.ring + (jc * U + t) * kSlot<BITS, LG, MX>, MX && mq[jc][t], cf[jc][t],
+                                      bias, acc, accz);
           }
         }
       }
@@ -814,7 +844,7 @@ __device__ __forceinline__ void a_stream(const SpmmParams& p, const ALane<LG>& L
   }
 }
 
-template <int BITS, int LG, int U>
+template <int BITS, int LG, int U, bool MX>
 __global__ void __launch_bounds__(kSpmmThreads) spmm_async_kernel(const SpmmParams p) {
   extern __shared__ __align__(16) uint8_t asm_[];
   constexpr int NG = 32 / LG;
@@ -822,7 +852,7 @@ __global__ void __launch_bounds__(kSpmmThreads) spmm_async_kernel(const SpmmPara
   const int g = lane / LG;
   ALane<LG> L;
   L.gl = lane % LG;
-  constexpr int SLOT = kSlot<BITS, LG>;
+  constexpr int SLOT = kSlot<BITS, LG, MX>;
   L.ring = asm_ + (w * NG + g) * (kAS * U * SLOT);
   L.sring = sm_addr(L.ring);
   L.gmask = (LG == 32 ? 0xffffffffu : ((1u << LG) - 1u)) << (g * LG);
@@ -835,6 +865,10 @@ __global__ void __launch_bounds__(kSpmmThreads) spmm_async_kernel(const SpmmPara
     L.nv = 0;
     L.src = p.packed + 16 * L.gl;
     L.stride = (uint32_t)p.pitch;
+    L.srcx = MX ? reinterpret_cast<const uint8_t*>(p.X + L.c0) : nullptr;
+    L.stridex = MX ? (uint32_t)(p.ldx * 4) : 0u;
+    L.nvm = MX ? max(0, min(4, (p.d - L.c0) / 4)) : 0;
+    L.swz = (L.gl >> 1) & 3;
   } else {
     L.src = reinterpret_cast<const uint8_t*>(p.X + 4 * L.gl);
     L.stride = (uint32_t)(p.ldx * 4);
@@ -855,7 +889,7 @@ __global__ void __launch_bounds__(kSpmmThreads) spmm_async_kernel(const SpmmPara
     chunk = (chunk + U - 1) / U * U;
     const int b0 = task.y + sid * chunk;
     const int b1 = min(b0 + chunk, task.z);
-    if (b0 < b1) a_stream<BITS, LG, U, false>(p, L, bias, b0, b1 - b0, 0, 0, acc, accz);
+    if (b0 < b1) a_stream<BITS, LG, U, false, MX>(p, L, bias, b0, b1 - b0, 0, 0, acc, accz);
     float o[16];
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
@@ -884,21 +918,22 @@ __global__ void __launch_bounds__(kSpmmThreads) spmm_async_kernel(const SpmmPara
   for (int64_t t = gid; t < p.n_light; t += ngroups) {
     const int2 run = __ldg(reinterpret_cast<const int2*>(p.light) + t);
     const int eb = __ldg(p.rowptr + run.x), ee = __ldg(p.rowptr + run.y);
-    a_stream<BITS, LG, U, true>(p, L, bias, eb, ee - eb, run.x, run.y, acc, accz);
+    a_stream<BITS, LG, U, true, MX>(p, L, bias, eb, ee - eb, run.x, run.y, acc, accz);
   }
 }
 
-template <int BITS, int LG, int U>
+template <int BITS, int LG, int U, bool MX>
 int launch_async(const SpmmParams& p, cudaStream_t s) {
   constexpr int NG = 32 / LG;
-  constexpr int SLOT = kSlot<BITS, LG>;
-  static_assert(BITS == 32 || SLOT / 16 <= kPiecesPerLane<BITS> * LG, "row pieces exceed the lanes' share");
-  if (BITS < 32 && p.pitch > SLOT) return GQ_ERR_UNSUPPORTED;
-  if (BITS == 32 && 4 * p.d > SLOT) return GQ_ERR_UNSUPPORTED;
+  constexpr int SLOT = kSlot<BITS, LG, MX>;
+  static_assert(BITS == 32 || kSlot<BITS, LG, false> / 16 <= kPiecesPerLane<BITS> * LG,
+                "row pieces exceed the lanes' share");
+  if (BITS < 32 && p.pitch > kSlot<BITS, LG, false>) return GQ_ERR_UNSUPPORTED;
+  if ((BITS == 32 || MX) && 4 * p.d > SLOT) return GQ_ERR_UNSUPPORTED;
   size_t smem = (size_t)kSpmmWarps * NG * kAS * U * SLOT;
   const size_t part = sizeof(float) * kSpmmWarps * p.d;
   if (smem < part) smem = part;
-  auto kern = spmm_async_kernel<BITS, LG, U>;
+  auto kern = spmm_async_kernel<BITS, LG, U, MX>;
   // (the kernel also holds a few bytes of static shared memory)
   if (smem > 32 * 1024) GQ_TRY_CUDA(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem));
   int per_sm = 0;
@@ -914,24 +949,26 @@ int launch_async(const SpmmParams& p, cudaStream_t s) {
   return launch_status();
 }
 
-template <int BITS, int U>
+template <int BITS, int U, bool MX>
 int launch_async_d(const SpmmParams& p, cudaStream_t s) {
-  if (p.d <= 16) return launch_async<BITS, 1, U>(p, s);
-  if (p.d <= 32) return launch_async<BITS, 2, U>(p, s);
-  if (p.d <= 64) return launch_async<BITS, 4, U>(p, s);
-  if (p.d <= 128) return launch_async<BITS, 8, U>(p, s);
-  if (p.d <= 256) return launch_async<BITS, 16, U>(p, s);
-  return launch_async<BITS, 32, U>(p, s);
+  if (p.d <= 16) return launch_async<BITS, 1, U, MX>(p, s);
+  if (p.d <= 32) return launch_async<BITS, 2, U, MX>(p, s);
+  if (p.d <= 64) return launch_async<BITS, 4, U, MX>(p, s);
+  if (p.d <= 128) return launch_async<BITS, 8, U, MX>(p, s);
+  if (p.d <= 256) return launch_async<BITS, 16, U, MX>(p, s);
+  return launch_async<BITS, 32, U, MX>(p, s);
 }
 
-// Coefficient-mode aggregation with d <= 512 and one kind of message row
-// (all packed, or all fp32); packed rows keep two edges per stage.
+// Coefficient-mode aggregation with d <= 512.  One kind of message row
+// (all packed, or all fp32): packed rows keep two edges per stage; a mask
+// mixing packed and fp32 rows: one edge per stage in fp32-sized slots.
 int launch_async_any(const SpmmParams& p, int bits, cudaStream_t s) {
+  const bool mx = bits < 32 && p.mask != nullptr;
   switch (bits) {
-    case 2: return launch_async_d<2, 2>(p, s);
-    case 4: return launch_async_d<4, 2>(p, s);
-    case 8: return launch_async_d<8, 2>(p, s);
-    default: return launch_async_d<32, 1>(p, s);
+    case 2: return mx ? launch_async_d<2, 1, true>(p, s) : launch_async_d<2, 2, false>(p, s);
+    case 4: return mx ? launch_async_d<4, 1, true>(p, s) : launch_async_d<4, 2, false>(p, s);
+    case 8: return mx ? launch_async_d<8, 1, true>(p, s) : launch_async_d<8, 2, false>(p, s);
+    default: return launch_async_d<32, 1, false>(p, s);
   }
 }
 
@@ -1044,11 +1081,9 @@ int dequant_spmm(const gq_graph* g, int transpose, int coef, const float* X, int
   } else if (coef != GQ_COEF_ONE) {
     return GQ_ERR_INVALID_ARG;
   }
-  // every message row of one kind (all packed, or all fp32; a row stride
-  // under 2^31 bytes): asynchronous pipeline; a mix of packed and fp32 rows (a mask): warp per light row,
-  // whose registers hold the 1 KB fp32 rows more cheaply than 1 KB ring slots
-  if (d <= 512 && !(bits < 32 && mask != nullptr) && (bits < 32 || ldx <= (int64_t)1 << 29))
-    return launch_async_any(p, bits, s);
+  // d <= 512 and an fp32 row stride under 2^31 bytes: asynchronous ring
+  // pipeline; otherwise warp per light row
+  if (d <= 512 && ldx <= (int64_t)1 << 29) return launch_async_any(p, bits, s);
   return launch_any<false>(p, bits, s);
 }
 

@@ -88,3 +88,19 @@ def test_to_bf16_round_nearest_even(orc):
     x = torch.tensor([[1.0, 1.0 + 2 ** -8, 1.0 + 3 * 2 ** -8, -2.5, 1e-30, 3.0e38]], device="cuda")
     got = q.to_bf16(x).float().cpu().numpy()
     np.testing.assert_array_equal(got, orc.bf16_round(x.cpu().numpy()))
+
+
+@pytest.mark.parametrize("rows,cols,lds,pad", [(1000, 47, 47, 8), (37, 1100, 1100, 8), (513, 256, 260, 8),
+                                              (3, 5, 7, 1), (129, 64, 66, 16)])
+def test_to_bf16_shapes(orc, rows, cols, lds, pad):
+    # ragged widths, rows wider than one block pass, strided (non-vector) sources,
+    # zero padding up to the padded width
+    q = gq()
+    base = synth.normal_matrix(rows, lds, seed=rows + cols, device="cuda")
+    x = base[:, :cols]
+    got = q.to_bf16(x, pad)
+    dcols = (cols + pad - 1) // pad * pad
+    full = got.as_strided((rows, dcols), (dcols, 1)).float().cpu().numpy()
+    ref = np.zeros((rows, dcols), np.float32)
+    ref[:, :cols] = orc.bf16_round(x.cpu().numpy())
+    np.testing.assert_array_equal(full, ref)
