@@ -340,7 +340,7 @@ def run_ours(args, w):
     for (name, l, b), times in stage_ms.items():
         stage_summary.setdefault(name, 0.0)
         stage_summary[name] += sum(times) / args.steps
-    roofline = {"kernel": "spmm_kernel (de-quantizing aggregation, forward and transposed)",
+    roofline = {"kernel": "spmm_bulk_kernel (de-quantizing aggregation, forward and transposed)",
                 "bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
                 "peak_source": f"hbm_gbs of {peak_kind}",
                 "traffic": traffic,

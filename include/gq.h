@@ -180,6 +180,12 @@ typedef struct gq_graph {
   int32_t split_edges;      /* heavy rows are cut into tasks of this size */
   int32_t max_deg;          /* largest in-degree                          */
   int32_t tr_max_deg;       /* largest out-degree                         */
+  int32_t* status;          /* device int in `storage`, zeroed by
+                               gq_graph_prepare: an aggregation kernel on
+                               this graph whose bounded wait for its own
+                               row copies gave up writes a non-zero code
+                               here (first writer wins; it stays set).
+                               Read it after synchronizing the stream.  */
 } gq_graph;
 
 /* Bytes of `storage` gq_graph_prepare needs for a graph of n nodes and nnz

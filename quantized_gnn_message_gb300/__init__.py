@@ -47,6 +47,7 @@ class Graph_t(ctypes.Structure):
         ("sched", Sched_t), ("tr_sched", Sched_t),
         ("hub_threshold", ctypes.c_int32), ("split_edges", ctypes.c_int32),
         ("max_deg", ctypes.c_int32), ("tr_max_deg", ctypes.c_int32),
+        ("status", ctypes.c_void_p),
     ]
 
 
@@ -225,6 +226,12 @@ class Graph:
     @property
     def inv_in(self):
         return self._view("inv_in", self.n, torch.float32)
+
+    @property
+    def status(self):
+        """The graph's device status word (non-zero: a bounded wait inside an
+        aggregation kernel gave up); a one-element int32 tensor view."""
+        return self._view("status", 1, torch.int32)
 
     @property
     def n_tasks(self):

@@ -275,7 +275,7 @@ int64_t max_light(int64_t n, int64_t nnz) {
 
 struct StorageLayout {
   size_t tr_rowptr, tr_col, tr_perm, dinv_in, dinv_out, inv_in, tasks, groups, tr_tasks, tr_groups, light, tr_light,
-      total;
+      status, total;
 };
 
 StorageLayout storage_layout(int64_t n, int64_t nnz) {
@@ -293,6 +293,7 @@ StorageLayout storage_layout(int64_t n, int64_t nnz) {
   L.tr_groups = o; o += align256(sizeof(int32_t) * 4 * max_groups(nnz));
   L.light = o;     o += align256(sizeof(int32_t) * 2 * max_light(n, nnz));
   L.tr_light = o;  o += align256(sizeof(int32_t) * 2 * max_light(n, nnz));
+  L.status = o;    o += align256(sizeof(int32_t));
   L.total = o;
   return L;
 }
@@ -442,6 +443,8 @@ extern "C" int gq_graph_prepare(int64_t n, int64_t nnz, const int32_t* rowptr, c
   G.inv_in = reinterpret_cast<float*>(st + SL.inv_in);
   G.hub_threshold = hub_threshold;
   G.split_edges = split_edges;
+  G.status = reinterpret_cast<int32_t*>(st + SL.status);
+  GQ_TRY_CUDA(cudaMemsetAsync(G.status, 0, sizeof(int32_t), s));
   int32_t* hubs = reinterpret_cast<int32_t*>(wb + WL.hubs);
   int32_t* tr_hubs = reinterpret_cast<int32_t*>(wb + WL.tr_hubs);
 

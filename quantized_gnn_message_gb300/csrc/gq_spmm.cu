@@ -63,6 +63,7 @@ struct SpmmParams {
   int* tickets;             // [group] arrivals, zero at launch
   const int32_t* light;     // runs of light rows {row_begin, row_end}
   int64_t n_light;
+  int* err;                 // device status word (bounded waits that gave up)
 };
 
 namespace {
@@ -1006,6 +1007,386 @@ int launch_any(const SpmmParams& p, int bits, cudaStream_t s) {
   }
 }
 
+
+// Bytes of an edge slot of the bulk-copy ring: a whole fp32 row of the width
+// bucket (d <= 32 CPL), which also holds any packed row of that bucket.
+template <int CPL>
+constexpr int kBSlot = 128 * CPL;
+
+// Four 8-bit codes (one word, column order) as the floats 2^23 + q.
+__device__ __forceinline__ void codes4_b8(uint32_t w, float (&v)[4]) {
+#pragma unroll
+  for (int i = 0; i < 4; ++i) v[i] = __uint_as_float(__byte_perm(w, kMagicBits, 0x7540u | i));
+}
+
+// Coefficient and mask bit of the lane's edge of a batch.
+template <int BITS, bool MX>
+__device__ __forceinline__ void r_meta(const SpmmParams& p, uint32_t x, bool valid, float& cf, bool& q) {
+  cf = 1.0f;
+  q = BITS < 32 && !MX;
+  if (valid) {
+    if (p.colscale != nullptr) cf = __ldg(p.colscale + x);
+    if (MX) q = __ldg(p.mask + x) != 0;
+  }
+}
+
+// acc[2 k], acc[2 k + 1] += cs * (q - c) for piece k (4 columns) of a packed
+// row in a slot: the lane's codes of the piece (one byte for b = 2, two for
+// b = 4, four for b = 8) become the floats 2^23 + q (a byte permute, or a
+// mask and an or), and one paired subtraction of 2^23 + c leaves q - c.
+template <int BITS, int CPL>
+__device__ __forceinline__ void bf_packed(const uint8_t* sl, f32x2 cs2, f32x2 bias, f32x2 (&acc)[4]) {
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int k = 0; k < CPL / 4; ++k) {
+    float v[4];
+    if constexpr (BITS == 2) {
+      const uint32_t w = sl[32 * k + lane];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) v[i] = __uint_as_float(kMagicBits | ((w >> (2 * i)) & 3u));
+    } else if constexpr (BITS == 4) {
+      const uint32_t w = *reinterpret_cast<const uint16_t*>(sl + 64 * k + 2 * lane);
+      const uint32_t lo = w & 0x0F0Fu, hi = (w >> 4) & 0x0F0Fu;  // codes 0, 2 / 1, 3 in bytes 0, 1
+      v[0] = __uint_as_float(__byte_perm(lo, kMagicBits, 0x7540u));
+      v[1] = __uint_as_float(__byte_perm(hi, kMagicBits, 0x7540u));
+      v[2] = __uint_as_float(__byte_perm(lo, kMagicBits, 0x7541u));
+      v[3] = __uint_as_float(__byte_perm(hi, kMagicBits, 0x7541u));
+    } else {
+      codes4_b8(*reinterpret_cast<const uint32_t*>(sl + 128 * k + 4 * lane), v);
+    }
+    acc[2 * k] = f2_fma(cs2, f2_add(f2_pack(v[0], v[1]), bias), acc[2 * k]);
+    acc[2 * k + 1] = f2_fma(cs2, f2_add(f2_pack(v[2], v[3]), bias), acc[2 * k + 1]);
+  }
+}
+
+// The lane's columns of (acc + accz) * s, written to row r of Y / Yb, or to
+// `part` (an fp32 partial row) when it is not null.
+template <int CPL>
+__device__ __forceinline__ void bf_write(const SpmmParams& p, bool a_on, bool b_on, int64_t r, float s, float* part,
+                                         const f32x2 (&acc)[4], float accz) {
+  const int c0 = 4 * (threadIdx.x & 31);
+#pragma unroll
+  for (int k = 0; k < CPL / 4; ++k) {
+    if (k == 0 ? a_on : b_on) {
+      const float2 u = f2_unpack(acc[2 * k]), v = f2_unpack(acc[2 * k + 1]);
+      const float o0 = (u.x + accz) * s, o1 = (u.y + accz) * s, o2 = (v.x + accz) * s, o3 = (v.y + accz) * s;
+      const int c = c0 + 128 * k;
+      if (part != nullptr)
+        st_f4(part + c, o0, o1, o2, o3);
+      else if (p.Yb != nullptr)
+        *reinterpret_cast<uint2*>(p.Yb + r * p.ldy + c) = make_uint2(pack_bf16x2(o0, o1), pack_bf16x2(o2, o3));
+      else
+        st_f4(p.Y + r * p.ldy + c, o0, o1, o2, o3);
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Bulk-copy ring aggregation (coefficient modes, 64 < d <= 256).
+//
+// The same warp-per-edge consumption as the ring above, with the gathers
+// done by the bulk-copy engine: the lane that holds an edge's metadata
+// copies the whole message row (d*4 bytes of an fp32 row, or the packed row
+// with its header) into one of the warp's R shared-memory slots with a
+// single cp.async.bulk that completes on the slot's mbarrier, and stores the
+// edge's coefficient and kind beside the slot.  The warp consumes the edges
+// in order, waiting on each slot's barrier (a bounded wait: on timeout it
+// records a code in the graph's status word, waits again, boundedly, for the
+// copies it still has in flight and gives up the rest of its work); after
+// every H edges consumed, the H freed slots are refilled with the edges R
+// ahead, one lane each.
+// ---------------------------------------------------------------------------
+constexpr int kSpmmWaitCode = 0x5350;  // status code: a slot's copy did not land in time
+
+__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+               "l"(src), "r"(bytes), "r"(bar)
+               : "memory");
+}
+__device__ __forceinline__ void bar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+__device__ __forceinline__ void bar_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ bool bar_try_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n"
+      "  .reg .pred p;\n"
+      "  mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+      "  selp.u32 %0, 1, 0, p;\n"
+      "}\n"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+// Bounded wait (about two seconds of SM clocks).
+__device__ __forceinline__ bool bar_wait(uint32_t bar, uint32_t parity) {
+  if (bar_try_wait(bar, parity)) return true;
+  const long long t0 = clock64();
+  while (!bar_try_wait(bar, parity))
+    if (clock64() - t0 > 4000000000LL) return false;
+  return true;
+}
+
+struct BLane {
+  const uint8_t* xb;   // fp32 rows (row 0)
+  const uint8_t* pb;   // packed rows (row 0)
+  uint32_t xstride, xbytes, pitch;
+  uint32_t sring;      // the warp's slots (shared address)
+  const uint8_t* ring;
+  uint32_t sbar;       // the warp's R barriers
+  float2* meta;        // the warp's R {coefficient, kind} entries
+  uint32_t used;       // edges this warp streamed before (slot use count)
+  bool a_on, b_on;
+  bool failed;
+};
+
+// Issue the wave of edges [f0, f0 + H) (f0 a multiple of H) from the batch
+// registers of the lanes holding them.
+template <int BITS, bool MX, int R, int H, int SLOT>
+__device__ __forceinline__ void b_issue(BLane& L, int f0, int n, uint32_t x, bool q, float cf) {
+  const int lane = threadIdx.x & 31;
+  const int l0 = f0 & 31;
+  const int f = f0 - l0 + lane;
+  if (lane >= l0 && lane < l0 + H && f < n) {
+    const uint32_t slot = (L.used + (uint32_t)f) & (R - 1);
+    const bool quant = BITS < 32 && (MX ? q : true);
+    L.meta[slot] = make_float2(cf, quant ? 1.0f : 0.0f);
+    const uint32_t bytes = quant ? L.pitch : L.xbytes;
+    const uint8_t* src = quant ? L.pb + (size_t)(x * (uint64_t)L.pitch) : L.xb + (size_t)(x * (uint64_t)L.xstride);
+    const uint32_t bar = L.sbar + 8 * slot;
+    bar_expect_tx(bar, bytes);
+    bulk_g2s(L.sring + slot * SLOT, src, bytes, bar);
+  }
+}
+
+// Stream the edges [eb, eb + n).  LIGHT: they are the edges of rows
+// [row0, row1), each row written once its last edge is consumed; otherwise
+// the sums are left in acc / accz.
+template <int BITS, int CPL, bool MX, int R, int H, bool LIGHT>
+__device__ __forceinline__ void b_stream(const SpmmParams& p, BLane& L, f32x2 bias, int eb, int n, int row0,
+                                         int row1, f32x2 (&acc)[4], float& accz) {
+  static_assert(R <= 32 && 32 % H == 0 && R % H == 0 && (R & (R - 1)) == 0, "ring shape");
+  constexpr int SLOT = kBSlot<CPL>;
+  const int lane = threadIdx.x & 31;
+  const int32_t* __restrict__ col = p.col + eb;
+  // lane i: edge kb + i (x0, q0, cf0) and kb + 32 + i (x1, q1, cf1); the
+  // column id of kb + 64 + i (x2)
+  uint32_t x0 = lane < n ? (uint32_t)__ldg(col + lane) : 0u;
+  uint32_t x1 = 32 + lane < n ? (uint32_t)__ldg(col + 32 + lane) : 0u;
+  uint32_t x2 = 64 + lane < n ? (uint32_t)__ldg(col + 64 + lane) : 0u;
+  float cf0, cf1;
+  bool q0, q1;
+  r_meta<BITS, MX>(p, x0, lane < n, cf0, q0);
+  r_meta<BITS, MX>(p, x1, 32 + lane < n, cf1, q1);
+  int kb = 0;
+  int rb = row0, ri = 0, rend = 0x7fffffff, rpl = 0x7fffffff;
+  float rsl = 1.0f;
+  if (LIGHT) {
+    if (row0 + lane < row1) {
+      rpl = __ldg(p.rowptr + row0 + 1 + lane) - eb;
+      if (p.rowscale) rsl = __ldg(p.rowscale + row0 + lane);
+    }
+    rend = __shfl_sync(FULL, rpl, 0);
+  }
+  // fill the ring (the first R edges are all in batch 0)
+#pragma unroll
+  for (int f0 = 0; f0 < R; f0 += H)
+    if (f0 < n) b_issue<BITS, MX, R, H, SLOT>(L, f0, n, x0, q0, cf0);
+  int issued = min(R, n);
+  int e = 0;
+  for (; e < n; ++e) {
+    if (e == kb + 32) {  // the consumer enters the next batch
+      kb += 32;
+      x0 = x1;
+      q0 = q1;
+      cf0 = cf1;
+      x1 = x2;
+      r_meta<BITS, MX>(p, x1, kb + 32 + lane < n, cf1, q1);
+      x2 = kb + 64 + lane < n ? (uint32_t)__ldg(col + kb + 64 + lane) : 0u;
+    }
+    const uint32_t u = L.used + (uint32_t)e;
+    const uint32_t slot = u & (R - 1);
+    if (!__all_sync(FULL, bar_wait(L.sbar + 8 * slot, (u / R) & 1u))) {  // a warp-wide verdict
+      L.failed = true;
+      break;
+    }
+    const float2 mt = L.meta[slot];
+    if (LIGHT) {
+      while (e >= rend) {
+        bf_write<CPL>(p, L.a_on, L.b_on, rb + ri, __shfl_sync(FULL, rsl, ri), nullptr, acc, accz);
+#pragma unroll
+        for (int i = 0; i < CPL / 2; ++i) acc[i] = 0ull;
+        accz = 0.0f;
+        if (++ri == 32) {
+          rb += 32;
+          ri = 0;
+          rpl = 0x7fffffff;
+          rsl = 1.0f;
+          if (rb + lane < row1) {
+            rpl = __ldg(p.rowptr + rb + 1 + lane) - eb;
+            if (p.rowscale) rsl = __ldg(p.rowscale + rb + lane);
+          }
+        }
+        rend = __shfl_sync(FULL, rpl, ri);
+      }
+    }
+    const uint8_t* sl = L.ring + slot * SLOT;
+    if (BITS < 32 && mt.y != 0.0f) {
+      constexpr float c = (float)(1 << ((BITS < 32 ? BITS : 8) - 1));
+      const float2 h = *reinterpret_cast<const float2*>(sl + p.hoff);
+      accz = __fmaf_rn(mt.x, __fmaf_rn(c, h.x, h.y), accz);
+      const float cs = mt.x * h.x;
+      bf_packed<BITS, CPL>(sl, f2_pack(cs, cs), bias, acc);
+    } else {
+      const f32x2 c2 = f2_pack(mt.x, mt.x);
+      const f32x2* a = reinterpret_cast<const f32x2*>(sl + 16 * lane);
+      acc[0] = f2_fma(c2, a[0], acc[0]);
+      acc[1] = f2_fma(c2, a[1], acc[1]);
+      if (CPL == 8) {
+        acc[2] = f2_fma(c2, a[64], acc[2]);
+        acc[3] = f2_fma(c2, a[65], acc[3]);
+      }
+    }
+    const int f0 = e + 1 - H + R;  // refill wave, once H slots are free
+    if (((e + 1) & (H - 1)) == 0 && f0 < n) {
+      __syncwarp();  // every lane is done with the freed slots
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      if (f0 >= kb + 32)
+        b_issue<BITS, MX, R, H, SLOT>(L, f0, n, x1, q1, cf1);
+      else
+        b_issue<BITS, MX, R, H, SLOT>(L, f0, n, x0, q0, cf0);
+      issued = min(f0 + H, n);
+    }
+  }
+  if (L.failed) {
+    // record the failure, then wait (boundedly) for the copies still in flight
+    if (lane == 0 && p.err != nullptr) atomicCAS(p.err, 0, kSpmmWaitCode);
+    for (int f = e; f < issued; ++f) {
+      const uint32_t u = L.used + (uint32_t)f;
+      bar_wait(L.sbar + 8 * (u & (R - 1)), (u / R) & 1u);
+    }
+    return;
+  }
+  L.used += (uint32_t)n;
+  if (LIGHT) {
+    // the last row, and any rows without edges after it
+    while (rb + ri < row1) {
+      bf_write<CPL>(p, L.a_on, L.b_on, rb + ri, __shfl_sync(FULL, rsl, ri), nullptr, acc, accz);
+#pragma unroll
+      for (int i = 0; i < CPL / 2; ++i) acc[i] = 0ull;
+      accz = 0.0f;
+      if (++ri == 32) {
+        rb += 32;
+        ri = 0;
+        rsl = 1.0f;
+        if (rb + lane < row1 && p.rowscale) rsl = __ldg(p.rowscale + rb + lane);
+      }
+    }
+  }
+}
+
+template <int BITS, int CPL, bool MX, int R, int H>
+__global__ void __launch_bounds__(kSpmmThreads, 3) spmm_bulk_kernel(const SpmmParams p) {
+  extern __shared__ __align__(128) uint8_t bsm[];
+  constexpr int SLOT = kBSlot<CPL>;
+  constexpr int HDR = kSpmmWarps * R * 16;  // barriers and {coefficient, kind} entries of all warps
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  BLane L;
+  L.xb = reinterpret_cast<const uint8_t*>(p.X);
+  L.pb = p.packed;
+  L.xstride = (uint32_t)(p.ldx * 4);
+  L.xbytes = (uint32_t)(p.d * 4);
+  L.pitch = (uint32_t)p.pitch;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(bsm) + w * R;
+  L.sbar = sm_addr(bars);
+  L.meta = reinterpret_cast<float2*>(bsm + kSpmmWarps * R * 8) + w * R;
+  L.ring = bsm + HDR + w * (R * SLOT);
+  L.sring = sm_addr(L.ring);
+  L.used = 0;
+  L.a_on = 4 * lane < p.d;
+  L.b_on = CPL == 8 && 128 + 4 * lane < p.d;
+  L.failed = false;
+  if (lane < R) bar_init(L.sbar + 8 * lane, 1);
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  __syncwarp();
+  const f32x2 bias = a_bias<BITS>();
+  f32x2 acc[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) acc[i] = 0ull;
+  float accz = 0.0f;
+  if ((int64_t)blockIdx.x < p.n_tasks) {
+    const int4 task = __ldg(reinterpret_cast<const int4*>(p.tasks) + blockIdx.x);
+    const int len = task.z - task.y;
+    const int chunk = (len + kSpmmWarps - 1) / kSpmmWarps;
+    const int b0 = task.y + w * chunk;
+    const int b1 = min(b0 + chunk, task.z);
+    if (b0 < b1) b_stream<BITS, CPL, MX, R, H, false>(p, L, bias, b0, b1 - b0, 0, 0, acc, accz);
+    __syncthreads();  // every ring is drained: reuse the slots for the warp partials
+    float* part = reinterpret_cast<float*>(bsm + HDR);
+#pragma unroll
+    for (int i = 0; i < CPL / 2; ++i) {
+      const float2 v = f2_unpack(acc[i]);
+      const int c = 4 * lane + 128 * (i >> 1) + 2 * (i & 1);
+      if ((i >> 1) == 0 ? L.a_on : L.b_on) {
+        part[w * p.d + c] = v.x + accz;
+        part[w * p.d + c + 1] = v.y + accz;
+      }
+    }
+    __syncthreads();
+    finish_heavy(p, task, part);
+    return;
+  }
+  const int64_t gw = ((int64_t)blockIdx.x - p.n_tasks) * kSpmmWarps + w;
+  const int64_t nw = ((int64_t)gridDim.x - p.n_tasks) * kSpmmWarps;
+  for (int64_t t = gw; t < p.n_light && !L.failed; t += nw) {
+    const int2 run = __ldg(reinterpret_cast<const int2*>(p.light) + t);
+    const int eb = __ldg(p.rowptr + run.x), ee = __ldg(p.rowptr + run.y);
+    b_stream<BITS, CPL, MX, R, H, true>(p, L, bias, eb, ee - eb, run.x, run.y, acc, accz);
+  }
+}
+
+template <int BITS, int CPL, bool MX, int R, int H>
+int launch_bulk(const SpmmParams& p, cudaStream_t s) {
+  constexpr int SLOT = kBSlot<CPL>;
+  if (BITS < 32 && p.pitch > SLOT) return GQ_ERR_UNSUPPORTED;
+  if (4 * p.d > SLOT) return GQ_ERR_UNSUPPORTED;
+  auto kern = spmm_bulk_kernel<BITS, CPL, MX, R, H>;
+  size_t smem = (size_t)kSpmmWarps * R * (16 + SLOT);
+  const size_t part = kSpmmWarps * R * 16 + sizeof(float) * kSpmmWarps * p.d;
+  if (smem < part) smem = part;
+  if (smem > 48 * 1024) GQ_TRY_CUDA(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem));
+  int per_sm = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kSpmmThreads, smem) != cudaSuccess || per_sm < 1)
+    return GQ_ERR_UNSUPPORTED;
+  int64_t light = (int64_t)sm_count() * per_sm;
+  const int64_t need = (p.n_light + kSpmmWarps - 1) / kSpmmWarps;
+  if (light > need) light = need;
+  if (light < 1) light = 1;
+  const int64_t grid = p.n_tasks + light;
+  if (grid > 0x7fffffff) return GQ_ERR_UNSUPPORTED;
+  kern<<<(unsigned)grid, kSpmmThreads, smem, s>>>(p);
+  return launch_status();
+}
+
+// 64 < d <= 256: mixed rows, all packed, or all fp32.
+int launch_bulk_any(const SpmmParams& p, int bits, cudaStream_t s) {
+  const bool mx = bits < 32 && p.mask != nullptr;
+  const bool wide = p.d > 128;
+#define GQ_BULK(B, M) return wide ? launch_bulk<B, 8, M, 8, 4>(p, s) : launch_bulk<B, 4, M, 16, 8>(p, s)
+  switch (bits) {
+    case 2: if (mx) GQ_BULK(2, true); GQ_BULK(2, false);
+    case 4: if (mx) GQ_BULK(4, true); GQ_BULK(4, false);
+    case 8: if (mx) GQ_BULK(8, true); GQ_BULK(8, false);
+    default: GQ_BULK(32, false);
+  }
+#undef GQ_BULK
+}
+
+
 }  // namespace
 
 // Common argument checks and message-source setup.
@@ -1040,6 +1421,7 @@ int spmm_setup(const gq_graph* g, int transpose, const float* X, int64_t ldx, co
   p.light = sc.light;
   p.n_light = sc.n_light;
   p.hub_threshold = g->hub_threshold;
+  p.err = g->status;
   if (sc.n_groups > 0) {
     if (ws == nullptr || ws_bytes < ws_bytes_for(sc, d) || !aligned(ws, 256)) return GQ_ERR_WORKSPACE;
     p.partial = static_cast<float*>(ws);
@@ -1081,8 +1463,11 @@ int dequant_spmm(const gq_graph* g, int transpose, int coef, const float* X, int
   } else if (coef != GQ_COEF_ONE) {
     return GQ_ERR_INVALID_ARG;
   }
-  // d <= 512 and an fp32 row stride under 2^31 bytes: asynchronous ring
-  // pipeline; otherwise warp per light row
+  // mixed packed / fp32 rows with 64 < d <= 256: bulk-copy ring, warp per
+  // edge; otherwise, d <= 512 and an fp32 row stride under 2^31 bytes:
+  // asynchronous ring pipeline; otherwise warp per light row
+  if (bits < 32 && mask != nullptr && d > 64 && d <= 256 && ldx <= (int64_t)1 << 29)
+    return launch_bulk_any(p, bits, s);
   if (d <= 512 && ldx <= (int64_t)1 << 29) return launch_async_any(p, bits, s);
   return launch_any<false>(p, bits, s);
 }
