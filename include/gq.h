@@ -337,7 +337,8 @@ GQ_API int gq_gcn_layer_bwd(const gq_graph* g, int coef, const float* dH_out, in
  * computed with the per-(v,k) maximum subtracted (same value), in fp32
  * (Tango Sec. 3.2 keeps the layer before softmax in full precision).
  * alpha and E_pre (nullable) are E x heads, indexed by CSR edge id.
- * heads in {1, 2, 4, 8}; S, D, alpha 16-byte aligned.  Workspace:
+ * heads in {1, 2, 4, 8}; S, D, alpha and E_pre 16-byte aligned
+ * (GQ_ERR_INVALID_ARG otherwise).  Workspace:
  * gq_edge_softmax_workspace_bytes (split heavy rows only; may be 0).
  * ---------------------------------------------------------------------- */
 GQ_API size_t gq_edge_softmax_workspace_bytes(const gq_graph* g, int heads);

@@ -48,6 +48,21 @@ __device__ __forceinline__ void load_k(const float* __restrict__ p, float (&v)[K
   }
 }
 
+template <int K>
+__device__ __forceinline__ void store_k(float* __restrict__ p, const float (&v)[K]) {
+  if constexpr (K == 4) {
+    *reinterpret_cast<float4*>(p) = make_float4(v[0], v[1], v[2], v[3]);
+  } else if constexpr (K == 8) {
+    *reinterpret_cast<float4*>(p) = make_float4(v[0], v[1], v[2], v[3]);
+    *reinterpret_cast<float4*>(p + 4) = make_float4(v[4], v[5], v[6], v[7]);
+  } else if constexpr (K == 2) {
+    *reinterpret_cast<float2*>(p) = make_float2(v[0], v[1]);
+  } else {
+#pragma unroll
+    for (int k = 0; k < K; ++k) p[k] = v[k];
+  }
+}
+
 __device__ __forceinline__ float lrelu(float x, float slope) { return x > 0.0f ? x : slope * x; }
 
 // online softmax state: fold value x into (m, l)
@@ -140,6 +155,69 @@ __device__ __forceinline__ void sm_pass2(const SoftmaxParams& p, int64_t first, 
   }
 }
 
+// One row [a, b) of at most 32 edges by one thread: scores, online max and
+// sum per head, then alpha = exp(E - max) / sum.  Edges go four at a time
+// (their column ids, then their S rows, loaded before any is used).
+template <int K>
+__device__ __forceinline__ void sm_scores4(const SoftmaxParams& p, int64_t e, int64_t b, const float (&dv)[K],
+                                           float (&ep)[4][K]) {
+  int32_t x[4];
+#pragma unroll
+  for (int t = 0; t < 4; ++t) x[t] = e + t < b ? __ldg(p.col + e + t) : 0;
+#pragma unroll
+  for (int t = 0; t < 4; ++t) {
+    float s[K];
+    load_k<K>(p.S + (int64_t)x[t] * K, s);
+#pragma unroll
+    for (int k = 0; k < K; ++k) ep[t][k] = s[k] + dv[k];
+  }
+}
+
+template <int K>
+__device__ __forceinline__ void sm_thread_row(const SoftmaxParams& p, int64_t r, int64_t a, int64_t b) {
+  float dv[K];
+  load_k<K>(p.D + r * K, dv);
+  float m[K], l[K];
+#pragma unroll
+  for (int k = 0; k < K; ++k) {
+    m[k] = kNegInf;
+    l[k] = 0.0f;
+  }
+  for (int64_t e = a; e < b; e += 4) {
+    float ep[4][K];
+    sm_scores4<K>(p, e, b, dv, ep);
+#pragma unroll
+    for (int t = 0; t < 4; ++t) {
+      if (e + t < b) {
+#pragma unroll
+        for (int k = 0; k < K; ++k) {
+          const float x = lrelu(ep[t][k], p.slope);
+          const float mn = fmaxf(m[k], x);
+          l[k] = l[k] * __expf(m[k] - mn) + __expf(x - mn);
+          m[k] = mn;
+        }
+      }
+    }
+  }
+  float inv[K];
+#pragma unroll
+  for (int k = 0; k < K; ++k) inv[k] = 1.0f / l[k];
+  for (int64_t e = a; e < b; e += 4) {
+    float ep[4][K];
+    sm_scores4<K>(p, e, b, dv, ep);
+#pragma unroll
+    for (int t = 0; t < 4; ++t) {
+      if (e + t < b) {
+        float al[K];
+#pragma unroll
+        for (int k = 0; k < K; ++k) al[k] = __expf(lrelu(ep[t][k], p.slope) - m[k]) * inv[k];
+        store_k<K>(p.alpha + (e + t) * K, al);
+        if (p.Epre != nullptr) store_k<K>(p.Epre + (e + t) * K, ep[t]);
+      }
+    }
+  }
+}
+
 template <int K>
 __device__ __forceinline__ void warp_merge(float (&m)[K], float (&l)[K]) {
 #pragma unroll
@@ -198,17 +276,34 @@ __global__ void __launch_bounds__(kGatThreads) edge_softmax_kernel(const Softmax
     sm_pass2<K>(p, (int64_t)p.rowptr[v] + threadIdx.x, p.rowptr[v + 1], kGatThreads, dv, m, l);
     return;
   }
+  // light rows, in groups of 32 consecutive rows per warp: a row of at most
+  // 32 edges is one thread's (two passes over its edges, the online max and
+  // sum in registers); the group's rows of 33 .. hub_threshold edges are
+  // then taken one at a time by the whole warp
   const int64_t gw = ((int64_t)blockIdx.x - p.sc.n_tasks) * kGatWarps + w;
   const int64_t nw = ((int64_t)gridDim.x - p.sc.n_tasks) * kGatWarps;
-  for (int64_t v = gw; v < p.n_rows; v += nw) {
-    const int64_t a = p.rowptr[v], b = p.rowptr[v + 1];
-    if (b - a > p.sc.hub_threshold) continue;
-    float dv[K];
-    load_k<K>(p.D + v * K, dv);
-    float m[K], l[K];
-    sm_pass1<K>(p, a + lane, b, 32, dv, m, l);
-    warp_merge<K>(m, l);
-    sm_pass2<K>(p, a + lane, b, 32, dv, m, l);
+  const int64_t groups = (p.n_rows + 31) / 32;
+  for (int64_t grp = gw; grp < groups; grp += nw) {
+    const int64_t r = grp * 32 + lane;
+    int64_t a = 0, b = 0;
+    if (r < p.n_rows) {
+      a = __ldg(p.rowptr + r);
+      b = __ldg(p.rowptr + r + 1);
+    }
+    if (r < p.n_rows && b - a <= 32) sm_thread_row<K>(p, r, a, b);
+    unsigned mid = __ballot_sync(FULL, r < p.n_rows && b - a > 32 && b - a <= p.sc.hub_threshold);
+    while (mid != 0) {
+      const int l0 = __ffs(mid) - 1;
+      mid &= mid - 1;
+      const int64_t v = grp * 32 + l0;
+      const int64_t va = __shfl_sync(FULL, a, l0), vb = __shfl_sync(FULL, b, l0);
+      float dv[K];
+      load_k<K>(p.D + v * K, dv);
+      float m[K], l[K];
+      sm_pass1<K>(p, va + lane, vb, 32, dv, m, l);
+      warp_merge<K>(m, l);
+      sm_pass2<K>(p, va + lane, vb, 32, dv, m, l);
+    }
   }
 }
 
@@ -440,6 +535,16 @@ __global__ void __launch_bounds__(kGatThreads) gat_node_bwd_kernel(const NodeBwd
   const int64_t nw = (int64_t)gridDim.x * kGatWarps;
   for (int64_t u = gw; u < p.n_rows; u += nw) {
     const int64_t a = p.tr_rowptr[u], b = p.tr_rowptr[u + 1];
+    // the node's rows first: they do not depend on the out-edge sums
+    float4 m0 = make_float4(0.f, 0.f, 0.f, 0.f), m1 = m0, h0 = m0, h1 = m0;
+    float ddh = 0.0f;
+    if (live) {
+      m0 = ldg_f4(p.dM + u * p.d + lane * 8);
+      m1 = ldg_f4(p.dM + u * p.d + lane * 8 + 4);
+      h0 = ldg_f4(p.Hp + u * p.d + lane * 8);
+      h1 = ldg_f4(p.Hp + u * p.d + lane * 8 + 4);
+      ddh = __ldg(p.dD + u * K + head);
+    }
     float ds[K];
 #pragma unroll
     for (int k = 0; k < K; ++k) ds[k] = 0.0f;
@@ -450,7 +555,7 @@ __global__ void __launch_bounds__(kGatThreads) gat_node_bwd_kernel(const NodeBwd
       for (int k = 0; k < K; ++k) ds[k] += x[k];
     }
     warp_sum<K>(ds);
-    float dsh = ds[0], ddh;
+    float dsh = ds[0];
 #pragma unroll
     for (int k = 1; k < K; ++k)
       if (head == k) dsh = ds[k];
@@ -462,9 +567,6 @@ __global__ void __launch_bounds__(kGatThreads) gat_node_bwd_kernel(const NodeBwd
       p.dS[u * K + lane] = t;
     }
     if (!live) continue;
-    ddh = __ldg(p.dD + u * K + head);
-    const float4 m0 = ldg_f4(p.dM + u * p.d + lane * 8), m1 = ldg_f4(p.dM + u * p.d + lane * 8 + 4);
-    const float4 h0 = ldg_f4(p.Hp + u * p.d + lane * 8), h1 = ldg_f4(p.Hp + u * p.d + lane * 8 + 4);
     const float mv[8] = {m0.x, m0.y, m0.z, m0.w, m1.x, m1.y, m1.z, m1.w};
     const float hv[8] = {h0.x, h0.y, h0.z, h0.w, h1.x, h1.y, h1.z, h1.w};
     float o[8];
@@ -556,7 +658,8 @@ int edge_softmax(const gq_graph* g, const float* S, const float* D, int heads, f
                  float* alpha, void* ws, size_t ws_bytes, cudaStream_t s) {
   if (g == nullptr || S == nullptr || D == nullptr || alpha == nullptr) return GQ_ERR_INVALID_ARG;
   if (!(heads == 1 || heads == 2 || heads == 4 || heads == 8)) return GQ_ERR_UNSUPPORTED;
-  if (!aligned(S, 16) || !aligned(D, 16)) return GQ_ERR_INVALID_ARG;
+  if (!aligned(S, 16) || !aligned(D, 16) || !aligned(alpha, 16) || (Epre != nullptr && !aligned(Epre, 16)))
+    return GQ_ERR_INVALID_ARG;
   SoftmaxParams p{};
   p.rowptr = g->rowptr;
   p.col = g->col;
@@ -622,7 +725,7 @@ int gat_edge_bwd(const gq_graph* g, const float* dOut, const float* Hp, const ui
 #undef GQ_EB
 }
 
-int node_bwd_blocks() { return sm_count() * 2; }
+int node_bwd_blocks() { return sm_count() * 3; }  // the blocks resident at 80 registers a thread
 
 size_t node_bwd_workspace(int d) { return (size_t)node_bwd_blocks() * 2 * d * sizeof(float) + 256; }
 

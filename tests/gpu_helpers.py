@@ -38,3 +38,20 @@ def hub_graph(n=3000, seed=3):
     """A graph with a dozen rows (in and out) above 256 edges, a heavier
     head up to ~650 edges, and a ragged tail of rows with few edges."""
     return synth.rmat_graph(scale=12, n=n, n_draws=n * 30, a=0.75, b=0.1, c=0.1, seed=seed)
+
+
+def sparse_rows_graph(n=6000, seed=5):
+    """CSR with rows of no edges (also first and last), many single-edge
+    rows (runs of more than 32 rows), mid-size rows, a few hubs of 300-700
+    edges and one of 2000 edges."""
+    rng = np.random.default_rng(seed)
+    kind = rng.random(n)
+    deg = np.where(kind < 0.3, 0, np.where(kind < 0.7, 1, rng.integers(2, 40, n)))
+    deg[rng.choice(n, 6, replace=False)] = rng.integers(300, 700, 6)
+    deg[n // 2] = 2000          # a hub cut into several tasks
+    deg[:3] = 0                 # rows without edges at both ends
+    deg[-3:] = 0
+    rowptr = np.zeros(n + 1, np.int64)
+    rowptr[1:] = np.cumsum(deg)
+    col = np.concatenate([np.sort(rng.choice(n, k, replace=False)) for k in deg]).astype(np.int32)
+    return synth.Graph(n, torch.from_numpy(rowptr.astype(np.int32)), torch.from_numpy(col))

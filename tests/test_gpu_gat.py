@@ -11,19 +11,21 @@ import pytest
 import torch
 
 import synth
-from gpu_helpers import close, gq, hub_graph, rmat_small
+from gpu_helpers import close, gq, hub_graph, rmat_small, sparse_rows_graph
 
 pytestmark = pytest.mark.gpu
 
 
 @pytest.mark.parametrize("heads", [1, 2, 4, 8])
-@pytest.mark.parametrize("graph", ["uniform", "rmat", "hubs_split"])
+@pytest.mark.parametrize("graph", ["uniform", "rmat", "hubs_split", "sparse_rows"])
 def test_edge_softmax(orc, heads, graph):
     q = gq()
     if graph == "uniform":
         g, kw = synth.uniform_graph(1024, 16384, seed=0), {}
     elif graph == "rmat":
         g, kw = rmat_small(), {}
+    elif graph == "sparse_rows":  # rows without edges, 1-edge rows, 2-39-edge rows, hubs
+        g, kw = sparse_rows_graph(), dict(hub_threshold=600, split_edges=512)
     else:
         g, kw = hub_graph(), dict(hub_threshold=32, split_edges=256)
     G = q.graph_prepare(g.rowptr.cuda(), g.col.cuda(), **kw)

@@ -9,7 +9,7 @@ import pytest
 import torch
 
 import synth
-from gpu_helpers import gq, close, rmat_small, hub_graph
+from gpu_helpers import gq, close, rmat_small, hub_graph, sparse_rows_graph
 
 pytestmark = pytest.mark.gpu
 
@@ -103,26 +103,9 @@ def test_edge_spmm(orc, transpose, bits):
     close(Y, ref)
 
 
-def _sparse_rows_graph(n=6000, seed=5):
-    """CSR with rows of no edges (also first and last), many single-edge
-    rows (runs of more than 32 rows), mid-size rows, a few hubs of 300-700
-    edges and one of 2000 edges."""
-    rng = np.random.default_rng(seed)
-    kind = rng.random(n)
-    deg = np.where(kind < 0.3, 0, np.where(kind < 0.7, 1, rng.integers(2, 40, n)))
-    deg[rng.choice(n, 6, replace=False)] = rng.integers(300, 700, 6)
-    deg[n // 2] = 2000          # a row spanning several 256-edge blocks
-    deg[:3] = 0                 # rows without edges at both ends
-    deg[-3:] = 0
-    rowptr = np.zeros(n + 1, np.int64)
-    rowptr[1:] = np.cumsum(deg)
-    col = np.concatenate([np.sort(rng.choice(n, k, replace=False)) for k in deg]).astype(np.int32)
-    return synth.Graph(n, torch.from_numpy(rowptr.astype(np.int32)), torch.from_numpy(col))
-
-
 @pytest.mark.parametrize("transpose", [False, True])
 @pytest.mark.parametrize("bits", [2, 4, 8])
 @pytest.mark.parametrize("d", [68, 128, 196, 256])
 def test_spmm_sparse_rows(orc, transpose, bits, d):
-    _spmm_case(orc, _sparse_rows_graph(), d, bits, 0, transpose, 0.45, hub_threshold=64, split_edges=256)
-    _spmm_case(orc, _sparse_rows_graph(), d, bits, 1, transpose, 0.45)
+    _spmm_case(orc, sparse_rows_graph(), d, bits, 0, transpose, 0.45, hub_threshold=64, split_edges=256)
+    _spmm_case(orc, sparse_rows_graph(), d, bits, 1, transpose, 0.45)
