@@ -560,9 +560,9 @@ def load_traffic(workload):
             rec = json.load(f)
     except (OSError, ValueError):
         return None
-    from quantized_gnn_message_gb300.build import source_digest
+    from quantized_gnn_message_gb300.build import AGGREGATION_SOURCES, source_digest
     ent = rec.get(workload)
-    if not ent or ent.get("source_digest") != source_digest():
+    if not ent or ent.get("source_digest") != source_digest(AGGREGATION_SOURCES):
         return None
     return ent.get("dram_bytes_per_launch")
 

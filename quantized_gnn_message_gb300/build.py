@@ -73,12 +73,19 @@ if __name__ == "__main__":
     print(build(force=True, verbose=True))
 
 
-def source_digest() -> str:
-    """sha256 over the CUDA sources and the public header (identifies the
-    kernels a profile was taken on)."""
+# The sources that define the aggregation kernels (a profile of them stays
+# valid while these files are unchanged).
+AGGREGATION_SOURCES = ("csrc/gq_spmm.cu", "csrc/gq_common.cuh", "csrc/gq_internal.cuh", "../include/gq.h")
+
+
+def source_digest(files=None) -> str:
+    """sha256 over the given sources (paths relative to this package; default:
+    every CUDA source and the public header), identifying the kernels a
+    profile was taken on."""
     import hashlib
+    paths = sorted(_deps()) if files is None else sorted(os.path.normpath(os.path.join(HERE, f)) for f in files)
     h = hashlib.sha256()
-    for p in sorted(_deps()):
+    for p in paths:
         h.update(os.path.basename(p).encode())
         with open(p, "rb") as f:
             h.update(f.read())
