@@ -405,6 +405,24 @@ GQ_API int gq_dequant_spmm_noalloc(const gq_graph* g, int transpose, int coef, c
                                    int64_t ldx, const uint8_t* packed, const uint8_t* mask, int d,
                                    int bits, float* Y, int64_t ldy, gq_stream stream);
 
+/* ------------------------------------------------------------------------
+ * gq_selftest_bounded_wait -- no counterpart on the pages: a check of the
+ * failure path of the library's bounded waits, without a GPU fault.  One
+ * warp waits for phase 0 of an mbarrier, through the wait helper of the
+ * GEMMs (helper 0) or of the aggregation kernels (helper 1), for at most
+ * limit_cycles SM cycles (1e3 .. 2e9).  With complete == 0 nothing ever
+ * arrives on the barrier: the wait gives up and writes 0x5354 to
+ * *dev_status (a device int; only if it still holds 0).  With complete != 0
+ * the barrier completes first and *dev_status is left unchanged.  In the
+ * library's kernels the same helpers write, on a timeout, the GEMM stage
+ * (1 .. 13) to the caller's dev_err word, or 0x5350 to the graph's status
+ * word (an aggregation row copy that did not land).
+ * Errors: GQ_ERR_INVALID_ARG (null dev_status, helper or limit out of
+ * range), GQ_ERR_CUDA.
+ * ---------------------------------------------------------------------- */
+GQ_API int gq_selftest_bounded_wait(int helper, int complete, long long limit_cycles, int* dev_status,
+                                    gq_stream stream);
+
 #ifdef __cplusplus
 }
 #endif

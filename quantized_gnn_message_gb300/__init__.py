@@ -106,6 +106,7 @@ def _SIGNATURES(P, I64, I, U64, F, S):
         ("gq_gcn_layer_fwd", [GP, I, P, I64, I, P, I, P, I, U64, I, P, I64, P, I64, P, S, P, P, P], I),
         ("gq_gcn_layer_bwd",
          [GP, I, P, I64, P, I64, P, I64, P, I, I, P, I, U64, I, I, P, P, I64, P, P, S, P, P, P], I),
+        ("gq_selftest_bounded_wait", [I, I, ctypes.c_longlong, P, P], I),
     ]
 
 
@@ -362,6 +363,14 @@ def to_bf16(src: torch.Tensor, pad_to: int = 8) -> torch.Tensor:
 # --------------------------------------------------------------------------
 # GCN / GraphSAGE-mean layer
 # --------------------------------------------------------------------------
+
+def selftest_bounded_wait(helper: int, complete: bool, limit_cycles: int, status: torch.Tensor):
+    """Run the bounded-wait self-test (gq_selftest_bounded_wait) into the
+    one-element int32 device tensor `status`, on the current stream."""
+    _cuda(status, torch.int32, "status")
+    _check(lib().gq_selftest_bounded_wait(helper, 1 if complete else 0, limit_cycles, _ptr(status), _stream()),
+           "gq_selftest_bounded_wait")
+
 
 class Workspace:
     """A reusable device scratch buffer that grows on demand."""

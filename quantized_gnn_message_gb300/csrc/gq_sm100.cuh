@@ -54,19 +54,47 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
 // or when another thread of the block already aborted, sets *abort, records
 // `where` in *err (first writer wins) and returns false.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort, int* err,
-                                          int where) {
+                                          int where, long long limit = kWaitCycles) {
   if (mbar_try_wait(bar, parity)) return true;
   const long long t0 = clock64();
   while (true) {
     if (mbar_try_wait(bar, parity)) return true;
     if (*abort) return false;
-    if (clock64() - t0 > kWaitCycles) {
+    if (clock64() - t0 > limit) {
       *abort = 1;
       if (err) atomicCAS(err, 0, where);
       return false;
     }
   }
 }
+
+// The same bounded wait for a barrier given by its shared-memory address,
+// without an abort flag: true once the phase with `parity` has completed,
+// false after about `limit` SM cycles (the caller reports the failure).
+__device__ __forceinline__ bool mbar_try_wait_u32(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n"
+      "  .reg .pred p;\n"
+      "  mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+      "  selp.u32 %0, 1, 0, p;\n"
+      "}\n"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+__device__ __forceinline__ bool mbar_wait_u32(uint32_t bar, uint32_t parity, long long limit = kWaitCycles) {
+  if (mbar_try_wait_u32(bar, parity)) return true;
+  const long long t0 = clock64();
+  while (!mbar_try_wait_u32(bar, parity))
+    if (clock64() - t0 > limit) return false;
+  return true;
+}
+
+// Status codes of bounded waits that gave up (written to a device status word).
+constexpr int kWaitCodeAggregation = 0x5350;  // an aggregation slot's row copy did not land
+constexpr int kWaitCodeSelfTest = 0x5354;     // the self-test's never-completed barrier
 
 // 2-D tiled TMA load (box defined by the tensor map) into shared memory,
 // completing `bytes` of transaction count on `bar`.

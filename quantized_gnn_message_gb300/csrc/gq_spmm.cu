@@ -33,6 +33,7 @@
 
 #include "gq_common.cuh"
 #include "gq_internal.cuh"
+#include "gq_sm100.cuh"
 
 namespace gq {
 
@@ -1096,7 +1097,6 @@ __device__ __forceinline__ void bf_write(const SpmmParams& p, bool a_on, bool b_
 // every H edges consumed, the H freed slots are refilled with the edges R
 // ahead, one lane each.
 // ---------------------------------------------------------------------------
-constexpr int kSpmmWaitCode = 0x5350;  // status code: a slot's copy did not land in time
 
 __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
   asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
@@ -1109,28 +1109,6 @@ __device__ __forceinline__ void bar_init(uint32_t bar, uint32_t count) {
 __device__ __forceinline__ void bar_expect_tx(uint32_t bar, uint32_t bytes) {
   asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
 }
-__device__ __forceinline__ bool bar_try_wait(uint32_t bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n"
-      "  .reg .pred p;\n"
-      "  mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
-      "  selp.u32 %0, 1, 0, p;\n"
-      "}\n"
-      : "=r"(ok)
-      : "r"(bar), "r"(parity)
-      : "memory");
-  return ok != 0;
-}
-// Bounded wait (about two seconds of SM clocks).
-__device__ __forceinline__ bool bar_wait(uint32_t bar, uint32_t parity) {
-  if (bar_try_wait(bar, parity)) return true;
-  const long long t0 = clock64();
-  while (!bar_try_wait(bar, parity))
-    if (clock64() - t0 > 4000000000LL) return false;
-  return true;
-}
-
 struct BLane {
   const uint8_t* xb;   // fp32 rows (row 0)
   const uint8_t* pb;   // packed rows (row 0)
@@ -1210,7 +1188,7 @@ __device__ __forceinline__ void b_stream(const SpmmParams& p, BLane& L, f32x2 bi
     }
     const uint32_t u = L.used + (uint32_t)e;
     const uint32_t slot = u & (R - 1);
-    if (!__all_sync(FULL, bar_wait(L.sbar + 8 * slot, (u / R) & 1u))) {  // a warp-wide verdict
+    if (!__all_sync(FULL, mbar_wait_u32(L.sbar + 8 * slot, (u / R) & 1u))) {  // a warp-wide verdict
       L.failed = true;
       break;
     }
@@ -1264,10 +1242,10 @@ __device__ __forceinline__ void b_stream(const SpmmParams& p, BLane& L, f32x2 bi
   }
   if (L.failed) {
     // record the failure, then wait (boundedly) for the copies still in flight
-    if (lane == 0 && p.err != nullptr) atomicCAS(p.err, 0, kSpmmWaitCode);
+    if (lane == 0 && p.err != nullptr) atomicCAS(p.err, 0, kWaitCodeAggregation);
     for (int f = e; f < issued; ++f) {
       const uint32_t u = L.used + (uint32_t)f;
-      bar_wait(L.sbar + 8 * (u & (R - 1)), (u / R) & 1u);
+      mbar_wait_u32(L.sbar + 8 * (u & (R - 1)), (u / R) & 1u);
     }
     return;
   }
