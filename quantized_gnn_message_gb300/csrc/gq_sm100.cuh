@@ -71,16 +71,19 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volati
 // The same bounded wait for a barrier given by its shared-memory address,
 // without an abort flag: true once the phase with `parity` has completed,
 // false after about `limit` SM cycles (the caller reports the failure).
+// The thread is suspended in hardware until the phase completes or about
+// kSuspendNs have passed, instead of spinning on the barrier.
+constexpr uint32_t kSuspendNs = 20000;
 __device__ __forceinline__ bool mbar_try_wait_u32(uint32_t bar, uint32_t parity) {
   uint32_t ok;
   asm volatile(
       "{\n"
       "  .reg .pred p;\n"
-      "  mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+      "  mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n"
       "  selp.u32 %0, 1, 0, p;\n"
       "}\n"
       : "=r"(ok)
-      : "r"(bar), "r"(parity)
+      : "r"(bar), "r"(parity), "n"(kSuspendNs)
       : "memory");
   return ok != 0;
 }

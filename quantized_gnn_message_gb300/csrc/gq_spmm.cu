@@ -1354,7 +1354,7 @@ int launch_bulk(const SpmmParams& p, cudaStream_t s) {
 int launch_bulk_any(const SpmmParams& p, int bits, cudaStream_t s) {
   const bool mx = bits < 32 && p.mask != nullptr;
   const bool wide = p.d > 128;
-#define GQ_BULK(B, M) return wide ? launch_bulk<B, 8, M, 8, 4>(p, s) : launch_bulk<B, 4, M, 16, 8>(p, s)
+#define GQ_BULK(B, M) return wide ? launch_bulk<B, 8, M, 4, 2>(p, s) : launch_bulk<B, 4, M, 8, 4>(p, s)
   switch (bits) {
     case 2: if (mx) GQ_BULK(2, true); GQ_BULK(2, false);
     case 4: if (mx) GQ_BULK(4, true); GQ_BULK(4, false);
