@@ -14,7 +14,10 @@ Routines follow:
       (stochastic integer quantization / de-quantization), Sec. 3.1 (only
       boundary messages are quantized);
   Sancus (IJCAI 2023) Sec. 2: normalized adjacency D~^-1/2 (A+I) D~^-1/2;
-  Tango (arXiv 2308.00890) Sec. 2.1, Fig. 1: GAT forward/backward steps.
+  Tango (arXiv 2308.00890) Sec. 2.1, Fig. 1: GAT forward/backward steps;
+  AdaQP Sec. 4.2 (Problem 11): per-message variance weight beta_k;
+  Tango Sec. 3.2 (Eq. 4): relative quantization error Error_X and the
+      bit-count rule built on it.
 
 Parity status: every routine is pinned by tests/test_oracle_*.py against the
 Tango worked example, closed forms, dense brute force or finite differences,
@@ -81,6 +84,8 @@ def _L():
                 "orc_sddmm_dot": ([I64, P, P, P, P, I, I, P], None),
                 "orc_edge_softmax_bwd": ([I64, P, P, P, P, I, D, P, P, P], None),
                 "orc_edge_segment_sums": ([I64, P, P, P, I, P, P], None),
+                "orc_beta": ([I64, P, P, I, P, I, P], None),
+                "orc_quant_error": ([P, I64, I, P, P, I, D], D),
             }
             for name, (args, res) in sig.items():
                 f = getattr(lib, name)
@@ -204,6 +209,41 @@ def spmm(rowptr, col, coef: int, M, transpose: bool = False) -> np.ndarray:
     f = _L().orc_spmm_t if transpose else _L().orc_spmm
     f(n, _p(rowptr), _p(col), coef, _p(M), d, _p(Y))
     return Y
+
+
+# --------------------------------------------------------------------------
+# message-level quantization metrics (AdaQP Sec. 4.2; Tango Sec. 3.2)
+# --------------------------------------------------------------------------
+
+def beta(rowptr, col, coef: int, X) -> np.ndarray:
+    """AdaQP's variance weight of every message row (Problem 11):
+    beta_k = sum_{v: k->v} a_{k,v}^2 * d * (max X[k] - min X[k])^2 / 6."""
+    rowptr = _c(rowptr, np.int32)
+    col = _c(col, np.int32)
+    X = _c(X, np.float32)
+    n, d = X.shape
+    out = np.zeros(n, np.float64)
+    _L().orc_beta(n, _p(rowptr), _p(col), coef, _p(X), d, _p(out))
+    return out
+
+
+def quant_error(X, packed, mask, bits: int, eps: float = 5e-4) -> float:
+    """Tango's relative quantization error Error_X of the tensor X against
+    its quantized rows (Eq. 4), with |X| + |Xq| + eps as denominator."""
+    X = _c(X, np.float32)
+    n, d = X.shape
+    packed = _c(packed, np.uint8)
+    m = None if mask is None else _c(mask, np.uint8)
+    return float(_L().orc_quant_error(_p(X), n, d, _p(packed), _p(m), bits, eps))
+
+
+def bits_for_error(X, mask, seed: int, threshold: float = 0.3, eps: float = 5e-4, choices=(2, 4, 8)) -> int:
+    """Tango's rule: the fewest bits whose Error_X stays below the threshold
+    (the largest choice if none does)."""
+    for b in choices:
+        if quant_error(X, quantize(X, mask, b, seed), mask, b, eps) < threshold:
+            return b
+    return choices[-1]
 
 
 # --------------------------------------------------------------------------

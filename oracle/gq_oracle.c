@@ -223,6 +223,71 @@ void orc_spmm_t(int64_t n, const int32_t* rowptr, const int32_t* col, int coef, 
 }
 
 /* ------------------------------------------------------------------------ */
+/* AdaQP Sec. 4.2 (Problem 11): variance weight of a message row            */
+/* ------------------------------------------------------------------------ */
+
+/* beta_k = sum_{v in N_T(k)} a_{k,v}^2 * D * (max(h_k) - min(h_k))^2 / 6,
+ * the weight of message k in the gradient-variance objective (the variance
+ * of its quantized copy at b bits is beta_k / (2^b - 1)^2).  On one GPU
+ * N_T(k) is every destination v of an edge k -> v, so the sum runs over
+ * row k of the transposed adjacency; X[k,:] is the message row, D = d. */
+void orc_beta(int64_t n, const int32_t* rowptr, const int32_t* col, int coef, const float* X, int d,
+              double* beta) {
+  int64_t* din = (int64_t*)malloc(sizeof(int64_t) * (size_t)(n + 1));
+  int64_t* dout = (int64_t*)malloc(sizeof(int64_t) * (size_t)(n + 1));
+  double* s2 = (double*)calloc((size_t)n + 1, sizeof(double));
+  degrees(n, rowptr, col, din, dout);
+  for (int64_t v = 0; v < n; ++v)
+    for (int64_t e = rowptr[v]; e < rowptr[v + 1]; ++e) {
+      const int64_t k = col[e];
+      const double a = coef_of(coef, din[v], dout[k]);
+      s2[k] += a * a;
+    }
+  for (int64_t k = 0; k < n; ++k) {
+    double mn = X[k * d], mx = X[k * d];
+    for (int j = 1; j < d; ++j) {
+      const double x = X[k * d + j];
+      if (x < mn) mn = x;
+      if (x > mx) mx = x;
+    }
+    beta[k] = s2[k] * (double)d * (mx - mn) * (mx - mn) / 6.0;
+  }
+  free(din);
+  free(dout);
+  free(s2);
+}
+
+/* ------------------------------------------------------------------------ */
+/* Tango Sec. 3.2 (Eq. 4): relative quantization error of a tensor          */
+/* ------------------------------------------------------------------------ */
+
+/* Error_X = (1/N) sum_i |X_i - Xq_i| / (|X_i| + |Xq_i| + eps) over the
+ * N = n*d elements, Xq_i the de-quantized value (AdaQP Eqn 5, fmaf(q, S,
+ * Z)) of a quantized row and X_i itself for a row that is not quantized
+ * (mask 0: a zero term).  The absolute values in the denominator are this
+ * build's reading: the page adds X_i and Xq_i for a symmetric quantizer,
+ * where both have one sign, and states that the metric lies in [0, 1]. */
+double orc_quant_error(const float* X, int64_t n, int d, const uint8_t* packed, const uint8_t* mask,
+                       int bits, double eps) {
+  const int64_t pitch = orc_pitch(d, bits);
+  const int64_t hoff = orc_header_offset(d, bits);
+  double sum = 0.0;
+  for (int64_t r = 0; r < n; ++r) {
+    if (mask != NULL && mask[r] == 0) continue;
+    const uint8_t* row = packed + r * pitch;
+    float S, mn;
+    memcpy(&S, row + hoff, 4);
+    memcpy(&mn, row + hoff + 4, 4);
+    for (int j = 0; j < d; ++j) {
+      const float xq = fmaf((float)packed_code(row, j, bits), S, mn);
+      const double x = X[r * d + j];
+      sum += fabs(x - (double)xq) / (fabs(x) + fabs((double)xq) + eps);
+    }
+  }
+  return n > 0 ? sum / ((double)n * (double)d) : 0.0;
+}
+
+/* ------------------------------------------------------------------------ */
 /* GAT (Tango Sec. 2.1, Fig. 1a)                                            */
 /* ------------------------------------------------------------------------ */
 
