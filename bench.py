@@ -503,13 +503,19 @@ def run_aggregate(args, w):
     rows = []
     tot_edges, tot_ms = 0, 0.0
     best = None
+    beta_rows = []
+    bt = torch.empty(n, dtype=torch.float32, device=dev)
     with ClockSampler(0) as clocks:
         for d in ds:
             Xd = X[:, :d]
             Yd = Y[:n * d].view(n, d)
+            tbeta = _timed(lambda: q.message_variance_weights(G, Xd, q.COEF_GCN, out=bt), args.steps, flush)
+            bbytes = n * d * 4 + (n + 1) * 4 + E * 4 + n * 4 + n * 4
+            beta_rows.append({"d": d, "beta_ms": tbeta, "beta_gbs": bbytes / (tbeta / 1e3) / 1e9})
             for b in bl:
                 pk = torch.empty(n, q.packed_pitch(d, b), dtype=torch.uint8, device=dev)
                 qz = lambda: q.quantize_pack(Xd, None, b, 7, out=pk)
+                qe = lambda: q.quant_error(Xd, pk, None, b)
                 fw = lambda: q.dequant_spmm(G, None, pk, None, d, b, out=Yd)
                 bw = lambda: q.dequant_spmm(G, None, pk, None, d, b, transpose=True, out=Yd)
                 for _ in range(args.warmup):
@@ -518,6 +524,7 @@ def run_aggregate(args, w):
                 tq = _timed(qz, args.steps, flush)
                 tf = _timed(fw, args.steps, flush)
                 tb = _timed(bw, args.steps, flush)
+                te = _timed(qe, args.steps, flush)
                 torch.cuda.profiler.stop()
                 pitch = q.packed_pitch(d, b)
                 comp = (n + 1) * 4 + E * 4 + 2 * n * 4 + n * pitch + n * d * 4
@@ -525,6 +532,7 @@ def run_aggregate(args, w):
                 qbytes = n * d * 4 + n * pitch
                 r = {"d": d, "bits": b, "quantize_ms": tq, "fwd_ms": tf, "bwd_ms": tb,
                      "quantize_gbs": qbytes / (tq / 1e3) / 1e9,
+                     "error_metric_ms": te, "error_metric_gbs": qbytes / (te / 1e3) / 1e9,
                      "fwd_gbs_compulsory": comp / (tf / 1e3) / 1e9, "bwd_gbs_compulsory": comp / (tb / 1e3) / 1e9,
                      "fwd_gbs_streaming": stream / (tf / 1e3) / 1e9, "bwd_gbs_streaming": stream / (tb / 1e3) / 1e9,
                      "edges_per_s_fwd": E / (tf / 1e3)}
@@ -540,7 +548,7 @@ def run_aggregate(args, w):
             "data": "synthetic",
             "config": {"workload": w.name, "nodes": n, "edges": E, "sweep_d": ds, "bits": bl,
                        "generation_s": t_gen, "prepare_s": t_prep, "l2": "flushed before every timed call"},
-            "sweep": rows,
+            "sweep": rows, "variance_weights": beta_rows,
             "roofline": {"kernel": "spmm_kernel forward (best of sweep)", "bound": "hbm",
                          "achieved": best["fwd_gbs_compulsory"], "peak": peak, "unit": "GB/s",
                          "frac": best["fwd_gbs_compulsory"] / peak, "peak_source": f"hbm_gbs of {kind}",

@@ -406,6 +406,43 @@ GQ_API int gq_dequant_spmm_noalloc(const gq_graph* g, int transpose, int coef, c
                                    int bits, float* Y, int64_t ldy, gq_stream stream);
 
 /* ------------------------------------------------------------------------
+ * gq_message_variance_weights -- AdaQP Sec. 4.2, the weight of message k in
+ * the gradient-variance objective (Problem 11):
+ *   beta[k] = sum_{v in N_T(k)} a_{k,v}^2 * d * (max X[k,:] - min X[k,:])^2 / 6
+ * with N_T(k) every destination v of an edge k -> v (on one GPU all of
+ * them live on the "target device") and a_{k,v} the coefficient `coef`
+ * (gq_coef) the aggregation applies; the aggregated error of message k
+ * quantized at b bits has variance beta[k] / (2^b - 1)^2.  X: n x d fp32
+ * (ldx), the message rows before quantization; beta: n fp32.  ws:
+ * gq_message_variance_weights_workspace_bytes(g) bytes (partial sums of
+ * the nodes with more out-edges than the hub threshold; may be NULL when 0).
+ * Sums in fp32 in a fixed order.  Errors: GQ_ERR_INVALID_ARG,
+ * GQ_ERR_WORKSPACE, GQ_ERR_CUDA.
+ * ---------------------------------------------------------------------- */
+GQ_API size_t gq_message_variance_weights_workspace_bytes(const gq_graph* g);
+GQ_API int gq_message_variance_weights(const gq_graph* g, int coef, const float* X, int64_t ldx, int d,
+                                       float* beta, void* ws, size_t ws_bytes, gq_stream stream);
+
+/* ------------------------------------------------------------------------
+ * gq_quant_error -- Tango Sec. 3.2, Eq. 4, the relative quantization error
+ * of a tensor:
+ *   *err = (1/(n d)) sum_{r, j} |X[r,j] - Xq[r,j]| / (|X[r,j]| + |Xq[r,j]| + eps)
+ * with Xq[r,j] = fmaf(q, S, Z) from the packed row r (bits 2, 4, 8) where
+ * mask[r] != 0 (mask NULL: every row), and Xq = X (a zero term) otherwise.
+ * The absolute values read the page's denominator X + Xq, written for a
+ * symmetric quantizer whose two values share one sign; the metric lies in
+ * [0, 1].  Tango takes eps = 0.0005 and keeps the fewest bits with an error
+ * below 0.3.  err: one device double.  ws: gq_quant_error_workspace_bytes()
+ * bytes (8-byte aligned).  fp32 per row, fp64 across rows, fixed order.
+ * Errors: GQ_ERR_INVALID_ARG (bad bits, eps <= 0, null or misaligned
+ * pointers), GQ_ERR_WORKSPACE, GQ_ERR_CUDA.
+ * ---------------------------------------------------------------------- */
+GQ_API size_t gq_quant_error_workspace_bytes(void);
+GQ_API int gq_quant_error(const float* X, int64_t n, int d, int64_t ldx, const uint8_t* packed,
+                          const uint8_t* mask, int bits, float eps, double* err, void* ws, size_t ws_bytes,
+                          gq_stream stream);
+
+/* ------------------------------------------------------------------------
  * gq_selftest_bounded_wait -- no counterpart on the pages: a check of the
  * failure path of the library's bounded waits, without a GPU fault.  One
  * warp waits for phase 0 of an mbarrier, through the wait helper of the

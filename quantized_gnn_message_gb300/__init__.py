@@ -107,6 +107,10 @@ def _SIGNATURES(P, I64, I, U64, F, S):
         ("gq_gcn_layer_bwd",
          [GP, I, P, I64, P, I64, P, I64, P, I, I, P, I, U64, I, I, P, P, I64, P, P, S, P, P, P], I),
         ("gq_selftest_bounded_wait", [I, I, ctypes.c_longlong, P, P], I),
+        ("gq_message_variance_weights_workspace_bytes", [GP], S),
+        ("gq_message_variance_weights", [GP, I, P, I64, I, P, P, S, P], I),
+        ("gq_quant_error_workspace_bytes", [], S),
+        ("gq_quant_error", [P, I64, I, I64, P, P, I, F, P, P, S, P], I),
     ]
 
 
@@ -363,6 +367,47 @@ def to_bf16(src: torch.Tensor, pad_to: int = 8) -> torch.Tensor:
 # --------------------------------------------------------------------------
 # GCN / GraphSAGE-mean layer
 # --------------------------------------------------------------------------
+
+def message_variance_weights(g: Graph, X: torch.Tensor, coef: int = COEF_GCN,
+                             out: torch.Tensor | None = None) -> torch.Tensor:
+    """AdaQP's beta_k of every message row X[k] (gq_message_variance_weights)."""
+    _cuda(X, torch.float32, "X")
+    n, d = X.shape
+    if out is None:
+        out = torch.empty(n, dtype=torch.float32, device=X.device)
+    L = lib()
+    wb = int(L.gq_message_variance_weights_workspace_bytes(g.ref))
+    ws = torch.empty(max(wb, 1), dtype=torch.uint8, device=X.device)
+    _check(L.gq_message_variance_weights(g.ref, coef, _ptr(X), _rows(X), d, _ptr(out), _ptr(ws), wb, _stream()),
+           "gq_message_variance_weights")
+    return out
+
+
+def quant_error(X: torch.Tensor, packed: torch.Tensor, mask: torch.Tensor | None, bits: int,
+                eps: float = 5e-4) -> torch.Tensor:
+    """Tango's Error_X of X against its packed rows (gq_quant_error), as a
+    one-element float64 device tensor."""
+    _cuda(X, torch.float32, "X")
+    _cuda(packed, torch.uint8, "packed")
+    n, d = X.shape
+    L = lib()
+    ws = torch.empty(int(L.gq_quant_error_workspace_bytes()), dtype=torch.uint8, device=X.device)
+    err = torch.empty(1, dtype=torch.float64, device=X.device)
+    m = None if mask is None else _cuda(mask, torch.uint8, "mask")
+    _check(L.gq_quant_error(_ptr(X), n, d, _rows(X), _ptr(packed), _ptr(m), bits, eps, _ptr(err), _ptr(ws),
+                            ws.numel(), _stream()), "gq_quant_error")
+    return err
+
+
+def bits_for_error(X: torch.Tensor, mask: torch.Tensor | None, seed: int, threshold: float = 0.3,
+                   eps: float = 5e-4, choices=(2, 4, 8)) -> int:
+    """Tango's bit-count rule on the GPU: the fewest bits whose Error_X stays
+    below the threshold (the largest choice if none does)."""
+    for b in choices:
+        if float(quant_error(X, quantize_pack(X, mask, b, seed), mask, b, eps).item()) < threshold:
+            return b
+    return choices[-1]
+
 
 def selftest_bounded_wait(helper: int, complete: bool, limit_cycles: int, status: torch.Tensor):
     """Run the bounded-wait self-test (gq_selftest_bounded_wait) into the

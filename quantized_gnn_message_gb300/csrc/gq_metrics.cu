@@ -1,0 +1,242 @@
+// gq_metrics.cu -- message-level quantization metrics.
+//
+// message_variance_weights (AdaQP Sec. 4.2, the weight beta_k of message k
+// in Problem 11):
+//   beta_k = sum_{v in N_T(k)} a_{k,v}^2 * D * (max h_k - min h_k)^2 / 6,
+// where N_T(k) is every destination v of an edge k -> v (one GPU holds all
+// of them) and a_{k,v} the aggregation coefficient; the variance of the
+// aggregated error of message k quantized at b bits is beta_k / (2^b-1)^2.
+// One warp per node: a min/max reduction over the row and a sum of a^2 over
+// the node's out-edges (its row of the transposed CSR); a node with more
+// out-edges than the graph's hub threshold is summed by blocks, one per
+// task of the transposed heavy-row schedule, whose partials are added in
+// task order.  Every sum has a fixed order.
+//
+// quant_error (Tango Sec. 3.2, Eq. 4):
+//   Error_X = (1/N) sum_i |X_i - Xq_i| / (|X_i| + |Xq_i| + eps)
+// over the N = n*d elements, Xq the de-quantized value (fmaf(q, S, Z)) of a
+// quantized row; a row with mask 0 is not quantized and adds nothing.  The
+// absolute values in the denominator read the page's X_i + Xq_i for an
+// asymmetric quantizer (the page's values share one sign).  A warp per row
+// sums its terms in fp32, each lane keeps an fp64 total; block partials are
+// added in block order by a second kernel.
+#include "gq_common.cuh"
+#include "gq_internal.cuh"
+
+namespace gq {
+namespace {
+
+constexpr int kMetricThreads = 256;
+constexpr int kMetricWarps = kMetricThreads / 32;
+
+struct BetaParams {
+  int64_t n;
+  const int32_t* tr_rowptr;
+  const int32_t* tr_col;
+  const float* dinv_in;
+  const float* dinv_out;
+  const float* inv_in;
+  int coef;
+  const float* X;
+  int64_t ldx;
+  int d;
+  float* beta;
+  const int32_t* tasks;   // heavy rows of the transposed CSR (gq_sched)
+  const int32_t* groups;
+  int64_t n_tasks;
+  int hub_threshold;
+  float* part;            // [task] partial sums of a^2
+};
+
+// a_{k,v} of the edge k -> v (v = a destination of node k)
+__device__ __forceinline__ float beta_coef(const BetaParams& p, float sk, int32_t v) {
+  return p.coef == GQ_COEF_GCN ? sk * __ldg(p.dinv_in + v) : (p.coef == GQ_COEF_SAGE ? __ldg(p.inv_in + v) : 1.0f);
+}
+
+// (lane-strided) sum of a^2 over the edges [a, b) of node k's row
+__device__ __forceinline__ float beta_s2(const BetaParams& p, float sk, int64_t a, int64_t b, int first, int stride) {
+  float s2 = 0.0f;
+  for (int64_t e = a + first; e < b; e += stride) {
+    const float c = beta_coef(p, sk, __ldg(p.tr_col + e));
+    s2 = __fmaf_rn(c, c, s2);
+  }
+  return s2;
+}
+
+// beta[k] from the warp's (lane 0) s2, after a min/max reduction over X[k]
+__device__ __forceinline__ void beta_finish(const BetaParams& p, int64_t k, float s2) {
+  const int lane = threadIdx.x & 31;
+  const float* x = p.X + k * p.ldx;
+  float mn = __int_as_float(0x7f800000), mx = -mn;  // +inf, -inf
+  for (int j = lane; j < p.d; j += 32) {
+    const float v = __ldg(x + j);
+    mn = fminf(mn, v);
+    mx = fmaxf(mx, v);
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    mn = fminf(mn, __shfl_xor_sync(FULL, mn, o));
+    mx = fmaxf(mx, __shfl_xor_sync(FULL, mx, o));
+  }
+  if (lane == 0) {
+    const float r = mx - mn;
+    p.beta[k] = s2 * (float)p.d * r * r * (1.0f / 6.0f);
+  }
+}
+
+// Blocks [0, n_tasks): one heavy-row task each, its partial sum of a^2 to
+// part[task].  Other blocks: one warp per light node (out-degree at most
+// hub_threshold), beta written directly.
+__global__ void __launch_bounds__(kMetricThreads) beta_kernel(const BetaParams p) {
+  __shared__ float red[kMetricWarps];
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  if ((int64_t)blockIdx.x < p.n_tasks) {
+    const int4 task = __ldg(reinterpret_cast<const int4*>(p.tasks) + blockIdx.x);
+    const float sk = p.coef == GQ_COEF_GCN ? __ldg(p.dinv_out + task.x) : 1.0f;
+    float s2 = beta_s2(p, sk, task.y, task.z, threadIdx.x, blockDim.x);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) s2 += __shfl_xor_sync(FULL, s2, o);
+    if (lane == 0) red[w] = s2;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      float t = 0.0f;
+      for (int i = 0; i < kMetricWarps; ++i) t += red[i];
+      p.part[blockIdx.x] = t;
+    }
+    return;
+  }
+  const int64_t gw = ((int64_t)blockIdx.x - p.n_tasks) * kMetricWarps + w;
+  const int64_t nw = ((int64_t)gridDim.x - p.n_tasks) * kMetricWarps;
+  for (int64_t k = gw; k < p.n; k += nw) {
+    const int64_t a = __ldg(p.tr_rowptr + k), b = __ldg(p.tr_rowptr + k + 1);
+    if (b - a > p.hub_threshold) continue;  // a heavy row: its tasks
+    const float sk = p.coef == GQ_COEF_GCN ? __ldg(p.dinv_out + k) : 1.0f;
+    float s2 = beta_s2(p, sk, a, b, lane, 32);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) s2 += __shfl_xor_sync(FULL, s2, o);
+    beta_finish(p, k, s2);
+  }
+}
+
+// One warp per heavy-row task: the first task of each row adds the row's
+// task partials in task order and writes beta.
+__global__ void __launch_bounds__(kMetricThreads) beta_heavy_kernel(const BetaParams p) {
+  const int64_t t = (blockIdx.x * (int64_t)blockDim.x + threadIdx.x) >> 5;
+  if (t >= p.n_tasks) return;
+  const int4 task = __ldg(reinterpret_cast<const int4*>(p.tasks) + t);
+  float s2;
+  if (task.w < 0) {
+    s2 = __ldcg(p.part + t);
+  } else {
+    const int4 grp = __ldg(reinterpret_cast<const int4*>(p.groups) + task.w);
+    if (grp.y != t) return;  // not the group's first task
+    s2 = 0.0f;
+    for (int i = 0; i < grp.z; ++i) s2 += __ldcg(p.part + grp.y + i);
+  }
+  beta_finish(p, task.x, s2);
+}
+
+__global__ void __launch_bounds__(kMetricThreads) quant_error_kernel(const float* __restrict__ X, int64_t n, int d,
+                                                                    int64_t ldx, const uint8_t* __restrict__ packed,
+                                                                    int64_t pitch, int64_t hoff,
+                                                                    const uint8_t* __restrict__ mask, int bits,
+                                                                    float eps, double* __restrict__ part) {
+  __shared__ double red[kMetricWarps];
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  const int64_t gw = (blockIdx.x * (int64_t)blockDim.x + threadIdx.x) >> 5;
+  const int64_t nw = (gridDim.x * (int64_t)blockDim.x) >> 5;
+  const uint32_t cmask = (1u << bits) - 1u;
+  double tot = 0.0;
+  for (int64_t r = gw; r < n; r += nw) {
+    if (mask != nullptr && __ldg(mask + r) == 0) continue;
+    const uint8_t* row = packed + r * pitch;
+    const float2 h = __ldg(reinterpret_cast<const float2*>(row + hoff));  // {S, Z}
+    const float* x = X + r * ldx;
+    float s = 0.0f;
+    for (int j = lane; j < d; j += 32) {
+      const int bit = j * bits;
+      const uint32_t q = ((uint32_t)__ldg(row + (bit >> 3)) >> (bit & 7)) & cmask;
+      const float xq = __fmaf_rn((float)q, h.x, h.y);
+      const float xv = __ldg(x + j);
+      s += fabsf(xv - xq) / (fabsf(xv) + fabsf(xq) + eps);
+    }
+    tot += (double)s;
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) tot += __shfl_xor_sync(FULL, tot, o);
+  if (lane == 0) red[w] = tot;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    double t = 0.0;
+    for (int i = 0; i < kMetricWarps; ++i) t += red[i];
+    part[blockIdx.x] = t;
+  }
+}
+
+__global__ void sum_parts_kernel(const double* __restrict__ part, int blocks, double inv_n, double* __restrict__ out) {
+  if (threadIdx.x == 0 && blockIdx.x == 0) {
+    double t = 0.0;
+    for (int i = 0; i < blocks; ++i) t += part[i];
+    *out = t * inv_n;
+  }
+}
+
+int error_blocks() { return sm_count() * 4; }
+
+}  // namespace
+}  // namespace gq
+
+extern "C" size_t gq_message_variance_weights_workspace_bytes(const gq_graph* g) {
+  if (g == nullptr) return 0;
+  return ((size_t)g->tr_sched.n_tasks * sizeof(float) + 255) / 256 * 256;
+}
+
+extern "C" int gq_message_variance_weights(const gq_graph* g, int coef, const float* X, int64_t ldx, int d,
+                                           float* beta, void* ws, size_t ws_bytes, gq_stream stream) {
+  using namespace gq;
+  if (g == nullptr || X == nullptr || beta == nullptr || d < 1 || ldx < d) return GQ_ERR_INVALID_ARG;
+  if (!(coef == GQ_COEF_GCN || coef == GQ_COEF_SAGE || coef == GQ_COEF_ONE)) return GQ_ERR_INVALID_ARG;
+  const gq_sched& sc = g->tr_sched;
+  if (sc.n_tasks > 0 && (ws == nullptr || ws_bytes < (size_t)sc.n_tasks * sizeof(float) || !aligned(ws, 4)))
+    return GQ_ERR_WORKSPACE;
+  BetaParams p{g->n, g->tr_rowptr, g->tr_col, g->dinv_in, g->dinv_out, g->inv_in, coef, X, ldx, d, beta,
+               sc.tasks, sc.groups, sc.n_tasks, g->hub_threshold, static_cast<float*>(ws)};
+  int64_t light = (g->n + kMetricWarps - 1) / kMetricWarps;
+  const int64_t cap = (int64_t)sm_count() * 8;
+  if (light > cap) light = cap;
+  if (light < 1) light = 1;
+  const int64_t grid = sc.n_tasks + light;
+  if (grid > 0x7fffffff) return GQ_ERR_UNSUPPORTED;
+  cudaStream_t s = (cudaStream_t)stream;
+  beta_kernel<<<(unsigned)grid, kMetricThreads, 0, s>>>(p);
+  GQ_TRY(launch_status());
+  if (sc.n_tasks > 0) {
+    beta_heavy_kernel<<<(unsigned)((sc.n_tasks + kMetricWarps - 1) / kMetricWarps), kMetricThreads, 0, s>>>(p);
+    GQ_TRY(launch_status());
+  }
+  return GQ_OK;
+}
+
+extern "C" size_t gq_quant_error_workspace_bytes(void) { return (size_t)gq::error_blocks() * sizeof(double); }
+
+extern "C" int gq_quant_error(const float* X, int64_t n, int d, int64_t ldx, const uint8_t* packed,
+                              const uint8_t* mask, int bits, float eps, double* err, void* ws, size_t ws_bytes,
+                              gq_stream stream) {
+  using namespace gq;
+  if (err == nullptr || n < 0 || d < 1 || ldx < d || !valid_bits(bits) || !(eps > 0.0f)) return GQ_ERR_INVALID_ARG;
+  if (n == 0) {  // an empty tensor: no elements, no error
+    GQ_TRY_CUDA(cudaMemsetAsync(err, 0, sizeof(double), (cudaStream_t)stream));
+    return GQ_OK;
+  }
+  if (X == nullptr || packed == nullptr || !aligned(packed, 16)) return GQ_ERR_INVALID_ARG;
+  const int blocks = error_blocks();
+  if (ws == nullptr || ws_bytes < (size_t)blocks * sizeof(double) || !aligned(ws, 8)) return GQ_ERR_WORKSPACE;
+  cudaStream_t s = (cudaStream_t)stream;
+  double* part = static_cast<double*>(ws);
+  quant_error_kernel<<<blocks, kMetricThreads, 0, s>>>(X, n, d, ldx, packed, packed_pitch(d, bits),
+                                                       header_offset(d, bits), mask, bits, eps, part);
+  GQ_TRY(launch_status());
+  const double inv_n = n > 0 ? 1.0 / ((double)n * (double)d) : 0.0;
+  sum_parts_kernel<<<1, 32, 0, s>>>(part, blocks, inv_n, err);
+  return launch_status();
+}

@@ -1,0 +1,92 @@
+"""Message-level quantization metrics on the GPU vs the oracle:
+AdaQP Sec. 4.2 beta_k (gq_message_variance_weights) and Tango Sec. 3.2
+Eq. 4 Error_X (gq_quant_error) with its bit-count rule.  beta within
+1e-4 (1 + |ref|) relative to the oracle's float64 value; Error_X on the
+GPU's own packed bytes within 1e-5 relative."""
+import numpy as np
+import pytest
+import torch
+
+import synth
+from gpu_helpers import gq, hub_graph, rmat_small, sparse_rows_graph
+
+pytestmark = pytest.mark.gpu
+
+
+def _rel_close(gpu, ref, rtol):
+    gpu = np.asarray(gpu, np.float64)
+    ref = np.asarray(ref, np.float64)
+    err = np.abs(gpu - ref) - rtol * np.maximum(np.abs(ref), 1e-30)
+    assert err.max() <= 0, (float(np.abs(gpu - ref).max()), int((err > 0).sum()))
+
+
+@pytest.mark.parametrize("graph", ["uniform", "rmat", "hubs", "hubs_split", "sparse_rows"])
+@pytest.mark.parametrize("coef", [0, 1, 2])
+@pytest.mark.parametrize("d", [7, 64, 256])
+def test_beta(orc, graph, coef, d):
+    q = gq()
+    g = {"uniform": lambda: synth.uniform_graph(1024, 16384, seed=0), "rmat": rmat_small,
+         "hubs": hub_graph, "hubs_split": hub_graph, "sparse_rows": sparse_rows_graph}[graph]()
+    kw = dict(hub_threshold=32, split_edges=256) if graph == "hubs_split" else {}
+    G = q.graph_prepare(g.rowptr.cuda(), g.col.cuda(), **kw)
+    if graph == "hubs_split":
+        assert G.c.tr_sched.n_groups > 0  # nodes whose out-edges are cut into several tasks
+    X = synth.normal_matrix(g.n, d, seed=d + coef).numpy()
+    beta = q.message_variance_weights(G, torch.from_numpy(X).cuda(), coef).cpu().numpy()
+    _rel_close(beta, orc.beta(g.rowptr.numpy(), g.col.numpy(), coef, X), 1e-4)
+
+
+def test_beta_padded_rows(orc):
+    q = gq()
+    g = rmat_small()
+    G = q.graph_prepare(g.rowptr.cuda(), g.col.cuda())
+    Xfull = synth.normal_matrix(g.n, 40, seed=3)
+    X = Xfull[:, :33]  # ldx = 40 > d = 33
+    beta = q.message_variance_weights(G, Xfull.cuda()[:, :33], 0).cpu().numpy()
+    _rel_close(beta, orc.beta(g.rowptr.numpy(), g.col.numpy(), 0, X.contiguous().numpy()), 1e-4)
+
+
+@pytest.mark.parametrize("bits", [2, 4, 8])
+@pytest.mark.parametrize("d", [5, 64, 100, 256])
+@pytest.mark.parametrize("mask_frac", [None, 0.4])
+def test_quant_error(orc, bits, d, mask_frac):
+    q = gq()
+    n = 3000
+    X = synth.normal_matrix(n, d, seed=bits * 7 + d).numpy()
+    mask = None if mask_frac is None else synth.bernoulli_mask(n, mask_frac, seed=2).numpy()
+    Xd = torch.from_numpy(X).cuda()
+    md = None if mask is None else torch.from_numpy(mask).cuda()
+    pk = q.quantize_pack(Xd, md, bits, 17)
+    err = float(q.quant_error(Xd, pk, md, bits).item())
+    ref = orc.quant_error(X, pk.cpu().numpy(), mask, bits)
+    assert err == pytest.approx(ref, rel=1e-5)
+    assert 0.0 <= err <= 1.0
+
+
+def test_quant_error_empty_and_constant_rows(orc):
+    q = gq()
+    X0 = torch.zeros(0, 16, device="cuda")
+    pk = q.quantize_pack(X0, None, 4, 1)
+    assert float(q.quant_error(X0, pk, None, 4).item()) == 0.0
+    X = np.full((10, 16), 2.5, np.float32)  # constant rows de-quantize exactly
+    Xd = torch.from_numpy(X).cuda()
+    assert float(q.quant_error(Xd, q.quantize_pack(Xd, None, 2, 1), None, 2).item()) == 0.0
+
+
+def test_bits_rule_matches_oracle(orc):
+    q = gq()
+    X = synth.normal_matrix(2000, 64, seed=8).numpy()
+    Xd = torch.from_numpy(X).cuda()
+    errs = {b: orc.quant_error(X, orc.quantize(X, None, b, 5), None, b) for b in (2, 4, 8)}
+    for thr in (0.5, errs[2] * 0.999, errs[4] * 1.001, errs[4] * 0.999, 1e-6):
+        assert q.bits_for_error(Xd, None, 5, threshold=thr) == orc.bits_for_error(X, None, 5, threshold=thr)
+
+
+def test_quant_error_rejects_bad_arguments():
+    q = gq()
+    X = torch.zeros(4, 8, device="cuda")
+    pk = q.quantize_pack(X, None, 4, 0)
+    with pytest.raises(q.GQError):
+        q.quant_error(X, pk, None, 3)
+    with pytest.raises(q.GQError):
+        q.quant_error(X, pk, None, 4, eps=0.0)
