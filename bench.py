@@ -512,6 +512,18 @@ def run_aggregate(args, w):
             tbeta = _timed(lambda: q.message_variance_weights(G, Xd, q.COEF_GCN, out=bt), args.steps, flush)
             bbytes = n * d * 4 + (n + 1) * 4 + E * 4 + n * 4 + n * 4
             beta_rows.append({"d": d, "beta_ms": tbeta, "beta_gbs": bbytes / (tbeta / 1e3) / 1e9})
+            if 64 < d <= 256:
+                # per-message widths drawn uniformly from {2, 4, 8} (AdaQP's sampling ablation)
+                u = synth.uniform01(synth.stream_seed(w.seed, 0x42), torch.arange(n, dtype=torch.int64, device=dev), 0)
+                rb = torch.tensor([2, 4, 8], dtype=torch.uint8, device=dev)[torch.clamp((u * 3).long(), max=2)]
+                pkm, roff = q.quantize_pack_mixed(Xd, rb, 7)
+                tmq = _timed(lambda: q.quantize_pack_mixed(Xd, rb, 7, roff=roff), args.steps, flush)
+                tmf = _timed(lambda: q.dequant_spmm_mixed(G, Xd, pkm, roff, rb, out=Yd), args.steps, flush)
+                mbytes = (n + 1) * 4 + E * 4 + 2 * n * 4 + n + n * 8 + int(roff[n].item()) + n * d * 4
+                beta_rows[-1].update({"mixed_quantize_ms": tmq, "mixed_fwd_ms": tmf,
+                                      "mixed_fwd_gbs_compulsory": mbytes / (tmf / 1e3) / 1e9,
+                                      "mixed_edges_per_s": E / (tmf / 1e3)})
+                del pkm, roff, rb, u
             for b in bl:
                 pk = torch.empty(n, q.packed_pitch(d, b), dtype=torch.uint8, device=dev)
                 qz = lambda: q.quantize_pack(Xd, None, b, 7, out=pk)
@@ -548,7 +560,7 @@ def run_aggregate(args, w):
             "data": "synthetic",
             "config": {"workload": w.name, "nodes": n, "edges": E, "sweep_d": ds, "bits": bl,
                        "generation_s": t_gen, "prepare_s": t_prep, "l2": "flushed before every timed call"},
-            "sweep": rows, "variance_weights": beta_rows,
+            "sweep": rows, "per_width": beta_rows,
             "roofline": {"kernel": "spmm_kernel forward (best of sweep)", "bound": "hbm",
                          "achieved": best["fwd_gbs_compulsory"], "peak": peak, "unit": "GB/s",
                          "frac": best["fwd_gbs_compulsory"] / peak, "peak_source": f"hbm_gbs of {kind}",

@@ -239,6 +239,34 @@ GQ_API int gq_dequant_spmm(const gq_graph* g, int transpose, int coef, const flo
                     int64_t ldy, void* ws, size_t ws_bytes, gq_stream stream);
 
 /* ------------------------------------------------------------------------
+ * Mixed bit-widths per row -- AdaQP Sec. 3.2 / 4.2 assign a bit-width to
+ * every message (or group of messages); the uniform-sampling ablation
+ * (Sec. 5.3) draws it per message from {2, 4, 8}.  A mixed packed buffer
+ * holds row r at byte roff[r], in the packed-row layout of its own width
+ * rbits[r] (pitch gq_packed_pitch(d, rbits[r])); rows whose width is not 2,
+ * 4 or 8 (e.g. 0) are full-precision rows and take no bytes.
+ *
+ * gq_packed_row_offsets -- roff[0..n] (n+1 int64, device) from rbits (n
+ * uint8, device): roff[r] = sum_{i<r} size of row i; roff[n] is the buffer
+ * size.  ws: gq_packed_row_offsets_workspace_bytes(n) bytes, 8-byte aligned.
+ * gq_quantize_pack_mixed -- AdaQP Eqn 4 on every row with width 2, 4 or 8,
+ * each at its own width; row r's bytes equal gq_quantize_pack's row r at
+ * that width and seed.  packed: roff[n] bytes, 16-byte aligned.
+ * gq_dequant_spmm_mixed -- gq_dequant_spmm over such a buffer (each packed
+ * row de-quantized at its own width, other rows read from X); 64 < d <= 256
+ * (GQ_ERR_UNSUPPORTED otherwise).  Workspace: gq_spmm_workspace_bytes.
+ * Errors: as gq_quantize_pack / gq_dequant_spmm.
+ * ---------------------------------------------------------------------- */
+GQ_API size_t gq_packed_row_offsets_workspace_bytes(int64_t n);
+GQ_API int gq_packed_row_offsets(const uint8_t* rbits, int64_t n, int d, int64_t* roff, void* ws,
+                                 size_t ws_bytes, gq_stream stream);
+GQ_API int gq_quantize_pack_mixed(const float* X, int64_t n, int d, int64_t ldx, const uint8_t* rbits,
+                                  const int64_t* roff, uint64_t seed, uint8_t* packed, gq_stream stream);
+GQ_API int gq_dequant_spmm_mixed(const gq_graph* g, int transpose, int coef, const float* X, int64_t ldx,
+                                 const uint8_t* packed, const int64_t* roff, const uint8_t* rbits, int d,
+                                 float* Y, int64_t ldy, void* ws, size_t ws_bytes, gq_stream stream);
+
+/* ------------------------------------------------------------------------
  * gq_edge_spmm -- multi-head attention aggregation (Tango Sec. 2.1, Fig. 1a
  * step 5, H^(l) = (G (.) alpha) H'), all heads in one pass, with the same
  * quantized / full-precision message mix as gq_dequant_spmm:

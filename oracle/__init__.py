@@ -185,6 +185,37 @@ def messages(X, packed, mask, d: int, bits: int) -> np.ndarray:
     return M.astype(np.float64)
 
 
+def quantize_mixed(X, rbits, seed: int):
+    """Mixed bit-widths per row: row r with width rbits[r] in {2, 4, 8} is
+    quantized at that width (the same bytes quantize() gives row r) and laid
+    at byte roff[r]; other rows take no bytes.  Returns (packed, roff)."""
+    X = _c(X, np.float32)
+    n, d = X.shape
+    rbits = np.asarray(rbits).astype(np.int64)
+    sizes = np.array([pitch(d, int(b)) if b in (2, 4, 8) else 0 for b in rbits], np.int64)
+    roff = np.zeros(n + 1, np.int64)
+    roff[1:] = np.cumsum(sizes)
+    packed = np.zeros(int(roff[-1]), np.uint8)
+    for b in (2, 4, 8):
+        sel = rbits == b
+        if sel.any():
+            rows = quantize(X, sel.astype(np.uint8), b, seed)
+            for r in np.nonzero(sel)[0]:
+                packed[roff[r]:roff[r + 1]] = rows[r]
+    return packed, roff
+
+
+def messages_mixed(X, packed, roff, rbits, d: int) -> np.ndarray:
+    """The message rows an aggregation reads from a mixed buffer: row r
+    de-quantized at its width rbits[r], or X[r] for a full-precision row."""
+    M = np.array(X, dtype=np.float32, copy=True)
+    packed = np.asarray(packed, np.uint8)
+    for r, b in enumerate(np.asarray(rbits).astype(np.int64)):
+        if b in (2, 4, 8):
+            M[r] = dequant(packed[roff[r]:roff[r + 1]][None, :], d, int(b))[0]
+    return M.astype(np.float64)
+
+
 # --------------------------------------------------------------------------
 # graph normalization and aggregation
 # --------------------------------------------------------------------------

@@ -107,6 +107,10 @@ def _SIGNATURES(P, I64, I, U64, F, S):
         ("gq_gcn_layer_bwd",
          [GP, I, P, I64, P, I64, P, I64, P, I, I, P, I, U64, I, I, P, P, I64, P, P, S, P, P, P], I),
         ("gq_selftest_bounded_wait", [I, I, ctypes.c_longlong, P, P], I),
+        ("gq_packed_row_offsets_workspace_bytes", [I64], S),
+        ("gq_packed_row_offsets", [P, I64, I, P, P, S, P], I),
+        ("gq_quantize_pack_mixed", [P, I64, I, I64, P, P, U64, P, P], I),
+        ("gq_dequant_spmm_mixed", [GP, I, I, P, I64, P, P, P, I, P, I64, P, S, P], I),
         ("gq_message_variance_weights_workspace_bytes", [GP], S),
         ("gq_message_variance_weights", [GP, I, P, I64, I, P, P, S, P], I),
         ("gq_quant_error_workspace_bytes", [], S),
@@ -292,6 +296,49 @@ def dequant_spmm(g: Graph, X: torch.Tensor | None, packed: torch.Tensor | None, 
     ws = torch.empty(max(wb, 1), dtype=torch.uint8, device=dev)
     _check(lib().gq_dequant_spmm(g.ref, int(transpose), coef, _ptr(X), ldx, _ptr(packed), _ptr(mask), d, bits,
                                  _ptr(out), _rows(out), _ptr(ws), wb, _stream()), "gq_dequant_spmm")
+    return out
+
+
+def packed_row_offsets(rbits: torch.Tensor, d: int) -> torch.Tensor:
+    """Byte offsets (n+1 int64) of the rows of a mixed packed buffer whose
+    row r has width rbits[r] (2, 4, 8; anything else: not packed)."""
+    _cuda(rbits, torch.uint8, "rbits")
+    n = rbits.numel()
+    L = lib()
+    roff = torch.empty(n + 1, dtype=torch.int64, device=rbits.device)
+    wb = int(L.gq_packed_row_offsets_workspace_bytes(n))
+    ws = torch.empty(max(wb, 8), dtype=torch.uint8, device=rbits.device)
+    _check(L.gq_packed_row_offsets(_ptr(rbits), n, d, _ptr(roff), _ptr(ws), wb, _stream()), "gq_packed_row_offsets")
+    return roff
+
+
+def quantize_pack_mixed(X: torch.Tensor, rbits: torch.Tensor, seed: int, roff: torch.Tensor | None = None):
+    """AdaQP Eqn 4 with a bit-width per row.  Returns (packed, roff)."""
+    _cuda(X, torch.float32, "X")
+    _cuda(rbits, torch.uint8, "rbits")
+    n, d = X.shape
+    if roff is None:
+        roff = packed_row_offsets(rbits, d)
+    total = int(roff[n].item())
+    packed = torch.zeros(max(total, 16), dtype=torch.uint8, device=X.device)
+    _check(lib().gq_quantize_pack_mixed(_ptr(X), n, d, _rows(X), _ptr(rbits), _ptr(roff),
+                                        seed & 0xFFFFFFFFFFFFFFFF, _ptr(packed), _stream()), "gq_quantize_pack_mixed")
+    return packed, roff
+
+
+def dequant_spmm_mixed(g: Graph, X: torch.Tensor, packed: torch.Tensor, roff: torch.Tensor, rbits: torch.Tensor,
+                       coef: int = COEF_GCN, transpose: bool = False, out: torch.Tensor | None = None) -> torch.Tensor:
+    """The de-quantizing aggregation over a mixed packed buffer."""
+    _cuda(X, torch.float32, "X")
+    n, d = X.shape
+    if out is None:
+        out = torch.empty(n, d, dtype=torch.float32, device=X.device)
+    L = lib()
+    wb = int(L.gq_spmm_workspace_bytes(g.ref, 1 if transpose else 0, d))
+    ws = torch.empty(max(wb, 256), dtype=torch.uint8, device=X.device)
+    _check(L.gq_dequant_spmm_mixed(g.ref, 1 if transpose else 0, coef, _ptr(X), _rows(X), _ptr(packed), _ptr(roff),
+                                   _ptr(rbits), d, _ptr(out), _rows(out), _ptr(ws), wb, _stream()),
+           "gq_dequant_spmm_mixed")
     return out
 
 

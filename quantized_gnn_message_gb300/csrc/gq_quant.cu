@@ -68,10 +68,14 @@ __device__ __forceinline__ void store_word(uint8_t* p, uint64_t w) {
 // takes 32 / G consecutive rows per iteration.  CPL > 0: the row stays in
 // registers (d <= 8 G CPL).  CPL == 0 (G = 32): two passes over global
 // memory (the second hits L1/L2), any d.
-template <int BITS, int CPL, int G>
+// Mixed bit-widths (MIX): `mask` holds each row's bit-width
+// and the kernel quantizes the rows whose width is BITS, row r at byte
+// roff[r] of `packed`.
+template <int BITS, int CPL, int G, bool MIX>
 __global__ void __launch_bounds__(kQuantThreads) quantize_pack_kernel(
     const float* __restrict__ X, int64_t n, int d, int64_t ldx, const uint8_t* __restrict__ mask,
-    uint32_t seed_key, uint8_t* __restrict__ packed, int64_t pitch, int hoff, bool vec) {
+    uint32_t seed_key, uint8_t* __restrict__ packed, int64_t pitch, int hoff, bool vec,
+    const int64_t* __restrict__ roff) {
   constexpr float L = (float)((1 << BITS) - 1);
   constexpr int NGR = 32 / G;
   const int lane = threadIdx.x & 31;
@@ -83,9 +87,9 @@ __global__ void __launch_bounds__(kQuantThreads) quantize_pack_kernel(
 
   for (int64_t r0 = warp * NGR; r0 < n; r0 += nwarps * NGR) {  // warp-uniform
     const int64_t r = r0 + lane / G;
-    const bool act = r < n && (mask == nullptr || mask[r] != 0);  // group-uniform
+    const bool act = r < n && (MIX ? mask[r] == BITS : (mask == nullptr || mask[r] != 0));  // group-uniform
     const float* x = X + (act ? r : 0) * ldx;
-    uint8_t* row = packed + r * pitch;
+    uint8_t* row = packed + (MIX ? (act ? roff[r] : 0) : r * pitch);
 
     float mn = __int_as_float(0x7f800000), mx = -__int_as_float(0x7f800000);
     float v[CPL > 0 ? CPL : 1][8];
@@ -181,9 +185,9 @@ int grid_for_rows(int64_t n) {
   return (int)g;
 }
 
-template <int BITS>
-int launch_quantize(const float* X, int64_t n, int d, int64_t ldx, const uint8_t* mask, uint64_t seed,
-                    uint8_t* packed, cudaStream_t s) {
+template <int BITS, bool MIX>
+int launch_quantize_t(const float* X, int64_t n, int d, int64_t ldx, const uint8_t* mask, uint64_t seed,
+                      uint8_t* packed, cudaStream_t s, const int64_t* roff) {
   const int64_t pitch = packed_pitch(d, BITS);
   const int hoff = (int)header_offset(d, BITS);
   const bool vec = aligned(X, 16) && (ldx % 4 == 0);
@@ -193,22 +197,29 @@ int launch_quantize(const float* X, int64_t n, int d, int64_t ldx, const uint8_t
   const int G = nch <= 1 ? 1 : nch <= 2 ? 2 : nch <= 4 ? 4 : nch <= 8 ? 8 : nch <= 16 ? 16 : 32;
   const int grid = grid_for_rows((n + 32 / G - 1) / (32 / G));
   switch (G) {
-    case 1: quantize_pack_kernel<BITS, 1, 1><<<grid, kQuantThreads, 0, s>>>(X, n, d, ldx, mask, h, packed, pitch, hoff, vec); break;
-    case 2: quantize_pack_kernel<BITS, 1, 2><<<grid, kQuantThreads, 0, s>>>(X, n, d, ldx, mask, h, packed, pitch, hoff, vec); break;
-    case 4: quantize_pack_kernel<BITS, 1, 4><<<grid, kQuantThreads, 0, s>>>(X, n, d, ldx, mask, h, packed, pitch, hoff, vec); break;
-    case 8: quantize_pack_kernel<BITS, 1, 8><<<grid, kQuantThreads, 0, s>>>(X, n, d, ldx, mask, h, packed, pitch, hoff, vec); break;
-    case 16: quantize_pack_kernel<BITS, 1, 16><<<grid, kQuantThreads, 0, s>>>(X, n, d, ldx, mask, h, packed, pitch, hoff, vec); break;
+    case 1: quantize_pack_kernel<BITS, 1, 1, MIX><<<grid, kQuantThreads, 0, s>>>(X, n, d, ldx, mask, h, packed, pitch, hoff, vec, roff); break;
+    case 2: quantize_pack_kernel<BITS, 1, 2, MIX><<<grid, kQuantThreads, 0, s>>>(X, n, d, ldx, mask, h, packed, pitch, hoff, vec, roff); break;
+    case 4: quantize_pack_kernel<BITS, 1, 4, MIX><<<grid, kQuantThreads, 0, s>>>(X, n, d, ldx, mask, h, packed, pitch, hoff, vec, roff); break;
+    case 8: quantize_pack_kernel<BITS, 1, 8, MIX><<<grid, kQuantThreads, 0, s>>>(X, n, d, ldx, mask, h, packed, pitch, hoff, vec, roff); break;
+    case 16: quantize_pack_kernel<BITS, 1, 16, MIX><<<grid, kQuantThreads, 0, s>>>(X, n, d, ldx, mask, h, packed, pitch, hoff, vec, roff); break;
     default:
       if (d <= 256)
-        quantize_pack_kernel<BITS, 1, 32><<<grid, kQuantThreads, 0, s>>>(X, n, d, ldx, mask, h, packed, pitch, hoff, vec);
+        quantize_pack_kernel<BITS, 1, 32, MIX><<<grid, kQuantThreads, 0, s>>>(X, n, d, ldx, mask, h, packed, pitch, hoff, vec, roff);
       else if (d <= 512)
-        quantize_pack_kernel<BITS, 2, 32><<<grid, kQuantThreads, 0, s>>>(X, n, d, ldx, mask, h, packed, pitch, hoff, vec);
+        quantize_pack_kernel<BITS, 2, 32, MIX><<<grid, kQuantThreads, 0, s>>>(X, n, d, ldx, mask, h, packed, pitch, hoff, vec, roff);
       else if (d <= 1024)
-        quantize_pack_kernel<BITS, 4, 32><<<grid, kQuantThreads, 0, s>>>(X, n, d, ldx, mask, h, packed, pitch, hoff, vec);
+        quantize_pack_kernel<BITS, 4, 32, MIX><<<grid, kQuantThreads, 0, s>>>(X, n, d, ldx, mask, h, packed, pitch, hoff, vec, roff);
       else
-        quantize_pack_kernel<BITS, 0, 32><<<grid, kQuantThreads, 0, s>>>(X, n, d, ldx, mask, h, packed, pitch, hoff, vec);
+        quantize_pack_kernel<BITS, 0, 32, MIX><<<grid, kQuantThreads, 0, s>>>(X, n, d, ldx, mask, h, packed, pitch, hoff, vec, roff);
   }
   return launch_status();
+}
+
+template <int BITS>
+int launch_quantize(const float* X, int64_t n, int d, int64_t ldx, const uint8_t* mask, uint64_t seed,
+                    uint8_t* packed, cudaStream_t s, const int64_t* roff = nullptr) {
+  return roff != nullptr ? launch_quantize_t<BITS, true>(X, n, d, ldx, mask, seed, packed, s, roff)
+                         : launch_quantize_t<BITS, false>(X, n, d, ldx, mask, seed, packed, s, roff);
 }
 
 template <int BITS>
@@ -219,7 +230,108 @@ int launch_dequant(const uint8_t* packed, int64_t n, int d, const uint8_t* mask,
   return launch_status();
 }
 
+// Row offsets of a mixed packed buffer: rows of 4096 per block; each block
+// adds up the sizes of the blocks before it, scans its own rows and writes
+// roff[r] (and roff[n], the buffer size).
+constexpr int kScanRows = 4096;
+constexpr int kScanThr = 1024;
+
+__device__ __forceinline__ int64_t row_bytes(uint8_t b, int d) {
+  return (b == 2 || b == 4 || b == 8) ? packed_pitch(d, b) : 0;
+}
+
+__global__ void __launch_bounds__(kScanThr) offsets_tile_kernel(const uint8_t* __restrict__ rbits, int64_t n, int d,
+                                                               int64_t* __restrict__ tile_sum) {
+  __shared__ int64_t red[kScanThr / 32];
+  const int64_t base = (int64_t)blockIdx.x * kScanRows;
+  int64_t t = 0;
+  for (int i = threadIdx.x; i < kScanRows; i += kScanThr)
+    if (base + i < n) t += row_bytes(rbits[base + i], d);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) t += __shfl_xor_sync(FULL, t, o);
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = t;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    int64_t s = 0;
+    for (int i = 0; i < kScanThr / 32; ++i) s += red[i];
+    tile_sum[blockIdx.x] = s;
+  }
+}
+
+__global__ void __launch_bounds__(kScanThr) offsets_scan_kernel(const uint8_t* __restrict__ rbits, int64_t n, int d,
+                                                               const int64_t* __restrict__ tile_sum,
+                                                               int64_t* __restrict__ roff) {
+  __shared__ int64_t wsum[kScanThr / 32];
+  __shared__ int64_t tile_base;
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  // the sizes of all earlier tiles, summed in tile order by warp 0
+  if (w == 0) {
+    int64_t t = 0;
+    for (int64_t i = lane; i < (int64_t)blockIdx.x; i += 32) t += tile_sum[i];
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) t += __shfl_xor_sync(FULL, t, o);
+    if (lane == 0) tile_base = t;
+  }
+  // each thread scans 4 consecutive rows of the tile
+  constexpr int PER = kScanRows / kScanThr;
+  const int64_t r0 = (int64_t)blockIdx.x * kScanRows + (int64_t)threadIdx.x * PER;
+  int64_t sz[PER], own = 0;
+#pragma unroll
+  for (int i = 0; i < PER; ++i) {
+    sz[i] = r0 + i < n ? row_bytes(rbits[r0 + i], d) : 0;
+    own += sz[i];
+  }
+  int64_t incl = own;  // inclusive scan over the warp
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int64_t y = __shfl_up_sync(FULL, incl, o);
+    if (lane >= o) incl += y;
+  }
+  if (lane == 31) wsum[w] = incl;
+  __syncthreads();
+  int64_t before = tile_base;
+  for (int i = 0; i < w; ++i) before += wsum[i];
+  before += incl - own;
+#pragma unroll
+  for (int i = 0; i < PER; ++i) {
+    if (r0 + i < n) roff[r0 + i] = before;
+    before += sz[i];
+  }
+  if (r0 + PER >= n && r0 < n) roff[n] = before;  // the thread holding the last row
+}
+
 }  // namespace
+
+int64_t offsets_tiles(int64_t n) { return (n + kScanRows - 1) / kScanRows; }
+
+int packed_row_offsets(const uint8_t* rbits, int64_t n, int d, int64_t* roff, void* ws, size_t ws_bytes,
+                       cudaStream_t s) {
+  if (n < 0 || d < 1 || roff == nullptr || (n > 0 && rbits == nullptr)) return GQ_ERR_INVALID_ARG;
+  if (n == 0) {
+    GQ_TRY_CUDA(cudaMemsetAsync(roff, 0, sizeof(int64_t), s));
+    return GQ_OK;
+  }
+  const int64_t tiles = offsets_tiles(n);
+  if (tiles > 0x7fffffff) return GQ_ERR_UNSUPPORTED;
+  if (ws == nullptr || ws_bytes < (size_t)tiles * sizeof(int64_t) || !aligned(ws, 8)) return GQ_ERR_WORKSPACE;
+  int64_t* tile_sum = static_cast<int64_t*>(ws);
+  offsets_tile_kernel<<<(unsigned)tiles, kScanThr, 0, s>>>(rbits, n, d, tile_sum);
+  GQ_TRY(launch_status());
+  offsets_scan_kernel<<<(unsigned)tiles, kScanThr, 0, s>>>(rbits, n, d, tile_sum, roff);
+  return launch_status();
+}
+
+int quantize_pack_mixed(const float* X, int64_t n, int d, int64_t ldx, const uint8_t* rbits, const int64_t* roff,
+                        uint64_t seed, uint8_t* packed, cudaStream_t s) {
+  if (n < 0 || d < 1 || ldx < d) return GQ_ERR_INVALID_ARG;
+  if (n > 0 && (X == nullptr || packed == nullptr || rbits == nullptr || roff == nullptr)) return GQ_ERR_INVALID_ARG;
+  if (!aligned(packed, 16)) return GQ_ERR_INVALID_ARG;
+  if (d > 16384) return GQ_ERR_UNSUPPORTED;
+  if (n == 0) return GQ_OK;
+  GQ_TRY(launch_quantize<2>(X, n, d, ldx, rbits, seed, packed, s, roff));
+  GQ_TRY(launch_quantize<4>(X, n, d, ldx, rbits, seed, packed, s, roff));
+  return launch_quantize<8>(X, n, d, ldx, rbits, seed, packed, s, roff);
+}
 
 int quantize_pack(const float* X, int64_t n, int d, int64_t ldx, const uint8_t* mask, int bits, uint64_t seed,
                   uint8_t* packed, cudaStream_t s) {
@@ -254,4 +366,18 @@ extern "C" int gq_dequant_unpack(const uint8_t* packed, int64_t n, int d, int bi
     case 4: return gq::launch_dequant<4>(packed, n, d, mask, Y, ldy, s);
     default: return gq::launch_dequant<8>(packed, n, d, mask, Y, ldy, s);
   }
+}
+
+extern "C" size_t gq_packed_row_offsets_workspace_bytes(int64_t n) {
+  return n > 0 ? (size_t)gq::offsets_tiles(n) * sizeof(int64_t) : 0;
+}
+
+extern "C" int gq_packed_row_offsets(const uint8_t* rbits, int64_t n, int d, int64_t* roff, void* ws,
+                                     size_t ws_bytes, gq_stream stream) {
+  return gq::packed_row_offsets(rbits, n, d, roff, ws, ws_bytes, (cudaStream_t)stream);
+}
+
+extern "C" int gq_quantize_pack_mixed(const float* X, int64_t n, int d, int64_t ldx, const uint8_t* rbits,
+                                      const int64_t* roff, uint64_t seed, uint8_t* packed, gq_stream stream) {
+  return gq::quantize_pack_mixed(X, n, d, ldx, rbits, roff, seed, packed, (cudaStream_t)stream);
 }

@@ -65,6 +65,8 @@ struct SpmmParams {
   const int32_t* light;     // runs of light rows {row_begin, row_end}
   int64_t n_light;
   int* err;                 // device status word (bounded waits that gave up)
+  const uint8_t* rbits;     // per-row bit-widths (mixed packed rows), or null
+  const int64_t* roff;      // byte offset of each packed row (mixed), or null
 };
 
 namespace {
@@ -610,7 +612,7 @@ constexpr float kMagic = 8388608.0f;
 // The loop-invariant pair -(2^23 + c), c = 2^(b-1), for the subtraction.
 template <int BITS>
 __device__ __forceinline__ f32x2 a_bias() {
-  constexpr float c = (float)(1 << (BITS < 32 ? BITS - 1 : 0));
+  constexpr float c = (float)(1 << (BITS > 0 && BITS < 32 ? BITS - 1 : 0));
   return f2_pack(-(kMagic + c), -(kMagic + c));
 }
 
@@ -1020,14 +1022,25 @@ __device__ __forceinline__ void codes4_b8(uint32_t w, float (&v)[4]) {
   for (int i = 0; i < 4; ++i) v[i] = __uint_as_float(__byte_perm(w, kMagicBits, 0x7540u | i));
 }
 
-// Coefficient and mask bit of the lane's edge of a batch.
+// Coefficient and row kind of the lane's edge of a batch: kind 0 = an fp32
+// row, else the packed row's bit-width.  BITS == 0: every row has its own
+// width (mixed packed rows; widths other than 2, 4, 8 mean fp32), and `off`
+// is the packed row's byte offset.
 template <int BITS, bool MX>
-__device__ __forceinline__ void r_meta(const SpmmParams& p, uint32_t x, bool valid, float& cf, bool& q) {
+__device__ __forceinline__ void r_meta(const SpmmParams& p, uint32_t x, bool valid, float& cf, uint32_t& kind,
+                                       int64_t& off) {
   cf = 1.0f;
-  q = BITS < 32 && !MX;
+  kind = (BITS > 0 && BITS < 32 && !MX) ? BITS : 0;
+  off = 0;
   if (valid) {
     if (p.colscale != nullptr) cf = __ldg(p.colscale + x);
-    if (MX) q = __ldg(p.mask + x) != 0;
+    if constexpr (BITS == 0) {
+      const uint32_t b = __ldg(p.rbits + x);
+      kind = (b == 2 || b == 4 || b == 8) ? b : 0;
+      if (kind != 0) off = __ldg(p.roff + x);
+    } else if (MX) {
+      kind = __ldg(p.mask + x) != 0 ? BITS : 0;
+    }
   }
 }
 
@@ -1113,6 +1126,7 @@ struct BLane {
   const uint8_t* xb;   // fp32 rows (row 0)
   const uint8_t* pb;   // packed rows (row 0)
   uint32_t xstride, xbytes, pitch;
+  int d;
   uint32_t sring;      // the warp's slots (shared address)
   const uint8_t* ring;
   uint32_t sbar;       // the warp's R barriers
@@ -1125,16 +1139,25 @@ struct BLane {
 // Issue the wave of edges [f0, f0 + H) (f0 a multiple of H) from the batch
 // registers of the lanes holding them.
 template <int BITS, bool MX, int R, int H, int SLOT>
-__device__ __forceinline__ void b_issue(BLane& L, int f0, int n, uint32_t x, bool q, float cf) {
+__device__ __forceinline__ void b_issue(BLane& L, int f0, int n, uint32_t x, uint32_t kind, float cf, int64_t off) {
   const int lane = threadIdx.x & 31;
   const int l0 = f0 & 31;
   const int f = f0 - l0 + lane;
   if (lane >= l0 && lane < l0 + H && f < n) {
     const uint32_t slot = (L.used + (uint32_t)f) & (R - 1);
-    const bool quant = BITS < 32 && (MX ? q : true);
-    L.meta[slot] = make_float2(cf, quant ? 1.0f : 0.0f);
-    const uint32_t bytes = quant ? L.pitch : L.xbytes;
-    const uint8_t* src = quant ? L.pb + (size_t)(x * (uint64_t)L.pitch) : L.xb + (size_t)(x * (uint64_t)L.xstride);
+    const bool quant = BITS < 32 && kind != 0;
+    L.meta[slot] = make_float2(cf, (float)kind);
+    uint32_t bytes = L.xbytes;
+    const uint8_t* src = L.xb + (size_t)(x * (uint64_t)L.xstride);
+    if (quant) {
+      if constexpr (BITS == 0) {
+        bytes = (uint32_t)packed_pitch(L.d, (int)kind);
+        src = L.pb + off;
+      } else {
+        bytes = L.pitch;
+        src = L.pb + (size_t)(x * (uint64_t)L.pitch);
+      }
+    }
     const uint32_t bar = L.sbar + 8 * slot;
     bar_expect_tx(bar, bytes);
     bulk_g2s(L.sring + slot * SLOT, src, bytes, bar);
@@ -1157,9 +1180,10 @@ __device__ __forceinline__ void b_stream(const SpmmParams& p, BLane& L, f32x2 bi
   uint32_t x1 = 32 + lane < n ? (uint32_t)__ldg(col + 32 + lane) : 0u;
   uint32_t x2 = 64 + lane < n ? (uint32_t)__ldg(col + 64 + lane) : 0u;
   float cf0, cf1;
-  bool q0, q1;
-  r_meta<BITS, MX>(p, x0, lane < n, cf0, q0);
-  r_meta<BITS, MX>(p, x1, 32 + lane < n, cf1, q1);
+  uint32_t q0, q1;
+  int64_t o0, o1;
+  r_meta<BITS, MX>(p, x0, lane < n, cf0, q0, o0);
+  r_meta<BITS, MX>(p, x1, 32 + lane < n, cf1, q1, o1);
   int kb = 0;
   int rb = row0, ri = 0, rend = 0x7fffffff, rpl = 0x7fffffff;
   float rsl = 1.0f;
@@ -1173,7 +1197,7 @@ __device__ __forceinline__ void b_stream(const SpmmParams& p, BLane& L, f32x2 bi
   // fill the ring (the first R edges are all in batch 0)
 #pragma unroll
   for (int f0 = 0; f0 < R; f0 += H)
-    if (f0 < n) b_issue<BITS, MX, R, H, SLOT>(L, f0, n, x0, q0, cf0);
+    if (f0 < n) b_issue<BITS, MX, R, H, SLOT>(L, f0, n, x0, q0, cf0, o0);
   int issued = min(R, n);
   int e = 0;
   for (; e < n; ++e) {
@@ -1182,8 +1206,9 @@ __device__ __forceinline__ void b_stream(const SpmmParams& p, BLane& L, f32x2 bi
       x0 = x1;
       q0 = q1;
       cf0 = cf1;
+      o0 = o1;
       x1 = x2;
-      r_meta<BITS, MX>(p, x1, kb + 32 + lane < n, cf1, q1);
+      r_meta<BITS, MX>(p, x1, kb + 32 + lane < n, cf1, q1, o1);
       x2 = kb + 64 + lane < n ? (uint32_t)__ldg(col + kb + 64 + lane) : 0u;
     }
     const uint32_t u = L.used + (uint32_t)e;
@@ -1213,8 +1238,22 @@ __device__ __forceinline__ void b_stream(const SpmmParams& p, BLane& L, f32x2 bi
       }
     }
     const uint8_t* sl = L.ring + slot * SLOT;
-    if (BITS < 32 && mt.y != 0.0f) {
-      constexpr float c = (float)(1 << ((BITS < 32 ? BITS : 8) - 1));
+    if (BITS == 0 && mt.y != 0.0f) {
+      // a packed row of its own width b: header at its own offset, c = 2^(b-1)
+      const int b = (int)mt.y;
+      const float c = (float)(1 << (b - 1));
+      const float2 h = *reinterpret_cast<const float2*>(sl + header_offset(p.d, b));
+      accz = __fmaf_rn(mt.x, __fmaf_rn(c, h.x, h.y), accz);
+      const float cs = mt.x * h.x;
+      const f32x2 bz = f2_pack(-(kMagic + c), -(kMagic + c));
+      if (b == 2)
+        bf_packed<2, CPL>(sl, f2_pack(cs, cs), bz, acc);
+      else if (b == 4)
+        bf_packed<4, CPL>(sl, f2_pack(cs, cs), bz, acc);
+      else
+        bf_packed<8, CPL>(sl, f2_pack(cs, cs), bz, acc);
+    } else if (BITS > 0 && BITS < 32 && mt.y != 0.0f) {
+      constexpr float c = (float)(1 << ((BITS > 0 && BITS < 32 ? BITS : 8) - 1));
       const float2 h = *reinterpret_cast<const float2*>(sl + p.hoff);
       accz = __fmaf_rn(mt.x, __fmaf_rn(c, h.x, h.y), accz);
       const float cs = mt.x * h.x;
@@ -1234,9 +1273,9 @@ __device__ __forceinline__ void b_stream(const SpmmParams& p, BLane& L, f32x2 bi
       __syncwarp();  // every lane is done with the freed slots
       asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
       if (f0 >= kb + 32)
-        b_issue<BITS, MX, R, H, SLOT>(L, f0, n, x1, q1, cf1);
+        b_issue<BITS, MX, R, H, SLOT>(L, f0, n, x1, q1, cf1, o1);
       else
-        b_issue<BITS, MX, R, H, SLOT>(L, f0, n, x0, q0, cf0);
+        b_issue<BITS, MX, R, H, SLOT>(L, f0, n, x0, q0, cf0, o0);
       issued = min(f0 + H, n);
     }
   }
@@ -1279,6 +1318,7 @@ __global__ void __launch_bounds__(kSpmmThreads, 3) spmm_bulk_kernel(const SpmmPa
   L.xstride = (uint32_t)(p.ldx * 4);
   L.xbytes = (uint32_t)(p.d * 4);
   L.pitch = (uint32_t)p.pitch;
+  L.d = p.d;
   uint64_t* bars = reinterpret_cast<uint64_t*>(bsm) + w * R;
   L.sbar = sm_addr(bars);
   L.meta = reinterpret_cast<float2*>(bsm + kSpmmWarps * R * 8) + w * R;
@@ -1450,6 +1490,30 @@ int dequant_spmm(const gq_graph* g, int transpose, int coef, const float* X, int
   return launch_any<false>(p, bits, s);
 }
 
+// Mixed bit-widths per row (rbits, roff from gq_packed_row_offsets).
+int dequant_spmm_mixed(const gq_graph* g, int transpose, int coef, const float* X, int64_t ldx, const uint8_t* packed,
+                       const int64_t* roff, const uint8_t* rbits, int d, float* Y, int64_t ldy, void* ws,
+                       size_t ws_bytes, cudaStream_t s) {
+  if (packed == nullptr || roff == nullptr || rbits == nullptr || !aligned(packed, 16)) return GQ_ERR_INVALID_ARG;
+  if (d <= 64 || d > 256) return GQ_ERR_UNSUPPORTED;
+  SpmmParams p;
+  GQ_TRY(spmm_setup(g, transpose, X, ldx, nullptr, nullptr, d, 32, Y, ldy, ws, ws_bytes, s, p));
+  if (ldx > (int64_t)1 << 29) return GQ_ERR_UNSUPPORTED;
+  if (coef == GQ_COEF_GCN) {
+    p.colscale = transpose ? g->dinv_in : g->dinv_out;
+    p.rowscale = transpose ? g->dinv_out : g->dinv_in;
+  } else if (coef == GQ_COEF_SAGE) {
+    p.colscale = transpose ? g->inv_in : nullptr;
+    p.rowscale = transpose ? nullptr : g->inv_in;
+  } else if (coef != GQ_COEF_ONE) {
+    return GQ_ERR_INVALID_ARG;
+  }
+  p.packed = packed;
+  p.rbits = rbits;
+  p.roff = roff;
+  return d > 128 ? launch_bulk<0, 8, true, 4, 2>(p, s) : launch_bulk<0, 4, true, 8, 4>(p, s);
+}
+
 int edge_spmm(const gq_graph* g, int transpose, const float* alpha, int heads, const float* X, int64_t ldx,
               const uint8_t* packed, const uint8_t* mask, int d, int bits, float* Y, int64_t ldy, void* ws,
               size_t ws_bytes, cudaStream_t s) {
@@ -1478,6 +1542,13 @@ extern "C" int gq_dequant_spmm(const gq_graph* g, int transpose, int coef, const
                                void* ws, size_t ws_bytes, gq_stream stream) {
   return gq::dequant_spmm(g, transpose, coef, X, ldx, packed, mask, d, bits, Y, ldy, ws, ws_bytes,
                           (cudaStream_t)stream, nullptr);
+}
+
+extern "C" int gq_dequant_spmm_mixed(const gq_graph* g, int transpose, int coef, const float* X, int64_t ldx,
+                                     const uint8_t* packed, const int64_t* roff, const uint8_t* rbits, int d,
+                                     float* Y, int64_t ldy, void* ws, size_t ws_bytes, gq_stream stream) {
+  return gq::dequant_spmm_mixed(g, transpose, coef, X, ldx, packed, roff, rbits, d, Y, ldy, ws, ws_bytes,
+                                (cudaStream_t)stream);
 }
 
 extern "C" int gq_edge_spmm(const gq_graph* g, int transpose, const float* alpha, int heads, const float* X,

@@ -137,3 +137,17 @@ def test_round_to_nearest_would_be_biased(orc):
     rn = np.floor(t + 0.5)
     st = np.mean([np.floor(t + np.float32(orc.uniform(s, 0, 1))) for s in range(4096)])
     assert abs(rn - t) > 0.25 and abs(st - t) < 0.05
+
+
+def test_mixed_layout_hand_example(orc):
+    # widths 2, none, 8, 4 at d = 4: pitches 16, 0, 16, 16 -> offsets 0, 16, 16, 32, 48;
+    # each row's bytes are the uniform quantizer's row at its own width
+    X = np.array([[0, 1, 2, 3], [5, 5, 5, 5], [-1, 0, 1, 254], [0, 15, 5, 10]], np.float32)
+    rbits = [2, 0, 8, 4]
+    packed, roff = orc.quantize_mixed(X, rbits, 7)
+    assert list(roff) == [0, 16, 16, 32, 48]
+    for r, b in ((0, 2), (2, 8), (3, 4)):
+        assert bytes(packed[roff[r]:roff[r + 1]]) == bytes(orc.quantize(X, None, b, 7)[r])
+    M = orc.messages_mixed(X, packed, roff, rbits, 4)
+    assert np.array_equal(M[0], [0, 1, 2, 3]) and np.array_equal(M[1], [5, 5, 5, 5])
+    assert np.array_equal(M[3], [0, 15, 5, 10])  # integer steps of S = 1: exact
