@@ -420,6 +420,11 @@ def run_gat(args, w):
     build()
     q.lib()
     dev = torch.device("cuda", 0)
+    if args.graph_scale is not None:
+        import dataclasses
+        S = args.graph_scale
+        w = dataclasses.replace(w, name=f"gat-rmat{S}", graph=dict(kind="rmat", scale=S, n=1 << S,
+                                                                   n_draws=16 << S, exact_edges=16 << S))
     g = w.make_graph(device=dev)
     d_in, heads, f = w.widths
     d = heads * f
@@ -597,7 +602,7 @@ def main():
     ap.add_argument("--sweep-d", default=None, help="aggregate workload: comma-separated widths")
     ap.add_argument("--sweep-bits", default=None, help="aggregate workload: comma-separated bit-widths")
     ap.add_argument("--graph-scale", type=int, default=None,
-                    help="aggregate workload: R-MAT scale S (2^S nodes, 32 draws per node) for smaller cases")
+                    help="aggregate / GAT workloads: R-MAT scale S (2^S nodes; 32 / 16 draws per node) for smaller cases")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
     w = BY_NAME[args.workload]

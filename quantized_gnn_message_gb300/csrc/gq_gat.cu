@@ -4,7 +4,10 @@
 //     E_pre[e,k] = S[u,k] + D[v,k]            (SDDMM add, e = u -> v)
 //     E[e,k]     = LeakyReLU(E_pre[e,k])
 //     alpha[e,k] = exp(E[e,k] - max_v) / sum_{e' in in(v)} exp(E[e',k] - max_v)
-//   one pass keeps an online (max, sum) per head, a second writes alpha.
+//   one pass keeps an online (max, sum) per head, a second writes alpha;
+//   a row of at most 32 edges is one thread's, rows up to the hub threshold
+//   a warp's, heavier rows are cut into tasks of one warp each, whose
+//   (max, sum) partials are merged in task order before their second pass.
 // gat_edge_bwd_kernel  (Fig. 1b), per destination row v:
 //     dalpha[e,k] = sum_f dOut[v,kF+f] m_u[kF+f]          (SDDMM dot)
 //     P[v,k]      = sum_e alpha[e,k] dalpha[e,k]
@@ -29,6 +32,7 @@ namespace {
 
 constexpr int kGatThreads = 256;
 constexpr int kGatWarps = kGatThreads / 32;
+
 constexpr float kNegInf = -__builtin_huge_valf();
 
 // ------------------------------------------------------------ helpers ---
@@ -230,58 +234,35 @@ __device__ __forceinline__ void warp_merge(float (&m)[K], float (&l)[K]) {
     }
 }
 
+// Heavy rows (more edges than the hub threshold) are cut into the graph's
+// tasks.  This kernel: one warp per task computes the online (max, sum) of
+// its edges into part[task] (first pass); then the light rows.  The second
+// pass of the heavy rows is edge_softmax_heavy_kernel.
 template <int K>
 __global__ void __launch_bounds__(kGatThreads) edge_softmax_kernel(const SoftmaxParams p) {
-  __shared__ float red[kGatWarps][2 * K];
   const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
-  if ((int64_t)blockIdx.x < p.sc.n_tasks) {
-    const int4 task = __ldg(reinterpret_cast<const int4*>(p.sc.tasks) + blockIdx.x);
-    const int64_t v = task.x;
+  const int64_t gw = (int64_t)blockIdx.x * kGatWarps + w;
+  const int64_t nw = (int64_t)gridDim.x * kGatWarps;
+  for (int64_t t = gw; t < p.sc.n_tasks; t += nw) {
+    const int4 task = __ldg(reinterpret_cast<const int4*>(p.sc.tasks) + t);
     float dv[K];
-    load_k<K>(p.D + v * K, dv);
+    load_k<K>(p.D + (int64_t)task.x * K, dv);
     float m[K], l[K];
-    sm_pass1<K>(p, (int64_t)task.y + threadIdx.x, task.z, kGatThreads, dv, m, l);
+    sm_pass1<K>(p, (int64_t)task.y + lane, task.z, 32, dv, m, l);
     warp_merge<K>(m, l);
-    if (lane == 0)
+    if (lane == 0) {
+      float* mine = p.sc.partial + t * 2 * K;
 #pragma unroll
       for (int k = 0; k < K; ++k) {
-        red[w][2 * k] = m[k];
-        red[w][2 * k + 1] = l[k];
+        mine[2 * k] = m[k];
+        mine[2 * k + 1] = l[k];
       }
-    __syncthreads();
-#pragma unroll
-    for (int k = 0; k < K; ++k) {  // every thread merges the warps in order
-      m[k] = red[0][2 * k];
-      l[k] = red[0][2 * k + 1];
-      for (int ww = 1; ww < kGatWarps; ++ww) online_merge(m[k], l[k], red[ww][2 * k], red[ww][2 * k + 1]);
     }
-    if (task.w < 0) {
-      sm_pass2<K>(p, (int64_t)task.y + threadIdx.x, task.z, kGatThreads, dv, m, l);
-      return;
-    }
-    const int4 grp = __ldg(reinterpret_cast<const int4*>(p.sc.groups) + task.w);
-    float* mine = p.sc.partial + (int64_t)(grp.w + ((int)blockIdx.x - grp.y)) * 2 * K;
-    if (threadIdx.x < K) {
-      mine[2 * threadIdx.x] = m[threadIdx.x];
-      mine[2 * threadIdx.x + 1] = l[threadIdx.x];
-    }
-    if (!last_of_group(p.sc, task.w, grp.z)) return;
-    const float* base = p.sc.partial + (int64_t)grp.w * 2 * K;
-#pragma unroll
-    for (int k = 0; k < K; ++k) {
-      m[k] = __ldcg(base + 2 * k);
-      l[k] = __ldcg(base + 2 * k + 1);
-      for (int t = 1; t < grp.z; ++t) online_merge(m[k], l[k], __ldcg(base + t * 2 * K + 2 * k), __ldcg(base + t * 2 * K + 2 * k + 1));
-    }
-    sm_pass2<K>(p, (int64_t)p.rowptr[v] + threadIdx.x, p.rowptr[v + 1], kGatThreads, dv, m, l);
-    return;
   }
   // light rows, in groups of 32 consecutive rows per warp: a row of at most
   // 32 edges is one thread's (two passes over its edges, the online max and
   // sum in registers); the group's rows of 33 .. hub_threshold edges are
   // then taken one at a time by the whole warp
-  const int64_t gw = ((int64_t)blockIdx.x - p.sc.n_tasks) * kGatWarps + w;
-  const int64_t nw = ((int64_t)gridDim.x - p.sc.n_tasks) * kGatWarps;
   const int64_t groups = (p.n_rows + 31) / 32;
   for (int64_t grp = gw; grp < groups; grp += nw) {
     const int64_t r = grp * 32 + lane;
@@ -305,6 +286,34 @@ __global__ void __launch_bounds__(kGatThreads) edge_softmax_kernel(const Softmax
       sm_pass2<K>(p, va + lane, vb, 32, dv, m, l);
     }
   }
+}
+
+// Second pass of the heavy rows: one warp per task merges the (max, sum)
+// partials of its row's tasks in task order (its own alone when the row is
+// one task) and writes alpha for the task's edges.
+template <int K>
+__global__ void __launch_bounds__(kGatThreads) edge_softmax_heavy_kernel(const SoftmaxParams p) {
+  const int lane = threadIdx.x & 31;
+  const int64_t t = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  if (t >= p.sc.n_tasks) return;
+  const int4 task = __ldg(reinterpret_cast<const int4*>(p.sc.tasks) + t);
+  int64_t t0 = t, nt = 1;
+  if (task.w >= 0) {
+    const int4 grp = __ldg(reinterpret_cast<const int4*>(p.sc.groups) + task.w);
+    t0 = grp.y;
+    nt = grp.z;
+  }
+  float m[K], l[K];
+  const float* base = p.sc.partial + t0 * 2 * K;
+#pragma unroll
+  for (int k = 0; k < K; ++k) {
+    m[k] = __ldcg(base + 2 * k);
+    l[k] = __ldcg(base + 2 * k + 1);
+    for (int64_t i = 1; i < nt; ++i) online_merge(m[k], l[k], __ldcg(base + i * 2 * K + 2 * k), __ldcg(base + i * 2 * K + 2 * k + 1));
+  }
+  float dv[K];
+  load_k<K>(p.D + (int64_t)task.x * K, dv);
+  sm_pass2<K>(p, (int64_t)task.y + lane, task.z, 32, dv, m, l);
 }
 
 // --------------------------------------------------- GAT edge backward ---
@@ -638,8 +647,17 @@ int light_grid(int64_t n_rows, int64_t n_tasks) {
 
 template <int K>
 int launch_softmax(const SoftmaxParams& p, cudaStream_t s) {
-  edge_softmax_kernel<K><<<light_grid(p.n_rows, p.sc.n_tasks), kGatThreads, 0, s>>>(p);
-  return launch_status();
+  int64_t blocks = ((p.n_rows + 31) / 32 + p.sc.n_tasks + kGatWarps - 1) / kGatWarps;
+  const int64_t cap = (int64_t)sm_count() * 8;
+  if (blocks > cap) blocks = cap;
+  if (blocks < 1) blocks = 1;
+  edge_softmax_kernel<K><<<(unsigned)blocks, kGatThreads, 0, s>>>(p);
+  GQ_TRY(launch_status());
+  if (p.sc.n_tasks > 0) {
+    edge_softmax_heavy_kernel<K><<<(unsigned)((p.sc.n_tasks + kGatWarps - 1) / kGatWarps), kGatThreads, 0, s>>>(p);
+    GQ_TRY(launch_status());
+  }
+  return GQ_OK;
 }
 
 template <int BITS, int K>
@@ -651,7 +669,10 @@ int launch_edge_bwd(const EdgeBwdParams& p, cudaStream_t s) {
 }  // namespace
 
 // ---------------------------------------------------------------- API ---
-size_t edge_softmax_workspace(const gq_graph* g, int heads) { return sched_ws(g->sched, 2 * heads); }
+// one (max, sum) pair per head for every heavy-row task
+size_t edge_softmax_workspace(const gq_graph* g, int heads) {
+  return ((size_t)g->sched.n_tasks * 2 * heads * sizeof(float) + 255) / 256 * 256;
+}
 size_t edge_bwd_workspace(const gq_graph* g, int heads) { return sched_ws(g->sched, heads); }
 
 int edge_softmax(const gq_graph* g, const float* S, const float* D, int heads, float slope, float* Epre,
@@ -671,8 +692,8 @@ int edge_softmax(const gq_graph* g, const float* S, const float* D, int heads, f
   p.n_rows = g->n;
   const size_t need = edge_softmax_workspace(g, heads);
   if (need > 0 && (ws == nullptr || ws_bytes < need || !aligned(ws, 256))) return GQ_ERR_WORKSPACE;
-  p.sc = make_sched(g->sched, g->hub_threshold, ws, 2 * heads);
-  if (g->sched.n_groups > 0) GQ_TRY_CUDA(cudaMemsetAsync(p.sc.tickets, 0, g->sched.n_groups * sizeof(int), s));
+  p.sc = make_sched(g->sched, g->hub_threshold, nullptr, 2 * heads);
+  p.sc.partial = static_cast<float*>(ws);
   switch (heads) {
     case 1: return launch_softmax<1>(p, s);
     case 2: return launch_softmax<2>(p, s);
