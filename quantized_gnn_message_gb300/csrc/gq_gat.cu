@@ -69,16 +69,6 @@ __device__ __forceinline__ void store_k(float* __restrict__ p, const float (&v)[
 
 __device__ __forceinline__ float lrelu(float x, float slope) { return x > 0.0f ? x : slope * x; }
 
-// online softmax state: fold value x into (m, l)
-__device__ __forceinline__ void online_add(float& m, float& l, float x) {
-  if (x > m) {
-    l = l * expf(m - x) + 1.0f;
-    m = x;
-  } else {
-    l += expf(x - m);
-  }
-}
-
 __device__ __forceinline__ void online_merge(float& m, float& l, float m2, float l2) {
   const float M = fmaxf(m, m2);
   if (M == kNegInf) return;  // both empty
@@ -128,6 +118,24 @@ __device__ __forceinline__ void sm_scores(const SoftmaxParams& p, int64_t e, con
   for (int k = 0; k < K; ++k) ep[k] = s[k] + dv[k];
 }
 
+// Scores of the thread's edges e, e + stride, e + 2 stride, e + 3 stride
+// (those below end): their column ids, then their S rows, loaded before any
+// is used.
+template <int K>
+__device__ __forceinline__ void sm_scores4s(const SoftmaxParams& p, int64_t e, int64_t end, int64_t stride,
+                                            const float (&dv)[K], float (&ep)[4][K]) {
+  int32_t x[4];
+#pragma unroll
+  for (int t = 0; t < 4; ++t) x[t] = e + t * stride < end ? __ldg(p.col + e + t * stride) : 0;
+#pragma unroll
+  for (int t = 0; t < 4; ++t) {
+    float s[K];
+    load_k<K>(p.S + (int64_t)x[t] * K, s);
+#pragma unroll
+    for (int k = 0; k < K; ++k) ep[t][k] = s[k] + dv[k];
+  }
+}
+
 // (max, sum) of this thread's edges e = first, first + stride, ...
 template <int K>
 __device__ __forceinline__ void sm_pass1(const SoftmaxParams& p, int64_t first, int64_t end, int64_t stride,
@@ -137,24 +145,43 @@ __device__ __forceinline__ void sm_pass1(const SoftmaxParams& p, int64_t first, 
     m[k] = kNegInf;
     l[k] = 0.0f;
   }
-  for (int64_t e = first; e < end; e += stride) {
-    float ep[K];
-    sm_scores<K>(p, e, dv, ep);
+  for (int64_t e = first; e < end; e += 4 * stride) {
+    float ep[4][K];
+    sm_scores4s<K>(p, e, end, stride, dv, ep);
 #pragma unroll
-    for (int k = 0; k < K; ++k) online_add(m[k], l[k], lrelu(ep[k], p.slope));
+    for (int t = 0; t < 4; ++t) {
+      if (e + t * stride < end) {
+#pragma unroll
+        for (int k = 0; k < K; ++k) {
+          const float x = lrelu(ep[t][k], p.slope);
+          const float mn = fmaxf(m[k], x);
+          l[k] = l[k] * __expf(m[k] - mn) + __expf(x - mn);
+          m[k] = mn;
+        }
+      }
+    }
   }
 }
 
 template <int K>
 __device__ __forceinline__ void sm_pass2(const SoftmaxParams& p, int64_t first, int64_t end, int64_t stride,
                                          const float (&dv)[K], const float (&M)[K], const float (&L)[K]) {
-  for (int64_t e = first; e < end; e += stride) {
-    float ep[K];
-    sm_scores<K>(p, e, dv, ep);
+  float inv[K];
 #pragma unroll
-    for (int k = 0; k < K; ++k) {
-      p.alpha[e * K + k] = expf(lrelu(ep[k], p.slope) - M[k]) / L[k];
-      if (p.Epre != nullptr) p.Epre[e * K + k] = ep[k];
+  for (int k = 0; k < K; ++k) inv[k] = 1.0f / L[k];
+  for (int64_t e = first; e < end; e += 4 * stride) {
+    float ep[4][K];
+    sm_scores4s<K>(p, e, end, stride, dv, ep);
+#pragma unroll
+    for (int t = 0; t < 4; ++t) {
+      const int64_t et = e + t * stride;
+      if (et < end) {
+        float al[K];
+#pragma unroll
+        for (int k = 0; k < K; ++k) al[k] = __expf(lrelu(ep[t][k], p.slope) - M[k]) * inv[k];
+        store_k<K>(p.alpha + et * K, al);
+        if (p.Epre != nullptr) store_k<K>(p.Epre + et * K, ep[t]);
+      }
     }
   }
 }
@@ -557,11 +584,19 @@ __global__ void __launch_bounds__(kGatThreads) gat_node_bwd_kernel(const NodeBwd
     float ds[K];
 #pragma unroll
     for (int k = 0; k < K; ++k) ds[k] = 0.0f;
-    for (int64_t e = a + lane; e < b; e += 32) {
-      float x[K];
-      load_k<K>(p.dEpre + (int64_t)__ldg(p.tr_perm + e) * K, x);
+    for (int64_t e = a + lane; e < b; e += 4 * 32) {  // four out-edges per lane at a time
+      int32_t pe[4];
 #pragma unroll
-      for (int k = 0; k < K; ++k) ds[k] += x[k];
+      for (int t = 0; t < 4; ++t) pe[t] = e + 32 * t < b ? __ldg(p.tr_perm + e + 32 * t) : -1;
+#pragma unroll
+      for (int t = 0; t < 4; ++t) {
+        if (pe[t] >= 0) {
+          float x[K];
+          load_k<K>(p.dEpre + (int64_t)pe[t] * K, x);
+#pragma unroll
+          for (int k = 0; k < K; ++k) ds[k] += x[k];
+        }
+      }
     }
     warp_sum<K>(ds);
     float dsh = ds[0];
