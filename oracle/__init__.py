@@ -17,7 +17,9 @@ Routines follow:
   Tango (arXiv 2308.00890) Sec. 2.1, Fig. 1: GAT forward/backward steps;
   AdaQP Sec. 4.2 (Problem 11): per-message variance weight beta_k;
   Tango Sec. 3.2 (Eq. 4): relative quantization error Error_X and the
-      bit-count rule built on it.
+      bit-count rule built on it;
+  Tango Sec. 3.3: the SpMM's edge values quantized at 8 bits (one AdaQP
+      Eqn 4 vector per destination and head).
 
 Parity status: every routine is pinned by tests/test_oracle_*.py against the
 Tango worked example, closed forms, dense brute force or finite differences,
@@ -86,6 +88,8 @@ def _L():
                 "orc_edge_segment_sums": ([I64, P, P, P, I, P, P], None),
                 "orc_beta": ([I64, P, P, I, P, I, P], None),
                 "orc_quant_error": ([P, I64, I, P, P, I, D], D),
+                "orc_quantize_edge_values": ([I64, P, P, I, U64, P, P], None),
+                "orc_dequant_edge_values": ([I64, P, P, P, I, P], None),
             }
             for name, (args, res) in sig.items():
                 f = getattr(lib, name)
@@ -370,6 +374,32 @@ def edge_spmm(rowptr, col, alpha, M, transpose: bool = False) -> np.ndarray:
     out = np.zeros((n, d), np.float64)
     f = _L().orc_edge_spmm_t if transpose else _L().orc_edge_spmm
     f(n, _p(rowptr), _p(col), _p(alpha), heads, _p(M), d, _p(out))
+    return out
+
+
+def quantize_edge_values(rowptr, alpha, seed: int):
+    """Tango Sec. 3.3: the SpMM's edge values alpha (E x heads, CSR edge
+    order) quantized at 8 bits, one AdaQP Eqn 4 vector per (destination,
+    head) segment, u hashed from (seed, edge id, head).  Returns (codes
+    uint8 E x heads, hdr float32 n x heads x 2 holding {S, Z})."""
+    rowptr = _c(rowptr, np.int32)
+    alpha = _c(alpha, np.float32)
+    n = rowptr.shape[0] - 1
+    E, heads = alpha.shape
+    codes = np.zeros((E, heads), np.uint8)
+    hdr = np.zeros((n, heads, 2), np.float32)
+    _L().orc_quantize_edge_values(n, _p(rowptr), _p(alpha), heads, seed & 0xFFFFFFFFFFFFFFFF, _p(codes), _p(hdr))
+    return codes, hdr
+
+
+def dequant_edge_values(rowptr, codes, hdr) -> np.ndarray:
+    """AdaQP Eqn 5 per segment: fmaf(q, S[v,k], Z[v,k]), float32 E x heads."""
+    rowptr = _c(rowptr, np.int32)
+    codes = _c(codes, np.uint8)
+    hdr = _c(hdr, np.float32)
+    n = rowptr.shape[0] - 1
+    out = np.zeros(codes.shape, np.float32)
+    _L().orc_dequant_edge_values(n, _p(rowptr), _p(codes), _p(hdr), codes.shape[1], _p(out))
     return out
 
 

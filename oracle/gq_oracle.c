@@ -397,3 +397,52 @@ void orc_edge_segment_sums(int64_t n, const int32_t* rowptr, const int32_t* col,
         dS[(int64_t)col[e] * heads + k] += X[e * heads + k];
       }
 }
+
+/* ------------------------------------------------------------------------ */
+/* Tango Sec. 3.3 (SPMM on quantized node and edge features): the attention */
+/* values alpha of the multi-head SpMM quantized at 8 bits.  Reading: each   */
+/* (destination v, head k) segment alpha[rowptr[v]..rowptr[v+1], k] is one   */
+/* vector quantized with AdaQP Eqn 4 (its own zero-point Z = min and scale   */
+/* S = (max - min)/255, the same fp32 steps as orc_quantize); the uniform u  */
+/* is hashed from (seed, edge id e, head k).  codes: E x heads bytes by CSR  */
+/* edge id; hdr: n x heads x {S, Z} fp32 ({0, 0} for a row with no edges).   */
+/* ------------------------------------------------------------------------ */
+void orc_quantize_edge_values(int64_t n, const int32_t* rowptr, const float* alpha, int heads,
+                              uint64_t seed, uint8_t* codes, float* hdr) {
+  for (int64_t v = 0; v < n; ++v)
+    for (int k = 0; k < heads; ++k) {
+      const int64_t a = rowptr[v], b = rowptr[v + 1];
+      float mn = 0.0f, mx = 0.0f, S = 0.0f;
+      if (b > a) {
+        mn = mx = alpha[a * heads + k];
+        for (int64_t e = a + 1; e < b; ++e) {
+          const float x = alpha[e * heads + k];
+          if (x < mn) mn = x;
+          if (x > mx) mx = x;
+        }
+        S = (mx - mn) / 255.0f;
+      }
+      for (int64_t e = a; e < b; ++e) {
+        int q = 0;
+        if (S >= FLT_MIN) {
+          const float inv = 1.0f / S;
+          const float t = (alpha[e * heads + k] - mn) * inv;
+          q = (int)floorf(t + orc_uniform(seed, (uint32_t)e, (uint32_t)k));
+          if (q > 255) q = 255;
+        }
+        codes[e * heads + k] = (uint8_t)q;
+      }
+      hdr[(v * heads + k) * 2] = S;
+      hdr[(v * heads + k) * 2 + 1] = mn;
+    }
+}
+
+/* AdaQP Eqn 5 on the segments: alpha^[e,k] = fmaf(q, S[v,k], Z[v,k]). */
+void orc_dequant_edge_values(int64_t n, const int32_t* rowptr, const uint8_t* codes, const float* hdr,
+                             int heads, float* out) {
+  for (int64_t v = 0; v < n; ++v)
+    for (int64_t e = rowptr[v]; e < rowptr[v + 1]; ++e)
+      for (int k = 0; k < heads; ++k)
+        out[e * heads + k] = fmaf((float)codes[e * heads + k], hdr[(v * heads + k) * 2],
+                                  hdr[(v * heads + k) * 2 + 1]);
+}
