@@ -435,7 +435,7 @@ def run_gat(args, w):
     a_d = synth.glorot(heads, f, seed=w.seed + 3, device=dev)
     dOut = synth.normal_matrix(g.n, d, seed=w.seed, tag=synth.TAG_GRAD, device=dev)
     bits = w.bits[0]
-    L = q.GATLayer(G, d_in, heads, f, 0.2, bits, None)
+    L = q.GATLayer(G, d_in, heads, f, 0.2, bits, None, alpha_bits=args.alpha_bits)
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
     fwd = lambda: L.forward(H, Wt, a_s, a_d, 1)
     bwd = lambda: L.backward(dOut, H, Wt, a_s, a_d, 2)
@@ -451,9 +451,15 @@ def run_gat(args, w):
     t_sm = _timed(lambda: q.sddmm_edge_softmax(G, L.S, L.D), args.steps, flush)
     out = torch.empty(g.n, d, device=dev)
     t_sp = _timed(lambda: q.edge_spmm(G, L.alpha, L.Hp, None, None, d, 32, out=out), args.steps, flush)
+    # the 8-bit attention path (Tango Sec. 3.3): quantizer and SpMM over the codes
+    codes, hdr = q.quantize_edge_values(G, L.alpha, 1)
+    t_aq = _timed(lambda: q.quantize_edge_values(G, L.alpha, 1), args.steps, flush)
+    t_sp8 = _timed(lambda: q.edge_spmm_alpha8(G, codes, hdr, L.Hp, None, None, d, 32, out=out), args.steps, flush)
     E, n = g.nnz, g.n
     sm_bytes = (n + 1) * 4 + E * 4 + 2 * n * heads * 4 + E * heads * 4
     sp_bytes = (n + 1) * 4 + E * 4 + E * heads * 4 + n * d * 4 * 2
+    aq_bytes = (n + 1) * 4 + E * heads * 4 + E * heads + n * heads * 8
+    sp8_bytes = (n + 1) * 4 + E * 4 + E * heads + n * heads * 8 + n * d * 4 * 2
     peaks, kind = measured_peaks()
     peak = float(peaks.get("hbm_gbs", FALLBACK_HBM_GBS))
     step_ms = t_f + t_b
@@ -461,10 +467,13 @@ def run_gat(args, w):
             "warmup": args.warmup, "ms_per_step": step_ms, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f32 accumulate; bf16 tensor-core GEMM inputs", "data": "synthetic",
             "config": {"workload": w.name, "nodes": n, "edges": E, "d_in": d_in, "heads": heads, "f": f,
-                       "bits": bits, "l2": "flushed before every timed call"},
-            "stages_ms": {"layer_fwd": t_f, "layer_bwd": t_b, "edge_softmax": t_sm, "edge_spmm": t_sp},
+                       "bits": bits, "alpha_bits": args.alpha_bits, "l2": "flushed before every timed call"},
+            "stages_ms": {"layer_fwd": t_f, "layer_bwd": t_b, "edge_softmax": t_sm, "edge_spmm": t_sp,
+                          "alpha_quantize": t_aq, "edge_spmm_alpha8": t_sp8},
             "kernels_gbs": {"edge_softmax": sm_bytes / (t_sm / 1e3) / 1e9,
-                            "edge_spmm": sp_bytes / (t_sp / 1e3) / 1e9},
+                            "edge_spmm": sp_bytes / (t_sp / 1e3) / 1e9,
+                            "alpha_quantize": aq_bytes / (t_aq / 1e3) / 1e9,
+                            "edge_spmm_alpha8": sp8_bytes / (t_sp8 / 1e3) / 1e9},
             "roofline": {"kernel": "edge_spmm_kernel (multi-head aggregation)", "bound": "hbm",
                          "achieved": sp_bytes / (t_sp / 1e3) / 1e9, "peak": peak, "unit": "GB/s",
                          "frac": sp_bytes / (t_sp / 1e3) / 1e9 / peak, "peak_source": f"hbm_gbs of {kind}",
@@ -603,6 +612,8 @@ def main():
     ap.add_argument("--sweep-bits", default=None, help="aggregate workload: comma-separated bit-widths")
     ap.add_argument("--graph-scale", type=int, default=None,
                     help="aggregate / GAT workloads: R-MAT scale S (2^S nodes; 32 / 16 draws per node) for smaller cases")
+    ap.add_argument("--alpha-bits", type=int, default=32, choices=[32, 8],
+                    help="GAT workload: 8 quantizes the attention values the SpMM reads")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
     w = BY_NAME[args.workload]

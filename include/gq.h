@@ -184,7 +184,10 @@ typedef struct gq_graph {
                                gq_graph_prepare: an aggregation kernel on
                                this graph whose bounded wait for its own
                                row copies gave up writes a non-zero code
-                               here (first writer wins; it stays set).
+                               here (first writer wins; it stays set);
+                               the attention-value kernels write 0x4551
+                               for a row or task whose edge range lies
+                               outside the graph (and skip it).
                                Read it after synchronizing the stream.  */
 } gq_graph;
 
@@ -282,6 +285,45 @@ GQ_API int gq_edge_spmm(const gq_graph* g, int transpose, const float* alpha, in
                  int64_t ldx, const uint8_t* packed, const uint8_t* mask, int d, int bits,
                  float* Y, int64_t ldy, void* ws, size_t ws_bytes, gq_stream stream);
 
+
+/* ------------------------------------------------------------------------
+ * 8-bit attention values for the multi-head SpMM (Tango Sec. 3.3: the SpMM
+ * reads quantized node and edge features, produced by a separate sequential
+ * quantization pass).  Each (destination v, head k) segment of alpha, i.e.
+ * alpha[e,k] for the CSR edges e = rowptr[v] .. rowptr[v+1]-1, is one
+ * vector quantized as in gq_quantize_pack with b = 8 (its own Z = min and
+ * S = (max - Z)/255, the same fp32 steps), except that u is hashed from
+ * (seed, e, k) in place of (seed, row, column):
+ *   codes  E x heads uint8, by CSR edge id (16-byte aligned)
+ *   hdr    n x heads x {S, Z} fp32 (16-byte aligned); {0, 0} for a row
+ *          without edges.
+ * Values must be finite.  Bit-for-bit reproducible.  Each row and task
+ * range is checked against the graph before use; an invalid one is skipped
+ * and recorded in the graph's status word (0x4551).
+ *
+ * gq_quantize_edge_values: alpha (E x heads fp32, 16-byte aligned) ->
+ *   codes, hdr.  heads in {1, 2, 4, 8} (GQ_ERR_UNSUPPORTED otherwise).
+ *   Workspace: gq_quantize_edge_values_workspace_bytes (split heavy rows
+ *   only; may be 0; 256-byte aligned).
+ * gq_dequant_edge_values: out[e,k] = fmaf(codes[e,k], S[v,k], Z[v,k])
+ *   (AdaQP Eqn 5), E x heads fp32, 16-byte aligned.
+ * gq_edge_spmm_alpha8: gq_edge_spmm with transpose == 0 whose weights are
+ *   the de-quantized codes (each computed as in gq_dequant_edge_values);
+ *   d <= 256 (GQ_ERR_UNSUPPORTED otherwise); other arguments, errors and
+ *   workspace as gq_edge_spmm.
+ * GQ_ALPHA_SEED_TAG: the GAT layer quantizes its attention values with
+ *   seed ^ GQ_ALPHA_SEED_TAG, so their noise is independent of the
+ *   messages' noise drawn with the same seed.
+ * ---------------------------------------------------------------------- */
+#define GQ_ALPHA_SEED_TAG 0x5851F42D4C957F2DULL
+GQ_API size_t gq_quantize_edge_values_workspace_bytes(const gq_graph* g, int heads);
+GQ_API int gq_quantize_edge_values(const gq_graph* g, const float* alpha, int heads, uint64_t seed,
+                                   uint8_t* codes, float* hdr, void* ws, size_t ws_bytes, gq_stream stream);
+GQ_API int gq_dequant_edge_values(const gq_graph* g, const uint8_t* codes, const float* hdr, int heads,
+                                  float* out, gq_stream stream);
+GQ_API int gq_edge_spmm_alpha8(const gq_graph* g, const uint8_t* codes, const float* hdr, int heads,
+                               const float* X, int64_t ldx, const uint8_t* packed, const uint8_t* mask, int d,
+                               int bits, float* Y, int64_t ldy, void* ws, size_t ws_bytes, gq_stream stream);
 
 /* ------------------------------------------------------------------------
  * Dense update GEMMs on the tcgen05 tensor cores (bf16 inputs, fp32
@@ -382,34 +424,43 @@ GQ_API int gq_sddmm_edge_softmax(const gq_graph* g, const float* S, const float*
  *   S, D  = H' a_src, H' a_dst per head (GEMM epilogue)      -> n x heads
  *   [bits < 32: the H' rows of marginal nodes are quantized  -> packed_save]
  *   alpha = edge softmax of LeakyReLU(S[u] + D[v])           -> E x heads
- *   out   = sum_{u->v} alpha[e,k] m_u[kF+f]                  -> n x d
+ *   [alpha_bits == 8: alpha quantized per destination and head with
+ *    seed ^ GQ_ALPHA_SEED_TAG (gq_quantize_edge_values) -> acode_save,
+ *    ahdr_save, and a^ = its de-quantized values; alpha_bits == 32: a^ =
+ *    alpha.  Other values: GQ_ERR_INVALID_ARG]
+ *   out   = sum_{u->v} a^[e,k] m_u[kF+f]                     -> n x d
  *   packed_save (n x gq_packed_pitch(d, bits), nullable) keeps the
  *   forward's quantized messages for the backward pass (required there
- *   when bits < 32).
+ *   when bits < 32); acode_save / ahdr_save (both or neither; nullable)
+ *   keep the attention codes, which the backward needs to use a^.
  * gq_gat_layer_bwd (the quantizer is the identity in backward):
  *   dalpha = SDDMM dot of dOut[v] with the forward messages m_u;
  *   dE_pre = alpha (dalpha - P) LeakyReLU'; dD = in-edge sums, dS =
  *   out-edge sums; dM = transposed multi-head SpMM of dOut (rows of
- *   marginal nodes quantized when bits < 32, seed);
+ *   marginal nodes quantized when bits < 32, seed) weighted by a^
+ *   (the forward's codes acode_save / ahdr_save when given, else alpha);
  *   dH' = dM + dS a_src + dD a_dst; da_src = sum_u dS[u] H'[u],
  *   da_dst likewise; dW = H^T dH'; dH = dH' W^T.
  *   dEpre_save (E x heads) and dHp_save (n x d fp32) are optional copies.
  * Limits: heads in {1,2,4,8}, f a power of two >= 16, d_in, d <= 256.
- * Workspace: gq_gat_layer_workspace_bytes(g, d_in, heads, f, bits).
+ * Workspace: gq_gat_layer_workspace_bytes(g, d_in, heads, f, bits,
+ * alpha_bits), with alpha_bits = 8 for a backward given attention codes.
  * ---------------------------------------------------------------------- */
-GQ_API size_t gq_gat_layer_workspace_bytes(const gq_graph* g, int d_in, int heads, int f, int bits);
+GQ_API size_t gq_gat_layer_workspace_bytes(const gq_graph* g, int d_in, int heads, int f, int bits,
+                                           int alpha_bits);
 GQ_API int gq_gat_layer_fwd(const gq_graph* g, const float* H, int64_t ldh, int d_in, const float* W,
                      const float* a_src, const float* a_dst, int heads, int f, float slope,
-                     const uint8_t* mask, int bits, uint64_t seed, float* Hp_save, float* S_save,
-                     float* D_save, float* alpha_save, uint8_t* packed_save, float* out, void* ws,
-                     size_t ws_bytes, int* dev_err, gq_stream stream);
+                     const uint8_t* mask, int bits, uint64_t seed, int alpha_bits, float* Hp_save,
+                     float* S_save, float* D_save, float* alpha_save, uint8_t* packed_save,
+                     uint8_t* acode_save, float* ahdr_save, float* out, void* ws, size_t ws_bytes,
+                     int* dev_err, gq_stream stream);
 GQ_API int gq_gat_layer_bwd(const gq_graph* g, const float* dOut, const float* H, int64_t ldh,
                      const float* Hp_save, const float* S_save, const float* D_save,
-                     const float* alpha_save, const uint8_t* packed_save, const float* W,
-                     const float* a_src, const float* a_dst, int d_in, int heads, int f, float slope,
-                     const uint8_t* mask, int bits, uint64_t seed, float* dW, float* da_src,
-                     float* da_dst, float* dH, float* dEpre_save, float* dHp_save, void* ws,
-                     size_t ws_bytes, int* dev_err, gq_stream stream);
+                     const float* alpha_save, const uint8_t* packed_save, const uint8_t* acode_save,
+                     const float* ahdr_save, const float* W, const float* a_src, const float* a_dst,
+                     int d_in, int heads, int f, float slope, const uint8_t* mask, int bits, uint64_t seed,
+                     float* dW, float* da_src, float* da_dst, float* dH, float* dEpre_save,
+                     float* dHp_save, void* ws, size_t ws_bytes, int* dev_err, gq_stream stream);
 
 /* ------------------------------------------------------------------------
  * gq_dequant_spmm_noalloc -- no counterpart on the pages: a convenience of

@@ -443,11 +443,20 @@ def edge_segment_sums(rowptr, col, X):
     return dD, dS
 
 
+# The layer draws the attention values' noise from seed ^ ALPHA_SEED_TAG, so
+# that it is independent of the messages' noise drawn with the same seed (a
+# fixed choice of this implementation; any constant with that property would
+# do).
+ALPHA_SEED_TAG = 0x5851F42D4C957F2D
+
+
 def gat_layer_fwd(rowptr, col, H, W, a_src, a_dst, heads, slope, mask=None, bits=32, seed=0,
-                  bf16: bool = True):
+                  bf16: bool = True, alpha_bits: int = 32):
     """Tango Fig. 1a: H' = H W (step 1); S, D head projections (step 2);
     SDDMM add + LeakyReLU (step 3); edge softmax (step 4); SpMM (step 5).
-    With bits < 32 the H' rows of marginal nodes are the quantized messages."""
+    With bits < 32 the H' rows of marginal nodes are the quantized messages;
+    with alpha_bits = 8 the SpMM weights are the attention values quantized
+    per destination and head (Tango Sec. 3.3), returned as ahat."""
     Hp = gemm(H, W, bf16)
     S = head_proj(Hp, a_src, heads)
     D = head_proj(Hp, a_dst, heads)
@@ -456,14 +465,19 @@ def gat_layer_fwd(rowptr, col, H, W, a_src, a_dst, heads, slope, mask=None, bits
     d = Hp.shape[1]
     packed = quantize(Hp32, mask, bits, seed) if bits < 32 else None
     M = messages(Hp32, packed, mask, d, bits) if bits < 32 else Hp
-    out = edge_spmm(rowptr, col, alpha, M)
-    return dict(Hp=Hp, S=S, D=D, Epre=Epre, alpha=alpha, packed=packed, M=M, out=out)
+    ahat = alpha
+    if alpha_bits == 8:
+        acode, ahdr = quantize_edge_values(rowptr, alpha.astype(np.float32), seed ^ ALPHA_SEED_TAG)
+        ahat = dequant_edge_values(rowptr, acode, ahdr).astype(np.float64)
+    out = edge_spmm(rowptr, col, ahat, M)
+    return dict(Hp=Hp, S=S, D=D, Epre=Epre, alpha=alpha, packed=packed, M=M, out=out, ahat=ahat)
 
 
 def gat_layer_bwd(rowptr, col, dOut, H, M, Hp, Epre, alpha, W, a_src, a_dst, heads, slope,
-                  mask=None, bits=32, seed=0, bf16: bool = True):
+                  mask=None, bits=32, seed=0, bf16: bool = True, ahat=None):
     """Tango Fig. 1b.  M = the forward messages (H' rows, de-quantized where
-    marginal).  dalpha by SDDMM dot; softmax derivative; LeakyReLU'; dD by
+    marginal); ahat = the forward's SpMM weights when they were quantized
+    (the transposed SpMM uses them; the softmax derivative uses alpha).  dalpha by SDDMM dot; softmax derivative; LeakyReLU'; dD by
     in-edge sums, dS by out-edge sums; dM = transposed edge SpMM of dOut
     (whose marginal rows travel quantized when bits < 32); then
     dH' = dM + dS a_src + dD a_dst, da_src/da_dst, dW = H^T dH', dH = dH' W^T."""
@@ -476,7 +490,7 @@ def gat_layer_bwd(rowptr, col, dOut, H, M, Hp, Epre, alpha, W, a_src, a_dst, hea
     dOut32 = dOut.astype(np.float32)
     packed = quantize(dOut32, mask, bits, seed) if bits < 32 else None
     Mb = messages(dOut32, packed, mask, d, bits) if bits < 32 else dOut
-    dM = edge_spmm(rowptr, col, alpha, Mb, transpose=True)
+    dM = edge_spmm(rowptr, col, alpha if ahat is None else ahat, Mb, transpose=True)
     a_src = np.asarray(a_src, np.float64).reshape(heads, F)
     a_dst = np.asarray(a_dst, np.float64).reshape(heads, F)
     dHp = dM + np.repeat(dS, F, axis=1) * a_src.reshape(1, d) + np.repeat(dD, F, axis=1) * a_dst.reshape(1, d)

@@ -99,10 +99,14 @@ def _SIGNATURES(P, I64, I, U64, F, S):
         ("gq_gcn_layer_workspace_bytes", [GP, I, I, I], S),
         ("gq_edge_softmax_workspace_bytes", [GP, I], S),
         ("gq_sddmm_edge_softmax", [GP, P, P, I, F, P, P, P, S, P], I),
-        ("gq_gat_layer_workspace_bytes", [GP, I, I, I, I], S),
-        ("gq_gat_layer_fwd", [GP, P, I64, I, P, P, P, I, I, F, P, I, U64, P, P, P, P, P, P, P, S, P, P], I),
-        ("gq_gat_layer_bwd", [GP, P, P, I64, P, P, P, P, P, P, P, P, I, I, I, F, P, I, U64, P, P, P, P, P, P, P, S,
-                              P, P], I),
+        ("gq_quantize_edge_values_workspace_bytes", [GP, I], S),
+        ("gq_quantize_edge_values", [GP, P, I, U64, P, P, P, S, P], I),
+        ("gq_dequant_edge_values", [GP, P, P, I, P, P], I),
+        ("gq_edge_spmm_alpha8", [GP, P, P, I, P, I64, P, P, I, I, P, I64, P, S, P], I),
+        ("gq_gat_layer_workspace_bytes", [GP, I, I, I, I, I], S),
+        ("gq_gat_layer_fwd", [GP, P, I64, I, P, P, P, I, I, F, P, I, U64, I, P, P, P, P, P, P, P, P, P, S, P, P], I),
+        ("gq_gat_layer_bwd", [GP, P, P, I64, P, P, P, P, P, P, P, P, P, P, I, I, I, F, P, I, U64, P, P, P, P, P, P,
+                              P, S, P, P], I),
         ("gq_gcn_layer_fwd", [GP, I, P, I64, I, P, I, P, I, U64, I, P, I64, P, I64, P, S, P, P, P], I),
         ("gq_gcn_layer_bwd",
          [GP, I, P, I64, P, I64, P, I64, P, I, I, P, I, U64, I, I, P, P, I64, P, P, S, P, P, P], I),
@@ -558,12 +562,60 @@ def sddmm_edge_softmax(g: Graph, S: torch.Tensor, D: torch.Tensor, slope: float 
     return (alpha, Epre) if with_epre else alpha
 
 
+ALPHA_SEED_TAG = 0x5851F42D4C957F2D  # GQ_ALPHA_SEED_TAG
+
+
+def quantize_edge_values(g: Graph, alpha: torch.Tensor, seed: int):
+    """8-bit codes (E x heads uint8) and {S, Z} headers (n x heads x 2 fp32)
+    of the attention values, one quantized vector per destination and head
+    (Tango Sec. 3.3, AdaQP Eqn 4)."""
+    _cuda(alpha, torch.float32, "alpha")
+    heads = alpha.shape[1]
+    codes = torch.empty(g.nnz, heads, dtype=torch.uint8, device=alpha.device)
+    hdr = torch.empty(g.n, heads, 2, dtype=torch.float32, device=alpha.device)
+    wb = int(lib().gq_quantize_edge_values_workspace_bytes(g.ref, heads))
+    ws = torch.empty(max(wb, 1), dtype=torch.uint8, device=alpha.device)
+    _check(lib().gq_quantize_edge_values(g.ref, _ptr(alpha.contiguous()), heads, seed & 0xFFFFFFFFFFFFFFFF,
+                                         _ptr(codes), _ptr(hdr), _ptr(ws), wb, _stream()), "gq_quantize_edge_values")
+    return codes, hdr
+
+
+def dequant_edge_values(g: Graph, codes: torch.Tensor, hdr: torch.Tensor) -> torch.Tensor:
+    """fmaf(q, S, Z) per edge and head (AdaQP Eqn 5), E x heads fp32."""
+    _cuda(codes, torch.uint8, "codes")
+    _cuda(hdr, torch.float32, "hdr")
+    out = torch.empty(codes.shape, dtype=torch.float32, device=codes.device)
+    _check(lib().gq_dequant_edge_values(g.ref, _ptr(codes), _ptr(hdr), codes.shape[1], _ptr(out), _stream()),
+           "gq_dequant_edge_values")
+    return out
+
+
+def edge_spmm_alpha8(g: Graph, codes: torch.Tensor, hdr: torch.Tensor, X: torch.Tensor | None,
+                     packed: torch.Tensor | None, mask: torch.Tensor | None, d: int, bits: int = 32,
+                     out: torch.Tensor | None = None) -> torch.Tensor:
+    """Forward multi-head SpMM whose attention weights are 8-bit codes."""
+    _cuda(codes, torch.uint8, "codes")
+    _cuda(hdr, torch.float32, "hdr")
+    _cuda(X, torch.float32, "X")
+    heads = codes.shape[1]
+    if out is None:
+        out = torch.empty(g.n, d, dtype=torch.float32, device=codes.device)
+    ldx = _rows(X) if X is not None else d
+    wb = int(lib().gq_spmm_workspace_bytes(g.ref, 0, d))
+    ws = torch.empty(max(wb, 1), dtype=torch.uint8, device=codes.device)
+    _check(lib().gq_edge_spmm_alpha8(g.ref, _ptr(codes), _ptr(hdr), heads, _ptr(X), ldx, _ptr(packed), _ptr(mask),
+                                     d, bits, _ptr(out), _rows(out), _ptr(ws), wb, _stream()), "gq_edge_spmm_alpha8")
+    return out
+
+
 class GATLayer:
-    """Buffers and calls of one GAT layer (heads x f, LeakyReLU slope)."""
+    """Buffers and calls of one GAT layer (heads x f, LeakyReLU slope).
+    alpha_bits = 8 quantizes the attention values the SpMM reads."""
 
     def __init__(self, g: Graph, d_in: int, heads: int, f: int, slope: float = 0.2, bits: int = 32,
-                 mask=None, device="cuda"):
+                 mask=None, device="cuda", alpha_bits: int = 32):
         self.g, self.d_in, self.heads, self.f, self.slope, self.bits, self.mask = g, d_in, heads, f, slope, bits, mask
+        self.alpha_bits = alpha_bits
         d = heads * f
         n = g.n
         self.Hp = torch.empty(n, d, dtype=torch.float32, device=device)
@@ -577,23 +629,27 @@ class GATLayer:
         self.da_src = torch.empty(heads, f, dtype=torch.float32, device=device)
         self.da_dst = torch.empty(heads, f, dtype=torch.float32, device=device)
         self.dH = torch.empty(n, d_in, dtype=torch.float32, device=device)
+        self.acode = (torch.empty(g.nnz, heads, dtype=torch.uint8, device=device) if alpha_bits == 8 else None)
+        self.ahdr = (torch.empty(n, heads, 2, dtype=torch.float32, device=device) if alpha_bits == 8 else None)
         self.err = torch.zeros(1, dtype=torch.int32, device=device)
         self.ws = Workspace(device)
-        self.ws.get(int(lib().gq_gat_layer_workspace_bytes(g.ref, d_in, heads, f, bits)))
+        self.ws.get(int(lib().gq_gat_layer_workspace_bytes(g.ref, d_in, heads, f, bits, alpha_bits)))
 
     def forward(self, H, W, a_src, a_dst, seed: int = 0):
         buf = self.ws.buf
         _check(lib().gq_gat_layer_fwd(self.g.ref, _ptr(H), _rows(H), self.d_in, _ptr(W), _ptr(a_src), _ptr(a_dst),
                                       self.heads, self.f, self.slope, _ptr(self.mask), self.bits,
-                                      seed & 0xFFFFFFFFFFFFFFFF, _ptr(self.Hp), _ptr(self.S), _ptr(self.D),
-                                      _ptr(self.alpha), _ptr(self.packed), _ptr(self.out), _ptr(buf), buf.numel(),
-                                      _ptr(self.err), _stream()), "gq_gat_layer_fwd")
+                                      seed & 0xFFFFFFFFFFFFFFFF, self.alpha_bits, _ptr(self.Hp), _ptr(self.S),
+                                      _ptr(self.D), _ptr(self.alpha), _ptr(self.packed), _ptr(self.acode),
+                                      _ptr(self.ahdr), _ptr(self.out), _ptr(buf), buf.numel(), _ptr(self.err),
+                                      _stream()), "gq_gat_layer_fwd")
         return self.out
 
     def backward(self, dOut, H, W, a_src, a_dst, seed: int = 0, dEpre=None, dHp=None):
         buf = self.ws.buf
         _check(lib().gq_gat_layer_bwd(self.g.ref, _ptr(dOut), _ptr(H), _rows(H), _ptr(self.Hp), _ptr(self.S),
-                                      _ptr(self.D), _ptr(self.alpha), _ptr(self.packed), _ptr(W), _ptr(a_src),
+                                      _ptr(self.D), _ptr(self.alpha), _ptr(self.packed), _ptr(self.acode),
+                                      _ptr(self.ahdr), _ptr(W), _ptr(a_src),
                                       _ptr(a_dst), self.d_in, self.heads, self.f, self.slope, _ptr(self.mask),
                                       self.bits, seed & 0xFFFFFFFFFFFFFFFF, _ptr(self.dW), _ptr(self.da_src),
                                       _ptr(self.da_dst), _ptr(self.dH), _ptr(dEpre), _ptr(dHp), _ptr(buf),

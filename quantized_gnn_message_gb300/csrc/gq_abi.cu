@@ -15,7 +15,7 @@ extern "C" const char* gq_status_string(int status) {
   }
 }
 
-extern "C" int gq_version(void) { return 100; }
+extern "C" int gq_version(void) { return 200; }
 
 extern "C" size_t gq_graph_struct_bytes(void) { return sizeof(gq_graph); }
 

@@ -107,8 +107,28 @@ struct SoftmaxParams {
   float* alpha;
   float* Epre;
   int64_t n_rows;
+  int64_t n_edges;
+  int64_t n_groups;
+  int* err;  // graph status word
   Sched sc;
 };
+
+// Self-checks of the softmax: each row, task and group range is checked
+// against the graph before it is walked, and each column id before its S
+// row is read; an invalid one is recorded in the graph status word
+// (kSoftmaxBadIndex) and the access is skipped (the row or task) or sent to
+// row 0 (a column id).  The column check is kept out of line.
+constexpr int kSoftmaxBadIndex = 0x534D;
+__device__ __noinline__ int32_t sm_checked_col(int32_t x, int64_t n, int* err) {
+  if (x >= 0 && x < n) return x;
+  atomicCAS(err, 0, kSoftmaxBadIndex);
+  return 0;
+}
+__device__ __forceinline__ bool sm_range_ok(const SoftmaxParams& p, int64_t v, int64_t a, int64_t b) {
+  const bool ok = v >= 0 && v < p.n_rows && a >= 0 && a <= b && b <= p.n_edges;
+  if (!ok) atomicCAS(p.err, 0, kSoftmaxBadIndex);
+  return ok;
+}
 
 template <int K>
 __device__ __forceinline__ void sm_scores(const SoftmaxParams& p, int64_t e, const float (&dv)[K], float (&ep)[K]) {
@@ -130,7 +150,7 @@ __device__ __forceinline__ void sm_scores4s(const SoftmaxParams& p, int64_t e, i
 #pragma unroll
   for (int t = 0; t < 4; ++t) {
     float s[K];
-    load_k<K>(p.S + (int64_t)x[t] * K, s);
+    load_k<K>(p.S + (int64_t)sm_checked_col(x[t], p.n_rows, p.err) * K, s);
 #pragma unroll
     for (int k = 0; k < K; ++k) ep[t][k] = s[k] + dv[k];
   }
@@ -198,7 +218,7 @@ __device__ __forceinline__ void sm_scores4(const SoftmaxParams& p, int64_t e, in
 #pragma unroll
   for (int t = 0; t < 4; ++t) {
     float s[K];
-    load_k<K>(p.S + (int64_t)x[t] * K, s);
+    load_k<K>(p.S + (int64_t)sm_checked_col(x[t], p.n_rows, p.err) * K, s);
 #pragma unroll
     for (int k = 0; k < K; ++k) ep[t][k] = s[k] + dv[k];
   }
@@ -271,7 +291,8 @@ __global__ void __launch_bounds__(kGatThreads) edge_softmax_kernel(const Softmax
   const int64_t gw = (int64_t)blockIdx.x * kGatWarps + w;
   const int64_t nw = (int64_t)gridDim.x * kGatWarps;
   for (int64_t t = gw; t < p.sc.n_tasks; t += nw) {
-    const int4 task = __ldg(reinterpret_cast<const int4*>(p.sc.tasks) + t);
+    int4 task = __ldg(reinterpret_cast<const int4*>(p.sc.tasks) + t);
+    if (!sm_range_ok(p, task.x, task.y, task.z)) task = make_int4(0, 0, 0, -1);
     float dv[K];
     load_k<K>(p.D + (int64_t)task.x * K, dv);
     float m[K], l[K];
@@ -297,6 +318,7 @@ __global__ void __launch_bounds__(kGatThreads) edge_softmax_kernel(const Softmax
     if (r < p.n_rows) {
       a = __ldg(p.rowptr + r);
       b = __ldg(p.rowptr + r + 1);
+      if (!sm_range_ok(p, r, a, b)) b = a;
     }
     if (r < p.n_rows && b - a <= 32) sm_thread_row<K>(p, r, a, b);
     unsigned mid = __ballot_sync(FULL, r < p.n_rows && b - a > 32 && b - a <= p.sc.hub_threshold);
@@ -325,10 +347,19 @@ __global__ void __launch_bounds__(kGatThreads) edge_softmax_heavy_kernel(const S
   if (t >= p.sc.n_tasks) return;
   const int4 task = __ldg(reinterpret_cast<const int4*>(p.sc.tasks) + t);
   int64_t t0 = t, nt = 1;
+  if (task.w >= p.n_groups) {
+    atomicCAS(p.err, 0, kSoftmaxBadIndex);
+    return;
+  }
   if (task.w >= 0) {
     const int4 grp = __ldg(reinterpret_cast<const int4*>(p.sc.groups) + task.w);
     t0 = grp.y;
     nt = grp.z;
+  }
+  if (!sm_range_ok(p, task.x, task.y, task.z) || t0 < 0 || nt < 1 || t0 + nt > p.sc.n_tasks || t < t0 ||
+      t >= t0 + nt) {
+    atomicCAS(p.err, 0, kSoftmaxBadIndex);
+    return;
   }
   float m[K], l[K];
   const float* base = p.sc.partial + t0 * 2 * K;
@@ -341,6 +372,277 @@ __global__ void __launch_bounds__(kGatThreads) edge_softmax_heavy_kernel(const S
   float dv[K];
   load_k<K>(p.D + (int64_t)task.x * K, dv);
   sm_pass2<K>(p, (int64_t)task.y + lane, task.z, 32, dv, m, l);
+}
+
+// ------------------------------------------- 8-bit attention values ---
+// Tango Sec. 3.3: the SpMM reads quantized edge features.  Each (destination
+// v, head k) segment alpha[rowptr[v] .. rowptr[v+1], k] is one vector of
+// AdaQP Sec. 2.3 Eqn 4 at 8 bits: Z = min, S = (max - min) / 255,
+// q = min(floor((alpha - Z) * (1/S) + u), 255) in fp32 round-to-nearest
+// steps, u hashed from (seed, edge id, head); a segment with S below the
+// smallest normal float codes as 0.  codes[e*K + k] bytes, hdr[(v*K + k)*2]
+// = {S, Z}, {0, 0} for a row without edges.  Same schedule as the softmax:
+// thread rows, warp rows, and heavy rows as warp tasks whose (min, max)
+// partials merge in a second kernel (min and max are exact in any order).
+struct EdgeQuantParams {
+  const int32_t* rowptr;
+  const float* alpha;
+  uint8_t* codes;
+  float* hdr;
+  uint32_t seed_key;
+  int64_t n_rows;
+  int64_t n_edges;
+  Sched sc;      // partial: [task][2K] {min, max}
+  float* deq;    // de-quantized values (edge_dequant_kernel)
+  int* err;      // graph status word: kEdgeQuantBadRange if a row or task range was invalid
+};
+
+// Every edge range is checked against the edge count before it is read or
+// written; an invalid one is recorded in the status word and skipped.
+constexpr int kEdgeQuantBadRange = 0x4551;
+__device__ __forceinline__ bool eq_range_ok(const EdgeQuantParams& p, int64_t v, int64_t a, int64_t b) {
+  const bool ok = v >= 0 && v < p.n_rows && a >= 0 && a <= b && b <= p.n_edges;
+  if (!ok) atomicCAS(p.err, 0, kEdgeQuantBadRange);
+  return ok;
+}
+
+template <int K>
+__device__ __forceinline__ void eq_minmax(const EdgeQuantParams& p, int64_t first, int64_t end, int64_t stride,
+                                          float (&mn)[K], float (&mx)[K]) {
+#pragma unroll
+  for (int k = 0; k < K; ++k) {
+    mn[k] = __builtin_huge_valf();
+    mx[k] = kNegInf;
+  }
+  int64_t e = first;
+  for (; e + 3 * stride < end; e += 4 * stride) {
+    float a[4][K];
+#pragma unroll
+    for (int t = 0; t < 4; ++t) load_k<K>(p.alpha + (e + t * stride) * K, a[t]);
+#pragma unroll
+    for (int t = 0; t < 4; ++t)
+#pragma unroll
+      for (int k = 0; k < K; ++k) {
+        mn[k] = fminf(mn[k], a[t][k]);
+        mx[k] = fmaxf(mx[k], a[t][k]);
+      }
+  }
+  for (; e < end; e += stride) {
+    float a[K];
+    load_k<K>(p.alpha + e * K, a);
+#pragma unroll
+    for (int k = 0; k < K; ++k) {
+      mn[k] = fminf(mn[k], a[k]);
+      mx[k] = fmaxf(mx[k], a[k]);
+    }
+  }
+}
+
+template <int K>
+__device__ __forceinline__ void warp_minmax(float (&mn)[K], float (&mx)[K]) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1)
+#pragma unroll
+    for (int k = 0; k < K; ++k) {
+      mn[k] = fminf(mn[k], __shfl_xor_sync(FULL, mn[k], o));
+      mx[k] = fmaxf(mx[k], __shfl_xor_sync(FULL, mx[k], o));
+    }
+}
+
+// Eqn 4 scale of each head's segment; writes the row's header when `head`.
+template <int K>
+__device__ __forceinline__ void eq_scale(const EdgeQuantParams& p, int64_t v, const float (&mn)[K],
+                                         const float (&mx)[K], bool head, float (&S)[K], float (&inv)[K]) {
+#pragma unroll
+  for (int k = 0; k < K; ++k) {
+    S[k] = __fdiv_rn(__fsub_rn(mx[k], mn[k]), 255.0f);
+    inv[k] = S[k] >= 1.17549435e-38f ? __frcp_rn(S[k]) : 0.0f;  // 0: constant segment
+    if (head) reinterpret_cast<float2*>(p.hdr)[v * K + k] = make_float2(S[k], mn[k]);
+  }
+}
+
+template <int K>
+__device__ __forceinline__ void store_codes(uint8_t* dst, const uint32_t (&q)[K]) {
+  if constexpr (K == 1) {
+    *dst = (uint8_t)q[0];
+  } else if constexpr (K == 2) {
+    *reinterpret_cast<uint16_t*>(dst) = (uint16_t)(q[0] | (q[1] << 8));
+  } else if constexpr (K == 4) {
+    *reinterpret_cast<uint32_t*>(dst) = q[0] | (q[1] << 8) | (q[2] << 16) | (q[3] << 24);
+  } else {
+    *reinterpret_cast<uint2*>(dst) = make_uint2(q[0] | (q[1] << 8) | (q[2] << 16) | (q[3] << 24),
+                                                q[4] | (q[5] << 8) | (q[6] << 16) | (q[7] << 24));
+  }
+}
+
+// Codes of this thread's edges e = first, first + stride, ...
+template <int K>
+__device__ __forceinline__ void eq_codes(const EdgeQuantParams& p, int64_t first, int64_t end, int64_t stride,
+                                         const float (&mn)[K], const float (&inv)[K]) {
+  for (int64_t e = first; e < end; e += stride) {
+    float a[K];
+    load_k<K>(p.alpha + e * K, a);
+    const uint32_t kr = row_key(p.seed_key, (uint32_t)e);
+    uint32_t q[K];
+#pragma unroll
+    for (int k = 0; k < K; ++k) {
+      q[k] = 0;
+      if (inv[k] != 0.0f) {
+        const float s = __fadd_rn(__fmul_rn(__fsub_rn(a[k], mn[k]), inv[k]), noise_u(kr, (uint32_t)k));
+        // floor(s) for s in [0, 2^23): add 2^23 rounding down, read the mantissa
+        q[k] = min(__float_as_uint(__fadd_rd(s, 8388608.0f)) - 0x4B000000u, 255u);
+      }
+    }
+    store_codes<K>(p.codes + e * K, q);
+  }
+}
+
+template <int K>
+__global__ void __launch_bounds__(kGatThreads) edge_quant_kernel(const EdgeQuantParams p) {
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  const int64_t gw = (int64_t)blockIdx.x * kGatWarps + w;
+  const int64_t nw = (int64_t)gridDim.x * kGatWarps;
+  // heavy rows: (min, max) of each task's edges into part[task]
+  for (int64_t t = gw; t < p.sc.n_tasks; t += nw) {
+    const int4 task = __ldg(reinterpret_cast<const int4*>(p.sc.tasks) + t);
+    float mn[K], mx[K];
+    const bool ok = eq_range_ok(p, task.x, task.y, task.z);
+    eq_minmax<K>(p, (int64_t)task.y + lane, ok ? task.z : task.y, 32, mn, mx);
+    warp_minmax<K>(mn, mx);
+    if (lane == 0) {
+      float* mine = p.sc.partial + t * 2 * K;
+#pragma unroll
+      for (int k = 0; k < K; ++k) {
+        mine[2 * k] = mn[k];
+        mine[2 * k + 1] = mx[k];
+      }
+    }
+  }
+  // light rows in groups of 32 consecutive rows per warp: a row of at most
+  // 32 edges is one thread's; the group's rows of 33 .. hub_threshold edges
+  // are then taken one at a time by the whole warp
+  const int64_t groups = (p.n_rows + 31) / 32;
+  for (int64_t grp = gw; grp < groups; grp += nw) {
+    const int64_t r = grp * 32 + lane;
+    int64_t a = 0, b = 0;
+    if (r < p.n_rows) {
+      a = __ldg(p.rowptr + r);
+      b = __ldg(p.rowptr + r + 1);
+    }
+    if (r < p.n_rows && !eq_range_ok(p, r, a, b)) {
+      b = a;  // skipped: neither a thread row nor a warp row
+    } else if (r < p.n_rows && b == a) {
+#pragma unroll
+      for (int k = 0; k < K; ++k) reinterpret_cast<float2*>(p.hdr)[r * K + k] = make_float2(0.0f, 0.0f);
+    } else if (r < p.n_rows && b - a <= 32) {
+      float mn[K], mx[K], S[K], inv[K];
+      eq_minmax<K>(p, a, b, 1, mn, mx);
+      eq_scale<K>(p, r, mn, mx, true, S, inv);
+      eq_codes<K>(p, a, b, 1, mn, inv);
+    }
+    unsigned mid = __ballot_sync(FULL, r < p.n_rows && b - a > 32 && b - a <= p.sc.hub_threshold);
+    while (mid != 0) {
+      const int l0 = __ffs(mid) - 1;
+      mid &= mid - 1;
+      const int64_t v = grp * 32 + l0;
+      const int64_t va = __shfl_sync(FULL, a, l0), vb = __shfl_sync(FULL, b, l0);
+      float mn[K], mx[K], S[K], inv[K];
+      eq_minmax<K>(p, va + lane, vb, 32, mn, mx);
+      warp_minmax<K>(mn, mx);
+      eq_scale<K>(p, v, mn, mx, lane == 0, S, inv);
+      eq_codes<K>(p, va + lane, vb, 32, mn, inv);
+    }
+  }
+}
+
+// Heavy rows, second kernel: one warp per task merges the (min, max) of its
+// row's tasks, the row's first task writes the header, every task its codes.
+template <int K>
+__global__ void __launch_bounds__(kGatThreads) edge_quant_heavy_kernel(const EdgeQuantParams p) {
+  const int lane = threadIdx.x & 31;
+  const int64_t t = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  if (t >= p.sc.n_tasks) return;
+  const int4 task = __ldg(reinterpret_cast<const int4*>(p.sc.tasks) + t);
+  int64_t t0 = t, nt = 1;
+  if (task.w >= 0) {
+    const int4 grp = __ldg(reinterpret_cast<const int4*>(p.sc.groups) + task.w);
+    t0 = grp.y;
+    nt = grp.z;
+  }
+  if (!eq_range_ok(p, task.x, task.y, task.z) || t0 < 0 || t0 + nt > p.sc.n_tasks || t < t0 || t >= t0 + nt) {
+    atomicCAS(p.err, 0, kEdgeQuantBadRange);
+    return;
+  }
+  float mn[K], mx[K], S[K], inv[K];
+  const float* base = p.sc.partial + t0 * 2 * K;
+#pragma unroll
+  for (int k = 0; k < K; ++k) {
+    mn[k] = __ldcg(base + 2 * k);
+    mx[k] = __ldcg(base + 2 * k + 1);
+    for (int64_t i = 1; i < nt; ++i) {
+      mn[k] = fminf(mn[k], __ldcg(base + i * 2 * K + 2 * k));
+      mx[k] = fmaxf(mx[k], __ldcg(base + i * 2 * K + 2 * k + 1));
+    }
+  }
+  eq_scale<K>(p, task.x, mn, mx, t == t0 && lane == 0, S, inv);
+  eq_codes<K>(p, (int64_t)task.y + lane, task.z, 32, mn, inv);
+}
+
+// AdaQP Eqn 5 on the attention codes: deq[e,k] = fmaf(q, S[v,k], Z[v,k]),
+// one kernel over the same thread / warp rows and heavy-row warp tasks.
+template <int K>
+__device__ __forceinline__ void eq_expand(const EdgeQuantParams& p, int64_t v, int64_t first, int64_t end,
+                                          int64_t stride) {
+  float2 h[K];
+#pragma unroll
+  for (int k = 0; k < K; ++k) h[k] = __ldg(reinterpret_cast<const float2*>(p.hdr) + v * K + k);
+  for (int64_t e = first; e < end; e += stride) {
+    uint32_t w[(K + 3) / 4];
+    if constexpr (K == 8) {
+      const uint2 x = __ldg(reinterpret_cast<const uint2*>(p.codes + e * K));
+      w[0] = x.x;
+      w[1] = x.y;
+    } else if constexpr (K == 4) {
+      w[0] = __ldg(reinterpret_cast<const uint32_t*>(p.codes + e * K));
+    } else if constexpr (K == 2) {
+      w[0] = __ldg(reinterpret_cast<const uint16_t*>(p.codes + e * K));
+    } else {
+      w[0] = __ldg(p.codes + e);
+    }
+    float a[K];
+#pragma unroll
+    for (int k = 0; k < K; ++k) a[k] = __fmaf_rn(code_to_float((w[k >> 2] >> (8 * (k & 3))) & 0xFFu), h[k].x, h[k].y);
+    store_k<K>(p.deq + e * K, a);
+  }
+}
+
+template <int K>
+__global__ void __launch_bounds__(kGatThreads) edge_dequant_kernel(const EdgeQuantParams p) {
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  const int64_t gw = (int64_t)blockIdx.x * kGatWarps + w;
+  const int64_t nw = (int64_t)gridDim.x * kGatWarps;
+  for (int64_t t = gw; t < p.sc.n_tasks; t += nw) {
+    const int4 task = __ldg(reinterpret_cast<const int4*>(p.sc.tasks) + t);
+    if (eq_range_ok(p, task.x, task.y, task.z)) eq_expand<K>(p, task.x, (int64_t)task.y + lane, task.z, 32);
+  }
+  const int64_t groups = (p.n_rows + 31) / 32;
+  for (int64_t grp = gw; grp < groups; grp += nw) {
+    const int64_t r = grp * 32 + lane;
+    int64_t a = 0, b = 0;
+    if (r < p.n_rows) {
+      a = __ldg(p.rowptr + r);
+      b = __ldg(p.rowptr + r + 1);
+    }
+    if (r < p.n_rows && !eq_range_ok(p, r, a, b)) b = a;
+    if (r < p.n_rows && b - a <= 32) eq_expand<K>(p, r, a, b, 1);
+    unsigned mid = __ballot_sync(FULL, r < p.n_rows && b - a > 32 && b - a <= p.sc.hub_threshold);
+    while (mid != 0) {
+      const int l0 = __ffs(mid) - 1;
+      mid &= mid - 1;
+      const int64_t va = __shfl_sync(FULL, a, l0), vb = __shfl_sync(FULL, b, l0);
+      eq_expand<K>(p, grp * 32 + l0, va + lane, vb, 32);
+    }
+  }
 }
 
 // --------------------------------------------------- GAT edge backward ---
@@ -695,6 +997,31 @@ int launch_softmax(const SoftmaxParams& p, cudaStream_t s) {
   return GQ_OK;
 }
 
+template <int K>
+int launch_edge_quant(const EdgeQuantParams& p, cudaStream_t s) {
+  int64_t blocks = ((p.n_rows + 31) / 32 + p.sc.n_tasks + kGatWarps - 1) / kGatWarps;
+  const int64_t cap = (int64_t)sm_count() * 8;
+  if (blocks > cap) blocks = cap;
+  if (blocks < 1) blocks = 1;
+  edge_quant_kernel<K><<<(unsigned)blocks, kGatThreads, 0, s>>>(p);
+  GQ_TRY(launch_status());
+  if (p.sc.n_tasks > 0) {
+    edge_quant_heavy_kernel<K><<<(unsigned)((p.sc.n_tasks + kGatWarps - 1) / kGatWarps), kGatThreads, 0, s>>>(p);
+    GQ_TRY(launch_status());
+  }
+  return GQ_OK;
+}
+
+template <int K>
+int launch_edge_dequant(const EdgeQuantParams& p, cudaStream_t s) {
+  int64_t blocks = ((p.n_rows + 31) / 32 + p.sc.n_tasks + kGatWarps - 1) / kGatWarps;
+  const int64_t cap = (int64_t)sm_count() * 8;
+  if (blocks > cap) blocks = cap;
+  if (blocks < 1) blocks = 1;
+  edge_dequant_kernel<K><<<(unsigned)blocks, kGatThreads, 0, s>>>(p);
+  return launch_status();
+}
+
 template <int BITS, int K>
 int launch_edge_bwd(const EdgeBwdParams& p, cudaStream_t s) {
   gat_edge_bwd_kernel<BITS, K><<<light_grid(p.n_rows, p.sc.n_tasks), kGatThreads, 0, s>>>(p);
@@ -725,6 +1052,9 @@ int edge_softmax(const gq_graph* g, const float* S, const float* D, int heads, f
   p.alpha = alpha;
   p.Epre = Epre;
   p.n_rows = g->n;
+  p.n_edges = g->nnz;
+  p.n_groups = g->sched.n_groups;
+  p.err = g->status;
   const size_t need = edge_softmax_workspace(g, heads);
   if (need > 0 && (ws == nullptr || ws_bytes < need || !aligned(ws, 256))) return GQ_ERR_WORKSPACE;
   p.sc = make_sched(g->sched, g->hub_threshold, nullptr, 2 * heads);
@@ -734,6 +1064,57 @@ int edge_softmax(const gq_graph* g, const float* S, const float* D, int heads, f
     case 2: return launch_softmax<2>(p, s);
     case 4: return launch_softmax<4>(p, s);
     default: return launch_softmax<8>(p, s);
+  }
+}
+
+// 8-bit attention values: one (min, max) pair per head for every heavy-row task
+size_t edge_quant_workspace(const gq_graph* g, int heads) { return edge_softmax_workspace(g, heads); }
+
+int quantize_edge_values(const gq_graph* g, const float* alpha, int heads, uint64_t seed, uint8_t* codes, float* hdr,
+                         void* ws, size_t ws_bytes, cudaStream_t s) {
+  if (g == nullptr || alpha == nullptr || codes == nullptr || hdr == nullptr) return GQ_ERR_INVALID_ARG;
+  if (!(heads == 1 || heads == 2 || heads == 4 || heads == 8)) return GQ_ERR_UNSUPPORTED;
+  if (!aligned(alpha, 16) || !aligned(codes, 16) || !aligned(hdr, 16)) return GQ_ERR_INVALID_ARG;
+  const size_t need = edge_quant_workspace(g, heads);
+  if (need > 0 && (ws == nullptr || ws_bytes < need || !aligned(ws, 256))) return GQ_ERR_WORKSPACE;
+  EdgeQuantParams p{};
+  p.rowptr = g->rowptr;
+  p.alpha = alpha;
+  p.codes = codes;
+  p.hdr = hdr;
+  p.seed_key = seed_key_host(seed);
+  p.n_rows = g->n;
+  p.n_edges = g->nnz;
+  p.err = g->status;
+  p.sc = make_sched(g->sched, g->hub_threshold, nullptr, 2 * heads);
+  p.sc.partial = static_cast<float*>(ws);
+  switch (heads) {
+    case 1: return launch_edge_quant<1>(p, s);
+    case 2: return launch_edge_quant<2>(p, s);
+    case 4: return launch_edge_quant<4>(p, s);
+    default: return launch_edge_quant<8>(p, s);
+  }
+}
+
+int dequant_edge_values(const gq_graph* g, const uint8_t* codes, const float* hdr, int heads, float* out,
+                        cudaStream_t s) {
+  if (g == nullptr || codes == nullptr || hdr == nullptr || out == nullptr) return GQ_ERR_INVALID_ARG;
+  if (!(heads == 1 || heads == 2 || heads == 4 || heads == 8)) return GQ_ERR_UNSUPPORTED;
+  if (!aligned(codes, 16) || !aligned(hdr, 16) || !aligned(out, 16)) return GQ_ERR_INVALID_ARG;
+  EdgeQuantParams p{};
+  p.rowptr = g->rowptr;
+  p.codes = const_cast<uint8_t*>(codes);
+  p.hdr = const_cast<float*>(hdr);
+  p.deq = out;
+  p.n_rows = g->n;
+  p.n_edges = g->nnz;
+  p.err = g->status;
+  p.sc = make_sched(g->sched, g->hub_threshold, nullptr, 0);
+  switch (heads) {
+    case 1: return launch_edge_dequant<1>(p, s);
+    case 2: return launch_edge_dequant<2>(p, s);
+    case 4: return launch_edge_dequant<4>(p, s);
+    default: return launch_edge_dequant<8>(p, s);
   }
 }
 
@@ -830,6 +1211,21 @@ int gat_node_bwd(const gq_graph* g, const float* dEpre, const float* dD, const f
 extern "C" size_t gq_edge_softmax_workspace_bytes(const gq_graph* g, int heads) {
   if (g == nullptr || heads < 1) return 0;
   return gq::edge_softmax_workspace(g, heads);
+}
+
+extern "C" size_t gq_quantize_edge_values_workspace_bytes(const gq_graph* g, int heads) {
+  if (g == nullptr || heads < 1) return 0;
+  return gq::edge_quant_workspace(g, heads);
+}
+
+extern "C" int gq_quantize_edge_values(const gq_graph* g, const float* alpha, int heads, uint64_t seed,
+                                       uint8_t* codes, float* hdr, void* ws, size_t ws_bytes, gq_stream stream) {
+  return gq::quantize_edge_values(g, alpha, heads, seed, codes, hdr, ws, ws_bytes, (cudaStream_t)stream);
+}
+
+extern "C" int gq_dequant_edge_values(const gq_graph* g, const uint8_t* codes, const float* hdr, int heads,
+                                      float* out, gq_stream stream) {
+  return gq::dequant_edge_values(g, codes, hdr, heads, out, (cudaStream_t)stream);
 }
 
 extern "C" int gq_sddmm_edge_softmax(const gq_graph* g, const float* S, const float* D, int heads, float slope,

@@ -20,6 +20,9 @@ int dequant_spmm(const gq_graph* g, int transpose, int coef, const float* X, int
 int edge_spmm(const gq_graph* g, int transpose, const float* alpha, int heads, const float* X, int64_t ldx,
               const uint8_t* packed, const uint8_t* mask, int d, int bits, float* Y, int64_t ldy, void* ws,
               size_t ws_bytes, cudaStream_t s);
+int edge_spmm_alpha8(const gq_graph* g, const uint8_t* acode, const float* ahdr, int heads, const float* X,
+                     int64_t ldx, const uint8_t* packed, const uint8_t* mask, int d, int bits, float* Y,
+                     int64_t ldy, void* ws, size_t ws_bytes, cudaStream_t s);
 
 int row_gemm(const void* A, int64_t M, int K, int64_t lda, const void* B, int N, int64_t ldb, int act, float* C,
              int64_t ldc, const float* a_src, const float* a_dst, float* S, float* D, int heads, int* err,
@@ -59,6 +62,11 @@ size_t edge_bwd_workspace(const gq_graph* g, int heads);
 size_t node_bwd_workspace(int d);
 int edge_softmax(const gq_graph* g, const float* S, const float* D, int heads, float slope, float* Epre,
                  float* alpha, void* ws, size_t ws_bytes, cudaStream_t s);
+size_t edge_quant_workspace(const gq_graph* g, int heads);
+int quantize_edge_values(const gq_graph* g, const float* alpha, int heads, uint64_t seed, uint8_t* codes, float* hdr,
+                         void* ws, size_t ws_bytes, cudaStream_t s);
+int dequant_edge_values(const gq_graph* g, const uint8_t* codes, const float* hdr, int heads, float* out,
+                        cudaStream_t s);
 int gat_edge_bwd(const gq_graph* g, const float* dOut, const float* Hp, const uint8_t* packed, const uint8_t* mask,
                  int bits, const float* alpha, const float* S, const float* D, int heads, int d, float slope,
                  float* dEpre, float* dD, void* ws, size_t ws_bytes, cudaStream_t s);

@@ -165,9 +165,13 @@ struct GatWs {
   size_t nb_bytes;
   void* wg;          // weight-GEMM partials
   size_t wg_bytes;
+  uint8_t* acode;    // 8-bit attention codes E x heads (fwd, if the caller keeps none)
+  float* ahdr;       // their {S, Z} per row and head
+  float* ahat;       // de-quantized attention values E x heads (bwd)
 };
 
-Carve carve_gat(const gq_graph* g, void* ws, size_t ws_bytes, int d_in, int heads, int d, int bits, GatWs& w) {
+Carve carve_gat(const gq_graph* g, void* ws, size_t ws_bytes, int d_in, int heads, int d, int bits, int alpha_bits,
+                GatWs& w) {
   const int64_t n = g->n;
   Carve c(ws, ws_bytes);
   w.hb = c.take((size_t)n * round8(d_in) * 2);
@@ -188,6 +192,16 @@ Carve carve_gat(const gq_graph* g, void* ws, size_t ws_bytes, int d_in, int head
   w.nb = c.take(w.nb_bytes);
   w.wg_bytes = wgrad_workspace(n, d_in, d);
   w.wg = c.take(w.wg_bytes);
+  if (alpha_bits == 8) {  // after every other buffer: the rest of the carve is the same either way
+    w.acode = static_cast<uint8_t*>(c.take((size_t)g->nnz * heads));
+    w.ahdr = static_cast<float*>(c.take((size_t)n * heads * 2 * sizeof(float)));
+    w.ahat = static_cast<float*>(c.take((size_t)g->nnz * heads * sizeof(float)));
+    // the quantizer's scratch (one pair per head and task) is the softmax's, in sx
+  } else {
+    w.acode = nullptr;
+    w.ahdr = nullptr;
+    w.ahat = nullptr;
+  }
   return c;
 }
 
@@ -204,26 +218,31 @@ int gat_check(const gq_graph* g, int d_in, int heads, int f, int bits) {
 }  // namespace
 }  // namespace gq
 
-extern "C" size_t gq_gat_layer_workspace_bytes(const gq_graph* g, int d_in, int heads, int f, int bits) {
+extern "C" size_t gq_gat_layer_workspace_bytes(const gq_graph* g, int d_in, int heads, int f, int bits,
+                                               int alpha_bits) {
   if (g == nullptr || d_in < 1 || heads < 1 || f < 1) return 0;
   gq::GatWs w;
-  return gq::carve_gat(g, nullptr, 0, d_in, heads, heads * f, bits, w).used + 256;
+  return gq::carve_gat(g, nullptr, 0, d_in, heads, heads * f, bits, alpha_bits, w).used + 256;
 }
 
 extern "C" int gq_gat_layer_fwd(const gq_graph* g, const float* H, int64_t ldh, int d_in, const float* W,
                                 const float* a_src, const float* a_dst, int heads, int f, float slope,
-                                const uint8_t* mask, int bits, uint64_t seed, float* Hp_save, float* S_save,
-                                float* D_save, float* alpha_save, uint8_t* packed_save, float* out, void* ws,
-                                size_t ws_bytes, int* dev_err, gq_stream stream) {
+                                const uint8_t* mask, int bits, uint64_t seed, int alpha_bits, float* Hp_save,
+                                float* S_save, float* D_save, float* alpha_save, uint8_t* packed_save,
+                                uint8_t* acode_save, float* ahdr_save, float* out, void* ws, size_t ws_bytes,
+                                int* dev_err, gq_stream stream) {
   using namespace gq;
   GQ_TRY(gat_check(g, d_in, heads, f, bits));
   if (H == nullptr || W == nullptr || a_src == nullptr || a_dst == nullptr || Hp_save == nullptr ||
       S_save == nullptr || D_save == nullptr || alpha_save == nullptr || out == nullptr || ldh < d_in)
     return GQ_ERR_INVALID_ARG;
+  if (!(alpha_bits == 32 || alpha_bits == 8) || ((acode_save == nullptr) != (ahdr_save == nullptr)))
+    return GQ_ERR_INVALID_ARG;
   cudaStream_t s = (cudaStream_t)stream;
   const int d = heads * f;
   GatWs w;
-  if (ws == nullptr || !carve_gat(g, ws, ws_bytes, d_in, heads, d, bits, w).ok()) return GQ_ERR_WORKSPACE;
+  if (ws == nullptr || !carve_gat(g, ws, ws_bytes, d_in, heads, d, bits, alpha_bits, w).ok())
+    return GQ_ERR_WORKSPACE;
   const int64_t ldhb = round8(d_in);
   // step 1: H' = H W ; step 2: S = H' a_src, D = H' a_dst (GEMM epilogue)
   GQ_TRY(to_bf16(H, g->n, d_in, ldh, w.hb, ldhb, (int)ldhb, nullptr, 0, s));
@@ -238,16 +257,24 @@ extern "C" int gq_gat_layer_fwd(const gq_graph* g, const float* H, int64_t ldh, 
   }
   // steps 3-4: SDDMM add + LeakyReLU + edge softmax ; step 5: SpMM
   GQ_TRY(edge_softmax(g, S_save, D_save, heads, slope, nullptr, alpha_save, w.sx, w.sx_bytes, s));
+  if (alpha_bits == 8) {
+    // the SpMM reads the attention values as 8-bit codes (Tango Sec. 3.3)
+    uint8_t* acode = acode_save != nullptr ? acode_save : w.acode;
+    float* ahdr = ahdr_save != nullptr ? ahdr_save : w.ahdr;
+    GQ_TRY(quantize_edge_values(g, alpha_save, heads, seed ^ GQ_ALPHA_SEED_TAG, acode, ahdr, w.sx, w.sx_bytes, s));
+    return edge_spmm_alpha8(g, acode, ahdr, heads, Hp_save, d, packed, mask, d, bits, out, d, w.sp, w.sp_bytes, s);
+  }
   return edge_spmm(g, 0, alpha_save, heads, Hp_save, d, packed, mask, d, bits, out, d, w.sp, w.sp_bytes, s);
 }
 
 extern "C" int gq_gat_layer_bwd(const gq_graph* g, const float* dOut, const float* H, int64_t ldh,
                                 const float* Hp_save, const float* S_save, const float* D_save,
-                                const float* alpha_save, const uint8_t* packed_save, const float* W,
-                                const float* a_src, const float* a_dst, int d_in, int heads, int f, float slope,
-                                const uint8_t* mask, int bits, uint64_t seed, float* dW, float* da_src,
-                                float* da_dst, float* dH, float* dEpre_save, float* dHp_save, void* ws,
-                                size_t ws_bytes, int* dev_err, gq_stream stream) {
+                                const float* alpha_save, const uint8_t* packed_save, const uint8_t* acode_save,
+                                const float* ahdr_save, const float* W, const float* a_src, const float* a_dst,
+                                int d_in, int heads, int f, float slope, const uint8_t* mask, int bits,
+                                uint64_t seed, float* dW, float* da_src, float* da_dst, float* dH,
+                                float* dEpre_save, float* dHp_save, void* ws, size_t ws_bytes, int* dev_err,
+                                gq_stream stream) {
   using namespace gq;
   GQ_TRY(gat_check(g, d_in, heads, f, bits));
   if (dOut == nullptr || H == nullptr || Hp_save == nullptr || S_save == nullptr || D_save == nullptr ||
@@ -255,17 +282,27 @@ extern "C" int gq_gat_layer_bwd(const gq_graph* g, const float* dOut, const floa
       da_src == nullptr || da_dst == nullptr || dH == nullptr || ldh < d_in)
     return GQ_ERR_INVALID_ARG;
   if (bits < 32 && packed_save == nullptr) return GQ_ERR_INVALID_ARG;
+  if ((acode_save == nullptr) != (ahdr_save == nullptr)) return GQ_ERR_INVALID_ARG;
+  const int alpha_bits = acode_save != nullptr ? 8 : 32;
   cudaStream_t s = (cudaStream_t)stream;
   const int d = heads * f;
   GatWs w;
-  if (ws == nullptr || !carve_gat(g, ws, ws_bytes, d_in, heads, d, bits, w).ok()) return GQ_ERR_WORKSPACE;
+  if (ws == nullptr || !carve_gat(g, ws, ws_bytes, d_in, heads, d, bits, alpha_bits, w).ok())
+    return GQ_ERR_WORKSPACE;
   float* dEpre = dEpre_save != nullptr ? dEpre_save : w.dEpre;
   // SDDMM dot -> dalpha; softmax derivative; LeakyReLU'; dD = in-edge sums
   GQ_TRY(gat_edge_bwd(g, dOut, Hp_save, packed_save, mask, bits, alpha_save, S_save, D_save, heads, d, slope, dEpre,
                       w.dD, w.sx, w.sx_bytes, s));
   // dM = transposed multi-head SpMM of dOut (marginal rows travel quantized)
+  // with 8-bit attention codes the forward multiplied by their values, so
+  // the transposed SpMM does too
   if (bits < 32) GQ_TRY(quantize_pack(dOut, g->n, d, d, mask, bits, seed, w.packed, s));
-  GQ_TRY(edge_spmm(g, 1, alpha_save, heads, dOut, d, w.packed, mask, d, bits, w.dM, d, w.sp, w.sp_bytes, s));
+  const float* aT = alpha_save;
+  if (alpha_bits == 8) {
+    GQ_TRY(dequant_edge_values(g, acode_save, ahdr_save, heads, w.ahat, s));
+    aT = w.ahat;
+  }
+  GQ_TRY(edge_spmm(g, 1, aT, heads, dOut, d, w.packed, mask, d, bits, w.dM, d, w.sp, w.sp_bytes, s));
   // dS = out-edge sums; dH' = dM + dS a_src + dD a_dst; da_src, da_dst
   GQ_TRY(gat_node_bwd(g, dEpre, w.dD, w.dM, Hp_save, a_src, a_dst, heads, d, w.dhb, d, dHp_save, nullptr, da_src,
                       da_dst, w.nb, w.nb_bytes, s));

@@ -43,7 +43,9 @@ struct SpmmParams {
   const int32_t* eperm;     // edge id of each entry (transposed CSR), or null = identity
   const float* colscale;    // per gathered row, or null (= 1)
   const float* rowscale;    // per output row, or null (= 1)
-  const float* alpha;       // per edge x heads (edge-weight mode)
+  const float* alpha;       // per edge x heads (edge-weight mode 1)
+  const uint8_t* acode;     // per edge x heads 8-bit codes (edge-weight mode 2)
+  const float* ahdr;        // per output row x heads {S, Z} of those codes
   int heads, fshift;        // head of column j = j >> fshift
   const float* X;
   int64_t ldx;
@@ -142,15 +144,23 @@ __device__ __forceinline__ void consume(bool quant, float coef, const Chunk<32>&
 
 // Accumulate, into this lane's chunks, the edges of batches
 // [e_beg + 32*first, ...) with a stride of `stride` batches.
-template <int BITS, int G, int CPL, bool EW>
-__device__ __forceinline__ void accumulate_row(const SpmmParams& p, int64_t e_beg, int64_t e_end, int first,
-                                               int stride, float (&acc)[CPL][8]) {
+template <int BITS, int G, int CPL, int EW>
+__device__ __forceinline__ void accumulate_row(const SpmmParams& p, int64_t row, int64_t e_beg, int64_t e_end,
+                                               int first, int stride, float (&acc)[CPL][8]) {
   constexpr int NG = 32 / G;
   constexpr int U = CPL == 1 ? 4 : (CPL == 2 ? 2 : 1);
   const int lane = threadIdx.x & 31;
   const int g = lane / G;
   const int gl = lane % G;
   const int nchunks = (p.d + 7) >> 3;
+  float2 az[CPL];  // mode 2: {S, Z} of the row's codes for the head of each chunk
+#pragma unroll
+  for (int i = 0; i < CPL; ++i) {
+    az[i] = make_float2(0.0f, 0.0f);
+    const int c = gl + G * i;
+    if (EW == 2 && c < nchunks)
+      az[i] = __ldg(reinterpret_cast<const float2*>(p.ahdr) + row * p.heads + ((c * 8) >> p.fshift));
+  }
   for (int64_t base = e_beg + 32 * (int64_t)first; base < e_end; base += 32 * (int64_t)stride) {
     const int64_t e = base + lane;
     const bool valid = e < e_end;
@@ -187,7 +197,10 @@ __device__ __forceinline__ void accumulate_row(const SpmmParams& p, int64_t e_be
           const int c = gl + G * i;
           cj[t][i] = cs;
           if (act[t] && c < nchunks) {
-            if (EW) cj[t][i] = __ldg(p.alpha + (int64_t)ej * p.heads + ((c * 8) >> p.fshift));
+            if (EW == 1) cj[t][i] = __ldg(p.alpha + (int64_t)ej * p.heads + ((c * 8) >> p.fshift));
+            if (EW == 2)
+              cj[t][i] = __fmaf_rn(code_to_float(__ldg(p.acode + (int64_t)ej * p.heads + ((c * 8) >> p.fshift))),
+                                   az[i].x, az[i].y);
             load_msg<BITS>(p, xj, qt[t], c, fb[t][i], qb[t][i]);
           }
         }
@@ -347,23 +360,25 @@ __device__ __forceinline__ void lflush(const SpmmParams& p, int64_t r, int c0, c
 
 // Per-edge metadata of U consecutive edges: column ids, then coefficients
 // and mask bits.
-template <int BITS, bool EW, int U>
+template <int BITS, int EW, int U>
 __device__ __forceinline__ void meta_cols(const SpmmParams& p, int64_t at, int64_t end, int32_t (&xs)[U]) {
 #pragma unroll
   for (int t = 0; t < U; ++t) xs[t] = (at + t < end) ? __ldg(p.col + at + t) : 0;
 }
 
-template <int BITS, bool EW, bool ALLQ, int U>
-__device__ __forceinline__ void meta_coef(const SpmmParams& p, int64_t at, int64_t end, int head,
+template <int BITS, int EW, bool ALLQ, int U>
+__device__ __forceinline__ void meta_coef(const SpmmParams& p, int64_t at, int64_t end, int head, float2 az,
                                           const int32_t (&xs)[U], float (&f)[U], bool (&q)[U]) {
 #pragma unroll
   for (int t = 0; t < U; ++t) {
     f[t] = 1.0f;
     q[t] = ALLQ;
     if (at + t < end) {
-      if (EW) {
+      if (EW == 1) {
         const int64_t eid = p.eperm ? __ldg(p.eperm + at + t) : at + t;
         f[t] = __ldg(p.alpha + eid * p.heads + head);
+      } else if (EW == 2) {  // forward only: the edge id is the CSR position
+        f[t] = __fmaf_rn(code_to_float(__ldg(p.acode + (at + t) * p.heads + head)), az.x, az.y);
       } else if (p.colscale) {
         f[t] = __ldg(p.colscale + xs[t]);
       }
@@ -374,15 +389,15 @@ __device__ __forceinline__ void meta_coef(const SpmmParams& p, int64_t at, int64
 
 // Accumulate the contiguous edges [e_beg, e_end) of one row into this
 // lane's 16 columns, in the three-stage pipeline described above.
-template <int BITS, bool EW, bool ALLQ>
+template <int BITS, int EW, bool ALLQ>
 __device__ __forceinline__ void stream_row(const SpmmParams& p, int64_t e_beg, int64_t e_end, int c0, int head,
-                                           float (&acc)[kLC], float& accz) {
+                                           float2 az, float (&acc)[kLC], float& accz) {
   constexpr int U = kLU;
   int32_t cx[U], nx[U];
   float cf[U];
   bool cq[U];
   meta_cols<BITS, EW, U>(p, e_beg, e_end, cx);
-  meta_coef<BITS, EW, ALLQ, U>(p, e_beg, e_end, head, cx, cf, cq);
+  meta_coef<BITS, EW, ALLQ, U>(p, e_beg, e_end, head, az, cx, cf, cq);
   meta_cols<BITS, EW, U>(p, e_beg + U, e_end, nx);
   for (int64_t e = e_beg; e < e_end; e += U) {
     LMsg<BITS, ALLQ> m[U];
@@ -391,7 +406,7 @@ __device__ __forceinline__ void stream_row(const SpmmParams& p, int64_t e_beg, i
       if (e + t < e_end && c0 < p.d) lload<BITS, ALLQ>(p, cx[t], cq[t], c0, m[t]);
     float nf[U];
     bool nq[U];
-    meta_coef<BITS, EW, ALLQ, U>(p, e + U, e_end, head, nx, nf, nq);
+    meta_coef<BITS, EW, ALLQ, U>(p, e + U, e_end, head, az, nx, nf, nq);
     int32_t nnx[U];
     meta_cols<BITS, EW, U>(p, e + 2 * U, e_end, nnx);
 #pragma unroll
@@ -451,7 +466,7 @@ __device__ __forceinline__ void finish_heavy(const SpmmParams& p, const int4& ta
   }
 }
 
-template <int BITS, int G, int CPL, int LG, bool EW, bool ALLQ>
+template <int BITS, int G, int CPL, int LG, int EW, bool ALLQ>
 __global__ void __launch_bounds__(kSpmmThreads) spmm_kernel(const SpmmParams p) {
   extern __shared__ float part[];  // [kSpmmWarps][d] for heavy rows
   const int lane = threadIdx.x & 31;
@@ -474,7 +489,10 @@ __global__ void __launch_bounds__(kSpmmThreads) spmm_kernel(const SpmmParams p) 
       const int head = EW ? (c0 >> p.fshift) : 0;
       float acc[kLC] = {};
       float accz = 0.0f;
-      if (b0 < b1) stream_row<BITS, EW, ALLQ>(p, b0, b1, c0, head, acc, accz);
+      const float2 az = EW == 2 && c0 < p.d
+                            ? __ldg(reinterpret_cast<const float2*>(p.ahdr) + (int64_t)task.x * p.heads + head)
+                            : make_float2(0.0f, 0.0f);
+      if (b0 < b1) stream_row<BITS, EW, ALLQ>(p, b0, b1, c0, head, az, acc, accz);
 #pragma unroll
       for (int k = 0; k < kLC; ++k) acc[k] += accz;
 #pragma unroll
@@ -487,7 +505,7 @@ __global__ void __launch_bounds__(kSpmmThreads) spmm_kernel(const SpmmParams p) 
           if (c0 + k < p.d) part[w * p.d + c0 + k] = acc[k];
     } else {
       float acc[CPL][8] = {};
-      accumulate_row<BITS, G, CPL, EW>(p, task.y, task.z, w, kSpmmWarps, acc);
+      accumulate_row<BITS, G, CPL, EW>(p, task.x, task.y, task.z, w, kSpmmWarps, acc);
       group_reduce<G, CPL>(acc);
       if (lane < G) {
 #pragma unroll
@@ -513,7 +531,7 @@ __global__ void __launch_bounds__(kSpmmThreads) spmm_kernel(const SpmmParams p) 
       const int64_t a = p.rowptr[r], b = p.rowptr[r + 1];
       if (b - a > p.hub_threshold) continue;  // a block task handles it
       float acc[CPL][8] = {};
-      accumulate_row<BITS, G, CPL, EW>(p, a, b, 0, 1, acc);
+      accumulate_row<BITS, G, CPL, EW>(p, r, a, b, 0, 1, acc);
       group_reduce<G, CPL>(acc);
       if (lane < G) {
         const float s = p.rowscale ? p.rowscale[r] : 1.0f;
@@ -976,7 +994,7 @@ int launch_async_any(const SpmmParams& p, int bits, cudaStream_t s) {
   }
 }
 
-template <int BITS, int G, int CPL, int LG, bool EW, bool ALLQ>
+template <int BITS, int G, int CPL, int LG, int EW, bool ALLQ>
 int launch_cfg(SpmmParams p, cudaStream_t s) {
   const size_t smem = sizeof(float) * kSpmmWarps * p.d;
   const int64_t rows_blocks = (p.n_rows + kSpmmWarps - 1) / kSpmmWarps;
@@ -989,7 +1007,7 @@ int launch_cfg(SpmmParams p, cudaStream_t s) {
   return launch_status();
 }
 
-template <int BITS, bool EW, bool ALLQ>
+template <int BITS, int EW, bool ALLQ>
 int launch_bits(const SpmmParams& p, cudaStream_t s) {
   if (p.d <= 16) return launch_cfg<BITS, 4, 1, 1, EW, ALLQ>(p, s);
   if (p.d <= 32) return launch_cfg<BITS, 4, 1, 2, EW, ALLQ>(p, s);
@@ -1000,7 +1018,7 @@ int launch_bits(const SpmmParams& p, cudaStream_t s) {
   return launch_cfg<BITS, 32, 4, 0, EW, ALLQ>(p, s);
 }
 
-template <bool EW>
+template <int EW>
 int launch_any(const SpmmParams& p, int bits, cudaStream_t s) {
   switch (bits) {
     case 2: return launch_bits<2, EW, false>(p, s);
@@ -1487,7 +1505,7 @@ int dequant_spmm(const gq_graph* g, int transpose, int coef, const float* X, int
   if (bits < 32 && mask != nullptr && d > 64 && d <= 256 && ldx <= (int64_t)1 << 29)
     return launch_bulk_any(p, bits, s);
   if (d <= 512 && ldx <= (int64_t)1 << 29) return launch_async_any(p, bits, s);
-  return launch_any<false>(p, bits, s);
+  return launch_any<0>(p, bits, s);
 }
 
 // Mixed bit-widths per row (rbits, roff from gq_packed_row_offsets).
@@ -1528,7 +1546,43 @@ int edge_spmm(const gq_graph* g, int transpose, const float* alpha, int heads, c
   p.heads = heads;
   p.fshift = fshift;
   p.eperm = transpose ? g->tr_perm : nullptr;
-  return launch_any<true>(p, bits, s);
+  return launch_any<1>(p, bits, s);
+}
+
+// Edge-weight mode 2 (8-bit attention codes with per-row, per-head {S, Z})
+// for widths up to 256, the GAT layer's range.
+template <int BITS>
+int launch_alpha8(const SpmmParams& p, cudaStream_t s) {
+  if (p.d <= 16) return launch_cfg<BITS, 4, 1, 1, 2, false>(p, s);
+  if (p.d <= 32) return launch_cfg<BITS, 4, 1, 2, 2, false>(p, s);
+  if (p.d <= 64) return launch_cfg<BITS, 8, 1, 4, 2, false>(p, s);
+  if (p.d <= 128) return launch_cfg<BITS, 16, 1, 8, 2, false>(p, s);
+  return launch_cfg<BITS, 32, 1, 16, 2, false>(p, s);
+}
+
+int edge_spmm_alpha8(const gq_graph* g, const uint8_t* acode, const float* ahdr, int heads, const float* X,
+                     int64_t ldx, const uint8_t* packed, const uint8_t* mask, int d, int bits, float* Y,
+                     int64_t ldy, void* ws, size_t ws_bytes, cudaStream_t s) {
+  if (acode == nullptr || ahdr == nullptr || heads < 1 || d % heads != 0 || !aligned(ahdr, 8))
+    return GQ_ERR_INVALID_ARG;
+  if (d > 256) return GQ_ERR_UNSUPPORTED;
+  const int F = d / heads;
+  int fshift = 0;
+  while ((1 << fshift) < F) ++fshift;
+  if ((1 << fshift) != F || F < 16) return GQ_ERR_UNSUPPORTED;  // head width: power of two >= 16
+  SpmmParams p;
+  GQ_TRY(spmm_setup(g, 0, X, ldx, packed, mask, d, bits, Y, ldy, ws, ws_bytes, s, p));
+  p.acode = acode;
+  p.ahdr = ahdr;
+  p.heads = heads;
+  p.fshift = fshift;
+  p.eperm = nullptr;
+  switch (bits) {
+    case 2: return launch_alpha8<2>(p, s);
+    case 4: return launch_alpha8<4>(p, s);
+    case 8: return launch_alpha8<8>(p, s);
+    default: return launch_alpha8<32>(p, s);
+  }
 }
 
 }  // namespace gq
@@ -1549,6 +1603,13 @@ extern "C" int gq_dequant_spmm_mixed(const gq_graph* g, int transpose, int coef,
                                      float* Y, int64_t ldy, void* ws, size_t ws_bytes, gq_stream stream) {
   return gq::dequant_spmm_mixed(g, transpose, coef, X, ldx, packed, roff, rbits, d, Y, ldy, ws, ws_bytes,
                                 (cudaStream_t)stream);
+}
+
+extern "C" int gq_edge_spmm_alpha8(const gq_graph* g, const uint8_t* acode, const float* ahdr, int heads,
+                                   const float* X, int64_t ldx, const uint8_t* packed, const uint8_t* mask, int d,
+                                   int bits, float* Y, int64_t ldy, void* ws, size_t ws_bytes, gq_stream stream) {
+  return gq::edge_spmm_alpha8(g, acode, ahdr, heads, X, ldx, packed, mask, d, bits, Y, ldy, ws, ws_bytes,
+                              (cudaStream_t)stream);
 }
 
 extern "C" int gq_edge_spmm(const gq_graph* g, int transpose, const float* alpha, int heads, const float* X,

@@ -37,7 +37,7 @@ def test_edge_softmax(orc, heads, graph):
     close(alpha.cpu().numpy(), a_ref, what="alpha")
 
 
-def _gat(orc, g, d_in, heads, f, bits, mask_frac, kw, seed=0):
+def _gat(orc, g, d_in, heads, f, bits, mask_frac, kw, seed=0, alpha_bits=32):
     q = gq()
     G = q.graph_prepare(g.rowptr.cuda(), g.col.cuda(), **kw)
     rp, co = g.rowptr.numpy(), g.col.numpy()
@@ -49,7 +49,7 @@ def _gat(orc, g, d_in, heads, f, bits, mask_frac, kw, seed=0):
     mask = synth.bernoulli_mask(g.n, mask_frac, seed=seed + 5)
     dOut = synth.normal_matrix(g.n, d, seed=seed + 6, tag=synth.TAG_GRAD)
     sf, sb = synth.layer_seed(seed, 0, False), synth.layer_seed(seed, 0, True)
-    L = q.GATLayer(G, d_in, heads, f, 0.2, bits, mask.cuda() if bits < 32 else None)
+    L = q.GATLayer(G, d_in, heads, f, 0.2, bits, mask.cuda() if bits < 32 else None, alpha_bits=alpha_bits)
     Hd, Wd, asd, add_ = H.cuda(), W.cuda(), a_s.cuda(), a_d.cuda()
     out = L.forward(Hd, Wd, asd, add_, sf)
     dEpre = torch.empty(g.nnz, heads, device="cuda")
@@ -74,7 +74,13 @@ def _gat(orc, g, d_in, heads, f, bits, mask_frac, kw, seed=0):
         ref_pk = orc.quantize(Hp, mn, bits, sf)
         np.testing.assert_array_equal(pk[mn == 1], ref_pk[mn == 1])
     M = orc.messages(Hp, pk, mn, d, bits)
-    close(out.cpu().numpy(), orc.edge_spmm(rp, co, ag, M), what="out")
+    ahat = ag
+    if alpha_bits == 8:  # the attention codes of the GPU's alpha, bit-exact
+        c_ref, h_ref = orc.quantize_edge_values(rp, ag, sf ^ orc.ALPHA_SEED_TAG)
+        np.testing.assert_array_equal(L.acode.cpu().numpy(), c_ref)
+        np.testing.assert_array_equal(L.ahdr.cpu().numpy(), h_ref)
+        ahat = orc.dequant_edge_values(rp, c_ref, h_ref)
+    close(out.cpu().numpy(), orc.edge_spmm(rp, co, ahat, M), what="out")
 
     # backward, teacher-forced on the GPU's forward tensors
     dalpha = orc.sddmm_dot(rp, co, dOut.numpy(), M, heads)
@@ -83,7 +89,7 @@ def _gat(orc, g, d_in, heads, f, bits, mask_frac, kw, seed=0):
     dD_ref, dS_ref = orc.edge_segment_sums(rp, co, dEpre.cpu().numpy())
     dO = dOut.numpy()
     pkb = orc.quantize(dO, mn, bits, sb) if bits < 32 else None
-    dM_ref = orc.edge_spmm(rp, co, ag, orc.messages(dO, pkb, mn, d, bits), transpose=True)
+    dM_ref = orc.edge_spmm(rp, co, ahat, orc.messages(dO, pkb, mn, d, bits), transpose=True)
     F = f
     dHp_ref = dM_ref + np.repeat(dS_ref, F, 1) * a_s.numpy().reshape(1, d) + np.repeat(dD_ref, F, 1) * a_d.numpy().reshape(1, d)
     close(dHp.cpu().numpy(), dHp_ref, what="dH'")
@@ -110,3 +116,9 @@ def test_gat_layer_quantized(orc, bits):
 def test_gat_layer_heavy_rows(orc):
     _gat(orc, hub_graph(), 100, 4, 32, 32, 0.0, dict(hub_threshold=32, split_edges=256))
     _gat(orc, hub_graph(), 64, 4, 16, 4, 0.4, dict(hub_threshold=32, split_edges=256))
+
+
+@pytest.mark.parametrize("bits", [32, 4])
+def test_gat_layer_quantized_alpha(orc, bits):
+    _gat(orc, rmat_small(), 128, 4, 64, bits, 0.5, {}, alpha_bits=8)
+    _gat(orc, hub_graph(), 64, 2, 32, bits, 0.4, dict(hub_threshold=32, split_edges=256), alpha_bits=8)

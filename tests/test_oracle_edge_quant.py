@@ -121,3 +121,31 @@ def test_aggregation_with_quantized_alpha_is_within_the_bound(orc):
     bound = orc.edge_spmm(rp, co, S, np.abs(M))
     assert np.all(np.abs(quant - exact) <= bound)
     assert np.abs(quant - exact).max() > 0
+
+
+def test_gat_layer_with_quantized_alpha(orc):
+    # The layer with alpha_bits = 8 aggregates with the quantized attention
+    # values (within their error bound of alpha), and its backward's
+    # transposed SpMM is the adjoint of that forward SpMM:
+    # <G, out> = <dM, M> holds with the forward's values ahat, not with alpha.
+    g = synth.rmat_graph(scale=7, n=120, n_draws=120 * 10, seed=4)
+    rp, co = g.rowptr.numpy(), g.col.numpy()
+    rng = np.random.default_rng(3)
+    heads, F, din = 2, 4, 6
+    H = rng.standard_normal((g.n, din))
+    W = rng.standard_normal((din, heads * F))
+    a_s, a_d = rng.standard_normal((heads, F)), rng.standard_normal((heads, F))
+    G = rng.standard_normal((g.n, heads * F))
+    o = orc.gat_layer_fwd(rp, co, H, W, a_s, a_d, heads, 0.2, bf16=False, seed=5, alpha_bits=8)
+    codes, hdr = orc.quantize_edge_values(rp, o["alpha"].astype(np.float32), 5 ^ orc.ALPHA_SEED_TAG)
+    v_of_e = np.repeat(np.arange(g.n), np.diff(rp))
+    S = hdr[v_of_e, :, 0].astype(np.float64)
+    assert np.all(np.abs(o["ahat"] - o["alpha"]) <= S + 1e-6)
+    assert np.abs(o["ahat"] - o["alpha"]).max() > 0
+    b = orc.gat_layer_bwd(rp, co, G, H, o["M"], o["Hp"], o["Epre"], o["alpha"], W, a_s, a_d, heads, 0.2,
+                          bf16=False, ahat=o["ahat"])
+    lhs, rhs = np.sum(G * o["out"]), np.sum(b["dM"] * o["M"])
+    assert abs(lhs - rhs) <= 1e-10 * (1 + abs(lhs))
+    b0 = orc.gat_layer_bwd(rp, co, G, H, o["M"], o["Hp"], o["Epre"], o["alpha"], W, a_s, a_d, heads, 0.2,
+                           bf16=False)
+    assert abs(np.sum(b0["dM"] * o["M"]) - lhs) > 1e-6
