@@ -15,9 +15,13 @@
  *               others are aggregated in full precision
  *   Sancus (IJCAI 2023, extended abstract), Sec. 2 Preliminaries:
  *               A^ = D~^{-1/2} (A + I) D~^{-1/2},  H' = sigma(A^ H W)
+ *     Sec. 3.2 / 4.2  a bit-width per message; Problem 11's per-message
+ *               variance weight beta_k
  *   Tango, "Rethinking quantization for graph neural network training on
  *   GPUs" (arXiv 2308.00890), Sec. 2.1, Fig. 1: GAT forward as GEMM, head
  *   projections, SDDMM add, LeakyReLU, edge softmax, SpMM; and its backward.
+ *     Sec. 3.2  Eq. 4: relative quantization error Error_X and the bit rule
+ *     Sec. 3.3  the SPMM reads quantized node and edge features
  *
  * Conventions shared by every entry point
  *   - Pointers are DEVICE pointers owned by the caller unless a parameter

@@ -17,8 +17,15 @@
 //     dS[u,k]     = sum_{e in out(u)} dE_pre[e,k]          (out-edge sum)
 //     dH'[u,c]    = dM[u,c] + dS[u,k] a_src[k,f] + dD[u,k] a_dst[k,f]
 //     partial sums of da_src = sum_u dS[u,k] H'[u,:], da_dst likewise.
-// Heavy rows follow the graph's static schedule (block tasks; split rows
-// combine per-task partials in task order in the last block to finish).
+// edge_quant_kernel / edge_quant_heavy_kernel / edge_dequant_kernel
+//   (Tango Sec. 3.3): the attention values as 8-bit codes, one AdaQP Eqn 4
+//   vector per (destination, head) segment, and their de-quantized values.
+// Heavy rows follow the graph's static schedule: the softmax and the
+// quantizer cut them into warp tasks whose partials a second kernel merges;
+// the edge backward uses block tasks that combine per-task partials in task
+// order in the last block to finish.  The softmax and the quantizer check
+// each range and index they read against the graph and record an invalid
+// one in the graph status word.
 // Scores, attention and their gradients stay fp32 (Tango Sec. 3.2: full
 // precision before the softmax).
 #include <cuda_bf16.h>
