@@ -89,6 +89,7 @@ def _L():
                 "orc_beta": ([I64, P, P, I, P, I, P], None),
                 "orc_quant_error": ([P, I64, I, P, P, I, D], D),
                 "orc_quantize_edge_values": ([I64, P, P, I, U64, P, P], None),
+                "orc_assign_bits": ([P, P, I64, I, D, D, P], None),
                 "orc_dequant_edge_values": ([I64, P, P, P, I, P], None),
             }
             for name, (args, res) in sig.items():
@@ -270,6 +271,19 @@ def quant_error(X, packed, mask, bits: int, eps: float = 5e-4) -> float:
     packed = _c(packed, np.uint8)
     m = None if mask is None else _c(mask, np.uint8)
     return float(_L().orc_quant_error(_p(X), n, d, _p(packed), _p(m), bits, eps))
+
+
+def assign_bits(beta, d: int, lam: float, gamma: float, mask=None) -> np.ndarray:
+    """AdaQP Sec. 4.2 Problems 10-12 on one device: per row, the width in
+    {2, 4, 8} minimizing lam * beta / (2^b - 1)^2 + (1 - lam) * gamma * d * b
+    (fp64, ties to the fewer bits); rows with mask 0 get 0 (full
+    precision).  uint8 per row, the rbits of quantize_mixed."""
+    beta = _c(beta, np.float32)
+    n = beta.shape[0]
+    m = None if mask is None else _c(mask, np.uint8)
+    out = np.zeros(n, np.uint8)
+    _L().orc_assign_bits(_p(beta), _p(m), n, d, float(lam), float(gamma), _p(out))
+    return out
 
 
 def bits_for_error(X, mask, seed: int, threshold: float = 0.3, eps: float = 5e-4, choices=(2, 4, 8)) -> int:

@@ -446,3 +446,36 @@ void orc_dequant_edge_values(int64_t n, const int32_t* rowptr, const uint8_t* co
         out[e * heads + k] = fmaf((float)codes[e * heads + k], hdr[(v * heads + k) * 2],
                                   hdr[(v * heads + k) * 2 + 1]);
 }
+
+/* ------------------------------------------------------------------------ */
+/* AdaQP Sec. 4.2, Problems 10-12 on one device: a single device pair, so   */
+/* the min-max over pairs of theta + gamma * sum_k D b_k keeps one term and */
+/* theta drops out; the weighted sum of the variance objective              */
+/* sum_k beta_k / (2^b_k - 1)^2 (weight lam) and the time objective (weight */
+/* 1 - lam) separates per message.  Each row takes                          */
+/*   b_k = argmin_{b in {2,4,8}} lam*beta_k/(2^b-1)^2 + ((1-lam)*gamma)*(D*b) */
+/* in fp64 in that operation order (ties to the fewer bits); rows with      */
+/* mask 0 stay full precision (width 0).                                     */
+/* ------------------------------------------------------------------------ */
+void orc_assign_bits(const float* beta, const uint8_t* mask, int64_t n, int d, double lam, double gamma,
+                     uint8_t* rbits) {
+  static const int B[3] = {2, 4, 8};
+  const double tw = (1.0 - lam) * gamma;
+  for (int64_t k = 0; k < n; ++k) {
+    if (mask && !mask[k]) {
+      rbits[k] = 0;
+      continue;
+    }
+    int best = B[0];
+    double best_c = 0.0;
+    for (int i = 0; i < 3; ++i) {
+      const double L = (double)((1 << B[i]) - 1);
+      const double c = lam * ((double)beta[k] / (L * L)) + tw * ((double)d * (double)B[i]);
+      if (i == 0 || c < best_c) {
+        best_c = c;
+        best = B[i];
+      }
+    }
+    rbits[k] = (uint8_t)best;
+  }
+}

@@ -111,3 +111,55 @@ def test_bits_rule_picks_the_fewest_bits_under_threshold(orc):
         b = orc.bits_for_error(X, None, 5, threshold=thr)
         ok = [c for c in (2, 4, 8) if errs[c] < thr]
         assert b == (ok[0] if ok else 8)
+
+
+# --------------------------------------------------------------------------
+# AdaQP Sec. 4.2, Problems 10-12 on one device: the per-row width choice
+# --------------------------------------------------------------------------
+
+def _objective(beta, bits, d, lam, gamma):
+    L = (2.0 ** bits - 1.0)
+    return lam * np.sum(beta / L ** 2) + (1 - lam) * gamma * np.sum(d * bits)
+
+
+def test_assign_bits_extremes(orc):
+    beta = np.array([0.0, 1e-6, 3.0, 5e4], np.float32)
+    assert orc.assign_bits(beta, 64, 1.0, 1.0).tolist() == [2, 8, 8, 8]  # variance only; beta 0 ties to 2
+    assert orc.assign_bits(beta, 64, 0.0, 1.0).tolist() == [2, 2, 2, 2]  # time only
+
+
+def test_assign_bits_switch_points(orc):
+    # the 2 -> 4 switch where lam beta (1/9 - 1/225) = (1 - lam) gamma d (4 - 2),
+    # the 4 -> 8 switch where lam beta (1/225 - 1/65025) = (1 - lam) gamma d (8 - 4)
+    d, lam, gamma = 32, 0.25, 0.5
+    t24 = (1 - lam) * gamma * d * 2 / (lam * (1 / 9 - 1 / 225))
+    t48 = (1 - lam) * gamma * d * 4 / (lam * (1 / 225 - 1 / 65025))
+    beta = np.array([t24 * 0.99, t24 * 1.01, t48 * 0.99, t48 * 1.01], np.float32)
+    assert orc.assign_bits(beta, d, lam, gamma).tolist() == [2, 4, 4, 8]
+
+
+def test_assign_bits_minimizes_the_weighted_sum(orc):
+    import itertools
+    rng = np.random.default_rng(4)
+    for trial in range(4):
+        beta = (10.0 ** rng.uniform(0, 4, size=6)).astype(np.float32)
+        d, lam, gamma = 16, float(rng.uniform(0.1, 0.9)), float(rng.uniform(0.1, 2.0))
+        got = orc.assign_bits(beta, d, lam, gamma).astype(np.float64)
+        best = min(_objective(beta.astype(np.float64), np.array(c, np.float64), d, lam, gamma)
+                   for c in itertools.product((2, 4, 8), repeat=6))
+        assert _objective(beta.astype(np.float64), got, d, lam, gamma) == pytest.approx(best, rel=1e-12)
+
+
+def test_assign_bits_mask_and_the_mixed_pipeline(orc):
+    # beta_k of a graph's messages -> widths -> the mixed-width quantizer
+    g = synth.rmat_graph(scale=9, n=500, n_draws=500 * 8, seed=2)
+    rp, co = g.rowptr.numpy(), g.col.numpy()
+    X = synth.normal_matrix(g.n, 96, seed=7).numpy()
+    beta = orc.beta(rp, co, orc.COEF_GCN, X).astype(np.float32)
+    mask = synth.bernoulli_mask(g.n, 0.5, seed=1).numpy()
+    rb = orc.assign_bits(beta, 96, 0.5, 1e-3, mask)
+    assert set(np.unique(rb[mask == 0]).tolist()) == {0}
+    assert set(np.unique(rb[mask == 1]).tolist()) <= {2, 4, 8}
+    assert len(set(rb[mask == 1].tolist())) > 1  # this lam and gamma mix the widths
+    pk, roff = orc.quantize_mixed(X, rb, 3)
+    assert roff[-1] == sum(orc.pitch(96, int(b)) for b in rb if b in (2, 4, 8))
