@@ -526,6 +526,11 @@ def run_aggregate(args, w):
             tbeta = _timed(lambda: q.message_variance_weights(G, Xd, q.COEF_GCN, out=bt), args.steps, flush)
             bbytes = n * d * 4 + (n + 1) * 4 + E * 4 + n * 4 + n * 4
             beta_rows.append({"d": d, "beta_ms": tbeta, "beta_gbs": bbytes / (tbeta / 1e3) / 1e9})
+            # AdaQP's per-message width choice from beta (Problems 10-12 on one device)
+            rbt = torch.empty(n, dtype=torch.uint8, device=dev)
+            tab = _timed(lambda: q.assign_bits(bt, d, 0.5, 1e-3, out=rbt), args.steps, flush)
+            beta_rows[-1].update({"assign_bits_ms": tab, "assign_bits_gbs": n * 5 / (tab / 1e3) / 1e9})
+            del rbt
             if 64 < d <= 256:
                 # per-message widths drawn uniformly from {2, 4, 8} (AdaQP's sampling ablation)
                 u = synth.uniform01(synth.stream_seed(w.seed, 0x42), torch.arange(n, dtype=torch.int64, device=dev), 0)

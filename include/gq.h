@@ -507,6 +507,24 @@ GQ_API int gq_message_variance_weights(const gq_graph* g, int coef, const float*
                                        float* beta, void* ws, size_t ws_bytes, gq_stream stream);
 
 /* ------------------------------------------------------------------------
+ * gq_assign_bits -- AdaQP Sec. 4.2, the bit-width choice (Problems 10-12)
+ * on one device.  With a single device pair the time objective is
+ * theta + gamma * sum_k d * b_k (theta a constant), and the weighted sum
+ * lam * sum_k beta_k / (2^b_k - 1)^2 + (1 - lam) * time separates per
+ * message, so each row k takes
+ *   rbits[k] = argmin_{b in {2,4,8}} lam*(beta[k]/(L*L)) + tw*(d*b),
+ *   L = 2^b - 1, tw = (1 - lam) * gamma,
+ * each operation an fp64 round-to-nearest in that order, ties to the fewer
+ * bits; rbits[k] = 0 (a full-precision row) where mask[k] == 0.  beta: n
+ * fp32 (gq_message_variance_weights); mask: n bytes or NULL (every row);
+ * rbits: n bytes, the per-row widths of gq_quantize_pack_mixed.  lam in
+ * [0, 1], gamma >= 0 (seconds per transferred bit in the pages' cost model;
+ * any consistent unit).  Errors: GQ_ERR_INVALID_ARG, GQ_ERR_CUDA.
+ * ---------------------------------------------------------------------- */
+GQ_API int gq_assign_bits(const float* beta, const uint8_t* mask, int64_t n, int d, double lam, double gamma,
+                          uint8_t* rbits, gq_stream stream);
+
+/* ------------------------------------------------------------------------
  * gq_quant_error -- Tango Sec. 3.2, Eq. 4, the relative quantization error
  * of a tensor:
  *   *err = (1/(n d)) sum_{r, j} |X[r,j] - Xq[r,j]| / (|X[r,j]| + |Xq[r,j]| + eps)

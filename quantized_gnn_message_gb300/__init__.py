@@ -118,6 +118,7 @@ def _SIGNATURES(P, I64, I, U64, F, S):
         ("gq_message_variance_weights_workspace_bytes", [GP], S),
         ("gq_message_variance_weights", [GP, I, P, I64, I, P, P, S, P], I),
         ("gq_quant_error_workspace_bytes", [], S),
+        ("gq_assign_bits", [P, P, I64, I, ctypes.c_double, ctypes.c_double, P, P], I),
         ("gq_quant_error", [P, I64, I, I64, P, P, I, F, P, P, S, P], I),
     ]
 
@@ -448,6 +449,20 @@ def quant_error(X: torch.Tensor, packed: torch.Tensor, mask: torch.Tensor | None
     _check(L.gq_quant_error(_ptr(X), n, d, _rows(X), _ptr(packed), _ptr(m), bits, eps, _ptr(err), _ptr(ws),
                             ws.numel(), _stream()), "gq_quant_error")
     return err
+
+
+def assign_bits(beta: torch.Tensor, d: int, lam: float, gamma: float, mask: torch.Tensor | None = None,
+                out: torch.Tensor | None = None) -> torch.Tensor:
+    """Per-row widths in {2, 4, 8} (0 where mask is 0) from the variance
+    weights beta: AdaQP Sec. 4.2 Problems 10-12 on one device (gq.h)."""
+    _cuda(beta, torch.float32, "beta")
+    _cuda(mask, torch.uint8, "mask")
+    n = beta.numel()
+    if out is None:
+        out = torch.empty(n, dtype=torch.uint8, device=beta.device)
+    _check(lib().gq_assign_bits(_ptr(beta.contiguous()), _ptr(mask), n, d, float(lam), float(gamma), _ptr(out),
+                                _stream()), "gq_assign_bits")
+    return out
 
 
 def bits_for_error(X: torch.Tensor, mask: torch.Tensor | None, seed: int, threshold: float = 0.3,

@@ -183,6 +183,38 @@ __global__ void sum_parts_kernel(const double* __restrict__ part, int blocks, do
 
 int error_blocks() { return sm_count() * 4; }
 
+// AdaQP Sec. 4.2, Problems 10-12 on one device: one device pair, so the
+// time objective is theta + gamma * sum_k d b_k with theta constant, and the
+// weighted sum with the variance objective separates per message.  Each row
+// takes the width b in {2, 4, 8} minimizing
+//   lam * (beta / (L * L)) + tw * (d * b),   L = 2^b - 1, tw = (1 - lam) * gamma
+// in fp64 with each operation rounded to nearest in that order (ties to the
+// fewer bits); rows with mask 0 stay full precision (width 0).
+__global__ void assign_bits_kernel(const float* __restrict__ beta, const uint8_t* __restrict__ mask, int64_t n,
+                                   double d, double lam, double tw, uint8_t* __restrict__ rbits) {
+  const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+  for (int64_t k = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; k < n; k += stride) {
+    if (mask != nullptr && __ldg(mask + k) == 0) {
+      rbits[k] = 0;
+      continue;
+    }
+    const double bk = (double)__ldg(beta + k);
+    int best = 2;
+    double best_c = 0.0;
+#pragma unroll
+    for (int i = 0; i < 3; ++i) {
+      const int b = 2 << i;
+      const double L = (double)((1 << b) - 1);
+      const double c = __dadd_rn(__dmul_rn(lam, __ddiv_rn(bk, __dmul_rn(L, L))), __dmul_rn(tw, __dmul_rn(d, (double)b)));
+      if (i == 0 || c < best_c) {
+        best_c = c;
+        best = b;
+      }
+    }
+    rbits[k] = (uint8_t)best;
+  }
+}
+
 }  // namespace
 }  // namespace gq
 
@@ -238,5 +270,19 @@ extern "C" int gq_quant_error(const float* X, int64_t n, int d, int64_t ldx, con
   GQ_TRY(launch_status());
   const double inv_n = n > 0 ? 1.0 / ((double)n * (double)d) : 0.0;
   sum_parts_kernel<<<1, 32, 0, s>>>(part, blocks, inv_n, err);
+  return launch_status();
+}
+
+extern "C" int gq_assign_bits(const float* beta, const uint8_t* mask, int64_t n, int d, double lam, double gamma,
+                              uint8_t* rbits, gq_stream stream) {
+  using namespace gq;
+  if (n < 0 || d < 1 || !(lam >= 0.0 && lam <= 1.0) || !(gamma >= 0.0) || gamma > 1e300) return GQ_ERR_INVALID_ARG;
+  if (n == 0) return GQ_OK;
+  if (beta == nullptr || rbits == nullptr) return GQ_ERR_INVALID_ARG;
+  const double tw = (1.0 - lam) * gamma;
+  int64_t blocks = (n + 255) / 256;
+  const int64_t cap = (int64_t)sm_count() * 8;
+  if (blocks > cap) blocks = cap;
+  assign_bits_kernel<<<(unsigned)blocks, 256, 0, (cudaStream_t)stream>>>(beta, mask, n, (double)d, lam, tw, rbits);
   return launch_status();
 }

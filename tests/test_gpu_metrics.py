@@ -90,3 +90,53 @@ def test_quant_error_rejects_bad_arguments():
         q.quant_error(X, pk, None, 3)
     with pytest.raises(q.GQError):
         q.quant_error(X, pk, None, 4, eps=0.0)
+
+
+# AdaQP Sec. 4.2 Problems 10-12 on one device: per-row widths, bit-exact
+@pytest.mark.parametrize("lam,gamma", [(0.5, 1e-3), (0.25, 0.5), (1.0, 1.0), (0.0, 1.0), (0.9, 1e-6)])
+def test_assign_bits(orc, lam, gamma):
+    q = gq()
+    rng = np.random.default_rng(11)
+    d = 64
+    beta = (10.0 ** rng.uniform(-3, 7, size=20000)).astype(np.float32)
+    if 0 < lam < 1:  # values just either side of the 2/4 and 4/8 switch points
+        t24 = (1 - lam) * gamma * d * 2 / (lam * (1 / 9 - 1 / 225))
+        t48 = (1 - lam) * gamma * d * 4 / (lam * (1 / 225 - 1 / 65025))
+        beta[:6] = np.array([t24 * (1 - 1e-6), t24, t24 * (1 + 1e-6), t48 * (1 - 1e-6), t48, t48 * (1 + 1e-6)])
+    beta[6] = 0.0
+    mask = synth.bernoulli_mask(beta.size, 0.7, seed=3).numpy()
+    for m in (None, mask):
+        got = q.assign_bits(torch.from_numpy(beta).cuda(), d, lam, gamma,
+                            None if m is None else torch.from_numpy(m).cuda()).cpu().numpy()
+        np.testing.assert_array_equal(got, orc.assign_bits(beta, d, lam, gamma, m))
+
+
+def test_assign_bits_empty_and_arguments():
+    q = gq()
+    assert q.assign_bits(torch.zeros(0, device="cuda"), 8, 0.5, 1.0).numel() == 0
+    b = torch.ones(4, device="cuda")
+    for lam, gamma in ((1.5, 1.0), (-0.1, 1.0), (0.5, -1.0), (0.5, float("nan"))):
+        with pytest.raises(q.GQError):
+            q.assign_bits(b, 8, lam, gamma)
+
+
+def test_beta_to_widths_to_mixed_aggregation(orc):
+    # the whole adaptive path on the GPU: beta -> widths -> mixed quantization
+    # -> mixed aggregation, checked against the oracle on the GPU's widths
+    q = gq()
+    g = rmat_small()
+    G = q.graph_prepare(g.rowptr.cuda(), g.col.cuda())
+    d = 128
+    X = synth.normal_matrix(g.n, d, seed=21).numpy()
+    Xd = torch.from_numpy(X).cuda()
+    mask = synth.bernoulli_mask(g.n, 0.6, seed=4).cuda()
+    beta = q.message_variance_weights(G, Xd, 0)
+    rb = q.assign_bits(beta, d, 0.5, 2e-3, mask)
+    rbh = rb.cpu().numpy()
+    np.testing.assert_array_equal(rbh, orc.assign_bits(beta.cpu().numpy(), d, 0.5, 2e-3, mask.cpu().numpy()))
+    assert len(set(rbh.tolist())) >= 3  # full-precision rows and at least two widths
+    pk, roff = q.quantize_pack_mixed(Xd, rb, 8)
+    Y = q.dequant_spmm_mixed(G, Xd, pk, roff, rb, coef=0).cpu().numpy()
+    M = orc.messages_mixed(X, pk.cpu().numpy(), roff.cpu().numpy(), rbh, d)
+    from gpu_helpers import close
+    close(Y, orc.spmm(g.rowptr.numpy(), g.col.numpy(), 0, M), what="beta -> widths -> aggregation")
