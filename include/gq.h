@@ -435,14 +435,16 @@ GQ_API int gq_sddmm_edge_softmax(const gq_graph* g, const float* S, const float*
  *   out   = sum_{u->v} a^[e,k] m_u[kF+f]                     -> n x d
  *   packed_save (n x gq_packed_pitch(d, bits), nullable) keeps the
  *   forward's quantized messages for the backward pass (required there
- *   when bits < 32); acode_save / ahdr_save (both or neither; nullable)
- *   keep the attention codes, which the backward needs to use a^.
+ *   when bits < 32); acode_save / ahdr_save (both or neither; nullable;
+ *   acode_save may be NULL on a graph without edges) keep the attention
+ *   codes, which the backward needs to use a^.
  * gq_gat_layer_bwd (the quantizer is the identity in backward):
  *   dalpha = SDDMM dot of dOut[v] with the forward messages m_u;
  *   dE_pre = alpha (dalpha - P) LeakyReLU'; dD = in-edge sums, dS =
  *   out-edge sums; dM = transposed multi-head SpMM of dOut (rows of
  *   marginal nodes quantized when bits < 32, seed) weighted by a^
- *   (the forward's codes acode_save / ahdr_save when given, else alpha);
+ *   (the forward's codes acode_save / ahdr_save when ahdr_save is given,
+ *   else alpha);
  *   dH' = dM + dS a_src + dD a_dst; da_src = sum_u dS[u] H'[u],
  *   da_dst likewise; dW = H^T dH'; dH = dH' W^T.
  *   dEpre_save (E x heads) and dHp_save (n x d fp32) are optional copies.

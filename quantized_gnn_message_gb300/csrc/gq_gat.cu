@@ -1046,8 +1046,10 @@ size_t edge_bwd_workspace(const gq_graph* g, int heads) { return sched_ws(g->sch
 
 int edge_softmax(const gq_graph* g, const float* S, const float* D, int heads, float slope, float* Epre,
                  float* alpha, void* ws, size_t ws_bytes, cudaStream_t s) {
-  if (g == nullptr || S == nullptr || D == nullptr || alpha == nullptr) return GQ_ERR_INVALID_ARG;
+  if (g == nullptr) return GQ_ERR_INVALID_ARG;
   if (!(heads == 1 || heads == 2 || heads == 4 || heads == 8)) return GQ_ERR_UNSUPPORTED;
+  if (g->nnz == 0) return GQ_OK;  // no edges: nothing to score
+  if (S == nullptr || D == nullptr || alpha == nullptr) return GQ_ERR_INVALID_ARG;
   if (!aligned(S, 16) || !aligned(D, 16) || !aligned(alpha, 16) || (Epre != nullptr && !aligned(Epre, 16)))
     return GQ_ERR_INVALID_ARG;
   SoftmaxParams p{};
@@ -1079,8 +1081,10 @@ size_t edge_quant_workspace(const gq_graph* g, int heads) { return edge_softmax_
 
 int quantize_edge_values(const gq_graph* g, const float* alpha, int heads, uint64_t seed, uint8_t* codes, float* hdr,
                          void* ws, size_t ws_bytes, cudaStream_t s) {
-  if (g == nullptr || alpha == nullptr || codes == nullptr || hdr == nullptr) return GQ_ERR_INVALID_ARG;
+  if (g == nullptr || hdr == nullptr) return GQ_ERR_INVALID_ARG;
   if (!(heads == 1 || heads == 2 || heads == 4 || heads == 8)) return GQ_ERR_UNSUPPORTED;
+  // with no edges alpha and codes are empty (and may be NULL); the headers are still written
+  if (g->nnz > 0 && (alpha == nullptr || codes == nullptr)) return GQ_ERR_INVALID_ARG;
   if (!aligned(alpha, 16) || !aligned(codes, 16) || !aligned(hdr, 16)) return GQ_ERR_INVALID_ARG;
   const size_t need = edge_quant_workspace(g, heads);
   if (need > 0 && (ws == nullptr || ws_bytes < need || !aligned(ws, 256))) return GQ_ERR_WORKSPACE;
@@ -1105,8 +1109,10 @@ int quantize_edge_values(const gq_graph* g, const float* alpha, int heads, uint6
 
 int dequant_edge_values(const gq_graph* g, const uint8_t* codes, const float* hdr, int heads, float* out,
                         cudaStream_t s) {
-  if (g == nullptr || codes == nullptr || hdr == nullptr || out == nullptr) return GQ_ERR_INVALID_ARG;
+  if (g == nullptr) return GQ_ERR_INVALID_ARG;
   if (!(heads == 1 || heads == 2 || heads == 4 || heads == 8)) return GQ_ERR_UNSUPPORTED;
+  if (g->nnz == 0) return GQ_OK;  // no edges: no values
+  if (codes == nullptr || hdr == nullptr || out == nullptr) return GQ_ERR_INVALID_ARG;
   if (!aligned(codes, 16) || !aligned(hdr, 16) || !aligned(out, 16)) return GQ_ERR_INVALID_ARG;
   EdgeQuantParams p{};
   p.rowptr = g->rowptr;

@@ -234,9 +234,12 @@ extern "C" int gq_gat_layer_fwd(const gq_graph* g, const float* H, int64_t ldh, 
   using namespace gq;
   GQ_TRY(gat_check(g, d_in, heads, f, bits));
   if (H == nullptr || W == nullptr || a_src == nullptr || a_dst == nullptr || Hp_save == nullptr ||
-      S_save == nullptr || D_save == nullptr || alpha_save == nullptr || out == nullptr || ldh < d_in)
+      S_save == nullptr || D_save == nullptr || (alpha_save == nullptr && g->nnz > 0) || out == nullptr ||
+      ldh < d_in)
     return GQ_ERR_INVALID_ARG;
-  if (!(alpha_bits == 32 || alpha_bits == 8) || ((acode_save == nullptr) != (ahdr_save == nullptr)))
+  // attention codes are kept in both buffers or in neither; with no edges the codes are empty (may be NULL)
+  if (!(alpha_bits == 32 || alpha_bits == 8) || (acode_save != nullptr && ahdr_save == nullptr) ||
+      (ahdr_save != nullptr && acode_save == nullptr && g->nnz > 0))
     return GQ_ERR_INVALID_ARG;
   cudaStream_t s = (cudaStream_t)stream;
   const int d = heads * f;
@@ -278,12 +281,13 @@ extern "C" int gq_gat_layer_bwd(const gq_graph* g, const float* dOut, const floa
   using namespace gq;
   GQ_TRY(gat_check(g, d_in, heads, f, bits));
   if (dOut == nullptr || H == nullptr || Hp_save == nullptr || S_save == nullptr || D_save == nullptr ||
-      alpha_save == nullptr || W == nullptr || a_src == nullptr || a_dst == nullptr || dW == nullptr ||
+      (alpha_save == nullptr && g->nnz > 0) || W == nullptr || a_src == nullptr || a_dst == nullptr || dW == nullptr ||
       da_src == nullptr || da_dst == nullptr || dH == nullptr || ldh < d_in)
     return GQ_ERR_INVALID_ARG;
   if (bits < 32 && packed_save == nullptr) return GQ_ERR_INVALID_ARG;
-  if ((acode_save == nullptr) != (ahdr_save == nullptr)) return GQ_ERR_INVALID_ARG;
-  const int alpha_bits = acode_save != nullptr ? 8 : 32;
+  if ((acode_save != nullptr && ahdr_save == nullptr) || (ahdr_save != nullptr && acode_save == nullptr && g->nnz > 0))
+    return GQ_ERR_INVALID_ARG;
+  const int alpha_bits = ahdr_save != nullptr ? 8 : 32;
   cudaStream_t s = (cudaStream_t)stream;
   const int d = heads * f;
   GatWs w;

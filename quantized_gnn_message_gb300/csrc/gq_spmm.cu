@@ -1537,7 +1537,7 @@ int edge_spmm(const gq_graph* g, int transpose, const float* alpha, int heads, c
               size_t ws_bytes, cudaStream_t s) {
   SpmmParams p;
   GQ_TRY(spmm_setup(g, transpose, X, ldx, packed, mask, d, bits, Y, ldy, ws, ws_bytes, s, p));
-  if (alpha == nullptr || heads < 1 || d % heads != 0) return GQ_ERR_INVALID_ARG;
+  if ((alpha == nullptr && g->nnz > 0) || heads < 1 || d % heads != 0) return GQ_ERR_INVALID_ARG;
   const int F = d / heads;
   int fshift = 0;
   while ((1 << fshift) < F) ++fshift;
@@ -1563,7 +1563,8 @@ int launch_alpha8(const SpmmParams& p, cudaStream_t s) {
 int edge_spmm_alpha8(const gq_graph* g, const uint8_t* acode, const float* ahdr, int heads, const float* X,
                      int64_t ldx, const uint8_t* packed, const uint8_t* mask, int d, int bits, float* Y,
                      int64_t ldy, void* ws, size_t ws_bytes, cudaStream_t s) {
-  if (acode == nullptr || ahdr == nullptr || heads < 1 || d % heads != 0 || !aligned(ahdr, 8))
+  if (g == nullptr || ahdr == nullptr || (acode == nullptr && g->nnz > 0) || heads < 1 || d % heads != 0 ||
+      !aligned(ahdr, 8))
     return GQ_ERR_INVALID_ARG;
   if (d > 256) return GQ_ERR_UNSUPPORTED;
   const int F = d / heads;
