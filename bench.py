@@ -402,7 +402,10 @@ def run_ours(args, w):
 
 
 def _timed(fn, iters, flush):
-    """Average device ms of fn() over `iters` calls, L2 flushed before each."""
+    """Average device ms of fn() over `iters` calls, L2 flushed before each,
+    after one untimed call (module loading, first workspace allocation)."""
+    fn()
+    torch.cuda.synchronize()
     evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(iters)]
     for a, b in evs:
         flush.fill_(1)

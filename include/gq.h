@@ -260,8 +260,9 @@ GQ_API int gq_dequant_spmm(const gq_graph* g, int transpose, int coef, const flo
  * each at its own width; row r's bytes equal gq_quantize_pack's row r at
  * that width and seed.  packed: roff[n] bytes, 16-byte aligned.
  * gq_dequant_spmm_mixed -- gq_dequant_spmm over such a buffer (each packed
- * row de-quantized at its own width, other rows read from X); 64 < d <= 256
- * (GQ_ERR_UNSUPPORTED otherwise).  Workspace: gq_spmm_workspace_bytes.
+ * row de-quantized at its own width, other rows read from X); d <= 256
+ * (GQ_ERR_UNSUPPORTED otherwise), d % 4 == 0.  Workspace:
+ * gq_spmm_workspace_bytes.
  * Errors: as gq_quantize_pack / gq_dequant_spmm.
  * ---------------------------------------------------------------------- */
 GQ_API size_t gq_packed_row_offsets_workspace_bytes(int64_t n);

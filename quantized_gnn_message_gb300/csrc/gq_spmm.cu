@@ -622,7 +622,7 @@ constexpr int kPiecesPerLane = BITS == 8 ? 2 : 1;
 // fp32 row (also when packed and fp32 rows mix: MX).  A compile-time stride
 // keeps every slot address an immediate offset from the group's ring.
 template <int BITS, int LG, bool MX>
-constexpr int kSlot = BITS < 32 && !MX ? ((2 * BITS * LG + 7) / 8 * 8 + 8 + 15) / 16 * 16 : 64 * LG;
+constexpr int kSlot = BITS > 0 && BITS < 32 && !MX ? ((2 * BITS * LG + 7) / 8 * 8 + 8 + 15) / 16 * 16 : 64 * LG;
 
 constexpr uint32_t kMagicBits = 0x4B000000u;  // 2^23 as fp32
 constexpr float kMagic = 8388608.0f;
@@ -653,6 +653,9 @@ struct ALane {
   const uint8_t* srcx;
   uint32_t stridex;
   int nvm, swz;
+  // per-row widths (BITS == 0): bit 2i / 2i + 1 = pieces gl / gl + LG exist
+  // in a row of width 2 << i
+  uint32_t hasw;
 };
 
 // Column of accumulator entry i (acc[i / 2], half i % 2) of this lane.
@@ -662,23 +665,13 @@ __device__ __forceinline__ int a_col(const ALane<LG>& L, int i) {
   else return 4 * (L.gl + LG * (i >> 2)) + (i & 3);
 }
 
-// Accumulate one edge from its slot sl with coefficient cf.
-template <int BITS, int LG, bool MX>
-__device__ __forceinline__ void a_consume(const SpmmParams& p, const ALane<LG>& L, const uint8_t* sl, bool quant,
-                                          float cf, f32x2 bias, f32x2 (&acc)[8], float& accz) {
-  if (MX && !quant) {
-    const f32x2 c2 = f2_pack(cf, cf);
-#pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      if (k < L.nvm) {
-        const f32x2* xr = reinterpret_cast<const f32x2*>(sl + 64 * L.gl + 16 * (k ^ L.swz));
-        acc[2 * k] = f2_fma(c2, xr[0], acc[2 * k]);
-        acc[2 * k + 1] = f2_fma(c2, xr[1], acc[2 * k + 1]);
-      }
-    }
-  } else if constexpr (BITS < 32) {
+// Accumulate a packed row of width BITS (header at hoff) from slot sl.
+template <int BITS, int LG>
+__device__ __forceinline__ void a_consume_packed(const ALane<LG>& L, const uint8_t* sl, int hoff, float cf,
+                                                 f32x2 bias, f32x2 (&acc)[8], float& accz) {
+  {
     constexpr float c = (float)(1 << (BITS - 1));
-    const float2 h = *reinterpret_cast<const float2*>(sl + p.hoff);
+    const float2 h = *reinterpret_cast<const float2*>(sl + hoff);
     const float cs = cf * h.x;
     accz = __fmaf_rn(cf, __fmaf_rn(c, h.x, h.y), accz);
     const f32x2 cs2 = f2_pack(cs, cs);
@@ -710,6 +703,42 @@ __device__ __forceinline__ void a_consume(const SpmmParams& p, const ALane<LG>& 
                               __uint_as_float(__byte_perm(sp[w1], kMagicBits, 0x7540u | b1)));
       acc[i] = f2_fma(cs2, f2_add(v, bias), acc[i]);
     }
+  }
+}
+
+// An fp32 row stored in the mixed layout (the lane's 16 columns as nvm
+// swizzled 16-byte pieces).
+template <int LG>
+__device__ __forceinline__ void a_consume_fp32x(const ALane<LG>& L, const uint8_t* sl, float cf, f32x2 (&acc)[8]) {
+  const f32x2 c2 = f2_pack(cf, cf);
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    if (k < L.nvm) {
+      const f32x2* xr = reinterpret_cast<const f32x2*>(sl + 64 * L.gl + 16 * (k ^ L.swz));
+      acc[2 * k] = f2_fma(c2, xr[0], acc[2 * k]);
+      acc[2 * k + 1] = f2_fma(c2, xr[1], acc[2 * k + 1]);
+    }
+  }
+}
+
+// Accumulate one edge from its slot sl with coefficient cf.  BITS == 0: the
+// row's kind (0 = fp32, else its width) is `kind`.
+template <int BITS, int LG, bool MX>
+__device__ __forceinline__ void a_consume(const SpmmParams& p, const ALane<LG>& L, const uint8_t* sl, bool quant,
+                                          int kind, float cf, f32x2 bias, f32x2 (&acc)[8], float& accz) {
+  if constexpr (BITS == 0) {
+    if (kind == 8)
+      a_consume_packed<8, LG>(L, sl, (int)header_offset(p.d, 8), cf, a_bias<8>(), acc, accz);
+    else if (kind == 4)
+      a_consume_packed<4, LG>(L, sl, (int)header_offset(p.d, 4), cf, a_bias<4>(), acc, accz);
+    else if (kind == 2)
+      a_consume_packed<2, LG>(L, sl, (int)header_offset(p.d, 2), cf, a_bias<2>(), acc, accz);
+    else
+      a_consume_fp32x<LG>(L, sl, cf, acc);
+  } else if (MX && !quant) {
+    a_consume_fp32x<LG>(L, sl, cf, acc);
+  } else if constexpr (BITS < 32) {
+    a_consume_packed<BITS, LG>(L, sl, p.hoff, cf, bias, acc, accz);
   } else {
     const f32x2 c2 = f2_pack(cf, cf);
 #pragma unroll
@@ -758,6 +787,7 @@ __device__ __forceinline__ void a_stream(const SpmmParams& p, const ALane<LG>& L
   uint32_t cx[kAS][U];
   float cf[kAS][U];
   bool mq[kAS][U];  // mixed rows: the gathered row is packed
+  int kd[kAS][U];   // per-row widths (BITS == 0): the gathered row's kind
   // column ids two steps ahead: cp points at edge 2 U of the current step,
   // rem counts the edges from there to the end of the stream
   const int32_t* __restrict__ cp = p.col + eb;
@@ -809,7 +839,23 @@ __device__ __forceinline__ void a_stream(const SpmmParams& p, const ALane<LG>& L
             cf[j][t] = colscale != nullptr ? __ldg(colscale + x) : 1.0f;
             const uint32_t dst = L.sring + (j * U + t) * kSlot<BITS, LG, MX>;
             const uint8_t* src = L.src + (size_t)x * L.stride;
-            if (MX && !mq[j][t]) {
+            if constexpr (BITS == 0) {
+              // the row's own width: the whole packed row at its offset, or the fp32 row
+              const uint32_t b = __ldg(p.rbits + x);
+              const int kind = (b == 2u || b == 4u || b == 8u) ? (int)b : 0;
+              kd[j][t] = kind;
+              if (kind == 0) {
+                const uint8_t* sx = L.srcx + (size_t)x * L.stridex;
+#pragma unroll
+                for (int k = 0; k < 4; ++k)
+                  if (k < L.nvm) cp_async16(dst + 64 * L.gl + 16 * (k ^ L.swz), sx + 16 * k);
+              } else {
+                const int sh = 2 * (kind == 2 ? 0 : (kind == 4 ? 1 : 2));
+                const uint8_t* sp = p.packed + __ldg(p.roff + x) + 16 * L.gl;
+                if ((L.hasw >> sh) & 1u) cp_async16(dst + 16 * L.gl, sp);
+                if ((L.hasw >> (sh + 1)) & 1u) cp_async16(dst + 16 * (L.gl + LG), sp + 16 * LG);
+              }
+            } else if (MX && !mq[j][t]) {
               const uint8_t* sx = L.srcx + (size_t)x * L.stridex;
 #pragma unroll
               for (int k = 0; k < 4; ++k)
@@ -849,8 +895,8 @@ __device__ __forceinline__ void a_stream(const SpmmParams& p, const ALane<LG>& L
               }
             }
             if (L.on)
-              a_consume<BITS, LG, MX>(p, L, L.ring + (jc * U + t) * kSlot<BITS, LG, MX>, MX && mq[jc][t], cf[jc][t],
-                                      bias, acc, accz);
+              a_consume<BITS, LG, MX>(p, L, L.ring + (jc * U + t) * kSlot<BITS, LG, MX>, MX && mq[jc][t],
+                                      BITS == 0 ? kd[jc][t] : 0, cf[jc][t], bias, acc, accz);
           }
         }
       }
@@ -878,11 +924,27 @@ __global__ void __launch_bounds__(kSpmmThreads) spmm_async_kernel(const SpmmPara
   L.ring = asm_ + (w * NG + g) * (kAS * U * SLOT);
   L.sring = sm_addr(L.ring);
   L.gmask = (LG == 32 ? 0xffffffffu : ((1u << LG) - 1u)) << (g * LG);
-  const int pieces = BITS < 32 ? (int)(p.pitch / 16) : 0;
+  const int pieces = BITS > 0 && BITS < 32 ? (int)(p.pitch / 16) : 0;
   L.has0 = L.gl < pieces;
   L.has1 = L.gl + LG < pieces;
   L.c0 = 16 * L.gl;
-  if constexpr (BITS < 32) {
+  L.hasw = 0u;
+  if constexpr (BITS == 0) {
+    // per-row widths: packed rows of any width and fp32 rows in the mixed layout
+    L.on = L.c0 < p.d;
+    L.nv = 0;
+    L.src = nullptr;
+    L.stride = 0u;
+    L.srcx = reinterpret_cast<const uint8_t*>(p.X + L.c0);
+    L.stridex = (uint32_t)(p.ldx * 4);
+    L.nvm = max(0, min(4, (p.d - L.c0) / 4));
+    L.swz = (L.gl >> 1) & 3;
+#pragma unroll
+    for (int i = 0; i < 3; ++i) {
+      const int pw = (int)(packed_pitch(p.d, 2 << i) / 16);
+      L.hasw |= (uint32_t)(L.gl < pw) << (2 * i) | (uint32_t)(L.gl + LG < pw) << (2 * i + 1);
+    }
+  } else if constexpr (BITS < 32) {
     L.on = L.c0 < p.d;
     L.nv = 0;
     L.src = p.packed + 16 * L.gl;
@@ -948,10 +1010,12 @@ template <int BITS, int LG, int U, bool MX>
 int launch_async(const SpmmParams& p, cudaStream_t s) {
   constexpr int NG = 32 / LG;
   constexpr int SLOT = kSlot<BITS, LG, MX>;
-  static_assert(BITS == 32 || kSlot<BITS, LG, false> / 16 <= kPiecesPerLane<BITS> * LG,
+  static_assert(BITS == 32 || BITS == 0 || kSlot<BITS, LG, false> / 16 <= kPiecesPerLane<BITS> * LG,
                 "row pieces exceed the lanes' share");
-  if (BITS < 32 && p.pitch > kSlot<BITS, LG, false>) return GQ_ERR_UNSUPPORTED;
-  if ((BITS == 32 || MX) && 4 * p.d > SLOT) return GQ_ERR_UNSUPPORTED;
+  if (BITS > 0 && BITS < 32 && p.pitch > kSlot<BITS, LG, false>) return GQ_ERR_UNSUPPORTED;
+  if ((BITS == 32 || BITS == 0 || MX) && 4 * p.d > SLOT) return GQ_ERR_UNSUPPORTED;
+  // per-row widths: a row of width 8 (the widest) takes at most two pieces per lane
+  if (BITS == 0 && packed_pitch(p.d, 8) > 32 * LG) return GQ_ERR_UNSUPPORTED;
   size_t smem = (size_t)kSpmmWarps * NG * kAS * U * SLOT;
   const size_t part = sizeof(float) * kSpmmWarps * p.d;
   if (smem < part) smem = part;
@@ -1513,7 +1577,7 @@ int dequant_spmm_mixed(const gq_graph* g, int transpose, int coef, const float* 
                        const int64_t* roff, const uint8_t* rbits, int d, float* Y, int64_t ldy, void* ws,
                        size_t ws_bytes, cudaStream_t s) {
   if (packed == nullptr || roff == nullptr || rbits == nullptr || !aligned(packed, 16)) return GQ_ERR_INVALID_ARG;
-  if (d <= 64 || d > 256) return GQ_ERR_UNSUPPORTED;
+  if (d > 256) return GQ_ERR_UNSUPPORTED;
   SpmmParams p;
   GQ_TRY(spmm_setup(g, transpose, X, ldx, nullptr, nullptr, d, 32, Y, ldy, ws, ws_bytes, s, p));
   if (ldx > (int64_t)1 << 29) return GQ_ERR_UNSUPPORTED;
@@ -1529,6 +1593,10 @@ int dequant_spmm_mixed(const gq_graph* g, int transpose, int coef, const float* 
   p.packed = packed;
   p.rbits = rbits;
   p.roff = roff;
+  // d <= 128: lane groups of d/16 lanes per edge, each row copied whole at
+  // its own width (cp.async ring); wider rows: one warp per edge, bulk copies
+  // (each measured the faster of the two in its range)
+  if (d <= 128) return launch_async_d<0, 1, false>(p, s);
   return d > 128 ? launch_bulk<0, 8, true, 4, 2>(p, s) : launch_bulk<0, 4, true, 8, 4>(p, s);
 }
 

@@ -2,7 +2,8 @@
 4.2: a bit-width per message; Sec. 5.3: widths drawn per message from
 {2, 4, 8}): row offsets exact, packed bytes bit-exact, the aggregation over
 the mixed buffer within 1e-4 (1 + |ref|) of the oracle on the GPU's own
-packed bytes."""
+packed bytes, for widths served by both kernels (d <= 128: lane groups with
+a cp.async ring; 128 < d <= 256: a warp per edge with bulk copies)."""
 import numpy as np
 import pytest
 import torch
@@ -21,7 +22,7 @@ def _widths(n, seed, central=0.4):
     return w
 
 
-@pytest.mark.parametrize("d", [68, 128, 256])
+@pytest.mark.parametrize("d", [16, 68, 128, 256])
 def test_offsets_and_packed_bytes(orc, d):
     q = gq()
     n = 5000
@@ -45,7 +46,7 @@ def test_offsets_many_tiles_and_empty(orc):
 
 
 @pytest.mark.parametrize("graph", ["rmat", "hubs_split", "sparse_rows"])
-@pytest.mark.parametrize("d", [68, 128, 196, 256])
+@pytest.mark.parametrize("d", [16, 36, 64, 68, 128, 196, 256])
 @pytest.mark.parametrize("transpose", [False, True])
 def test_mixed_aggregation(orc, graph, d, transpose):
     q = gq()
@@ -84,8 +85,8 @@ def test_mixed_rejects_unsupported_width():
     q = gq()
     g = rmat_small()
     G = q.graph_prepare(g.rowptr.cuda(), g.col.cuda())
-    Xd = synth.normal_matrix(g.n, 32, seed=3, device="cuda")
+    Xd = synth.normal_matrix(g.n, 320, seed=3, device="cuda")
     rb = torch.full((g.n,), 2, dtype=torch.uint8, device="cuda")
     pk, roff = q.quantize_pack_mixed(Xd, rb, 1)
     with pytest.raises(q.GQError):
-        q.dequant_spmm_mixed(G, Xd, pk, roff, rb)  # d = 32 is outside 64 < d <= 256
+        q.dequant_spmm_mixed(G, Xd, pk, roff, rb)  # d = 320 is above 256
