@@ -534,7 +534,7 @@ def run_aggregate(args, w):
             tab = _timed(lambda: q.assign_bits(bt, d, 0.5, 1e-3, out=rbt), args.steps, flush)
             beta_rows[-1].update({"assign_bits_ms": tab, "assign_bits_gbs": n * 5 / (tab / 1e3) / 1e9})
             del rbt
-            if 64 < d <= 256:
+            if d <= 256 and d % 4 == 0:
                 # per-message widths drawn uniformly from {2, 4, 8} (AdaQP's sampling ablation)
                 u = synth.uniform01(synth.stream_seed(w.seed, 0x42), torch.arange(n, dtype=torch.int64, device=dev), 0)
                 rb = torch.tensor([2, 4, 8], dtype=torch.uint8, device=dev)[torch.clamp((u * 3).long(), max=2)]
