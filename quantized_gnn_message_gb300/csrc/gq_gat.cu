@@ -137,14 +137,6 @@ __device__ __forceinline__ bool sm_range_ok(const SoftmaxParams& p, int64_t v, i
   return ok;
 }
 
-template <int K>
-__device__ __forceinline__ void sm_scores(const SoftmaxParams& p, int64_t e, const float (&dv)[K], float (&ep)[K]) {
-  float s[K];
-  load_k<K>(p.S + (int64_t)__ldg(p.col + e) * K, s);
-#pragma unroll
-  for (int k = 0; k < K; ++k) ep[k] = s[k] + dv[k];
-}
-
 // Scores of the thread's edges e, e + stride, e + 2 stride, e + 3 stride
 // (those below end): their column ids, then their S rows, loaded before any
 // is used.

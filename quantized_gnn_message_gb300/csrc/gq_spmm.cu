@@ -333,31 +333,6 @@ __device__ __forceinline__ void lconsume(const LMsg<BITS, ALLQ>& m, float coef, 
   }
 }
 
-__device__ __forceinline__ void lflush(const SpmmParams& p, int64_t r, int c0, const float (&acc)[kLC], float accz) {
-  if (c0 >= p.d) return;
-  const float s = p.rowscale ? __ldg(p.rowscale + r) : 1.0f;
-  float o[kLC];
-#pragma unroll
-  for (int k = 0; k < kLC; ++k) o[k] = (acc[k] + accz) * s;
-  if (p.Yb != nullptr) {
-    __nv_bfloat16* y = p.Yb + r * p.ldy + c0;
-#pragma unroll
-    for (int k = 0; k < kLC; k += 8) {
-      if (c0 + k + 8 <= p.d) {
-        *reinterpret_cast<uint4*>(y + k) = make_uint4(pack_bf16x2(o[k], o[k + 1]), pack_bf16x2(o[k + 2], o[k + 3]),
-                                                      pack_bf16x2(o[k + 4], o[k + 5]), pack_bf16x2(o[k + 6], o[k + 7]));
-      } else if (c0 + k + 4 <= p.d) {
-        *reinterpret_cast<uint2*>(y + k) = make_uint2(pack_bf16x2(o[k], o[k + 1]), pack_bf16x2(o[k + 2], o[k + 3]));
-      }
-    }
-  } else {
-    float* y = p.Y + r * p.ldy + c0;
-#pragma unroll
-    for (int k = 0; k < kLC; k += 4)
-      if (c0 + k < p.d) st_f4(y + k, o[k], o[k + 1], o[k + 2], o[k + 3]);
-  }
-}
-
 // Per-edge metadata of U consecutive edges: column ids, then coefficients
 // and mask bits.
 template <int BITS, int EW, int U>
@@ -594,11 +569,6 @@ __device__ __forceinline__ f32x2 f2_fma(f32x2 a, f32x2 b, f32x2 c) {
 __device__ __forceinline__ f32x2 f2_add(f32x2 a, f32x2 b) {
   f32x2 d;
   asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
-  return d;
-}
-__device__ __forceinline__ f32x2 f2_mul(f32x2 a, f32x2 b) {
-  f32x2 d;
-  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
   return d;
 }
 
