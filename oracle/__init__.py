@@ -15,7 +15,8 @@ Routines follow:
       boundary messages are quantized);
   Sancus (IJCAI 2023) Sec. 2: normalized adjacency D~^-1/2 (A+I) D~^-1/2;
   Tango (arXiv 2308.00890) Sec. 2.1, Fig. 1: GAT forward/backward steps;
-  AdaQP Sec. 4.2 (Problem 11): per-message variance weight beta_k;
+  AdaQP Sec. 4.2 (Problem 11): per-message variance weight beta_k, and
+      the width choice of Problems 10-12 on one device;
   Tango Sec. 3.2 (Eq. 4): relative quantization error Error_X and the
       bit-count rule built on it;
   Tango Sec. 3.3: the SpMM's edge values quantized at 8 bits (one AdaQP

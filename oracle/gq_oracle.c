@@ -14,10 +14,14 @@
  *      Sec. 3.1  only messages that cross the boundary are quantized
  *  - Sancus (IJCAI 2023, extended abstract), Sec. 2 Preliminaries:
  *      A^ = D~^{-1/2} (A+I) D~^{-1/2},  H' = sigma(A^ H W)
+ *      Sec. 4.2  Problem 11's variance weight beta_k; Problems 10-12 (the
+ *                width choice) on one device
  *  - Tango, "Rethinking quantization for graph neural network training on
  *    GPUs" (arXiv 2308.00890), Sec. 2.1 / Fig. 1: GAT as GEMM -> head
  *    projections -> SDDMM add -> LeakyReLU -> edge softmax -> SpMM, and the
- *    backward steps (SDDMM dot, softmax derivative, in/out-edge sums).
+ *    backward steps (SDDMM dot, softmax derivative, in/out-edge sums);
+ *    Sec. 3.2 (Eq. 4) the relative quantization error; Sec. 3.3 the SpMM
+ *    on quantized edge features.
  *
  * Precision: the quantizer works in IEEE fp32 round-to-nearest with no FMA
  * contraction (build with -ffp-contract=off), because its integer codes must
