@@ -55,6 +55,22 @@ def dist_env():
     return ws, rank, local
 
 
+def max_over_ranks(x: float, ws: int, device) -> float:
+    """The largest x over all ranks: a job's time is its slowest rank's."""
+    if ws <= 1:
+        return x
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(units_per_rank_step: float, ws: int, ms_per_step: float) -> float:
+    """Whole-job units per second: every rank processes its own units in the
+    same (slowest-rank) time."""
+    return units_per_rank_step * ws / (ms_per_step / 1e3)
+
+
 def measured_peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -292,14 +308,10 @@ def run_ours(args, w):
     if int(model.err.item()) != 0:
         raise RuntimeError(f"device wait timed out (code {int(model.err.item())})")
     step_ms = [starts[k].elapsed_time(ends[k]) for k in range(args.steps)]
-    total_ms = sum(step_ms)
-    if ws > 1:
-        t = torch.tensor([total_ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = max_over_ranks(sum(step_ms), ws, dev)
     ms_per_step = total_ms / args.steps
     edges_per_step = L * len(bits_list) * g.nnz
-    value = edges_per_step * ws / (ms_per_step / 1e3)
+    value = job_throughput(edges_per_step, ws, ms_per_step)
 
     # per-stage device time, from the events recorded inside the timed steps
     stage_ms = {}
@@ -369,12 +381,8 @@ def run_ours(args, w):
                 hw.copy_(dw, non_blocking=True)
         e_e[k].record()
     torch.cuda.synchronize()
-    e2e_ms = sum(e_s[k].elapsed_time(e_e[k]) for k in range(args.steps)) / args.steps
-    if ws > 1:
-        t = torch.tensor([e2e_ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        e2e_ms = float(t.item())
-    e2e = {"value": edges_per_step * ws / (e2e_ms / 1e3), "unit": UNIT, "h2d_bytes_per_step": h2d,
+    e2e_ms = max_over_ranks(sum(e_s[k].elapsed_time(e_e[k]) for k in range(args.steps)) / args.steps, ws, dev)
+    e2e = {"value": job_throughput(edges_per_step, ws, e2e_ms), "unit": UNIT, "h2d_bytes_per_step": h2d,
            "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms}
 
     launches = sum(model.launches(b) for b in bits_list) * args.steps
