@@ -55,3 +55,24 @@ def sparse_rows_graph(n=6000, seed=5):
     rowptr[1:] = np.cumsum(deg)
     col = np.concatenate([np.sort(rng.choice(n, k, replace=False)) for k in deg]).astype(np.int32)
     return synth.Graph(n, torch.from_numpy(rowptr.astype(np.int32)), torch.from_numpy(col))
+
+
+def sample_rows(rowptr, k, seed, n_heavy=None):
+    """k destination rows: the heaviest rows (k // 4 unless given) plus a
+    seeded uniform draw."""
+    deg = np.diff(rowptr)
+    heavy = np.argsort(-deg, kind="stable")[: k // 4 if n_heavy is None else n_heavy]
+    rng = np.random.default_rng(seed)
+    rest = rng.choice(deg.size, size=k - heavy.size, replace=False)
+    return np.unique(np.concatenate([heavy, rest]))
+
+
+def sub_csr(rowptr, col, rows):
+    """The in-edges of `rows` as their own CSR (rows renumbered 0..m-1),
+    their CSR edge ids, and their sources renumbered into `src` (the
+    distinct sources, in ascending order)."""
+    starts, ends = rowptr[rows], rowptr[rows + 1]
+    eids = np.concatenate([np.arange(a, b) for a, b in zip(starts, ends)]).astype(np.int64)
+    sub_rp = np.concatenate([[0], np.cumsum(ends - starts)]).astype(np.int32)
+    src, local = np.unique(col[eids], return_inverse=True)
+    return sub_rp, local.astype(np.int32), eids, src
