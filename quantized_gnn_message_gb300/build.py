@@ -78,15 +78,40 @@ if __name__ == "__main__":
 AGGREGATION_SOURCES = ("csrc/gq_spmm.cu", "csrc/gq_common.cuh", "csrc/gq_internal.cuh", "../include/gq.h")
 
 
+def _code_only(text: str) -> str:
+    """C/C++ source without its comments, trailing blanks and blank lines
+    (string and character literals kept as written)."""
+    out, i, n = [], 0, len(text)
+    while i < n:
+        c = text[i]
+        if c in "\"'":
+            j = i + 1
+            while j < n and text[j] != c:
+                j += 2 if text[j] == "\\" else 1
+            out.append(text[i:j + 1])
+            i = j + 1
+        elif text.startswith("//", i):
+            j = text.find("\n", i)
+            i = n if j < 0 else j
+        elif text.startswith("/*", i):
+            j = text.find("*/", i + 2)
+            i = n if j < 0 else j + 2
+            out.append(" ")
+        else:
+            out.append(c)
+            i += 1
+    return "\n".join(line.rstrip() for line in "".join(out).split("\n") if line.strip())
+
+
 def source_digest(files=None) -> str:
-    """sha256 over the given sources (paths relative to this package; default:
-    every CUDA source and the public header), identifying the kernels a
-    profile was taken on."""
+    """sha256 over the code of the given sources, comments excluded (paths
+    relative to this package; default: every CUDA source and the public
+    header), identifying the kernels a profile was taken on."""
     import hashlib
     paths = sorted(_deps()) if files is None else sorted(os.path.normpath(os.path.join(HERE, f)) for f in files)
     h = hashlib.sha256()
     for p in paths:
         h.update(os.path.basename(p).encode())
-        with open(p, "rb") as f:
-            h.update(f.read())
+        with open(p, encoding="utf-8") as f:
+            h.update(_code_only(f.read()).encode())
     return h.hexdigest()[:16]

@@ -13,21 +13,27 @@
 // cuts every row of degree > hub_threshold into thread-block tasks (heaviest
 // first, so they start before the light rows); a row cut into several tasks
 // writes one partial row per task to the workspace and the last task to
-// finish (arrival ticket) adds them in task order.  Two kernels share it:
-//   - spmm_async_kernel (coefficient mode, d <= 512, every message row of one
-//     kind: all packed or all fp32).  A group of LG lanes walks a stream of
-//     edges (a slice of a heavy task, or one of the schedule's runs of
-//     consecutive light rows) and gathers message rows into a shared-memory
-//     ring with cp.async, kAS - 1 steps ahead of the step it consumes, so
-//     each SM keeps ~100 KB of gathers in flight.
-//   - spmm_kernel (attention weights, a mask mixing packed and fp32 rows, or
-//     d > 512).  A light row is one warp's job: lane groups of G lanes take
-//     one edge at a time, each lane owning 8 consecutive columns (CPL chunks
-//     of 8 for d > 256); edge metadata is loaded 32 edges at a time and
-//     broadcast with shuffles, and U edges per group are gathered before any
-//     is consumed.  A heavy task's 8 warps split its edges into contiguous
-//     streams (stream_row) whose partial rows are summed in shared memory in
-//     warp order.
+// finish (arrival ticket) adds them in task order.  Three kernels share it:
+//   - spmm_bulk_kernel (packed and fp32 rows mixed by a mask, or rows of
+//     mixed widths, 64 < d <= 256).  One warp per edge: the lane holding an
+//     edge's metadata copies the whole message row into a slot of the warp's
+//     shared-memory ring with one bulk copy onto the slot's mbarrier, and all
+//     32 lanes consume it.
+//   - spmm_async_kernel (d <= 512: rows of one kind, all packed or all fp32;
+//     packed and fp32 rows mixed by a mask; or rows of mixed widths for
+//     d <= 128).  A group of LG lanes walks a stream of edges (a slice of a
+//     heavy task, or one of the schedule's runs of consecutive light rows)
+//     and gathers message rows into a shared-memory ring with cp.async,
+//     kAS - 1 steps ahead of the step it consumes, so each SM keeps ~100 KB
+//     of gathers in flight.
+//   - spmm_kernel (attention weights, fp32 or 8-bit, or d > 512).  A light
+//     row is one warp's job: lane groups of G lanes take one edge at a time,
+//     each lane owning 8 consecutive columns (CPL chunks of 8 for d > 256);
+//     edge metadata is loaded 32 edges at a time and broadcast with
+//     shuffles, and U edges per group are gathered before any is consumed.
+//     A heavy task's 8 warps split its edges into contiguous streams
+//     (stream_row) whose partial rows are summed in shared memory in warp
+//     order.
 // Every sum runs in a fixed order, so results are identical run to run.
 #include <cuda_bf16.h>
 
