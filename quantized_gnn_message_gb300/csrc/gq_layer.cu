@@ -15,6 +15,12 @@
 //   5. dH_in = A^T-aggregation of the mixed messages (transposed CSR)
 // The quantizer is treated as the identity in backward (straight-through):
 // its codes are constants of the forward pass.
+//
+// The GAT layer (Tango Sec. 2.1, Fig. 1a / 1b) composes the GEMM with head
+// projections, the edge softmax, the optional 8-bit attention values (Tango
+// Sec. 3.3) and the multi-head SpMM forward; backward, the edge pass, the
+// transposed multi-head SpMM on the forward's weights, the node pass and
+// the two GEMMs.
 #include <cuda_bf16.h>
 
 #include "gq_common.cuh"

@@ -20,6 +20,10 @@
 // asymmetric quantizer (the page's values share one sign).  A warp per row
 // sums its terms in fp32, each lane keeps an fp64 total; block partials are
 // added in block order by a second kernel.
+//
+// assign_bits (AdaQP Sec. 4.2, Problems 10-12 on one device): each row's
+// width in {2, 4, 8} minimizing lam * beta / (2^b - 1)^2 + (1 - lam) * gamma
+// * d * b, in fp64 in a fixed operation order (ties to the fewer bits).
 #include "gq_common.cuh"
 #include "gq_internal.cuh"
 
