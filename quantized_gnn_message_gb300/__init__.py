@@ -91,6 +91,7 @@ def _SIGNATURES(P, I64, I, U64, F, S):
         ("gq_graph_prepare", [I64, I64, P, P, I, I, P, S, P, S, GP, P], I),
         ("gq_spmm_workspace_bytes", [GP, I, I], S),
         ("gq_dequant_spmm", [GP, I, I, P, I64, P, P, I, I, P, I64, P, S, P], I),
+        ("gq_dequant_spmm_noalloc", [GP, I, I, P, I64, P, P, I, I, P, I64, P], I),
         ("gq_edge_spmm", [GP, I, P, I, P, I64, P, P, I, I, P, I64, P, S, P], I),
         ("gq_gemm_bf16_nt", [P, I64, I, I64, P, I, I64, I, P, I64, P, P], I),
         ("gq_gemm_bf16_tn_workspace_bytes", [I64, I, I], S),
@@ -344,6 +345,22 @@ def dequant_spmm_mixed(g: Graph, X: torch.Tensor, packed: torch.Tensor, roff: to
     _check(L.gq_dequant_spmm_mixed(g.ref, 1 if transpose else 0, coef, _ptr(X), _rows(X), _ptr(packed), _ptr(roff),
                                    _ptr(rbits), d, _ptr(out), _rows(out), _ptr(ws), wb, _stream()),
            "gq_dequant_spmm_mixed")
+    return out
+
+
+def dequant_spmm_noalloc(g: Graph, X: torch.Tensor | None, packed: torch.Tensor | None,
+                         mask: torch.Tensor | None, d: int, bits: int, coef: int = COEF_GCN,
+                         transpose: bool = False, out: torch.Tensor | None = None) -> torch.Tensor:
+    """dequant_spmm without a workspace: its scratch is the library's fixed
+    array (gq_noalloc_scratch_bytes); larger needs raise GQError."""
+    _cuda(X, torch.float32, "X")
+    _cuda(packed, torch.uint8, "packed")
+    _cuda(mask, torch.uint8, "mask")
+    if out is None:
+        out = torch.empty(g.n, d, dtype=torch.float32, device=g.rowptr.device)
+    ldx = _rows(X) if X is not None else d
+    _check(lib().gq_dequant_spmm_noalloc(g.ref, int(transpose), coef, _ptr(X), ldx, _ptr(packed), _ptr(mask), d,
+                                         bits, _ptr(out), _rows(out), _stream()), "gq_dequant_spmm_noalloc")
     return out
 
 

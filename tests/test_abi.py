@@ -68,3 +68,48 @@ def test_argument_checks_without_launch(q):
     assert L.gq_graph_prepare(0, 0, fake, fake, 0, 0, fake, 0, fake, 0, None, None) == 1
     assert L.gq_status_string(3) == b"graph fails CSR validation"
     assert L.gq_dequant_spmm(None, 0, 0, None, 0, None, None, 16, 8, None, 16, None, 0, None) == 1
+
+
+def _declarations():
+    """{name: [parameter types]} of every GQ_API function in include/*.h."""
+    out = {}
+    for fn in os.listdir(os.path.join(ROOT, "include")):
+        if not fn.endswith(".h"):
+            continue
+        src = open(os.path.join(ROOT, "include", fn)).read()
+        src = re.sub(r"/\*.*?\*/", " ", src, flags=re.S)
+        for m in re.finditer(r"GQ_API\s+[\w\s\*]*?\b(gq_\w+)\s*\(([^)]*)\)\s*;", src):
+            params = " ".join(m.group(2).split())
+            out[m.group(1)] = [] if params in ("", "void") else [p.strip() for p in params.split(",")]
+    return out
+
+
+def _kind(c_param):
+    """Size and signedness class of a C parameter declaration."""
+    t = c_param.rsplit(" ", 1)[0] if " " in c_param else c_param
+    t = t.replace("const ", "").strip()
+    if "*" in c_param or t == "gq_stream":
+        return "pointer"
+    return {"int": "i32", "int32_t": "i32", "int64_t": "i64", "long long": "i64", "uint64_t": "u64",
+            "size_t": "u64", "float": "f32", "double": "f64"}.get(t, t)
+
+
+def test_binding_signatures_match_the_header(q):
+    import ctypes as C
+    decl = _declarations()
+    table = {name: args for name, args, _ in
+             q._SIGNATURES(C.c_void_p, C.c_int64, C.c_int, C.c_uint64, C.c_float, C.c_size_t)}
+    def ctype_kind(a):
+        if a in (C.c_float, C.c_double):
+            return "f32" if a is C.c_float else "f64"
+        if a is C.c_void_p or not hasattr(a, "_type_") or isinstance(a._type_, type):
+            return "pointer"  # c_void_p, POINTER(...)
+        signed = a(-1).value < 0
+        return ("i" if signed else "u") + str(8 * C.sizeof(a))
+    unbound = sorted(set(decl) - set(table))
+    assert not unbound, f"declared but not bound: {unbound}"
+    for name, args in table.items():
+        assert name in decl, f"{name} is bound but not declared"
+        want = [_kind(p) for p in decl[name]]
+        got = [ctype_kind(a) for a in args]
+        assert got == want, f"{name}: binding {got} vs header {want}"
