@@ -36,7 +36,9 @@
  *     16-byte aligned with a leading dimension that is a multiple of 4.
  *   - Graphs are CSR by DESTINATION: row v lists the sources u of the edges
  *     u -> v, in ascending order, int32.  Every node should carry its own
- *     self-loop (the "+ I" of A + I); the library does not add one.
+ *     self-loop (the "+ I" of A + I); the library does not add one.  On a
+ *     graph without edges, per-edge buffers (col, alpha, E_pre, attention
+ *     codes) are empty and may be NULL.
  *   - Errors: every call returns a gq_status.  Arguments are checked on the
  *     host before any launch; a failed check launches nothing.  A CUDA launch
  *     error is reported as GQ_ERR_CUDA.  No kernel traps or asserts.
