@@ -641,6 +641,8 @@ def main():
             else:
                 run_reference(args, w)
         return
+    if w.kind != "gcn" and dist_env()[0] > 1 and dist_env()[1] != 0:
+        return  # the GAT and sweep workloads run on one GPU (rank 0); their lines say n_gpus 1
     if w.kind == "gat":
         run_gat(args, w)
     elif w.kind == "aggregate":

@@ -34,3 +34,10 @@ def test_reference_arm_other_ranks_are_silent():
     out = _run(["--impl", "reference", "--steps", "1", "--warmup", "0"], {"RANK": "1", "WORLD_SIZE": "2",
                                                                            "LOCAL_RANK": "1"})
     assert out.strip() == ""
+
+
+def test_single_gpu_workloads_other_ranks_are_silent():
+    for wl in ("gat-rmat20-1m", "aggregate-rmat24-16.8m"):
+        out = _run(["--workload", wl, "--steps", "1", "--warmup", "0"], {"RANK": "1", "WORLD_SIZE": "2",
+                                                                         "LOCAL_RANK": "1"})
+        assert out.strip() == ""
