@@ -113,3 +113,32 @@ def test_binding_signatures_match_the_header(q):
         want = [_kind(p) for p in decl[name]]
         got = [ctype_kind(a) for a in args]
         assert got == want, f"{name}: binding {got} vs header {want}"
+
+
+def test_newer_entry_points_check_arguments_on_the_host(q):
+    # each call below is refused (1 = GQ_ERR_INVALID_ARG) or is an empty
+    # no-op (0) before any CUDA call, so it runs without a GPU
+    import ctypes as C
+    L = q.lib()
+    fake = C.c_void_p(0x1000)
+    # the width choice
+    assert L.gq_assign_bits(fake, None, 0, 8, 0.5, 1.0, fake, None) == 0
+    assert L.gq_assign_bits(fake, None, 10, 8, 1.5, 1.0, fake, None) == 1
+    assert L.gq_assign_bits(fake, None, 10, 8, 0.5, -1.0, fake, None) == 1
+    assert L.gq_assign_bits(fake, None, 10, 0, 0.5, 1.0, fake, None) == 1
+    assert L.gq_assign_bits(None, None, 10, 8, 0.5, 1.0, fake, None) == 1
+    # attention codes and the SpMM over them, without a graph
+    assert L.gq_quantize_edge_values(None, fake, 4, 0, fake, fake, None, 0, None) == 1
+    assert L.gq_dequant_edge_values(None, fake, fake, 4, fake, None) == 1
+    assert L.gq_edge_spmm_alpha8(None, fake, fake, 4, fake, 64, None, None, 64, 32, fake, 64, None, 0, None) == 1
+    # mixed widths: packed rows must be given and 16-byte aligned
+    assert L.gq_dequant_spmm_mixed(None, 0, 0, fake, 64, None, fake, fake, 64, fake, 64, None, 0, None) == 1
+    assert L.gq_dequant_spmm_mixed(None, 0, 0, fake, 64, C.c_void_p(0x1008), fake, fake, 64, fake, 64, None, 0,
+                                   None) == 1
+    # the GAT layer: alpha_bits other than 8 and 32, and codes without headers
+    g = q.Graph_t()
+    args = lambda ab, acode, ahdr: (C.byref(g), fake, 64, 64, fake, fake, fake, 4, 16, C.c_float(0.2), None, 32, 0,
+                                    ab, fake, fake, fake, fake, None, acode, ahdr, fake, fake, 1 << 20, None, None)
+    assert L.gq_gat_layer_fwd(*args(4, None, None)) == 1
+    assert L.gq_gat_layer_fwd(*args(8, fake, None)) == 1
+    assert L.gq_gat_layer_workspace_bytes(None, 64, 4, 16, 32, 8) == 0
