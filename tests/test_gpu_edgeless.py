@@ -3,7 +3,6 @@ of every edge kernel: the aggregations give zero rows, the edge softmax has
 nothing to score, the attention-value headers are {0, 0}, and the GAT layer's
 outputs and gradients are exactly zero (every sum over an empty edge set is
 exactly 0, and so is every product with it)."""
-import numpy as np
 import pytest
 import torch
 

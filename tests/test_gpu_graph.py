@@ -5,7 +5,7 @@ import pytest
 import torch
 
 import synth
-from gpu_helpers import gq, rmat_small, hub_graph
+from gpu_helpers import gq, hub_graph
 
 pytestmark = pytest.mark.gpu
 

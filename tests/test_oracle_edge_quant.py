@@ -6,7 +6,6 @@ quantizer's error bound |alpha^ - alpha| <= S (AdaQP Sec. 2.3), its
 unbiasedness over seeds (Eqn 6), and the codes it must give the segment's
 minimum and constant segments."""
 import numpy as np
-import pytest
 
 import synth
 

@@ -5,9 +5,8 @@ import json
 import os
 
 import numpy as np
-import pytest
 
-from test_oracle_graph import small_graph, dense_adj
+from test_oracle_graph import small_graph
 
 FX = json.load(open(os.path.join(os.path.dirname(__file__), "golden", "tango_gat_example.json")))
 RP = np.array(FX["rowptr"], np.int32)

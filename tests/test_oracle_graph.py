@@ -3,7 +3,6 @@ built from the pages' definitions (Sancus Sec. 2: A^ = D~^-1/2 (A+I) D~^-1/2;
 AdaQP Sec. 2.1 weighted sum), closed forms and finite differences."""
 import numpy as np
 import pytest
-import torch
 
 import synth
 

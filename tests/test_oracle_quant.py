@@ -10,7 +10,6 @@ import numpy as np
 import pytest
 
 import synth
-import torch
 
 GOLD = os.path.join(os.path.dirname(__file__), "golden")
 
