@@ -148,3 +148,28 @@ def test_gat_layer_with_quantized_alpha(orc):
     b0 = orc.gat_layer_bwd(rp, co, G, H, o["M"], o["Hp"], o["Epre"], o["alpha"], W, a_s, a_d, heads, 0.2,
                            bf16=False)
     assert abs(np.sum(b0["dM"] * o["M"]) - lhs) > 1e-6
+
+
+def test_quantized_gat_forward_is_unbiased(orc):
+    # AdaQP Eqn 6 for both quantizers at once: with 2-bit messages and 8-bit
+    # attention values the layer's output averaged over T seeds stays within
+    # a CLT bound of the unquantized layer.  (Independence of the two noise
+    # streams, which the alpha seed tag provides, is not what this checks:
+    # at equal indices the shared stream would correlate too few pairs here
+    # to move the mean past the bound.)
+    g = synth.rmat_graph(scale=6, n=60, n_draws=60 * 6, seed=8)
+    rp, co = g.rowptr.numpy(), g.col.numpy()
+    rng = np.random.default_rng(1)
+    heads, F, din = 2, 4, 5
+    H = rng.standard_normal((g.n, din))
+    W = rng.standard_normal((din, heads * F))
+    a_s, a_d = rng.standard_normal((heads, F)), rng.standard_normal((heads, F))
+    exact = orc.gat_layer_fwd(rp, co, H, W, a_s, a_d, heads, 0.2, bf16=False)["out"]
+    T = 1024
+    outs = np.stack([orc.gat_layer_fwd(rp, co, H, W, a_s, a_d, heads, 0.2, bits=2, seed=s, bf16=False,
+                                       alpha_bits=8)["out"] for s in range(T)])
+    sd = outs.std(axis=0)
+    # plus fp32 rounding: the quantized path works on fp32 H' and alpha (a
+    # one-edge row's min and max code deterministically, so they vary not at all)
+    assert np.all(np.abs(outs.mean(axis=0) - exact) <= 5 * sd / np.sqrt(T) + 1e-5 * (1 + np.abs(exact)))
+    assert sd.max() > 0
