@@ -387,7 +387,8 @@ def run_ours(args, w):
     line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None,
-            "dtype": "f32 accumulate; 2/4/8-bit message codes; bf16 tensor-core GEMM inputs",
+            "dtype": "f32",
+            "arithmetic": "f32 accumulation; 2/4/8-bit message codes; bf16 tensor-core GEMM inputs",
             "data": "synthetic",
             "config": {"workload": w.name, "nodes": g.n, "edges": g.nnz, "widths": list(w.widths),
                        "bits": bits_list, "marginal_fraction": w.mask_frac, "coefficients": "gcn",
@@ -474,7 +475,8 @@ def run_gat(args, w):
     step_ms = t_f + t_b
     line = {"metric": METRIC, "value": E / (step_ms / 1e3), "unit": UNIT, "n_gpus": 1, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": step_ms, "higher_is_better": True, "scaling": "weak",
-            "vs_baseline": None, "dtype": "f32 accumulate; bf16 tensor-core GEMM inputs", "data": "synthetic",
+            "vs_baseline": None, "dtype": "f32",
+            "arithmetic": "f32 accumulation; bf16 tensor-core GEMM inputs", "data": "synthetic",
             "config": {"workload": w.name, "nodes": n, "edges": E, "d_in": d_in, "heads": heads, "f": f,
                        "bits": bits, "alpha_bits": args.alpha_bits, "l2": "flushed before every timed call"},
             "stages_ms": {"layer_fwd": t_f, "layer_bwd": t_b, "edge_softmax": t_sm, "edge_spmm": t_sp,
@@ -584,7 +586,8 @@ def run_aggregate(args, w):
                 del pk
     line = {"metric": METRIC, "value": tot_edges / (tot_ms / 1e3), "unit": UNIT, "n_gpus": 1,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": tot_ms, "higher_is_better": True,
-            "scaling": "weak", "vs_baseline": None, "dtype": "f32 accumulate; 2/4/8-bit message codes",
+            "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+            "arithmetic": "f32 accumulation; 2/4/8-bit message codes",
             "data": "synthetic",
             "config": {"workload": w.name, "nodes": n, "edges": E, "sweep_d": ds, "bits": bl,
                        "generation_s": t_gen, "prepare_s": t_prep, "l2": "flushed before every timed call"},
