@@ -75,6 +75,8 @@ def _L():
                 "orc_header_offset": ([I, I], I64),
                 "orc_pitch": ([I, I], I64),
                 "orc_quantize": ([P, I64, I, I64, P, I, U64, P], None),
+                "orc_quantize_rows": ([P, I64, I, I64, P, I, U64, P], None),
+                "orc_spmm_rows": ([I64, P, P, I, I, I64, P, I64, P, P, I, P], I),
                 "orc_dequant": ([P, I64, I, I, P, P, I64], None),
                 "orc_codes": ([P, I64, I, I, P], None),
                 "orc_degree_norms": ([I64, P, P, P, P, P], None),
@@ -150,6 +152,19 @@ def quantize(X, mask, bits: int, seed: int, out: np.ndarray | None = None) -> np
     if out is None:
         out = np.zeros((n, pitch(d, bits)), dtype=np.uint8)
     _L().orc_quantize(_p(X), n, d, d, _p(m), bits, seed & 0xFFFFFFFFFFFFFFFF, _p(out))
+    return out
+
+
+def quantize_rows(X, ids, bits: int, seed: int) -> np.ndarray:
+    """The quantizer on a list of rows: row k of X is node ids[k], whose id
+    keys its noise, so the bytes equal rows ids[k] of quantize() on the
+    whole matrix.  Returns len(ids) x pitch bytes."""
+    X = _c(X, np.float32)
+    k, d = X.shape
+    ids = _c(ids, np.int64)
+    assert ids.shape == (k,)
+    out = np.zeros((k, pitch(d, bits)), dtype=np.uint8)
+    _L().orc_quantize_rows(_p(X), k, d, d, _p(ids), bits, seed & 0xFFFFFFFFFFFFFFFF, _p(out))
     return out
 
 
@@ -245,6 +260,28 @@ def spmm(rowptr, col, coef: int, M, transpose: bool = False) -> np.ndarray:
     Y = np.zeros((n, d), dtype=np.float64)
     f = _L().orc_spmm_t if transpose else _L().orc_spmm
     f(n, _p(rowptr), _p(col), coef, _p(M), d, _p(Y))
+    return Y
+
+
+def spmm_rows(rowptr, col, coef: int, rows, ids, M, transpose: bool = False) -> np.ndarray:
+    """spmm() evaluated at the output rows `rows` only (ascending node ids),
+    coefficients from the degrees of the whole graph.  M[i] is the message
+    row of node ids[i] (ids ascending); every node an output row reads must
+    be listed.  Returns len(rows) x d, float64."""
+    rowptr = _c(rowptr, np.int32)
+    col = _c(col, np.int32)
+    rows = _c(rows, np.int64)
+    ids = _c(ids, np.int64)
+    M = _c(M, np.float64)
+    n = rowptr.shape[0] - 1
+    d = M.shape[1]
+    assert M.shape[0] == ids.shape[0]
+    assert np.all(np.diff(rows) > 0) and np.all(np.diff(ids) > 0)
+    Y = np.zeros((rows.shape[0], d), dtype=np.float64)
+    rc = _L().orc_spmm_rows(n, _p(rowptr), _p(col), coef, 1 if transpose else 0, rows.shape[0], _p(rows),
+                            ids.shape[0], _p(ids), _p(M), d, _p(Y))
+    if rc != 0:
+        raise ValueError("spmm_rows: a message row the output rows read is not among ids")
     return Y
 
 

@@ -12,10 +12,10 @@
  *                Z = min(h), S = (max(h)-min(h))/(2^b-1), b in {2,4,8};
  *                Eqn 5 de-quantization h^ = q*S + Z;  Eqn 6 unbiasedness
  *      Sec. 3.1  only messages that cross the boundary are quantized
- *  - Sancus (IJCAI 2023, extended abstract), Sec. 2 Preliminaries:
- *      A^ = D~^{-1/2} (A+I) D~^{-1/2},  H' = sigma(A^ H W)
  *      Sec. 4.2  Problem 11's variance weight beta_k; Problems 10-12 (the
  *                width choice) on one device
+ *  - Sancus (IJCAI 2023, extended abstract), Sec. 2 Preliminaries:
+ *      A^ = D~^{-1/2} (A+I) D~^{-1/2},  H' = sigma(A^ H W)
  *  - Tango, "Rethinking quantization for graph neural network training on
  *    GPUs" (arXiv 2308.00890), Sec. 2.1 / Fig. 1: GAT as GEMM -> head
  *    projections -> SDDMM add -> LeakyReLU -> edge softmax -> SpMM, and the
@@ -28,7 +28,7 @@
  * be reproduced bit for bit.  Everything else takes fp32 inputs widened
  * exactly to double and accumulates in double, in the order of the CSR.
  *
- * Readings where the pages are silent (all listed in the design notes):
+ * Readings where the pages are silent:
  *  - the stochastic-rounding uniform u comes from a counter hash of
  *    (seed, row, col): MurmurHash3's published 32-bit finalizer "fmix32";
  *  - S is computed as an fp32 division, the code as floor((x-mn)*(1/S) + u)
@@ -88,38 +88,51 @@ int64_t orc_pitch(int d, int bits) { return (orc_header_offset(d, bits) + 8 + 15
 /* ------------------------------------------------------------------------ */
 /* AdaQP Sec. 2.3, Eqn 4: stochastic integer quantization of message rows    */
 /* ------------------------------------------------------------------------ */
-void orc_quantize(const float* X, int64_t n, int d, int64_t ldx, const uint8_t* mask,
-                  int bits, uint64_t seed, uint8_t* packed) {
+/* One message row x (node id r) quantized into `row` (pitch bytes). */
+static void quantize_row(const float* x, int d, int bits, uint64_t seed, int64_t r, uint8_t* row) {
   const int64_t pitch = orc_pitch(d, bits);
   const int64_t hoff = orc_header_offset(d, bits);
   const int levels = (1 << bits) - 1;
+  /* zero-point Z = min(h), range from max(h) */
+  float mn = x[0], mx = x[0];
+  for (int j = 1; j < d; ++j) {
+    if (x[j] < mn) mn = x[j];
+    if (x[j] > mx) mx = x[j];
+  }
+  float S = (mx - mn) / (float)levels;
+  memset(row, 0, (size_t)pitch);
+  for (int j = 0; j < d; ++j) {
+    int q = 0;
+    if (S >= FLT_MIN) { /* S == 0 or subnormal: the row codes as constant */
+      float inv = 1.0f / S;
+      float t = (x[j] - mn) * inv;                 /* (h - Z) / S          */
+      float v = t + orc_uniform(seed, (uint32_t)r, (uint32_t)j); /* + u    */
+      q = (int)floorf(v);                          /* round_st             */
+      if (q > levels) q = levels;
+    }
+    int64_t bit = (int64_t)j * bits;
+    row[bit / 8] |= (uint8_t)(q << (bit % 8));
+  }
+  memcpy(row + hoff, &S, 4);
+  memcpy(row + hoff + 4, &mn, 4);
+}
+
+void orc_quantize(const float* X, int64_t n, int d, int64_t ldx, const uint8_t* mask,
+                  int bits, uint64_t seed, uint8_t* packed) {
+  const int64_t pitch = orc_pitch(d, bits);
   for (int64_t r = 0; r < n; ++r) {
     if (mask && !mask[r]) continue;
-    const float* x = X + r * ldx;
-    uint8_t* row = packed + r * pitch;
-    /* zero-point Z = min(h), range from max(h) */
-    float mn = x[0], mx = x[0];
-    for (int j = 1; j < d; ++j) {
-      if (x[j] < mn) mn = x[j];
-      if (x[j] > mx) mx = x[j];
-    }
-    float S = (mx - mn) / (float)levels;
-    memset(row, 0, (size_t)pitch);
-    for (int j = 0; j < d; ++j) {
-      int q = 0;
-      if (S >= FLT_MIN) { /* S == 0 or subnormal: the row codes as constant */
-        float inv = 1.0f / S;
-        float t = (x[j] - mn) * inv;                 /* (h - Z) / S          */
-        float v = t + orc_uniform(seed, (uint32_t)r, (uint32_t)j); /* + u    */
-        q = (int)floorf(v);                          /* round_st             */
-        if (q > levels) q = levels;
-      }
-      int64_t bit = (int64_t)j * bits;
-      row[bit / 8] |= (uint8_t)(q << (bit % 8));
-    }
-    memcpy(row + hoff, &S, 4);
-    memcpy(row + hoff + 4, &mn, 4);
+    quantize_row(X + r * ldx, d, bits, seed, r, packed + r * pitch);
   }
+}
+
+/* The same quantizer on a list of rows: row k of X is node ids[k] (its id
+ * keys the noise), written to row k of `packed`.  Every listed row is
+ * quantized. */
+void orc_quantize_rows(const float* X, int64_t k, int d, int64_t ldx, const int64_t* ids, int bits,
+                       uint64_t seed, uint8_t* packed) {
+  const int64_t pitch = orc_pitch(d, bits);
+  for (int64_t i = 0; i < k; ++i) quantize_row(X + i * ldx, d, bits, seed, ids[i], packed + i * pitch);
 }
 
 /* Read code j of a packed row. */
@@ -224,6 +237,59 @@ void orc_spmm_t(int64_t n, const int32_t* rowptr, const int32_t* col, int coef, 
     }
   free(din);
   free(dout);
+}
+
+/* Both aggregations evaluated at a list of output rows only (the same
+ * definitions as orc_spmm / orc_spmm_t, coefficients from the degrees of the
+ * whole graph).  rows[0..k) are the output rows, ascending; the message rows
+ * are given for the node ids ids[0..m), ascending, as M[i] = message of node
+ * ids[i].  Forward: Y[i] = sum_{e = (u -> rows[i])} a_{u,rows[i]} M[u], in CSR
+ * order.  Transposed: Y[i] = sum_{e = (rows[i] -> v)} a_{rows[i],v} M[v], in
+ * the order of the destinations v.  Returns -1 if a needed message row is
+ * missing from ids, else 0. */
+static int64_t find_id(const int64_t* ids, int64_t m, int64_t x) {
+  int64_t lo = 0, hi = m;
+  while (lo < hi) {
+    int64_t mid = lo + (hi - lo) / 2;
+    if (ids[mid] < x) lo = mid + 1; else hi = mid;
+  }
+  return (lo < m && ids[lo] == x) ? lo : -1;
+}
+
+int orc_spmm_rows(int64_t n, const int32_t* rowptr, const int32_t* col, int coef, int transpose,
+                  int64_t k, const int64_t* rows, int64_t m, const int64_t* ids, const double* M, int d,
+                  double* Y) {
+  int64_t* din = (int64_t*)malloc(sizeof(int64_t) * (size_t)(n + 1));
+  int64_t* dout = (int64_t*)malloc(sizeof(int64_t) * (size_t)(n + 1));
+  int bad = 0;
+  degrees(n, rowptr, col, din, dout);
+  memset(Y, 0, sizeof(double) * (size_t)k * (size_t)d);
+  if (!transpose) {
+    for (int64_t i = 0; i < k; ++i) {
+      const int64_t v = rows[i];
+      for (int64_t e = rowptr[v]; e < rowptr[v + 1]; ++e) {
+        const int64_t u = col[e];
+        const int64_t at = find_id(ids, m, u);
+        if (at < 0) { bad = 1; continue; }
+        double a = coef_of(coef, din[v], dout[u]);
+        for (int j = 0; j < d; ++j) Y[i * d + j] += a * M[at * d + j];
+      }
+    }
+  } else {
+    for (int64_t v = 0; v < n; ++v)
+      for (int64_t e = rowptr[v]; e < rowptr[v + 1]; ++e) {
+        const int64_t u = col[e];
+        const int64_t i = find_id(rows, k, u);
+        if (i < 0) continue;
+        const int64_t at = find_id(ids, m, v);
+        if (at < 0) { bad = 1; continue; }
+        double a = coef_of(coef, din[v], dout[u]);
+        for (int j = 0; j < d; ++j) Y[i * d + j] += a * M[at * d + j];
+      }
+  }
+  free(din);
+  free(dout);
+  return bad ? -1 : 0;
 }
 
 /* ------------------------------------------------------------------------ */
