@@ -18,7 +18,9 @@ def _run(args, env_extra=None):
 
 
 def test_reference_arm_json_line():
-    out = _run(["--impl", "reference", "--steps", "1", "--warmup", "0"]).strip().splitlines()
+    # the 131,072-node workload keeps the graph generation on the CPU short
+    out = _run(["--impl", "reference", "--workload", "gcn3-rmat17-131k", "--steps", "1",
+                "--warmup", "0"]).strip().splitlines()
     line = json.loads(out[-1])
     for k in ("metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step", "higher_is_better", "scaling",
               "vs_baseline", "dtype", "data", "config", "cpu_baseline", "e2e"):
@@ -27,12 +29,13 @@ def test_reference_arm_json_line():
     assert line["n_gpus"] == 1 and line["steps"] == 1 and line["config"]["workload"] == "gcn3-rmat17-131k"
     assert line["value"] > 0 and line["cpu_baseline"]["value"] == line["value"] == line["e2e"]["value"]
     assert line["cpu_baseline"]["kind"] == "oracle" and line["cpu_baseline"]["cores"] >= 1
+    assert "scaled linearly" in line["cpu_baseline"]["sample"] and line["scaled_step_s"] > 0
     assert line["e2e"]["h2d_bytes_per_step"] == 0 and line["e2e"]["d2h_bytes_per_step"] == 0
 
 
 def test_reference_arm_other_ranks_are_silent():
-    out = _run(["--impl", "reference", "--steps", "1", "--warmup", "0"], {"RANK": "1", "WORLD_SIZE": "2",
-                                                                           "LOCAL_RANK": "1"})
+    out = _run(["--impl", "reference", "--workload", "gcn3-rmat17-131k", "--steps", "1", "--warmup", "0"],
+               {"RANK": "1", "WORLD_SIZE": "2", "LOCAL_RANK": "1"})
     assert out.strip() == ""
 
 
