@@ -33,7 +33,7 @@ def launches_bwd(bits: int, need_dinput: bool) -> int:
 
 class GCNStack:
     def __init__(self, g: Graph, widths, mask: torch.Tensor | None, coef: int = COEF_GCN,
-                 device="cuda"):
+                 device="cuda", keep_dA: bool = False):
         self.g = g
         self.widths = tuple(widths)
         self.L = len(widths) - 1
@@ -46,6 +46,9 @@ class GCNStack:
         self.H = [torch.empty(n, widths[l + 1], dtype=torch.float32, device=device) for l in range(self.L)]
         self.dH = [torch.empty(n, widths[l], dtype=torch.float32, device=device) for l in range(self.L)]
         self.dW = [torch.empty(widths[l], widths[l + 1], dtype=torch.float32, device=device) for l in range(self.L)]
+        # the backward's dA = dZ W^T of each layer (the messages it quantizes), kept on request
+        self.dA = [torch.empty(n, widths[l], dtype=torch.float32, device=device) if keep_dA else None
+                   for l in range(self.L)]
         self.err = torch.zeros(1, dtype=torch.int32, device=device)
         L = lib()
         self.ws.get(max(int(L.gq_gcn_layer_workspace_bytes(g.ref, widths[l], widths[l + 1], 2))
@@ -70,7 +73,7 @@ class GCNStack:
             ev = None if events is None else events[l]
             gcn_layer_bwd(self.g, g, self.A[l], self.H[l], Ws[l], self.mask, bits, seeds[l], self.act(l), need,
                           coef=self.coef, ws=self.ws, dW=self.dW[l], dH_in=self.dH[l] if need else None,
-                          dev_err=self.err, events=ev)
+                          dA_save=self.dA[l] if need else None, dev_err=self.err, events=ev)
             g = self.dH[l]
         return self.dW
 
