@@ -27,6 +27,8 @@
  *   - Pointers are DEVICE pointers owned by the caller unless a parameter
  *     says "host".  The library allocates no device memory: scratch comes
  *     from a caller buffer sized by the matching *_workspace_bytes query.
+ *     The one exception is gq_dequant_spmm_noalloc, whose scratch is a
+ *     fixed array compiled into the library (see there).
  *   - Every call is asynchronous on `stream` (a cudaStream_t; NULL is the
  *     legacy default stream) and performs no host<->device copy and no
  *     synchronization, except gq_graph_prepare, which synchronizes `stream`
@@ -43,7 +45,9 @@
  *     host before any launch; a failed check launches nothing.  A CUDA launch
  *     error is reported as GQ_ERR_CUDA.  No kernel traps or asserts.
  *   - Thread safety: no global mutable host state; calls on different
- *     streams may run concurrently if their buffers do not overlap.
+ *     streams may run concurrently if their buffers do not overlap, except
+ *     gq_dequant_spmm_noalloc, whose calls share one device array and must
+ *     not overlap on the GPU.
  */
 #ifndef GQ_H
 #define GQ_H
@@ -480,13 +484,17 @@ GQ_API int gq_gat_layer_bwd(const gq_graph* g, const float* dOut, const float* H
  * Its scratch is one fixed array of gq_noalloc_scratch_bytes() bytes (8 MiB)
  * compiled into the library, held on every GPU that loads the library until
  * the process exits.  The call allocates nothing.
- *   - The first call on a device looks up the array's address with that
- *     device current; make it before any stream capture.
+ *   - Each call looks up the array's address on the current device (a
+ *     host-side lookup).  Under CUDA's lazy module loading the first call on
+ *     a device may load the library's module and reserve the array there
+ *     (and can fail for lack of device memory, as any module load can);
+ *     make that first call before any stream capture.
  *   - All calls on a device share the array and find the previous call's
  *     contents in it; each call clears what must start at zero.  Calls that
  *     overlap on the GPU race on the array.
- *   - A graph and width whose scratch need (gq_spmm_workspace_bytes)
- *     exceeds the array return GQ_ERR_SCRATCH_LIMIT; nothing is launched.
+ *   - The arguments are checked as gq_dequant_spmm checks them; then a
+ *     graph and width whose scratch need (gq_spmm_workspace_bytes) exceeds
+ *     the array return GQ_ERR_SCRATCH_LIMIT.  Nothing is launched on error.
  * ---------------------------------------------------------------------- */
 GQ_API size_t gq_noalloc_scratch_bytes(void);
 GQ_API int gq_dequant_spmm_noalloc(const gq_graph* g, int transpose, int coef, const float* X,
@@ -547,6 +555,25 @@ GQ_API size_t gq_quant_error_workspace_bytes(void);
 GQ_API int gq_quant_error(const float* X, int64_t n, int d, int64_t ldx, const uint8_t* packed,
                           const uint8_t* mask, int bits, float eps, double* err, void* ws, size_t ws_bytes,
                           gq_stream stream);
+
+/* ------------------------------------------------------------------------
+ * gq_bits_for_error -- Tango Sec. 3.2, Eq. 4 and the rule built on it: the
+ * fewest bits whose relative quantization error Error_X stays below a
+ * threshold (Tango: 0.3, eps = 0.0005), chosen from 2, 4 and 8 (8 when none
+ * does).  One pass over X: for every row with mask[r] != 0 (mask NULL:
+ * every row) the codes gq_quantize_pack writes at each width with this seed
+ * (same fp32 operations, same noise), de-quantized by fmaf(q, S, Z), enter
+ * the three sums of gq_quant_error; nothing is written but the results.
+ * err3: NULL or three device doubles, Error_X at 2, 4 and 8 bits.  bits: one
+ * device int32, the chosen width.  ws: gq_bits_for_error_workspace_bytes()
+ * bytes (8-byte aligned).  Asynchronous; the caller reads *bits after a
+ * synchronization.  Errors: GQ_ERR_INVALID_ARG (null bits or X, d < 1,
+ * ldx < d, eps <= 0, threshold <= 0), GQ_ERR_WORKSPACE, GQ_ERR_CUDA.
+ * ---------------------------------------------------------------------- */
+GQ_API size_t gq_bits_for_error_workspace_bytes(void);
+GQ_API int gq_bits_for_error(const float* X, int64_t n, int d, int64_t ldx, const uint8_t* mask, uint64_t seed,
+                             double threshold, float eps, double* err3, int32_t* bits, void* ws, size_t ws_bytes,
+                             gq_stream stream);
 
 /* ------------------------------------------------------------------------
  * gq_selftest_bounded_wait -- no counterpart on the pages: a check of the

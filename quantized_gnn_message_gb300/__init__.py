@@ -121,6 +121,8 @@ def _SIGNATURES(P, I64, I, U64, F, S):
         ("gq_quant_error_workspace_bytes", [], S),
         ("gq_assign_bits", [P, P, I64, I, ctypes.c_double, ctypes.c_double, P, P], I),
         ("gq_quant_error", [P, I64, I, I64, P, P, I, F, P, P, S, P], I),
+        ("gq_bits_for_error_workspace_bytes", [], S),
+        ("gq_bits_for_error", [P, I64, I, I64, P, U64, ctypes.c_double, F, P, P, P, S, P], I),
     ]
 
 
@@ -483,13 +485,20 @@ def assign_bits(beta: torch.Tensor, d: int, lam: float, gamma: float, mask: torc
 
 
 def bits_for_error(X: torch.Tensor, mask: torch.Tensor | None, seed: int, threshold: float = 0.3,
-                   eps: float = 5e-4, choices=(2, 4, 8)) -> int:
-    """Tango's bit-count rule on the GPU: the fewest bits whose Error_X stays
-    below the threshold (the largest choice if none does)."""
-    for b in choices:
-        if float(quant_error(X, quantize_pack(X, mask, b, seed), mask, b, eps).item()) < threshold:
-            return b
-    return choices[-1]
+                   eps: float = 5e-4, err3: torch.Tensor | None = None) -> torch.Tensor:
+    """Tango's bit-count rule (gq_bits_for_error): the fewest of 2, 4, 8 bits
+    whose Error_X stays below the threshold, as a one-element int32 device
+    tensor; err3 (three float64) receives Error_X at each width if given."""
+    _cuda(X, torch.float32, "X")
+    _cuda(mask, torch.uint8, "mask")
+    _cuda(err3, torch.float64, "err3")
+    n, d = X.shape
+    L = lib()
+    ws = torch.empty(int(L.gq_bits_for_error_workspace_bytes()), dtype=torch.uint8, device=X.device)
+    bits = torch.empty(1, dtype=torch.int32, device=X.device)
+    _check(L.gq_bits_for_error(_ptr(X), n, d, _rows(X), _ptr(mask), seed & 0xFFFFFFFFFFFFFFFF, float(threshold),
+                               eps, _ptr(err3), _ptr(bits), _ptr(ws), ws.numel(), _stream()), "gq_bits_for_error")
+    return bits
 
 
 def selftest_bounded_wait(helper: int, complete: bool, limit_cycles: int, status: torch.Tensor):

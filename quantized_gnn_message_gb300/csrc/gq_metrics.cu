@@ -187,6 +187,95 @@ __global__ void sum_parts_kernel(const double* __restrict__ part, int blocks, do
 
 int error_blocks() { return sm_count() * 4; }
 
+// Error_X of the quantizer at 2, 4 and 8 bits in one pass over X, and
+// Tango's rule on top of it (Sec. 3.2, Eq. 4: the fewest bits whose error
+// stays below the threshold).  A warp per row: the row's min and max once,
+// then, per element, the noise u once and, for each width, the code the
+// quantizer writes (the same fp32 operations: S = (max - min) / (2^b - 1),
+// t = (x - Z) * (1/S), q = min(floor(t + u), 2^b - 1), Xq = fmaf(q, S, Z))
+// and the term |x - Xq| / (|x| + |Xq| + eps).  Sums as in quant_error_kernel:
+// fp32 per lane and row, fp64 across rows, block partials in block order.
+__global__ void __launch_bounds__(kMetricThreads) error3_kernel(const float* __restrict__ X, int64_t n, int d,
+                                                               int64_t ldx, const uint8_t* __restrict__ mask,
+                                                               uint32_t seed_key, float eps,
+                                                               double* __restrict__ part) {
+  __shared__ double red[3][kMetricWarps];
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  const int64_t gw = (blockIdx.x * (int64_t)blockDim.x + threadIdx.x) >> 5;
+  const int64_t nw = (gridDim.x * (int64_t)blockDim.x) >> 5;
+  double tot[3] = {0.0, 0.0, 0.0};
+  for (int64_t r = gw; r < n; r += nw) {
+    if (mask != nullptr && __ldg(mask + r) == 0) continue;
+    const float* x = X + r * ldx;
+    float mn = __ldg(x), mx = mn;
+    for (int j = lane; j < d; j += 32) {
+      const float v = __ldg(x + j);
+      mn = fminf(mn, v);
+      mx = fmaxf(mx, v);
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      mn = fminf(mn, __shfl_xor_sync(FULL, mn, o));
+      mx = fmaxf(mx, __shfl_xor_sync(FULL, mx, o));
+    }
+    float S[3], inv[3];
+    bool constant[3];
+#pragma unroll
+    for (int i = 0; i < 3; ++i) {
+      S[i] = __fdiv_rn(__fsub_rn(mx, mn), (float)((1u << (2 << i)) - 1u));
+      constant[i] = !(S[i] >= 1.17549435e-38f);
+      inv[i] = constant[i] ? 0.0f : __frcp_rn(S[i]);
+    }
+    const uint32_t kr = row_key(seed_key, (uint32_t)r);
+    float s[3] = {0.0f, 0.0f, 0.0f};
+    for (int j = lane; j < d; j += 32) {
+      const float v = __ldg(x + j);
+      const float u = noise_u(kr, (uint32_t)j);
+#pragma unroll
+      for (int i = 0; i < 3; ++i) {
+        uint32_t q = 0;
+        if (!constant[i]) {
+          const float t = __fmul_rn(__fsub_rn(v, mn), inv[i]);
+          q = __float_as_uint(__fadd_rd(__fadd_rn(t, u), 8388608.0f)) - 0x4B000000u;
+          q = min(q, (1u << (2 << i)) - 1u);
+        }
+        const float xq = __fmaf_rn((float)q, S[i], mn);
+        s[i] += fabsf(v - xq) / (fabsf(v) + fabsf(xq) + eps);
+      }
+    }
+#pragma unroll
+    for (int i = 0; i < 3; ++i) tot[i] += (double)s[i];
+  }
+#pragma unroll
+  for (int i = 0; i < 3; ++i) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) tot[i] += __shfl_xor_sync(FULL, tot[i], o);
+    if (lane == 0) red[i][w] = tot[i];
+  }
+  __syncthreads();
+  if (threadIdx.x < 3) {
+    double t = 0.0;
+    for (int k = 0; k < kMetricWarps; ++k) t += red[threadIdx.x][k];
+    part[(int64_t)threadIdx.x * gridDim.x + blockIdx.x] = t;
+  }
+}
+
+// err3[i] = the block partials of width 2 << i, in block order, / (n d);
+// *bits = the fewest of 2, 4, 8 whose error is below the threshold, else 8.
+__global__ void error3_finish_kernel(const double* __restrict__ part, int blocks, double inv_n, double threshold,
+                                     double* __restrict__ err3, int32_t* __restrict__ bits) {
+  if (blockIdx.x != 0 || threadIdx.x != 0) return;
+  int pick = 8;
+  for (int i = 2; i >= 0; --i) {
+    double t = 0.0;
+    for (int k = 0; k < blocks; ++k) t += part[(int64_t)i * blocks + k];
+    t *= inv_n;
+    if (err3 != nullptr) err3[i] = t;
+    if (t < threshold) pick = 2 << i;
+  }
+  *bits = pick;
+}
+
 // AdaQP Sec. 4.2, Problems 10-12 on one device: one device pair, so the
 // time objective is theta + gamma * sum_k d b_k with theta constant, and the
 // weighted sum with the variance objective separates per message.  Each row
@@ -288,5 +377,27 @@ extern "C" int gq_assign_bits(const float* beta, const uint8_t* mask, int64_t n,
   const int64_t cap = (int64_t)sm_count() * 8;
   if (blocks > cap) blocks = cap;
   assign_bits_kernel<<<(unsigned)blocks, 256, 0, (cudaStream_t)stream>>>(beta, mask, n, (double)d, lam, tw, rbits);
+  return launch_status();
+}
+
+extern "C" size_t gq_bits_for_error_workspace_bytes(void) {
+  return (size_t)3 * gq::error_blocks() * sizeof(double);
+}
+
+extern "C" int gq_bits_for_error(const float* X, int64_t n, int d, int64_t ldx, const uint8_t* mask, uint64_t seed,
+                                 double threshold, float eps, double* err3, int32_t* bits, void* ws, size_t ws_bytes,
+                                 gq_stream stream) {
+  using namespace gq;
+  if (bits == nullptr || n < 0 || d < 1 || ldx < d || !(eps > 0.0f) || !(threshold > 0.0) || threshold > 1e300)
+    return GQ_ERR_INVALID_ARG;
+  if (n > 0 && X == nullptr) return GQ_ERR_INVALID_ARG;
+  const int blocks = error_blocks();
+  if (ws == nullptr || ws_bytes < (size_t)3 * blocks * sizeof(double) || !aligned(ws, 8)) return GQ_ERR_WORKSPACE;
+  cudaStream_t s = (cudaStream_t)stream;
+  double* part = static_cast<double*>(ws);
+  error3_kernel<<<blocks, kMetricThreads, 0, s>>>(X, n, d, ldx, mask, seed_key_host(seed), eps, part);
+  GQ_TRY(launch_status());
+  const double inv_n = n > 0 ? 1.0 / ((double)n * (double)d) : 0.0;
+  error3_finish_kernel<<<1, 32, 0, s>>>(part, blocks, inv_n, threshold, err3, bits);
   return launch_status();
 }

@@ -73,13 +73,41 @@ def test_quant_error_empty_and_constant_rows(orc):
     assert float(q.quant_error(Xd, q.quantize_pack(Xd, None, 2, 1), None, 2).item()) == 0.0
 
 
-def test_bits_rule_matches_oracle(orc):
+@pytest.mark.parametrize("n,d,mask_frac", [(2000, 64, None), (777, 100, 0.5), (300, 1000, 0.8), (64, 3, None)])
+def test_bits_rule_matches_oracle(orc, n, d, mask_frac):
+    """Tango Sec. 3.2: the one-pass rule (gq_bits_for_error) gives the
+    oracle's Error_X at 2, 4 and 8 bits (1e-5 relative) and, wherever the
+    threshold is not within 1e-4 of an error, the oracle's choice of bits."""
     q = gq()
-    X = synth.normal_matrix(2000, 64, seed=8).numpy()
+    X = synth.normal_matrix(n, d, seed=8 + d).numpy()
+    mask = None if mask_frac is None else synth.bernoulli_mask(n, mask_frac, seed=3).numpy()
     Xd = torch.from_numpy(X).cuda()
-    errs = {b: orc.quant_error(X, orc.quantize(X, None, b, 5), None, b) for b in (2, 4, 8)}
-    for thr in (0.5, errs[2] * 0.999, errs[4] * 1.001, errs[4] * 0.999, 1e-6):
-        assert q.bits_for_error(Xd, None, 5, threshold=thr) == orc.bits_for_error(X, None, 5, threshold=thr)
+    md = None if mask is None else torch.from_numpy(mask).cuda()
+    errs = {b: orc.quant_error(X, orc.quantize(X, mask, b, 5), mask, b) for b in (2, 4, 8)}
+    e3 = torch.empty(3, dtype=torch.float64, device="cuda")
+    thrs = (0.5, errs[2] * 0.999, errs[2] * 1.001, errs[4] * 1.001, errs[4] * 0.999, errs[8] * 1.001, 1e-6)
+    for thr in thrs:
+        b = int(q.bits_for_error(Xd, md, 5, threshold=thr, err3=e3).item())
+        assert e3.cpu().numpy() == pytest.approx([errs[2], errs[4], errs[8]], rel=1e-5)
+        if all(abs(errs[k] - thr) > 1e-4 * thr for k in (2, 4, 8)):
+            assert b == orc.bits_for_error(X, mask, 5, threshold=thr), thr
+    # the same errors as gq_quant_error on the quantizer's own packed rows
+    for i, bb in enumerate((2, 4, 8)):
+        pk = q.quantize_pack(Xd, md, bb, 5)
+        assert float(q.quant_error(Xd, pk, md, bb).item()) == pytest.approx(float(e3[i].item()), rel=1e-6)
+
+
+def test_bits_rule_empty_and_constant(orc):
+    q = gq()
+    X0 = torch.zeros(0, 16, device="cuda")
+    e3 = torch.empty(3, dtype=torch.float64, device="cuda")
+    assert int(q.bits_for_error(X0, None, 1, err3=e3).item()) == 2 and float(e3.abs().max()) == 0.0
+    Xc = torch.full((10, 16), 2.5, device="cuda")  # constant rows: no error at any width
+    assert int(q.bits_for_error(Xc, None, 1, err3=e3).item()) == 2 and float(e3.abs().max()) == 0.0
+    with pytest.raises(q.GQError):
+        q.bits_for_error(Xc, None, 1, threshold=0.0)
+    with pytest.raises(q.GQError):
+        q.bits_for_error(Xc, None, 1, eps=0.0)
 
 
 def test_quant_error_rejects_bad_arguments():
