@@ -11,19 +11,23 @@
 //
 // Facts a caller must know (also in gq.h):
 //   - the array holds kNoallocScratchBytes (8 MiB) on every GPU that loads
-//     the library, until the process exits;
-//   - the first call on a device looks up the array's device address (with
-//     that device current); make that first call before any stream capture;
+//     the library, until the process exits.  With CUDA's lazy module
+//     loading the module that holds it may be loaded, and the array
+//     reserved, by the first call on a device; make that first call before
+//     any stream capture (it can fail for lack of device memory like any
+//     module load);
+//   - every call looks up the array's device address on the current device
+//     (a host-side lookup, no allocation), so the address stays right after
+//     a device reset or a new primary context;
 //   - every call on a device shares the one array, which keeps whatever the
 //     last call left in it.  The arrival counters are cleared at the start
 //     of each call; partial rows are written before they are read.  Calls
 //     that overlap on the GPU (different streams, no ordering) race on it;
-//   - a graph / width whose scratch need exceeds the array is rejected with
-//     GQ_ERR_SCRATCH_LIMIT before anything is launched;
+//   - the arguments are checked first (as gq_dequant_spmm checks them); a
+//     graph / width whose scratch need exceeds the array is then rejected
+//     with GQ_ERR_SCRATCH_LIMIT before anything is launched;
 //   - the call allocates nothing: no cudaMalloc, no cudaFree, no allocating
 //     library routine.
-#include <mutex>
-
 #include "gq_common.cuh"
 #include "gq_internal.cuh"
 
@@ -34,24 +38,13 @@ constexpr size_t kNoallocScratchBytes = (size_t)8 << 20;
 
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoallocScratchBytes];
 
-constexpr int kMaxDevices = 128;
-std::mutex g_scratch_mu;
-void* g_scratch_addr[kMaxDevices] = {};
-
-// Device address of g_noalloc_scratch on the current device, looked up once
-// per device.  In host code the array's name only stands in for the symbol;
-// this address is what a kernel can use.
+// Device address of g_noalloc_scratch on the current device.  In host code
+// the array's name only stands in for the symbol; this address is what a
+// kernel can use.
 int scratch_address(void** out) {
-  int dev = 0;
-  GQ_TRY_CUDA(cudaGetDevice(&dev));
-  if (dev < 0 || dev >= kMaxDevices) return GQ_ERR_UNSUPPORTED;
-  std::lock_guard<std::mutex> lock(g_scratch_mu);
-  if (g_scratch_addr[dev] == nullptr) {
-    void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr) return GQ_ERR_CUDA;
-    g_scratch_addr[dev] = p;
-  }
-  *out = g_scratch_addr[dev];
+  void* p = nullptr;
+  if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr) return GQ_ERR_CUDA;
+  *out = p;
   return GQ_OK;
 }
 
@@ -64,10 +57,10 @@ extern "C" int gq_dequant_spmm_noalloc(const gq_graph* g, int transpose, int coe
                                        const uint8_t* packed, const uint8_t* mask, int d, int bits, float* Y,
                                        int64_t ldy, gq_stream stream) {
   using namespace gq;
-  if (g == nullptr || d < 1) return GQ_ERR_INVALID_ARG;
+  GQ_TRY(spmm_check(g, X, ldx, packed, mask, d, bits, Y, ldy, nullptr));
+  if (spmm_workspace(g, transpose, d) > kNoallocScratchBytes) return GQ_ERR_SCRATCH_LIMIT;
   void* scratch = nullptr;
   GQ_TRY(scratch_address(&scratch));
-  if (spmm_workspace(g, transpose, d) > kNoallocScratchBytes) return GQ_ERR_SCRATCH_LIMIT;
   return dequant_spmm(g, transpose, coef, X, ldx, packed, mask, d, bits, Y, ldy, scratch, kNoallocScratchBytes,
                       (cudaStream_t)stream, nullptr);
 }

@@ -1471,9 +1471,9 @@ size_t ws_bytes_for(const gq_sched& sc, int d) {
   return ((size_t)sc.n_slots * d * sizeof(float) + 255) / 256 * 256 + (size_t)sc.n_groups * sizeof(int) + 256;
 }
 
-int spmm_setup(const gq_graph* g, int transpose, const float* X, int64_t ldx, const uint8_t* packed,
-               const uint8_t* mask, int d, int bits, float* Y, int64_t ldy, void* ws, size_t ws_bytes,
-               cudaStream_t s, SpmmParams& p, void* Yb = nullptr) {
+// The argument checks of the aggregation entry points (nothing launched).
+int spmm_check(const gq_graph* g, const float* X, int64_t ldx, const uint8_t* packed, const uint8_t* mask, int d,
+               int bits, const float* Y, int64_t ldy, const void* Yb) {
   if (g == nullptr || (Y == nullptr && Yb == nullptr) || d < 1 || ldy < d) return GQ_ERR_INVALID_ARG;
   if (!(bits == 32 || valid_bits(bits))) return GQ_ERR_INVALID_ARG;
   if (d > 1024) return GQ_ERR_UNSUPPORTED;
@@ -1487,6 +1487,13 @@ int spmm_setup(const gq_graph* g, int transpose, const float* X, int64_t ldx, co
   } else if (d % 4 != 0 || ldy % 4 != 0 || !aligned(Y, 16)) {
     return GQ_ERR_INVALID_ARG;
   }
+  return GQ_OK;
+}
+
+int spmm_setup(const gq_graph* g, int transpose, const float* X, int64_t ldx, const uint8_t* packed,
+               const uint8_t* mask, int d, int bits, float* Y, int64_t ldy, void* ws, size_t ws_bytes,
+               cudaStream_t s, SpmmParams& p, void* Yb = nullptr) {
+  GQ_TRY(spmm_check(g, X, ldx, packed, mask, d, bits, Y, ldy, Yb));
   p = SpmmParams{};
   p.rowptr = transpose ? g->tr_rowptr : g->rowptr;
   p.col = transpose ? g->tr_col : g->col;
