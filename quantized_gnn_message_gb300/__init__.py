@@ -479,7 +479,8 @@ def assign_bits(beta: torch.Tensor, d: int, lam: float, gamma: float, mask: torc
     n = beta.numel()
     if out is None:
         out = torch.empty(n, dtype=torch.uint8, device=beta.device)
-    _check(lib().gq_assign_bits(_ptr(beta.contiguous()), _ptr(mask), n, d, float(lam), float(gamma), _ptr(out),
+    beta = beta.contiguous()  # held until the call has been enqueued
+    _check(lib().gq_assign_bits(_ptr(beta), _ptr(mask), n, d, float(lam), float(gamma), _ptr(out),
                                 _stream()), "gq_assign_bits")
     return out
 
@@ -553,7 +554,8 @@ def gcn_layer_fwd(g: Graph, H_in: torch.Tensor, W: torch.Tensor, mask, bits: int
     L = lib()
     wb = int(L.gq_gcn_layer_workspace_bytes(g.ref, d_in, d_out, bits))
     buf = (ws or Workspace(dev)).get(wb)
-    _check(L.gq_gcn_layer_fwd(g.ref, coef, _ptr(H_in), _rows(H_in), d_in, _ptr(W.contiguous()), d_out, _ptr(mask),
+    W = W.contiguous()  # held until the call has been enqueued
+    _check(L.gq_gcn_layer_fwd(g.ref, coef, _ptr(H_in), _rows(H_in), d_in, _ptr(W), d_out, _ptr(mask),
                               bits, seed & 0xFFFFFFFFFFFFFFFF, act, _ptr(A_save), _rows(A_save), _ptr(H_out),
                               _rows(H_out), _ptr(buf), buf.numel(), _ptr(dev_err), _events(events), _stream()),
            "gq_gcn_layer_fwd")
@@ -574,11 +576,12 @@ def gcn_layer_bwd(g: Graph, dH_out: torch.Tensor, A_save: torch.Tensor, H_out: t
         dW = torch.empty(d_in, d_out, dtype=torch.float32, device=dev)
     if need_dinput and dH_in is None:
         dH_in = torch.empty(n, d_in, dtype=torch.float32, device=dev)
+    Wc = W.contiguous()  # held until the call has been enqueued
     L = lib()
     wb = int(L.gq_gcn_layer_workspace_bytes(g.ref, d_in, d_out, bits))
     buf = (ws or Workspace(dev)).get(wb)
     _check(L.gq_gcn_layer_bwd(g.ref, coef, _ptr(dH_out), _rows(dH_out), _ptr(A_save), _rows(A_save), _ptr(H_out),
-                              _rows(H_out) if H_out is not None else 0, _ptr(W.contiguous()), d_in, d_out,
+                              _rows(H_out) if H_out is not None else 0, _ptr(Wc), d_in, d_out,
                               _ptr(mask), bits, seed & 0xFFFFFFFFFFFFFFFF, act, int(need_dinput), _ptr(dW),
                               _ptr(dH_in), _rows(dH_in) if dH_in is not None else 0, _ptr(dA_save), _ptr(buf),
                               buf.numel(), _ptr(dev_err), _events(events), _stream()), "gq_gcn_layer_bwd")
@@ -598,7 +601,8 @@ def sddmm_edge_softmax(g: Graph, S: torch.Tensor, D: torch.Tensor, slope: float 
     Epre = torch.empty_like(alpha) if with_epre else None
     wb = int(lib().gq_edge_softmax_workspace_bytes(g.ref, heads))
     ws = torch.empty(max(wb, 1), dtype=torch.uint8, device=S.device)
-    _check(lib().gq_sddmm_edge_softmax(g.ref, _ptr(S.contiguous()), _ptr(D.contiguous()), heads, slope, _ptr(Epre),
+    S, D = S.contiguous(), D.contiguous()  # held until the call has been enqueued
+    _check(lib().gq_sddmm_edge_softmax(g.ref, _ptr(S), _ptr(D), heads, slope, _ptr(Epre),
                                        _ptr(alpha), _ptr(ws), wb, _stream()), "gq_sddmm_edge_softmax")
     return (alpha, Epre) if with_epre else alpha
 
@@ -616,7 +620,8 @@ def quantize_edge_values(g: Graph, alpha: torch.Tensor, seed: int):
     hdr = torch.empty(g.n, heads, 2, dtype=torch.float32, device=alpha.device)
     wb = int(lib().gq_quantize_edge_values_workspace_bytes(g.ref, heads))
     ws = torch.empty(max(wb, 1), dtype=torch.uint8, device=alpha.device)
-    _check(lib().gq_quantize_edge_values(g.ref, _ptr(alpha.contiguous()), heads, seed & 0xFFFFFFFFFFFFFFFF,
+    alpha = alpha.contiguous()  # held until the call has been enqueued
+    _check(lib().gq_quantize_edge_values(g.ref, _ptr(alpha), heads, seed & 0xFFFFFFFFFFFFFFFF,
                                          _ptr(codes), _ptr(hdr), _ptr(ws), wb, _stream()), "gq_quantize_edge_values")
     return codes, hdr
 

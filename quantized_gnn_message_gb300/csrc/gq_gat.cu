@@ -124,10 +124,11 @@ struct SoftmaxParams {
 // against the graph before it is walked, and each column id before its S
 // row is read; an invalid one is recorded in the graph status word
 // (kSoftmaxBadIndex) and the access is skipped (the row or task) or sent to
-// row 0 (a column id).  The column check is kept out of line.
+// row 0 (a column id), so no index read from memory can leave its buffer.
+// The column check is one unsigned compare on the common path (n < 2^31).
 constexpr int kSoftmaxBadIndex = 0x534D;
-__device__ __noinline__ int32_t sm_checked_col(int32_t x, int64_t n, int* err) {
-  if (x >= 0 && x < n) return x;
+__device__ __forceinline__ int32_t sm_checked_col(int32_t x, int64_t n, int* err) {
+  if ((uint32_t)x < (uint32_t)n) return x;
   atomicCAS(err, 0, kSoftmaxBadIndex);
   return 0;
 }
