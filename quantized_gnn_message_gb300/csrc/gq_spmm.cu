@@ -13,12 +13,11 @@
 // cuts every row of degree > hub_threshold into thread-block tasks (heaviest
 // first, so they start before the light rows); a row cut into several tasks
 // writes one partial row per task to the workspace and the last task to
-// finish (arrival ticket) adds them in task order.  Three kernels share it:
-//   - spmm_bulk_kernel (packed and fp32 rows mixed by a mask, or rows of
-//     mixed widths, 64 < d <= 256).  One warp per edge: the lane holding an
-//     edge's metadata copies the whole message row into a slot of the warp's
-//     shared-memory ring with one bulk copy onto the slot's mbarrier, and all
-//     32 lanes consume it.
+// finish (arrival ticket) adds them in task order.  Four kernels share it:
+//   - spmm_warp_kernel (packed and fp32 rows mixed by a mask, or fp32 rows
+//     alone, 64 < d <= 256).  One warp per edge; lane l owns 4 or 8
+//     columns and loads its part of the message row straight into
+//     registers, a few edges in flight per warp and many warps per SM.
 //   - spmm_async_kernel (d <= 512: rows of one kind, all packed or all fp32;
 //     packed and fp32 rows mixed by a mask; or rows of mixed widths for
 //     d <= 128).  A group of LG lanes walks a stream of edges (a slice of a
@@ -26,6 +25,10 @@
 //     and gathers message rows into a shared-memory ring with cp.async,
 //     kAS - 1 steps ahead of the step it consumes, so each SM keeps ~100 KB
 //     of gathers in flight.
+//   - spmm_bulk_kernel (rows of mixed widths, 128 < d <= 256).  One warp per
+//     edge: the lane holding an edge's metadata copies the whole message row
+//     into a slot of the warp's shared-memory ring with one bulk copy onto
+//     the slot's mbarrier, and all 32 lanes consume it.
 //   - spmm_kernel (attention weights, fp32 or 8-bit, or d > 512).  A light
 //     row is one warp's job: lane groups of G lanes take one edge at a time,
 //     each lane owning 8 consecutive columns (CPL chunks of 8 for d > 256);
@@ -1154,9 +1157,9 @@ __device__ __forceinline__ void bf_write(const SpmmParams& p, bool a_on, bool b_
 }
 
 // ---------------------------------------------------------------------------
-// Bulk-copy ring aggregation (coefficient modes, 64 < d <= 256).
+// Bulk-copy ring aggregation (rows of mixed widths, 64 < d <= 256).
 //
-// The same warp-per-edge consumption as the ring above, with the gathers
+// Warp-per-edge consumption as in spmm_warp_kernel, with the gathers
 // done by the bulk-copy engine: the lane that holds an edge's metadata
 // copies the whole message row (d*4 bytes of an fp32 row, or the packed row
 // with its header) into one of the warp's R shared-memory slots with a
@@ -1448,18 +1451,288 @@ int launch_bulk(const SpmmParams& p, cudaStream_t s) {
   return launch_status();
 }
 
-// 64 < d <= 256: mixed rows, all packed, or all fp32.
-int launch_bulk_any(const SpmmParams& p, int bits, cudaStream_t s) {
-  const bool mx = bits < 32 && p.mask != nullptr;
-  const bool wide = p.d > 128;
-#define GQ_BULK(B, M) return wide ? launch_bulk<B, 8, M, 4, 2>(p, s) : launch_bulk<B, 4, M, 8, 4>(p, s)
-  switch (bits) {
-    case 2: if (mx) GQ_BULK(2, true); GQ_BULK(2, false);
-    case 4: if (mx) GQ_BULK(4, true); GQ_BULK(4, false);
-    case 8: if (mx) GQ_BULK(8, true); GQ_BULK(8, false);
-    default: GQ_BULK(32, false);
+
+// ---------------------------------------------------------------------------
+// Warp-per-edge register aggregation (coefficient modes, 64 < d <= 256).
+//
+// The whole warp takes one edge at a time (so the packed-or-fp32 choice of
+// a mixing mask is uniform across it); lane l owns the C = 4 or 8 columns
+// [C l, C l + C) and loads its part of the gathered message row straight
+// into registers with plain loads: C b / 8 bytes of codes plus the row's
+// {S, Z}, or C floats.  U edges are loaded before any is consumed, and the
+// kernel keeps few registers so that many warps per SM cover the latency
+// (plain loads at high occupancy gather random rows several times faster
+// than the bulk-copy and cp.async rings above).  Per batch of 32 edges,
+// lane j loads edge j's column id, coefficient and kind once (the next
+// batch's column ids one batch ahead) and the warp broadcasts them with
+// shuffles; the kind rides in the sign of the coefficient.
+// De-quantization as in the kernels above: a (q S + Z) = (a S)(q - c) +
+// a (Z + c S), the code placed at bit offset o of the float 2^23 (one
+// bitwise op), one paired subtraction of 2^23 + c 2^o and a paired FMA
+// with a S 2^-o.
+// ---------------------------------------------------------------------------
+
+template <int BITS, bool MX, int C>
+struct WSlot {
+  static constexpr int NW = (BITS == 32 || MX) ? C : (C * BITS + 31) / 32;
+  uint32_t w[NW];
+  float2 h;
+};
+
+template <int C>
+struct WLane {
+  int c0;    // first owned column
+  int nv;    // owned columns inside the row (a multiple of 4)
+};
+
+template <int BITS, bool MX, int C>
+__device__ __forceinline__ void w_load(const SpmmParams& p, const WLane<C>& L, uint32_t x, bool packed,
+                                       WSlot<BITS, MX, C>& s) {
+  if constexpr (BITS < 32) {
+    if (!MX || packed) {
+      const uint8_t* row = p.packed + (size_t)x * (size_t)p.pitch;
+      s.h = __ldg(reinterpret_cast<const float2*>(row + p.hoff));
+      const uint8_t* pl = row + L.c0 * BITS / 8;
+      // the lane's C * BITS / 8 bytes (2 .. 8, aligned to their size); a
+      // partial last lane reads the same span, which stays inside the
+      // payload padded to 8 bytes
+      if constexpr (C * BITS == 64) {
+        const uint2 t = __ldg(reinterpret_cast<const uint2*>(pl));
+        s.w[0] = t.x;
+        s.w[1] = t.y;
+      } else if constexpr (C * BITS == 32) {
+        s.w[0] = __ldg(reinterpret_cast<const uint32_t*>(pl));
+      } else if constexpr (C * BITS == 16) {
+        s.w[0] = __ldg(reinterpret_cast<const uint16_t*>(pl));
+      } else {
+        s.w[0] = __ldg(pl);
+      }
+      return;
+    }
   }
-#undef GQ_BULK
+  if constexpr (BITS == 32 || MX) {
+    const float* xr = p.X + (size_t)x * (size_t)p.ldx + L.c0;
+#pragma unroll
+    for (int k = 0; k < C / 4; ++k) {
+      float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (4 * k < L.nv) a = ldg_f4(xr + 4 * k);
+      s.w[4 * k] = __float_as_uint(a.x); s.w[4 * k + 1] = __float_as_uint(a.y);
+      s.w[4 * k + 2] = __float_as_uint(a.z); s.w[4 * k + 3] = __float_as_uint(a.w);
+    }
+  }
+}
+
+// acc += cf * m over the lane's C columns (acc[i] holds columns 2i, 2i + 1).
+template <int BITS, bool MX, int C>
+__device__ __forceinline__ void w_consume(const WSlot<BITS, MX, C>& s, bool packed, float cf, f32x2 (&acc)[C / 2],
+                                          float& accz) {
+  if constexpr (BITS < 32) {
+    if (!MX || packed) {
+      constexpr float c = (float)(1 << (BITS - 1));
+      const float cs = cf * s.h.x;
+      accz = __fmaf_rn(cf, __fmaf_rn(c, s.h.x, s.h.y), accz);
+      if constexpr (BITS == 8) {
+        const f32x2 cs2 = f2_pack(cs, cs);
+        const f32x2 bias = f2_pack(-(kMagic + c), -(kMagic + c));
+#pragma unroll
+        for (int k = 0; k < C / 4; ++k) {
+          const uint32_t w = s.w[k];
+          const f32x2 v0 = f2_pack(__uint_as_float(__byte_perm(w, kMagicBits, 0x7540u)),
+                                   __uint_as_float(__byte_perm(w, kMagicBits, 0x7541u)));
+          const f32x2 v1 = f2_pack(__uint_as_float(__byte_perm(w, kMagicBits, 0x7542u)),
+                                   __uint_as_float(__byte_perm(w, kMagicBits, 0x7543u)));
+          acc[2 * k] = f2_fma(cs2, f2_add(v0, bias), acc[2 * k]);
+          acc[2 * k + 1] = f2_fma(cs2, f2_add(v1, bias), acc[2 * k + 1]);
+        }
+      } else {
+        // code i of the lane sits at bit BITS * i of w[0]; columns 2j, 2j + 1
+        // at offsets o0 = 2 j BITS and o0 + BITS within their 16-bit half
+        // word (a pair never straddles two halves), so q 2^o < 2^23
+        constexpr uint32_t M = (1u << BITS) - 1u;
+#pragma unroll
+        for (int j = 0; j < C / 2; ++j) {
+          const int o0 = (2 * j * BITS) & 15, o1 = o0 + BITS;
+          const uint32_t hw = (2 * j * BITS) >= 16 ? (s.w[0] >> 16) : s.w[0];
+          const f32x2 v = f2_pack(__uint_as_float(kMagicBits | (hw & (M << o0))),
+                                  __uint_as_float(kMagicBits | (hw & (M << o1))));
+          const f32x2 bias = f2_pack(-(kMagic + c * (float)(1 << o0)), -(kMagic + c * (float)(1 << o1)));
+          const f32x2 sc = f2_pack(cs * (1.0f / (float)(1 << o0)), cs * (1.0f / (float)(1 << o1)));
+          acc[j] = f2_fma(sc, f2_add(v, bias), acc[j]);
+        }
+      }
+      return;
+    }
+  }
+  if constexpr (BITS == 32 || MX) {
+    const f32x2 c2 = f2_pack(cf, cf);
+#pragma unroll
+    for (int k = 0; k < C / 2; ++k)
+      acc[k] = f2_fma(c2, f2_pack(__uint_as_float(s.w[2 * k]), __uint_as_float(s.w[2 * k + 1])), acc[k]);
+  }
+}
+
+// The lane's columns of (acc + accz) * rs to row r of Y / Yb, or to the
+// fp32 partial row `part`.
+template <int C>
+__device__ __forceinline__ void w_flush(const SpmmParams& p, const WLane<C>& L, int64_t r, float rs, float* part,
+                                        const f32x2 (&acc)[C / 2], float accz) {
+#pragma unroll
+  for (int k = 0; k < C / 4; ++k) {
+    if (4 * k < L.nv) {
+      const float2 u = f2_unpack(acc[2 * k]), v = f2_unpack(acc[2 * k + 1]);
+      const float o0 = (u.x + accz) * rs, o1 = (u.y + accz) * rs, o2 = (v.x + accz) * rs, o3 = (v.y + accz) * rs;
+      const int col = L.c0 + 4 * k;
+      if (part != nullptr)
+        st_f4(part + col, o0, o1, o2, o3);
+      else if (p.Yb != nullptr)
+        *reinterpret_cast<uint2*>(p.Yb + r * p.ldy + col) = make_uint2(pack_bf16x2(o0, o1), pack_bf16x2(o2, o3));
+      else
+        st_f4(p.Y + r * p.ldy + col, o0, o1, o2, o3);
+    }
+  }
+}
+
+// The coefficient of gathered row x with the row's kind in its sign bit
+// (set: a packed row of a mixing mask); coefficients are >= 0.
+template <int BITS, bool MX>
+__device__ __forceinline__ float w_cfk(const SpmmParams& p, uint32_t x) {
+  const float cf = p.colscale != nullptr ? __ldg(p.colscale + x) : 1.0f;
+  if (MX && __ldg(p.mask + x) != 0) return __uint_as_float(__float_as_uint(cf) | 0x80000000u);
+  return cf;
+}
+__device__ __forceinline__ bool w_packed_kind(float cfk) { return (__float_as_uint(cfk) >> 31) != 0; }
+__device__ __forceinline__ float w_coef(float cfk) { return __uint_as_float(__float_as_uint(cfk) & 0x7fffffffu); }
+
+// Stream the edges [eb, ee).  LIGHT: the edges of rows [row0, row1), each
+// row written once its last edge is consumed; otherwise the sums are left
+// in acc / accz.
+template <int BITS, bool MX, int C, int U, bool LIGHT>
+__device__ __forceinline__ void w_stream(const SpmmParams& p, const WLane<C>& L, int eb, int ee, int row0, int row1,
+                                         f32x2 (&acc)[C / 2], float& accz) {
+  const int lane = threadIdx.x & 31;
+  const int32_t* __restrict__ col = p.col;
+  uint32_t xn = eb + lane < ee ? (uint32_t)__ldg(col + eb + lane) : 0u;  // column ids of the next batch
+  int row = row0, rend = 0x7fffffff, rnext = 0x7fffffff;
+  float rs = 1.0f, rsn = 1.0f;
+  if (LIGHT) {
+    rend = __ldg(p.rowptr + row0 + 1);
+    rnext = row0 + 1 < row1 ? __ldg(p.rowptr + row0 + 2) : 0x7fffffff;
+    if (p.rowscale) {
+      rs = __ldg(p.rowscale + row0);
+      rsn = row0 + 1 < row1 ? __ldg(p.rowscale + row0 + 1) : 1.0f;
+    }
+  }
+  for (int base = eb; base < ee; base += 32) {
+    const uint32_t xb = xn;
+    const float cb = base + lane < ee ? w_cfk<BITS, MX>(p, xb) : 1.0f;
+    xn = base + 32 + lane < ee ? (uint32_t)__ldg(col + base + 32 + lane) : 0u;
+    const int cnt = min(32, ee - base);
+    for (int t0 = 0; t0 < cnt; t0 += U) {
+      WSlot<BITS, MX, C> m[U];
+      float cf[U];
+#pragma unroll
+      for (int t = 0; t < U; ++t) {
+        const uint32_t x = __shfl_sync(FULL, xb, (t0 + t) & 31);
+        cf[t] = __shfl_sync(FULL, cb, (t0 + t) & 31);
+        if (t0 + t < cnt && L.nv > 0) w_load<BITS, MX, C>(p, L, x, w_packed_kind(cf[t]), m[t]);
+      }
+#pragma unroll
+      for (int t = 0; t < U; ++t) {
+        if (t0 + t < cnt) {
+          if (LIGHT) {
+            while (base + t0 + t >= rend) {
+              if (L.nv > 0) w_flush<C>(p, L, row, rs, nullptr, acc, accz);
+#pragma unroll
+              for (int i = 0; i < C / 2; ++i) acc[i] = 0ull;
+              accz = 0.0f;
+              ++row;
+              rend = rnext;
+              rnext = row + 1 < row1 ? __ldg(p.rowptr + row + 2) : 0x7fffffff;
+              rs = rsn;
+              if (p.rowscale) rsn = row + 1 < row1 ? __ldg(p.rowscale + row + 1) : 1.0f;
+            }
+          }
+          if (L.nv > 0) w_consume<BITS, MX, C>(m[t], w_packed_kind(cf[t]), w_coef(cf[t]), acc, accz);
+        }
+      }
+    }
+  }
+  if (LIGHT) {
+    for (; row < row1; ++row) {
+      if (L.nv > 0) w_flush<C>(p, L, row, p.rowscale ? __ldg(p.rowscale + row) : 1.0f, nullptr, acc, accz);
+#pragma unroll
+      for (int i = 0; i < C / 2; ++i) acc[i] = 0ull;
+      accz = 0.0f;
+    }
+  }
+}
+
+template <int BITS, bool MX, int C, int U, int MINB>
+__global__ void __launch_bounds__(kSpmmThreads, MINB) spmm_warp_kernel(const SpmmParams p) {
+  extern __shared__ __align__(16) float wpart[];  // [kSpmmWarps][d] for heavy rows
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  WLane<C> L;
+  L.c0 = C * lane;
+  L.nv = min(C, max(0, p.d - L.c0));
+  f32x2 acc[C / 2];
+#pragma unroll
+  for (int i = 0; i < C / 2; ++i) acc[i] = 0ull;
+  float accz = 0.0f;
+  if ((int64_t)blockIdx.x < p.n_tasks) {
+    const int4 task = __ldg(reinterpret_cast<const int4*>(p.tasks) + blockIdx.x);
+    const int len = task.z - task.y;
+    const int chunk = (len + kSpmmWarps - 1) / kSpmmWarps;
+    const int b0 = min(task.y + w * chunk, task.z);
+    const int b1 = min(b0 + chunk, task.z);
+    if (b0 < b1) w_stream<BITS, MX, C, U, false>(p, L, b0, b1, 0, 0, acc, accz);
+    if (L.nv > 0) w_flush<C>(p, L, 0, 1.0f, wpart + w * p.d, acc, accz);
+    __syncthreads();
+    finish_heavy(p, task, wpart);
+    return;
+  }
+  const int64_t gw = ((int64_t)blockIdx.x - p.n_tasks) * kSpmmWarps + w;
+  const int64_t nw = ((int64_t)gridDim.x - p.n_tasks) * kSpmmWarps;
+  for (int64_t t = gw; t < p.n_light; t += nw) {
+    const int2 run = __ldg(reinterpret_cast<const int2*>(p.light) + t);
+    const int eb = __ldg(p.rowptr + run.x), ee = __ldg(p.rowptr + run.y);
+    w_stream<BITS, MX, C, U, true>(p, L, eb, ee, run.x, run.y, acc, accz);
+  }
+}
+
+template <int BITS, bool MX, int C, int U, int MINB>
+int launch_warp(const SpmmParams& p, cudaStream_t s) {
+  if (p.d > 32 * C || p.d % 4 != 0) return GQ_ERR_UNSUPPORTED;
+  const size_t smem = sizeof(float) * kSpmmWarps * p.d;
+  auto kern = spmm_warp_kernel<BITS, MX, C, U, MINB>;
+  int per_sm = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kSpmmThreads, smem) != cudaSuccess || per_sm < 1)
+    return GQ_ERR_UNSUPPORTED;
+  int64_t light = (int64_t)sm_count() * per_sm;
+  const int64_t need = (p.n_light + kSpmmWarps - 1) / kSpmmWarps;
+  if (light > need) light = need;
+  if (light < 1) light = 1;
+  const int64_t grid = p.n_tasks + light;
+  if (grid > 0x7fffffff) return GQ_ERR_UNSUPPORTED;
+  kern<<<(unsigned)grid, kSpmmThreads, smem, s>>>(p);
+  return launch_status();
+}
+
+// 64 < d <= 256 on the warp-per-edge register kernel: 4 columns per lane and
+// 4 edges in flight up to d = 128, 8 columns and 2 edges above; 4 blocks
+// per SM (each measured the fastest of its range on the large GCN graph).
+template <int BITS, bool MX>
+int launch_warp_d(const SpmmParams& p, cudaStream_t s) {
+  return p.d <= 128 ? launch_warp<BITS, MX, 4, 4, 4>(p, s) : launch_warp<BITS, MX, 8, 2, 4>(p, s);
+}
+
+int launch_warp_any(const SpmmParams& p, int bits, cudaStream_t s) {
+  const bool mx = bits < 32 && p.mask != nullptr;
+  switch (bits) {
+    case 2: return mx ? launch_warp_d<2, true>(p, s) : launch_warp_d<2, false>(p, s);
+    case 4: return mx ? launch_warp_d<4, true>(p, s) : launch_warp_d<4, false>(p, s);
+    case 8: return mx ? launch_warp_d<8, true>(p, s) : launch_warp_d<8, false>(p, s);
+    default: return launch_warp_d<32, false>(p, s);
+  }
 }
 
 
@@ -1546,11 +1819,12 @@ int dequant_spmm(const gq_graph* g, int transpose, int coef, const float* X, int
   } else if (coef != GQ_COEF_ONE) {
     return GQ_ERR_INVALID_ARG;
   }
-  // mixed packed / fp32 rows with 64 < d <= 256: bulk-copy ring, warp per
-  // edge; otherwise, d <= 512 and an fp32 row stride under 2^31 bytes:
-  // asynchronous ring pipeline; otherwise warp per light row
-  if (bits < 32 && mask != nullptr && d > 64 && d <= 256 && ldx <= (int64_t)1 << 29)
-    return launch_bulk_any(p, bits, s);
+  // packed and fp32 rows mixed by a mask, or fp32 rows alone, with
+  // 64 < d <= 256: warp per edge, plain loads into registers; otherwise,
+  // d <= 512 and an fp32 row stride under 2^31 bytes: asynchronous ring
+  // pipeline; otherwise warp per light row
+  if ((bits == 32 || mask != nullptr) && d > 64 && d <= 256 && ldx <= (int64_t)1 << 29)
+    return launch_warp_any(p, bits, s);
   if (d <= 512 && ldx <= (int64_t)1 << 29) return launch_async_any(p, bits, s);
   return launch_any<0>(p, bits, s);
 }
