@@ -36,6 +36,10 @@ constexpr int kTileM = 128;
 constexpr int kChunkK = 64;                       // bf16 elements per 128-byte swizzle row
 constexpr int kATileBytes = kTileM * kChunkK * 2;  // 16 KB
 constexpr int kSmemBudget = 225 * 1024;
+// epilogue staging: per epilogue warp, 32 rows x 16 columns of fp32 at a row
+// pitch of 20 floats (conflict-free 16-byte writes by row)
+constexpr int kStgPitch = 20;
+constexpr int kStgBytes = 4 * 32 * kStgPitch * 4;
 
 // ---------------------------------------------------------------- host ---
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
@@ -103,6 +107,7 @@ __global__ void __launch_bounds__(kRgThreads, 1)
   uint64_t* tempty = tfull + 2;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tempty + 2);
   volatile int* abort = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  float* stg_all = reinterpret_cast<float*>(sA + (size_t)p.stages * kATileBytes + 256);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
@@ -187,6 +192,7 @@ __global__ void __launch_bounds__(kRgThreads, 1)
   } else {
     const int q = warp & 3;
     const int row_in_tile = q * 32 + lane;
+    float* stg = stg_all + q * 32 * kStgPitch;
     int i = 0;
     for (int64_t t = blockIdx.x; t < ntiles; t += gridDim.x, ++i) {
       const int a = i & 1;
@@ -211,13 +217,25 @@ __global__ void __launch_bounds__(kRgThreads, 1)
           v[j] = __uint_as_float(r[j]);
           if (p.act == GQ_ACT_RELU) v[j] = fmaxf(v[j], 0.0f);
         }
-        if (live) {
-          if (p.vec && c0 + 16 <= p.N) {
+        if (p.vec && c0 + 16 <= p.N) {
+          // through shared memory, so that each store instruction writes 8
+          // rows x 64 contiguous bytes instead of 32 rows x 16 bytes
 #pragma unroll
-            for (int j = 0; j < 16; j += 4) st_f4(crow + c0 + j, v[j], v[j + 1], v[j + 2], v[j + 3]);
-          } else {
-            for (int j = 0; j < 16 && c0 + j < p.N; ++j) crow[c0 + j] = v[j];
+          for (int j = 0; j < 16; j += 4)
+            *reinterpret_cast<float4*>(stg + lane * kStgPitch + j) = make_float4(v[j], v[j + 1], v[j + 2], v[j + 3]);
+          __syncwarp();
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            const int rr = 8 * k + (lane >> 2), cg = 4 * (lane & 3);
+            const int64_t grow = t * kTileM + q * 32 + rr;
+            const float4 o = *reinterpret_cast<const float4*>(stg + rr * kStgPitch + cg);
+            if (grow < p.M) *reinterpret_cast<float4*>(p.C + grow * p.ldc + c0 + cg) = o;
           }
+          __syncwarp();
+        } else if (live) {
+          for (int j = 0; j < 16 && c0 + j < p.N; ++j) crow[c0 + j] = v[j];
+        }
+        if (live) {
           if (p.S != nullptr && c0 < p.N) {
 #pragma unroll
             for (int j = 0; j < 16; ++j) {
@@ -468,7 +486,7 @@ int row_gemm(const void* A, int64_t M, int K, int64_t lda, const void* B, int N,
   p.K = K;
   p.kch = (K + kChunkK - 1) / kChunkK;
   const int b_bytes = p.kch * p.Npad * 128;
-  p.stages = (kSmemBudget - 2048 - b_bytes) / kATileBytes;
+  p.stages = (kSmemBudget - 2048 - b_bytes - kStgBytes) / kATileBytes;
   if (p.stages > 8) p.stages = 8;
   if (p.stages < 2) return GQ_ERR_UNSUPPORTED;
   p.tmem_cols = pow2_at_least(2 * (uint32_t)p.Npad);
@@ -487,7 +505,7 @@ int row_gemm(const void* A, int64_t M, int K, int64_t lda, const void* B, int N,
   CUtensorMap tmA, tmB;
   GQ_TRY(make_tmap(&tmA, A, (uint64_t)K, (uint64_t)M, (uint64_t)lda, kChunkK, kTileM));
   GQ_TRY(make_tmap(&tmB, B, (uint64_t)K, (uint64_t)N, (uint64_t)ldb, kChunkK, (uint32_t)p.Npad));
-  const size_t smem = 1024 + (size_t)b_bytes + (size_t)p.stages * kATileBytes + 256;
+  const size_t smem = 1024 + (size_t)b_bytes + (size_t)p.stages * kATileBytes + 256 + kStgBytes;
   GQ_TRY_CUDA(cudaFuncSetAttribute(row_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem));
   const int64_t ntiles = (M + kTileM - 1) / kTileM;
   const int grid = (int)(ntiles < sm_count() ? ntiles : sm_count());
