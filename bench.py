@@ -463,7 +463,7 @@ def run_ours(args, w):
     for (name, l, b), times in stage_ms.items():
         stage_summary.setdefault(name, 0.0)
         stage_summary[name] += sum(times) / args.steps
-    roofline = {"kernel": "spmm_bulk_kernel (de-quantizing aggregation, forward and transposed)",
+    roofline = {"kernel": "spmm_warp_kernel (de-quantizing aggregation, forward and transposed)",
                 "bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
                 "peak_source": f"hbm_gbs of {peak_kind}",
                 "traffic": traffic,
@@ -554,8 +554,10 @@ def largest_aggregation(args, dev, q, flush, d=256, bits=8):
     t_setup = time.perf_counter() - t0
     n, E = g.n, g.nnz
     with ClockSampler(dev.index or 0) as clocks:
+        torch.cuda.profiler.start()
         tf = _timed(lambda: q.dequant_spmm(G, None, pk, None, d, bits, out=Y), args.steps, flush)
         tb = _timed(lambda: q.dequant_spmm(G, None, pk, None, d, bits, transpose=True, out=Y), args.steps, flush)
+        torch.cuda.profiler.stop()
     if int(G.status.cpu()[0]) != 0:
         raise RuntimeError(f"aggregation status word {int(G.status.cpu()[0]):#x}")
     pitch = q.packed_pitch(d, bits)
