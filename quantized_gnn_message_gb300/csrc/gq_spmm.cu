@@ -1606,11 +1606,12 @@ __device__ __forceinline__ float w_coef(float cfk) { return __uint_as_float(__fl
 // Stream the edges [eb, ee).  LIGHT: the edges of rows [row0, row1), each
 // row written once its last edge is consumed; otherwise the sums are left
 // in acc / accz.
-template <int BITS, bool MX, int C, int U, bool LIGHT>
+template <int BITS, bool MX, int C, int U, bool LIGHT, int EW>
 __device__ __forceinline__ void w_stream(const SpmmParams& p, const WLane<C>& L, int eb, int ee, int row0, int row1,
                                          f32x2 (&acc)[C / 2], float& accz) {
   const int lane = threadIdx.x & 31;
   const int32_t* __restrict__ col = p.col;
+  const int head = EW ? (L.c0 >> p.fshift) : 0;  // the lane's columns lie in one head (F >= 16 >= C)
   uint32_t xn = eb + lane < ee ? (uint32_t)__ldg(col + eb + lane) : 0u;  // column ids of the next batch
   int row = row0, rend = 0x7fffffff, rnext = 0x7fffffff;
   float rs = 1.0f, rsn = 1.0f;
@@ -1624,16 +1625,25 @@ __device__ __forceinline__ void w_stream(const SpmmParams& p, const WLane<C>& L,
   }
   for (int base = eb; base < ee; base += 32) {
     const uint32_t xb = xn;
+    // coefficient (edge-weight modes: +-1) with the row's kind in its sign bit
     const float cb = base + lane < ee ? w_cfk<BITS, MX>(p, xb) : 1.0f;
+    // edge-weight modes: the CSR edge id of each edge of the batch
+    const int32_t eidb = EW && p.eperm != nullptr && base + lane < ee ? __ldg(p.eperm + base + lane) : base + lane;
     xn = base + 32 + lane < ee ? (uint32_t)__ldg(col + base + 32 + lane) : 0u;
     const int cnt = min(32, ee - base);
     for (int t0 = 0; t0 < cnt; t0 += U) {
       WSlot<BITS, MX, C> m[U];
       float cf[U];
+      float aw[U];  // edge-weight modes: the attention weight of the lane's head
 #pragma unroll
       for (int t = 0; t < U; ++t) {
         const uint32_t x = __shfl_sync(FULL, xb, (t0 + t) & 31);
         cf[t] = __shfl_sync(FULL, cb, (t0 + t) & 31);
+        aw[t] = 0.0f;
+        if (EW) {
+          const int32_t eid = __shfl_sync(FULL, eidb, (t0 + t) & 31);
+          if (t0 + t < cnt && L.nv > 0) aw[t] = __ldg(p.alpha + (int64_t)eid * p.heads + head);
+        }
         if (t0 + t < cnt && L.nv > 0) w_load<BITS, MX, C>(p, L, x, w_packed_kind(cf[t]), m[t]);
       }
 #pragma unroll
@@ -1652,7 +1662,7 @@ __device__ __forceinline__ void w_stream(const SpmmParams& p, const WLane<C>& L,
               if (p.rowscale) rsn = row + 1 < row1 ? __ldg(p.rowscale + row + 1) : 1.0f;
             }
           }
-          if (L.nv > 0) w_consume<BITS, MX, C>(m[t], w_packed_kind(cf[t]), w_coef(cf[t]), acc, accz);
+          if (L.nv > 0) w_consume<BITS, MX, C>(m[t], w_packed_kind(cf[t]), EW ? aw[t] : w_coef(cf[t]), acc, accz);
         }
       }
     }
@@ -1667,7 +1677,7 @@ __device__ __forceinline__ void w_stream(const SpmmParams& p, const WLane<C>& L,
   }
 }
 
-template <int BITS, bool MX, int C, int U, int MINB>
+template <int BITS, bool MX, int C, int U, int MINB, int EW>
 __global__ void __launch_bounds__(kSpmmThreads, MINB) spmm_warp_kernel(const SpmmParams p) {
   extern __shared__ __align__(16) float wpart[];  // [kSpmmWarps][d] for heavy rows
   const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
@@ -1684,7 +1694,7 @@ __global__ void __launch_bounds__(kSpmmThreads, MINB) spmm_warp_kernel(const Spm
     const int chunk = (len + kSpmmWarps - 1) / kSpmmWarps;
     const int b0 = min(task.y + w * chunk, task.z);
     const int b1 = min(b0 + chunk, task.z);
-    if (b0 < b1) w_stream<BITS, MX, C, U, false>(p, L, b0, b1, 0, 0, acc, accz);
+    if (b0 < b1) w_stream<BITS, MX, C, U, false, EW>(p, L, b0, b1, 0, 0, acc, accz);
     if (L.nv > 0) w_flush<C>(p, L, 0, 1.0f, wpart + w * p.d, acc, accz);
     __syncthreads();
     finish_heavy(p, task, wpart);
@@ -1695,15 +1705,15 @@ __global__ void __launch_bounds__(kSpmmThreads, MINB) spmm_warp_kernel(const Spm
   for (int64_t t = gw; t < p.n_light; t += nw) {
     const int2 run = __ldg(reinterpret_cast<const int2*>(p.light) + t);
     const int eb = __ldg(p.rowptr + run.x), ee = __ldg(p.rowptr + run.y);
-    w_stream<BITS, MX, C, U, true>(p, L, eb, ee, run.x, run.y, acc, accz);
+    w_stream<BITS, MX, C, U, true, EW>(p, L, eb, ee, run.x, run.y, acc, accz);
   }
 }
 
-template <int BITS, bool MX, int C, int U, int MINB>
+template <int BITS, bool MX, int C, int U, int MINB, int EW = 0>
 int launch_warp(const SpmmParams& p, cudaStream_t s) {
   if (p.d > 32 * C || p.d % 4 != 0) return GQ_ERR_UNSUPPORTED;
   const size_t smem = sizeof(float) * kSpmmWarps * p.d;
-  auto kern = spmm_warp_kernel<BITS, MX, C, U, MINB>;
+  auto kern = spmm_warp_kernel<BITS, MX, C, U, MINB, EW>;
   int per_sm = 0;
   if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kSpmmThreads, smem) != cudaSuccess || per_sm < 1)
     return GQ_ERR_UNSUPPORTED;
@@ -1720,18 +1730,21 @@ int launch_warp(const SpmmParams& p, cudaStream_t s) {
 // 64 < d <= 256 on the warp-per-edge register kernel: 4 columns per lane and
 // 4 edges in flight up to d = 128, 8 columns and 2 edges above; 4 blocks
 // per SM (each measured the fastest of its range on the large GCN graph).
-template <int BITS, bool MX>
+template <int BITS, bool MX, int EW>
 int launch_warp_d(const SpmmParams& p, cudaStream_t s) {
-  return p.d <= 128 ? launch_warp<BITS, MX, 4, 4, 4>(p, s) : launch_warp<BITS, MX, 8, 2, 4>(p, s);
+  return p.d <= 128 ? launch_warp<BITS, MX, 4, 4, 4, EW>(p, s) : launch_warp<BITS, MX, 8, 2, 4, EW>(p, s);
 }
 
+// EW = 1: per-edge, per-head attention weights (fp32) instead of the
+// per-source coefficient.
+template <int EW>
 int launch_warp_any(const SpmmParams& p, int bits, cudaStream_t s) {
   const bool mx = bits < 32 && p.mask != nullptr;
   switch (bits) {
-    case 2: return mx ? launch_warp_d<2, true>(p, s) : launch_warp_d<2, false>(p, s);
-    case 4: return mx ? launch_warp_d<4, true>(p, s) : launch_warp_d<4, false>(p, s);
-    case 8: return mx ? launch_warp_d<8, true>(p, s) : launch_warp_d<8, false>(p, s);
-    default: return launch_warp_d<32, false>(p, s);
+    case 2: return mx ? launch_warp_d<2, true, EW>(p, s) : launch_warp_d<2, false, EW>(p, s);
+    case 4: return mx ? launch_warp_d<4, true, EW>(p, s) : launch_warp_d<4, false, EW>(p, s);
+    case 8: return mx ? launch_warp_d<8, true, EW>(p, s) : launch_warp_d<8, false, EW>(p, s);
+    default: return launch_warp_d<32, false, EW>(p, s);
   }
 }
 
@@ -1824,7 +1837,7 @@ int dequant_spmm(const gq_graph* g, int transpose, int coef, const float* X, int
   // d <= 512 and an fp32 row stride under 2^31 bytes: asynchronous ring
   // pipeline; otherwise warp per light row
   if ((bits == 32 || mask != nullptr) && d > 64 && d <= 256 && ldx <= (int64_t)1 << 29)
-    return launch_warp_any(p, bits, s);
+    return launch_warp_any<0>(p, bits, s);
   if (d <= 512 && ldx <= (int64_t)1 << 29) return launch_async_any(p, bits, s);
   return launch_any<0>(p, bits, s);
 }
@@ -1871,6 +1884,10 @@ int edge_spmm(const gq_graph* g, int transpose, const float* alpha, int heads, c
   p.heads = heads;
   p.fshift = fshift;
   p.eperm = transpose ? g->tr_perm : nullptr;
+  // 64 < d <= 256: warp per edge, plain loads into registers; otherwise a
+  // warp per light row
+  if (d > 64 && d <= 256 && (bits == 32 || mask != nullptr) && ldx <= (int64_t)1 << 29)
+    return launch_warp_any<1>(p, bits, s);
   return launch_any<1>(p, bits, s);
 }
 
