@@ -762,6 +762,42 @@ def run_aggregate(args, w):
     print(json.dumps(line), flush=True)
 
 
+def gemm_rates(args):
+    """The dense int8 and bf16 GEMM rates of this GPU through cuBLAS
+    (torch._int_mm with int32 accumulation, torch.matmul in bf16) on square
+    shapes and on the update GEMM's shape of the large GCN workload: the
+    measurement behind keeping the update GEMMs in bf16 (Tango Sec. 3.3 /
+    4.3 take int8 GEMMs where int8 runs faster than fp16)."""
+    dev = torch.device("cuda", 0)
+
+    def timed(fn, iters=20):
+        for _ in range(3):
+            fn()
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        for _ in range(iters):
+            fn()
+        b.record()
+        torch.cuda.synchronize()
+        return a.elapsed_time(b) / iters
+
+    out = {"measurement": "dense GEMM rates through cuBLAS", "unit": "TFLOP/s (int8: TOPS)"}
+    shapes = [(n, n, n) for n in (4096, 8192)] + [(GCN3_LARGE.graph["n"], 256, 256)]
+    for M, K, N in shapes:
+        key = f"{M}x{K}x{N}"
+        A = torch.randn(M, K, device=dev, dtype=torch.bfloat16)
+        B = torch.randn(K, N, device=dev, dtype=torch.bfloat16)
+        t = timed(lambda: A @ B)
+        out[f"bf16_{key}"] = {"ms": t, "rate": 2 * M * K * N / t / 1e9}
+        Ai = torch.randint(-100, 100, (M, K), device=dev, dtype=torch.int8)
+        Bi = torch.randint(-100, 100, (K, N), device=dev, dtype=torch.int8)
+        t = timed(lambda: torch._int_mm(Ai, Bi))
+        out[f"int8_{key}"] = {"ms": t, "rate": 2 * M * K * N / t / 1e9}
+        del A, B, Ai, Bi
+    print(json.dumps(out), flush=True)
+
+
 def load_traffic(workload):
     """DRAM traffic per launch of the aggregation kernel from the committed
     ncu summary, if it was taken on the kernel source as it is now."""
@@ -794,7 +830,12 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-largest", action="store_true",
                     help="skip the record of the aggregation on the largest graph")
+    ap.add_argument("--gemm-rates", action="store_true",
+                    help="print the dense int8 and bf16 GEMM rates (cuBLAS) instead of a benchmark line")
     args = ap.parse_args()
+    if args.gemm_rates:
+        gemm_rates(args)
+        return
     w = BY_NAME[args.workload]
     if args.impl == "reference":
         ws, rank, _ = dist_env()
