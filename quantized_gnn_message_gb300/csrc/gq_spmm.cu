@@ -1612,6 +1612,10 @@ __device__ __forceinline__ void w_stream(const SpmmParams& p, const WLane<C>& L,
   const int lane = threadIdx.x & 31;
   const int32_t* __restrict__ col = p.col;
   const int head = EW ? (L.c0 >> p.fshift) : 0;  // the lane's columns lie in one head (F >= 16 >= C)
+  // EW = 2 (8-bit attention codes, forward): {S, Z} of the current row's head
+  float2 az = make_float2(0.0f, 0.0f);
+  if (EW == 2 && L.nv > 0 && row0 < p.n_rows)
+    az = __ldg(reinterpret_cast<const float2*>(p.ahdr) + (int64_t)row0 * p.heads + head);
   uint32_t xn = eb + lane < ee ? (uint32_t)__ldg(col + eb + lane) : 0u;  // column ids of the next batch
   int row = row0, rend = 0x7fffffff, rnext = 0x7fffffff;
   float rs = 1.0f, rsn = 1.0f;
@@ -1634,15 +1638,18 @@ __device__ __forceinline__ void w_stream(const SpmmParams& p, const WLane<C>& L,
     for (int t0 = 0; t0 < cnt; t0 += U) {
       WSlot<BITS, MX, C> m[U];
       float cf[U];
-      float aw[U];  // edge-weight modes: the attention weight of the lane's head
+      float aw[U];  // edge-weight modes: the attention weight (EW = 1) or code (EW = 2) of the lane's head
 #pragma unroll
       for (int t = 0; t < U; ++t) {
         const uint32_t x = __shfl_sync(FULL, xb, (t0 + t) & 31);
         cf[t] = __shfl_sync(FULL, cb, (t0 + t) & 31);
         aw[t] = 0.0f;
-        if (EW) {
+        if (EW == 1) {
           const int32_t eid = __shfl_sync(FULL, eidb, (t0 + t) & 31);
           if (t0 + t < cnt && L.nv > 0) aw[t] = __ldg(p.alpha + (int64_t)eid * p.heads + head);
+        } else if (EW == 2) {  // forward only: the edge id is the CSR position
+          if (t0 + t < cnt && L.nv > 0)
+            aw[t] = code_to_float(__ldg(p.acode + (int64_t)(base + t0 + t) * p.heads + head));
         }
         if (t0 + t < cnt && L.nv > 0) w_load<BITS, MX, C>(p, L, x, w_packed_kind(cf[t]), m[t]);
       }
@@ -1660,9 +1667,12 @@ __device__ __forceinline__ void w_stream(const SpmmParams& p, const WLane<C>& L,
               rnext = row + 1 < row1 ? __ldg(p.rowptr + row + 2) : 0x7fffffff;
               rs = rsn;
               if (p.rowscale) rsn = row + 1 < row1 ? __ldg(p.rowscale + row + 1) : 1.0f;
+              if (EW == 2 && L.nv > 0 && row < row1)
+                az = __ldg(reinterpret_cast<const float2*>(p.ahdr) + (int64_t)row * p.heads + head);
             }
           }
-          if (L.nv > 0) w_consume<BITS, MX, C>(m[t], w_packed_kind(cf[t]), EW ? aw[t] : w_coef(cf[t]), acc, accz);
+          const float coef = EW == 1 ? aw[t] : (EW == 2 ? __fmaf_rn(aw[t], az.x, az.y) : w_coef(cf[t]));
+          if (L.nv > 0) w_consume<BITS, MX, C>(m[t], w_packed_kind(cf[t]), coef, acc, accz);
         }
       }
     }
@@ -1694,7 +1704,7 @@ __global__ void __launch_bounds__(kSpmmThreads, MINB) spmm_warp_kernel(const Spm
     const int chunk = (len + kSpmmWarps - 1) / kSpmmWarps;
     const int b0 = min(task.y + w * chunk, task.z);
     const int b1 = min(b0 + chunk, task.z);
-    if (b0 < b1) w_stream<BITS, MX, C, U, false, EW>(p, L, b0, b1, 0, 0, acc, accz);
+    if (b0 < b1) w_stream<BITS, MX, C, U, false, EW>(p, L, b0, b1, task.x, task.x + 1, acc, accz);
     if (L.nv > 0) w_flush<C>(p, L, 0, 1.0f, wpart + w * p.d, acc, accz);
     __syncthreads();
     finish_heavy(p, task, wpart);
@@ -1920,6 +1930,9 @@ int edge_spmm_alpha8(const gq_graph* g, const uint8_t* acode, const float* ahdr,
   p.heads = heads;
   p.fshift = fshift;
   p.eperm = nullptr;
+  // 64 < d <= 256: warp per edge, plain loads into registers
+  if (d > 64 && d <= 256 && (bits == 32 || mask != nullptr) && ldx <= (int64_t)1 << 29)
+    return launch_warp_any<2>(p, bits, s);
   switch (bits) {
     case 2: return launch_alpha8<2>(p, s);
     case 4: return launch_alpha8<4>(p, s);
