@@ -381,12 +381,21 @@ GQ_API int gq_to_bf16(const float* src, int64_t rows, int cols, int64_t lds, uin
  *
  * gq_gcn_layer_bwd (same arguments read in reverse; the quantizer is the
  * identity in backward):
- *   dZ    = dH_out * [H_out > 0]  (act = RELU; dH_out for act = NONE)
+ *   dZ    = dH_out * [H_out > 0]  (act = RELU; dH_out for act = NONE), in
+ *           bf16; or dZ_in when non-NULL (bf16, n x d_out, ldzi >= d_out,
+ *           ldzi % 8 == 0), already made by the layer above, and then
+ *           dH_out and H_out are not read (may be NULL)
  *   dW    = A^T dZ                -> fp32 d_in x d_out (ld d_out)
  *   if need_dinput:
  *     dA    = dZ W^T              -> dA_save if non-NULL (n x d_in, ld d_in)
  *     packed= quantize_pack(dA rows with mask != 0, bits, seed)
  *     dH_in = A^T-aggregation of the mixed messages -> n x d_in (ldi)
+ *     or, when dZ_prev is non-NULL, the layer below's dZ in its place:
+ *     dZ_prev = bf16(dH_in * [gate_in > 0]) -> n x d_in (ldzp >= d_in,
+ *     ldzp % 8 == 0; columns d_in .. ldzp are not written), with gate_in
+ *     the layer's input H_in (the layer below's ReLU output, n x d_in,
+ *     ldgi; NULL: no gate) -- the row flush of the aggregation applies the
+ *     gate and the rounding, so no fp32 dH_in is written.
  * Both take a workspace of gq_gcn_layer_workspace_bytes(g, d_in, d_out,
  * bits) bytes (256-byte aligned) and a nullable device error word (see
  * the GEMMs).  Errors: GQ_ERR_INVALID_ARG, GQ_ERR_UNSUPPORTED,
@@ -403,11 +412,12 @@ GQ_API int gq_gcn_layer_fwd(const gq_graph* g, int coef, const float* H_in, int6
                      uint16_t* A_save, int64_t lda, float* H_out, int64_t ldo, void* ws,
                      size_t ws_bytes, int* dev_err, void* const* stage_events, gq_stream stream);
 GQ_API int gq_gcn_layer_bwd(const gq_graph* g, int coef, const float* dH_out, int64_t ldd,
-                     const uint16_t* A_save, int64_t lda, const float* H_out, int64_t ldo,
-                     const float* W, int d_in, int d_out, const uint8_t* mask, int bits, uint64_t seed,
-                     int act, int need_dinput, float* dW, float* dH_in, int64_t ldi, float* dA_save,
-                     void* ws, size_t ws_bytes, int* dev_err, void* const* stage_events,
-                     gq_stream stream);
+                     const uint16_t* dZ_in, int64_t ldzi, const uint16_t* A_save, int64_t lda,
+                     const float* H_out, int64_t ldo, const float* W, int d_in, int d_out,
+                     const uint8_t* mask, int bits, uint64_t seed, int act, int need_dinput, float* dW,
+                     float* dH_in, int64_t ldi, const float* gate_in, int64_t ldgi, uint16_t* dZ_prev,
+                     int64_t ldzp, float* dA_save, void* ws, size_t ws_bytes, int* dev_err,
+                     void* const* stage_events, gq_stream stream);
 
 /* ------------------------------------------------------------------------
  * gq_sddmm_edge_softmax -- Tango Sec. 2.1, Fig. 1a steps 3-4, per

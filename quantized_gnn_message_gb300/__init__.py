@@ -110,7 +110,8 @@ def _SIGNATURES(P, I64, I, U64, F, S):
                               P, S, P, P], I),
         ("gq_gcn_layer_fwd", [GP, I, P, I64, I, P, I, P, I, U64, I, P, I64, P, I64, P, S, P, P, P], I),
         ("gq_gcn_layer_bwd",
-         [GP, I, P, I64, P, I64, P, I64, P, I, I, P, I, U64, I, I, P, P, I64, P, P, S, P, P, P], I),
+         [GP, I, P, I64, P, I64, P, I64, P, I64, P, I, I, P, I, U64, I, I, P, P, I64, P, I64, P, I64, P, P, S, P,
+          P, P], I),
         ("gq_selftest_bounded_wait", [I, I, ctypes.c_longlong, P, P], I),
         ("gq_packed_row_offsets_workspace_bytes", [I64], S),
         ("gq_packed_row_offsets", [P, I64, I, P, P, S, P], I),
@@ -562,29 +563,42 @@ def gcn_layer_fwd(g: Graph, H_in: torch.Tensor, W: torch.Tensor, mask, bits: int
     return A_save[:, :d_in], H_out
 
 
-def gcn_layer_bwd(g: Graph, dH_out: torch.Tensor, A_save: torch.Tensor, H_out: torch.Tensor, W: torch.Tensor,
-                  mask, bits: int, seed: int, act: int, need_dinput: bool = True, coef: int = COEF_GCN,
-                  ws: Workspace | None = None, dW=None, dH_in=None, dA_save=None,
-                  dev_err: torch.Tensor | None = None, events=None):
-    """Returns (dW [d_in x d_out], dH_in [n x d_in] or None)."""
+def gcn_layer_bwd(g: Graph, dH_out: torch.Tensor | None, A_save: torch.Tensor, H_out: torch.Tensor | None,
+                  W: torch.Tensor, mask, bits: int, seed: int, act: int, need_dinput: bool = True,
+                  coef: int = COEF_GCN, ws: Workspace | None = None, dW=None, dH_in=None, dA_save=None,
+                  dev_err: torch.Tensor | None = None, events=None, dZ_in: torch.Tensor | None = None,
+                  gate_in: torch.Tensor | None = None, dZ_prev: torch.Tensor | None = None):
+    """Returns (dW [d_in x d_out], dH_in [n x d_in] or None).  dZ_in: the
+    layer's bf16 dZ made by the layer above (dH_out, H_out unused); dZ_prev:
+    write the layer below's bf16 dZ = dH_in * [gate_in > 0] instead of an
+    fp32 dH_in (then None is returned for dH_in)."""
     _cuda(dH_out, torch.float32, "dH_out")
     _cuda(A_save, torch.bfloat16, "A_save")
-    n, d_out = dH_out.shape
-    d_in = W.shape[0]
-    dev = dH_out.device
+    _cuda(dZ_in, torch.bfloat16, "dZ_in")
+    _cuda(dZ_prev, torch.bfloat16, "dZ_prev")
+    _cuda(gate_in, torch.float32, "gate_in")
+    n = A_save.shape[0]
+    d_in, d_out = W.shape
+    dev = A_save.device
     if dW is None:
         dW = torch.empty(d_in, d_out, dtype=torch.float32, device=dev)
-    if need_dinput and dH_in is None:
+    if need_dinput and dH_in is None and dZ_prev is None:
         dH_in = torch.empty(n, d_in, dtype=torch.float32, device=dev)
+    if dZ_prev is not None:
+        dH_in = None
     Wc = W.contiguous()  # held until the call has been enqueued
     L = lib()
     wb = int(L.gq_gcn_layer_workspace_bytes(g.ref, d_in, d_out, bits))
     buf = (ws or Workspace(dev)).get(wb)
-    _check(L.gq_gcn_layer_bwd(g.ref, coef, _ptr(dH_out), _rows(dH_out), _ptr(A_save), _rows(A_save), _ptr(H_out),
-                              _rows(H_out) if H_out is not None else 0, _ptr(Wc), d_in, d_out,
-                              _ptr(mask), bits, seed & 0xFFFFFFFFFFFFFFFF, act, int(need_dinput), _ptr(dW),
-                              _ptr(dH_in), _rows(dH_in) if dH_in is not None else 0, _ptr(dA_save), _ptr(buf),
-                              buf.numel(), _ptr(dev_err), _events(events), _stream()), "gq_gcn_layer_bwd")
+    _check(L.gq_gcn_layer_bwd(g.ref, coef, _ptr(dH_out), _rows(dH_out) if dH_out is not None else 0,
+                              _ptr(dZ_in), _rows(dZ_in) if dZ_in is not None else 0,
+                              _ptr(A_save), _rows(A_save), _ptr(H_out), _rows(H_out) if H_out is not None else 0,
+                              _ptr(Wc), d_in, d_out, _ptr(mask), bits, seed & 0xFFFFFFFFFFFFFFFF, act,
+                              int(need_dinput), _ptr(dW), _ptr(dH_in), _rows(dH_in) if dH_in is not None else 0,
+                              _ptr(gate_in), _rows(gate_in) if gate_in is not None else 0,
+                              _ptr(dZ_prev), _rows(dZ_prev) if dZ_prev is not None else 0, _ptr(dA_save),
+                              _ptr(buf), buf.numel(), _ptr(dev_err), _events(events), _stream()),
+           "gq_gcn_layer_bwd")
     return dW, (dH_in if need_dinput else None)
 
 

@@ -12,13 +12,14 @@ namespace gq {
 int quantize_pack(const float* X, int64_t n, int d, int64_t ldx, const uint8_t* mask, int bits, uint64_t seed,
                   uint8_t* packed, cudaStream_t s);
 
-// Aggregation; Yb != nullptr writes the output in bf16 (leading dim ldy).
+// Aggregation; Yb != nullptr writes the output in bf16 (leading dim ldy);
+// gate != nullptr zeroes every output element whose gate element is not > 0.
 size_t spmm_workspace(const gq_graph* g, int transpose, int d);
 int spmm_check(const gq_graph* g, const float* X, int64_t ldx, const uint8_t* packed, const uint8_t* mask, int d,
                int bits, const float* Y, int64_t ldy, const void* Yb);
 int dequant_spmm(const gq_graph* g, int transpose, int coef, const float* X, int64_t ldx, const uint8_t* packed,
                  const uint8_t* mask, int d, int bits, float* Y, int64_t ldy, void* ws, size_t ws_bytes,
-                 cudaStream_t s, void* Yb);
+                 cudaStream_t s, void* Yb, const float* gate = nullptr, int64_t ldg = 0);
 int edge_spmm(const gq_graph* g, int transpose, const float* alpha, int heads, const float* X, int64_t ldx,
               const uint8_t* packed, const uint8_t* mask, int d, int bits, float* Y, int64_t ldy, void* ws,
               size_t ws_bytes, cudaStream_t s);

@@ -106,46 +106,66 @@ extern "C" int gq_gcn_layer_fwd(const gq_graph* g, int coef, const float* H_in, 
 }
 
 extern "C" int gq_gcn_layer_bwd(const gq_graph* g, int coef, const float* dH_out, int64_t ldd,
-                                const uint16_t* A_save, int64_t lda, const float* H_out, int64_t ldo,
-                                const float* W, int d_in, int d_out, const uint8_t* mask, int bits, uint64_t seed,
-                                int act, int need_dinput, float* dW, float* dH_in, int64_t ldi, float* dA_save,
-                                void* ws, size_t ws_bytes, int* dev_err, void* const* stage_events,
-                                gq_stream stream) {
+                                const uint16_t* dZ_in, int64_t ldzi, const uint16_t* A_save, int64_t lda,
+                                const float* H_out, int64_t ldo, const float* W, int d_in, int d_out,
+                                const uint8_t* mask, int bits, uint64_t seed, int act, int need_dinput, float* dW,
+                                float* dH_in, int64_t ldi, const float* gate_in, int64_t ldgi, uint16_t* dZ_prev,
+                                int64_t ldzp, float* dA_save, void* ws, size_t ws_bytes, int* dev_err,
+                                void* const* stage_events, gq_stream stream) {
   using namespace gq;
   cudaStream_t s = (cudaStream_t)stream;
-  if (g == nullptr || dH_out == nullptr || A_save == nullptr || W == nullptr || dW == nullptr)
+  if (g == nullptr || A_save == nullptr || W == nullptr || dW == nullptr) return GQ_ERR_INVALID_ARG;
+  if (dZ_in == nullptr) {
+    if (dH_out == nullptr || ldd < d_out) return GQ_ERR_INVALID_ARG;
+    if (act == GQ_ACT_RELU && H_out == nullptr) return GQ_ERR_INVALID_ARG;
+  } else if (ldzi < d_out || ldzi % 8 || !aligned(dZ_in, 16)) {
     return GQ_ERR_INVALID_ARG;
-  if (act == GQ_ACT_RELU && H_out == nullptr) return GQ_ERR_INVALID_ARG;
-  if (d_in < 1 || d_out < 1 || d_in % 4 || lda < d_in || lda % 8 || ldd < d_out) return GQ_ERR_INVALID_ARG;
-  if (need_dinput && (dH_in == nullptr || ldi < d_in)) return GQ_ERR_INVALID_ARG;
+  }
+  if (d_in < 1 || d_out < 1 || d_in % 4 || lda < d_in || lda % 8) return GQ_ERR_INVALID_ARG;
+  if (need_dinput) {
+    if (dZ_prev != nullptr) {
+      if (ldzp < d_in || ldzp % 8 || !aligned(dZ_prev, 16)) return GQ_ERR_INVALID_ARG;
+      if (gate_in != nullptr && (ldgi < d_in || ldgi % 4 || !aligned(gate_in, 16))) return GQ_ERR_INVALID_ARG;
+    } else if (dH_in == nullptr || ldi < d_in) {
+      return GQ_ERR_INVALID_ARG;
+    }
+  }
   if (!(bits == 32 || valid_bits(bits))) return GQ_ERR_INVALID_ARG;
   if (d_in > 256 || d_out > 256) return GQ_ERR_UNSUPPORTED;
   GcnWs w;
   if (ws == nullptr || !carve_gcn(g, ws, ws_bytes, d_in, d_out, bits, w).ok()) return GQ_ERR_WORKSPACE;
   const Trace tr{stage_events, s};
-  const int64_t ldz = round8(d_out);
-  // 1. dZ = dH_out * relu'(Z), with relu'(Z) = [H_out > 0]
+  // 1. dZ = dH_out * relu'(Z), with relu'(Z) = [H_out > 0]  (given by the caller as dZ_in, or made here)
+  const void* dz = dZ_in != nullptr ? static_cast<const void*>(dZ_in) : w.dz;
+  const int64_t ldz = dZ_in != nullptr ? ldzi : round8(d_out);
   GQ_TRY(tr.begin(0));
-  GQ_TRY(to_bf16(dH_out, g->n, d_out, ldd, w.dz, ldz, (int)ldz, act == GQ_ACT_RELU ? H_out : nullptr, ldo, s));
+  if (dZ_in == nullptr)
+    GQ_TRY(to_bf16(dH_out, g->n, d_out, ldd, w.dz, ldz, (int)ldz, act == GQ_ACT_RELU ? H_out : nullptr, ldo, s));
   GQ_TRY(tr.end(0));
   // 2. dW = A^T dZ
   GQ_TRY(tr.begin(1));
-  GQ_TRY(wgrad_gemm(A_save, g->n, d_in, lda, w.dz, d_out, ldz, dW, d_out, 0, w.wg, w.wg_bytes, dev_err, s));
+  GQ_TRY(wgrad_gemm(A_save, g->n, d_in, lda, dz, d_out, ldz, dW, d_out, 0, w.wg, w.wg_bytes, dev_err, s));
   GQ_TRY(tr.end(1));
   if (!need_dinput) return GQ_OK;
   // 3. dA = dZ W^T : B operand is W itself, [d_in][d_out] in bf16
   float* dA = dA_save != nullptr ? dA_save : w.dA;
+  const int64_t ldw = round8(d_out);
   GQ_TRY(tr.begin(2));
-  GQ_TRY(to_bf16(W, d_in, d_out, d_out, w.wt, ldz, (int)ldz, nullptr, 0, s));
-  GQ_TRY(row_gemm(w.dz, g->n, d_out, ldz, w.wt, d_in, ldz, GQ_ACT_NONE, dA, d_in, nullptr, nullptr, nullptr,
-                  nullptr, 0, dev_err, s));
+  GQ_TRY(to_bf16(W, d_in, d_out, d_out, w.wt, ldw, (int)ldw, nullptr, 0, s));
+  GQ_TRY(row_gemm(dz, g->n, d_out, ldz, w.wt, d_in, ldw, GQ_ACT_NONE, dA, d_in, nullptr, nullptr, nullptr, nullptr,
+                  0, dev_err, s));
   GQ_TRY(tr.end(2));
-  // 4-5. quantize the marginal rows of dA, aggregate over the transpose
+  // 4-5. quantize the marginal rows of dA, aggregate over the transpose: fp32
+  // dH_in, or the previous layer's dZ = bf16(dH_in * [gate_in > 0])
   GQ_TRY(tr.begin(3));
   if (bits < 32) GQ_TRY(quantize_pack(dA, g->n, d_in, d_in, mask, bits, seed, w.packed, s));
   GQ_TRY(tr.end(3));
   GQ_TRY(tr.begin(4));
-  GQ_TRY(dequant_spmm(g, 1, coef, dA, d_in, w.packed, mask, d_in, bits, dH_in, ldi, w.sp, w.sp_bytes, s, nullptr));
+  if (dZ_prev != nullptr)
+    GQ_TRY(dequant_spmm(g, 1, coef, dA, d_in, w.packed, mask, d_in, bits, nullptr, ldzp, w.sp, w.sp_bytes, s,
+                        dZ_prev, gate_in, ldgi));
+  else
+    GQ_TRY(dequant_spmm(g, 1, coef, dA, d_in, w.packed, mask, d_in, bits, dH_in, ldi, w.sp, w.sp_bytes, s, nullptr));
   return tr.end(4);
 }
 

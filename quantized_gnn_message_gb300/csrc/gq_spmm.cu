@@ -65,6 +65,8 @@ struct SpmmParams {
   float* Y;
   __nv_bfloat16* Yb;        // if set, the output is written in bf16 here instead
   int64_t ldy;
+  const float* gate;        // if set, an output element whose gate[r][c] is not > 0 is written as 0
+  int64_t ldg;
   int64_t n_rows;
   int d;
   const int32_t* tasks;     // heavy-row schedule (see gq_sched)
@@ -236,7 +238,26 @@ __device__ __forceinline__ void group_reduce(float (&acc)[CPL][8]) {
       for (int k = 0; k < 8; ++k) acc[i][k] += __shfl_xor_sync(FULL, acc[i][k], o);
 }
 
-__device__ __forceinline__ void store_chunk(const SpmmParams& p, int64_t r, int c, float s, const float (&a)[8]) {
+// The output value of row r, column c after the optional ReLU gate (the
+// derivative of the activation of the layer whose input this output is).
+__device__ __forceinline__ float gated(const SpmmParams& p, int64_t r, int c, float v) {
+  return (p.gate != nullptr && !(__ldg(p.gate + r * p.ldg + c) > 0.0f)) ? 0.0f : v;
+}
+__device__ __forceinline__ float4 gated4(const SpmmParams& p, int64_t r, int c, float4 v) {
+  if (p.gate != nullptr) {
+    const float4 g = __ldg(reinterpret_cast<const float4*>(p.gate + r * p.ldg + c));
+    if (!(g.x > 0.0f)) v.x = 0.0f;
+    if (!(g.y > 0.0f)) v.y = 0.0f;
+    if (!(g.z > 0.0f)) v.z = 0.0f;
+    if (!(g.w > 0.0f)) v.w = 0.0f;
+  }
+  return v;
+}
+
+__device__ __forceinline__ void store_chunk(const SpmmParams& p, int64_t r, int c, float s, const float (&a_in)[8]) {
+  float a[8];
+#pragma unroll
+  for (int k = 0; k < 8; ++k) a[k] = (c * 8 + k < p.d) ? gated(p, r, c * 8 + k, a_in[k]) : a_in[k];
   if (p.Yb != nullptr) {
     __nv_bfloat16* y = p.Yb + r * p.ldy + c * 8;
     if (c * 8 + 4 < p.d) {
@@ -419,9 +440,9 @@ __device__ __forceinline__ void finish_heavy(const SpmmParams& p, const int4& ta
 #pragma unroll
       for (int ww = 0; ww < kSpmmWarps; ++ww) t += part[ww * p.d + j];
       if (p.Yb != nullptr)
-        p.Yb[r * p.ldy + j] = __float2bfloat16_rn(t * s);
+        p.Yb[r * p.ldy + j] = __float2bfloat16_rn(gated(p, r, j, t * s));
       else
-        p.Y[r * p.ldy + j] = t * s;
+        p.Y[r * p.ldy + j] = gated(p, r, j, t * s);
     }
     return;
   }
@@ -444,9 +465,9 @@ __device__ __forceinline__ void finish_heavy(const SpmmParams& p, const int4& ta
     float t = 0.0f;
     for (int k = 0; k < grp.z; ++k) t += __ldcg(base + (int64_t)k * p.d + j);
     if (p.Yb != nullptr)
-      p.Yb[r * p.ldy + j] = __float2bfloat16_rn(t * s);
+      p.Yb[r * p.ldy + j] = __float2bfloat16_rn(gated(p, r, j, t * s));
     else
-      p.Y[r * p.ldy + j] = t * s;
+      p.Y[r * p.ldy + j] = gated(p, r, j, t * s);
   }
 }
 
@@ -746,6 +767,10 @@ __device__ __forceinline__ void a_flush(const SpmmParams& p, const ALane<LG>& L,
   for (int k = 0; k < 4; ++k) {
     const int col = a_col<BITS, LG>(L, 4 * k);
     if (col < p.d) {
+      if (p.gate != nullptr) {
+        const float4 g = gated4(p, r, col, make_float4(o[4 * k], o[4 * k + 1], o[4 * k + 2], o[4 * k + 3]));
+        o[4 * k] = g.x; o[4 * k + 1] = g.y; o[4 * k + 2] = g.z; o[4 * k + 3] = g.w;
+      }
       if (p.Yb != nullptr)
         *reinterpret_cast<uint2*>(p.Yb + r * p.ldy + col) =
             make_uint2(pack_bf16x2(o[4 * k], o[4 * k + 1]), pack_bf16x2(o[4 * k + 2], o[4 * k + 3]));
@@ -1144,8 +1169,12 @@ __device__ __forceinline__ void bf_write(const SpmmParams& p, bool a_on, bool b_
   for (int k = 0; k < CPL / 4; ++k) {
     if (k == 0 ? a_on : b_on) {
       const float2 u = f2_unpack(acc[2 * k]), v = f2_unpack(acc[2 * k + 1]);
-      const float o0 = (u.x + accz) * s, o1 = (u.y + accz) * s, o2 = (v.x + accz) * s, o3 = (v.y + accz) * s;
+      float o0 = (u.x + accz) * s, o1 = (u.y + accz) * s, o2 = (v.x + accz) * s, o3 = (v.y + accz) * s;
       const int c = c0 + 128 * k;
+      if (part == nullptr && p.gate != nullptr) {
+        const float4 g = gated4(p, r, c, make_float4(o0, o1, o2, o3));
+        o0 = g.x; o1 = g.y; o2 = g.z; o3 = g.w;
+      }
       if (part != nullptr)
         st_f4(part + c, o0, o1, o2, o3);
       else if (p.Yb != nullptr)
@@ -1580,8 +1609,12 @@ __device__ __forceinline__ void w_flush(const SpmmParams& p, const WLane<C>& L, 
   for (int k = 0; k < C / 4; ++k) {
     if (4 * k < L.nv) {
       const float2 u = f2_unpack(acc[2 * k]), v = f2_unpack(acc[2 * k + 1]);
-      const float o0 = (u.x + accz) * rs, o1 = (u.y + accz) * rs, o2 = (v.x + accz) * rs, o3 = (v.y + accz) * rs;
+      float o0 = (u.x + accz) * rs, o1 = (u.y + accz) * rs, o2 = (v.x + accz) * rs, o3 = (v.y + accz) * rs;
       const int col = L.c0 + 4 * k;
+      if (part == nullptr && p.gate != nullptr) {
+        const float4 g = gated4(p, r, col, make_float4(o0, o1, o2, o3));
+        o0 = g.x; o1 = g.y; o2 = g.z; o3 = g.w;
+      }
       if (part != nullptr)
         st_f4(part + col, o0, o1, o2, o3);
       else if (p.Yb != nullptr)
@@ -1828,9 +1861,12 @@ size_t spmm_workspace(const gq_graph* g, int transpose, int d) {
 
 int dequant_spmm(const gq_graph* g, int transpose, int coef, const float* X, int64_t ldx, const uint8_t* packed,
                  const uint8_t* mask, int d, int bits, float* Y, int64_t ldy, void* ws, size_t ws_bytes,
-                 cudaStream_t s, void* Yb) {
+                 cudaStream_t s, void* Yb, const float* gate, int64_t ldg) {
+  if (gate != nullptr && (ldg < d || ldg % 4 != 0 || !aligned(gate, 16))) return GQ_ERR_INVALID_ARG;
   SpmmParams p;
   GQ_TRY(spmm_setup(g, transpose, X, ldx, packed, mask, d, bits, Y, ldy, ws, ws_bytes, s, p, Yb));
+  p.gate = gate;
+  p.ldg = ldg;
   if (coef == GQ_COEF_GCN) {
     // a_{u,v} = dinv_out[u] * dinv_in[v]
     p.colscale = transpose ? g->dinv_in : g->dinv_out;

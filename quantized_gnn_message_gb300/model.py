@@ -22,10 +22,10 @@ def launches_fwd(bits: int) -> int:
     return (1 if bits < 32 else 0) + 3
 
 
-def launches_bwd(bits: int, need_dinput: bool) -> int:
-    """dZ + weight GEMM + split reduction [+ W convert + dA GEMM +
+def launches_bwd(bits: int, need_dinput: bool, dz_given: bool = False) -> int:
+    """[dZ] + weight GEMM + split reduction [+ W convert + dA GEMM +
     [quantize] + transposed aggregate]."""
-    n = 3
+    n = 2 if dz_given else 3
     if need_dinput:
         n += 3 + (1 if bits < 32 else 0)
     return n
@@ -33,7 +33,7 @@ def launches_bwd(bits: int, need_dinput: bool) -> int:
 
 class GCNStack:
     def __init__(self, g: Graph, widths, mask: torch.Tensor | None, coef: int = COEF_GCN,
-                 device="cuda", keep_dA: bool = False):
+                 device="cuda", keep_dA: bool = False, fuse_dz: bool = True):
         self.g = g
         self.widths = tuple(widths)
         self.L = len(widths) - 1
@@ -49,6 +49,12 @@ class GCNStack:
         # the backward's dA = dZ W^T of each layer (the messages it quantizes), kept on request
         self.dA = [torch.empty(n, widths[l], dtype=torch.float32, device=device) if keep_dA else None
                    for l in range(self.L)]
+        # fuse_dz: the transposed aggregation of layer l writes layer l-1's dZ
+        # (bf16, ReLU gate applied) instead of an fp32 gradient, which layer
+        # l-1 then takes as its dZ
+        self.fuse_dz = fuse_dz
+        self.dZ = [torch.empty(n, r8(widths[l + 1]), dtype=torch.bfloat16, device=device)
+                   if fuse_dz and l < self.L - 1 else None for l in range(self.L)]
         self.err = torch.zeros(1, dtype=torch.int32, device=device)
         L = lib()
         self.ws.get(max(int(L.gq_gcn_layer_workspace_bytes(g.ref, widths[l], widths[l + 1], 2))
@@ -71,11 +77,17 @@ class GCNStack:
         for l in reversed(range(self.L)):
             need = need_input_grad or l > 0
             ev = None if events is None else events[l]
-            gcn_layer_bwd(self.g, g, self.A[l], self.H[l], Ws[l], self.mask, bits, seeds[l], self.act(l), need,
-                          coef=self.coef, ws=self.ws, dW=self.dW[l], dH_in=self.dH[l] if need else None,
-                          dA_save=self.dA[l] if need else None, dev_err=self.err, events=ev)
+            dz_in = self.dZ[l]                               # made by layer l+1 (fused), else None
+            fuse = self.fuse_dz and l > 0                    # layer l makes layer l-1's dZ
+            gcn_layer_bwd(self.g, None if dz_in is not None else g, self.A[l],
+                          None if dz_in is not None else self.H[l], Ws[l], self.mask, bits, seeds[l],
+                          self.act(l), need, coef=self.coef, ws=self.ws, dW=self.dW[l],
+                          dH_in=self.dH[l] if need and not fuse else None,
+                          dA_save=self.dA[l] if need else None, dev_err=self.err, events=ev, dZ_in=dz_in,
+                          gate_in=self.H[l - 1] if fuse else None, dZ_prev=self.dZ[l - 1] if fuse else None)
             g = self.dH[l]
         return self.dW
 
     def launches(self, bits: int, need_input_grad: bool = False) -> int:
-        return sum(launches_fwd(bits) + launches_bwd(bits, need_input_grad or l > 0) for l in range(self.L))
+        return sum(launches_fwd(bits) + launches_bwd(bits, need_input_grad or l > 0, self.dZ[l] is not None)
+                   for l in range(self.L))

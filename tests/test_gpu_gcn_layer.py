@@ -81,3 +81,45 @@ def test_gcn_layer_hubs(orc):
 def test_gcn_layer_all_central_and_all_marginal(orc):
     _case(orc, rmat_small(), 64, 32, 8, 1, coef=0, mask_frac=0.0)
     _case(orc, rmat_small(), 64, 32, 8, 1, coef=0, mask_frac=1.0)
+
+
+@pytest.mark.parametrize("bits", [2, 8, 32])
+def test_gcn_layer_fused_dz_handoff(orc, bits):
+    """The transposed aggregation writes the layer below's dZ = bf16(dH_in *
+    [H_in > 0]) (the ReLU gate of the layer below), and the layer below takes
+    it as its dZ: dZ within the bf16 bar of the oracle's gated dH_in, and the
+    layer below's dW from it at the GEMM bars."""
+    q = gq()
+    g = rmat_small()
+    G = q.graph_prepare(g.rowptr.cuda(), g.col.cuda())
+    rp, co = g.rowptr.numpy(), g.col.numpy()
+    d0, d1, d2 = 100, 128, 64
+    X = synth.normal_matrix(g.n, d0, seed=31)
+    W0 = synth.glorot(d0, d1, seed=32)
+    W1 = synth.glorot(d1, d2, seed=33)
+    mask = synth.bernoulli_mask(g.n, 0.6, seed=34)
+    dY = synth.normal_matrix(g.n, d2, seed=35, tag=synth.TAG_GRAD)
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    md = mask.cuda()
+    A0, H0 = q.gcn_layer_fwd(G, X.cuda(), W0.cuda(), md, bits, 1, q.ACT_RELU, dev_err=err)
+    A1, H1 = q.gcn_layer_fwd(G, H0, W1.cuda(), md, bits, 2, q.ACT_NONE, dev_err=err)
+    dA1 = torch.empty(g.n, d1, device="cuda")
+    dZ0 = torch.full((g.n, d1), float("nan"), dtype=torch.bfloat16, device="cuda")
+    dW1, none = q.gcn_layer_bwd(G, dY.cuda(), A1, H1, W1.cuda(), md, bits, 3, q.ACT_NONE, True, dA_save=dA1,
+                                dev_err=err, gate_in=H0, dZ_prev=dZ0)
+    assert none is None
+    dW0, _ = q.gcn_layer_bwd(G, None, A0, None, W0.cuda(), md, bits, 4, q.ACT_RELU, False, dev_err=err,
+                             dZ_in=dZ0)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0 and int(G.status.cpu()[0]) == 0
+    mn = mask.numpy()
+    dAg = dA1.cpu().numpy()
+    pkb = orc.quantize(dAg, mn, bits, 3) if bits < 32 else None
+    dH = orc.spmm(rp, co, orc.COEF_GCN, orc.messages(dAg, pkb, mn, d1, bits), transpose=True)
+    dZ_ref = dH * (H0.cpu().numpy() > 0)
+    dZg = dZ0.float().cpu().numpy()
+    close(dZg, dZ_ref, rtol=5e-3, what="fused dZ (bf16)")
+    assert np.all(dZg[H0.cpu().numpy() <= 0] == 0.0)
+    dW0_ref = orc.gemm(A0[:, :d0].float().cpu().numpy().T, dZg, bf16=True)
+    close(dW0.cpu().numpy(), dW0_ref, rtol=2e-2, what="dW from the fused dZ bar")
+    close(dW0.cpu().numpy(), dW0_ref, rtol=1e-3, what="dW from the fused dZ")

@@ -7,7 +7,9 @@ degrees):
     3-layer stack the benchmark times (model.GCNStack), every layer forward
     and backward, teacher-forced on the GPU's own stage inputs: A (bf16
     store, 5e-3), H_out (bf16 GEMM inputs: 2e-2 bar, 1e-3 checked), dW over
-    all rows, dA, and dH_in (1e-4), on sampled rows including the heaviest;
+    all rows, dA, and the layer below's dZ that the transposed aggregation
+    writes (its dH_in with the ReLU gate, bf16 store: 5e-3), on sampled rows
+    including the heaviest;
   - the aggregation on the largest graph (16,777,216 nodes, ~537M edges,
     d = 256, b = 8, every row packed: 4.6 GB of packed rows, above 4 GiB),
     forward and transposed, with the quantized bytes of every row read
@@ -94,14 +96,15 @@ def test_large_gcn_stack_sampled(orc):
         close(Hg, H_ref, rtol=1e-3, what=f"layer {l} H_out")
         H_in = model.H[l]
 
-    G_out = dY
+    # the stack's backward is fused: the transposed aggregation of layer l
+    # writes layer l-1's dZ (bf16, ReLU gate applied), which layer l-1 takes
+    assert model.fuse_dz
     for l in reversed(range(L)):
         d_in = widths[l]
         Wn = Ws[l].cpu().numpy()
-        gate = (model.H[l] > 0).float() if l < L - 1 else None
         # dW over every row (a reduction over the whole graph)
         A_all = model.A[l][:, :d_in].float().cpu().numpy()
-        dZ_all = (G_out * gate if gate is not None else G_out).cpu().numpy().astype(np.float64)
+        dZ_all = (dY if l == L - 1 else model.dZ[l]).float().cpu().numpy().astype(np.float64)[:, :widths[l + 1]]
         dW_ref = orc.gemm(A_all.T, dZ_all, bf16=True)
         close(model.dW[l].cpu().numpy(), dW_ref, rtol=2e-2, what=f"layer {l} dW bar")
         # a sum over 2.45M rows whose terms largely cancel: fp32 accumulation
@@ -119,8 +122,10 @@ def test_large_gcn_stack_sampled(orc):
         dst = _out_targets(rp, co, rows_out, n)
         M, _, _ = _messages(orc, model.dA[l], dst, mask, d_in, bits, sb[l])
         dH_ref = orc.spmm_rows(rp, co, orc.COEF_GCN, rows_out, dst, M, transpose=True)
-        close(model.dH[l][oidx].cpu().numpy(), dH_ref, rtol=1e-4, what=f"layer {l} dH_in")
-        G_out = model.dH[l]
+        gate = model.H[l - 1][oidx].cpu().numpy() > 0
+        dZg = model.dZ[l - 1][oidx].float().cpu().numpy()[:, :d_in]
+        close(dZg, dH_ref * gate, rtol=5e-3, what=f"layer {l - 1} dZ (bf16, from layer {l}'s dH_in)")
+        assert np.all(dZg[~gate] == 0.0)
 
 
 def test_largest_aggregation_sampled(orc):

@@ -104,3 +104,24 @@ def test_three_layer_stack_error_shrinks_with_bits(orc):
         err[b] = float(torch.linalg.norm(y - ref) / torch.linalg.norm(ref))
     assert err[2] > err[4] > err[8], err
     assert err[8] < 2e-2 and err[2] < 1.0, err
+
+
+def test_stack_fused_dz_is_bit_identical(orc):
+    """The stack's fused backward (each transposed aggregation writes the
+    layer below's gated bf16 dZ) gives exactly the weight gradients of the
+    unfused one (fp32 gradient, then a separate gate-and-round pass)."""
+    from quantized_gnn_message_gb300.model import GCNStack
+    widths = (100, 128, 128, 47)
+    L = len(widths) - 1
+    q, g, G, X, Ws, mask, dY = _setup(widths, 0.6, seed=7)
+    Wd = [w.cuda() for w in Ws]
+    out = []
+    for fuse in (True, False):
+        model = GCNStack(G, widths, mask.cuda(), fuse_dz=fuse)
+        model.forward(X.cuda(), Wd, 2, _seeds(9, L, False))
+        model.backward(dY.cuda(), Wd, 2, _seeds(9, L, True), need_input_grad=True)
+        torch.cuda.synchronize()
+        assert int(model.err.item()) == 0
+        out.append([w.clone() for w in model.dW] + [model.dH[0].clone()])
+    for a, b in zip(*out):
+        assert torch.equal(a, b)
