@@ -1625,6 +1625,14 @@ __device__ __forceinline__ void w_flush(const SpmmParams& p, const WLane<C>& L, 
   }
 }
 
+// Ask L2 for the lane's part of row r's gate when the row becomes current, so
+// that the gate load of its flush, many edges later, does not wait on DRAM.
+template <int C>
+__device__ __forceinline__ void w_gate_prefetch(const SpmmParams& p, const WLane<C>& L, int64_t r) {
+  if (p.gate != nullptr && L.nv > 0)
+    asm volatile("prefetch.global.L2 [%0];" ::"l"(p.gate + r * p.ldg + L.c0));
+}
+
 // The coefficient of gathered row x with the row's kind in its sign bit
 // (set: a packed row of a mixing mask); coefficients are >= 0.
 template <int BITS, bool MX>
@@ -1653,6 +1661,7 @@ __device__ __forceinline__ void w_stream(const SpmmParams& p, const WLane<C>& L,
   int row = row0, rend = 0x7fffffff, rnext = 0x7fffffff;
   float rs = 1.0f, rsn = 1.0f;
   if (LIGHT) {
+    w_gate_prefetch(p, L, row0);
     rend = __ldg(p.rowptr + row0 + 1);
     rnext = row0 + 1 < row1 ? __ldg(p.rowptr + row0 + 2) : 0x7fffffff;
     if (p.rowscale) {
@@ -1696,6 +1705,7 @@ __device__ __forceinline__ void w_stream(const SpmmParams& p, const WLane<C>& L,
               for (int i = 0; i < C / 2; ++i) acc[i] = 0ull;
               accz = 0.0f;
               ++row;
+              if (row < row1) w_gate_prefetch(p, L, row);
               rend = rnext;
               rnext = row + 1 < row1 ? __ldg(p.rowptr + row + 2) : 0x7fffffff;
               rs = rsn;
