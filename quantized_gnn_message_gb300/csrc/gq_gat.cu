@@ -13,8 +13,10 @@
 //     P[v,k]      = sum_e alpha[e,k] dalpha[e,k]
 //     dE_pre[e,k] = alpha (dalpha - P) * (E_pre > 0 ? 1 : slope)
 //     dD[v,k]     = sum_e dE_pre[e,k]                      (in-edge sum)
-// gat_node_bwd_kernel  per source row u (transposed CSR):
-//     dS[u,k]     = sum_{e in out(u)} dE_pre[e,k]          (out-edge sum)
+// gat_node_heavy_kernel + gat_node_bwd_kernel  per source row u (transposed CSR):
+//     dS[u,k]     = sum_{e in out(u)} dE_pre[e,k]          (out-edge sum; rows
+//                   above the hub threshold as block tasks, the rest by lane
+//                   or warp within groups of 32 rows)
 //     dH'[u,c]    = dM[u,c] + dS[u,k] a_src[k,f] + dD[u,k] a_dst[k,f]
 //     partial sums of da_src = sum_u dS[u,k] H'[u,:], da_dst likewise.
 // edge_quant_kernel / edge_quant_heavy_kernel / edge_dequant_kernel
@@ -655,90 +657,16 @@ struct EdgeBwdParams {
   const float* S;
   const float* D;      // n x K
   float slope;
-  float* dEpre;        // E x K (holds dalpha between the passes)
+  float* dEpre;        // E x K (holds dalpha of the rows of more than 32 edges between the passes)
   float* dD;           // n x K
   int64_t n_rows;
-  int d, gshift;       // lanes per head = 1 << gshift (F / 8)
-  Sched sc;
+  int d, lph;          // lanes per head = F / 8
+  const int32_t* light;  // runs of light rows
+  int64_t n_light;
+  Sched sc;            // heavy-row tasks
+  float* Ppart;        // [task][K] sum of alpha dalpha over the task's edges
+  float* dDpart;       // [task][K] sum of dE_pre over the task's edges
 };
-
-// Pass 1 over edges [first batch ...): dalpha for each edge (all lanes of
-// the warp on one edge, lane l owning columns 8l..8l+7), stored to dEpre;
-// returns this warp's partial P for the lane's head (meaningful on the
-// head's first lane).
-template <int BITS, int K>
-__device__ __forceinline__ float eb_pass1(const EdgeBwdParams& p, int64_t beg, int64_t end, int first, int stride,
-                                          const float (&g)[8]) {
-  constexpr int U = 4;
-  const int lane = threadIdx.x & 31;
-  const int nchunks = p.d >> 3;
-  const bool live = lane < nchunks;
-  const int head = lane >> p.gshift;
-  const bool leader = live && (lane & ((1 << p.gshift) - 1)) == 0;
-  float P = 0.0f;
-  for (int64_t base = beg + 32 * (int64_t)first; base < end; base += 32 * (int64_t)stride) {
-    const int64_t e = base + lane;
-    int32_t x = 0;
-    bool qx = false;
-    if (e < end) {
-      x = __ldg(p.col + e);
-      qx = is_quant<BITS>(p.msg, x);
-    }
-    const int cnt = (int)min((int64_t)32, end - base);
-    for (int jj = 0; jj < cnt; jj += U) {
-      RawChunk<BITS> r[U];
-#pragma unroll
-      for (int t = 0; t < U; ++t) {
-        const int j = jj + t < cnt ? jj + t : 0;
-        const int32_t xj = __shfl_sync(FULL, x, j);
-        const bool qj = __shfl_sync(FULL, (int)qx, j) != 0;
-        if (live && jj + t < cnt) load_raw<BITS>(p.msg, xj, qj, lane, r[t]);
-      }
-#pragma unroll
-      for (int t = 0; t < U; ++t) {
-        float dot = 0.0f;
-        if (live && jj + t < cnt) {
-          float v[8];
-          decode<BITS>(r[t], v);
-#pragma unroll
-          for (int i = 0; i < 8; ++i) dot = __fmaf_rn(g[i], v[i], dot);
-        }
-        for (int o = 1; o < (1 << p.gshift); o <<= 1) dot += __shfl_xor_sync(FULL, dot, o);
-        if (leader && jj + t < cnt) {
-          const int64_t ej = base + jj + t;
-          const float a = __ldg(p.alpha + ej * K + head);
-          p.dEpre[ej * K + head] = dot;
-          P = __fmaf_rn(a, dot, P);
-        }
-      }
-    }
-  }
-  return P;
-}
-
-// Pass 2 (thread per edge): dE_pre from dalpha, P; returns the thread's
-// partial dD per head.
-template <int K>
-__device__ __forceinline__ void eb_pass2(const EdgeBwdParams& p, int64_t v, int64_t first, int64_t end,
-                                         int64_t stride, const float (&P)[K], float (&dd)[K]) {
-  float dv[K];
-  load_k<K>(p.D + v * K, dv);
-#pragma unroll
-  for (int k = 0; k < K; ++k) dd[k] = 0.0f;
-  for (int64_t e = first; e < end; e += stride) {
-    float s[K], a[K];
-    load_k<K>(p.S + (int64_t)__ldg(p.col + e) * K, s);
-    load_k<K>(p.alpha + e * K, a);
-#pragma unroll
-    for (int k = 0; k < K; ++k) {
-      const float da = __ldcg(p.dEpre + e * K + k);
-      const float dE = a[k] * (da - P[k]);
-      const float g = (s[k] + dv[k]) > 0.0f ? dE : p.slope * dE;
-      p.dEpre[e * K + k] = g;
-      dd[k] += g;
-    }
-  }
-}
 
 template <int K>
 __device__ __forceinline__ void warp_sum(float (&x)[K]) {
@@ -748,84 +676,225 @@ __device__ __forceinline__ void warp_sum(float (&x)[K]) {
     for (int k = 0; k < K; ++k) x[k] += __shfl_xor_sync(FULL, x[k], o);
 }
 
+// The SDDMM dot of the 32 edges [c0, c0 + cnt) (cnt <= 32; lane j holds
+// edge c0 + j's column id x): all lanes on one edge at a time, lane l owning
+// columns 8l .. 8l+7, U gathers in flight; the per-head sum ends in
+// sda[t * K + head] for edge c0 + t.
+template <int BITS, int K, int U>
+__device__ __forceinline__ void eb_dots(const EdgeBwdParams& p, int cnt, int32_t x, bool qx, const float (&g)[8],
+                                        float* sda) {
+  const int lane = threadIdx.x & 31;
+  const bool live = lane < (p.d >> 3);
+  const int head = live ? lane / p.lph : 0;
+  const bool leader = live && lane % p.lph == 0;
+  for (int t0 = 0; t0 < cnt; t0 += U) {
+    RawChunk<BITS> r[U];
+#pragma unroll
+    for (int t = 0; t < U; ++t) {
+      const int32_t xt = __shfl_sync(FULL, x, (t0 + t) & 31);
+      const bool qt = BITS < 32 && __shfl_sync(FULL, (int)qx, (t0 + t) & 31) != 0;
+      if (live && t0 + t < cnt) load_raw<BITS>(p.msg, xt, qt, lane, r[t]);
+    }
+#pragma unroll
+    for (int t = 0; t < U; ++t) {
+      float dot = 0.0f;
+      if (live && t0 + t < cnt) {
+        float v[8];
+        decode<BITS>(r[t], v);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) dot = __fmaf_rn(g[i], v[i], dot);
+      }
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1)
+        if (o < p.lph) dot += __shfl_xor_sync(FULL, dot, o);
+      if (leader && t0 + t < cnt) sda[(t0 + t) * K + head] = dot;
+    }
+  }
+}
+
+// dE_pre of one edge from dalpha, P and the LeakyReLU branch of its score.
+template <int K>
+__device__ __forceinline__ void eb_grad(const EdgeBwdParams& p, const float (&a)[K], const float (&da)[K],
+                                        const float (&P)[K], const float (&s)[K], const float (&dv)[K],
+                                        float (&dE)[K]) {
+#pragma unroll
+  for (int k = 0; k < K; ++k) {
+    const float t = a[k] * (da[k] - P[k]);
+    dE[k] = (s[k] + dv[k]) > 0.0f ? t : p.slope * t;
+  }
+}
+
+// Pass 1 over the edges [e0, e1) of one destination row (or a part of one):
+// the SDDMM dots, stored to dEpre when `keep` (the pass 2 reads them back),
+// and this lane's part of P = sum alpha dalpha.  For a single batch of at
+// most 32 edges the lane's edge, alpha, dalpha and S row stay in registers.
+template <int BITS, int K, int U>
+__device__ __forceinline__ void eb_pass1(const EdgeBwdParams& p, int64_t e0, int64_t e1, const float (&g)[8],
+                                         float* sda, bool keep, float (&P)[K], int32_t& x, float (&a)[K],
+                                         float (&da)[K], float (&s)[K]) {
+  const int lane = threadIdx.x & 31;
+  x = 0;
+#pragma unroll
+  for (int k = 0; k < K; ++k) P[k] = a[k] = da[k] = s[k] = 0.0f;
+  for (int64_t c0 = e0; c0 < e1; c0 += 32) {
+    const int64_t e = c0 + lane;
+    const bool has = e < e1;
+    x = has ? __ldg(p.col + e) : 0;
+    const bool qx = has && is_quant<BITS>(p.msg, x);
+#pragma unroll
+    for (int k = 0; k < K; ++k) a[k] = 0.0f;
+    if (has) load_k<K>(p.alpha + e * K, a);
+    if (!keep && has) load_k<K>(p.S + (int64_t)x * K, s);  // for pass 2, in flight during the dots
+    eb_dots<BITS, K, U>(p, (int)min((int64_t)32, e1 - c0), x, qx, g, sda);
+    __syncwarp();
+#pragma unroll
+    for (int k = 0; k < K; ++k) da[k] = has ? sda[lane * K + k] : 0.0f;
+    __syncwarp();  // sda is rewritten by the next batch
+    if (keep && has) store_k<K>(p.dEpre + e * K, da);
+#pragma unroll
+    for (int k = 0; k < K; ++k) P[k] = __fmaf_rn(a[k], da[k], P[k]);
+  }
+}
+
+// Pass 2 over [e0, e1) reading dalpha back from dEpre (thread per edge,
+// `stride` threads); returns the thread's part of dD.
+template <int K>
+__device__ __forceinline__ void eb_pass2_mem(const EdgeBwdParams& p, int64_t v, int64_t first, int64_t e1,
+                                             int64_t stride, const float (&P)[K], float (&dd)[K]) {
+  float dv[K];
+  load_k<K>(p.D + v * K, dv);
+#pragma unroll
+  for (int k = 0; k < K; ++k) dd[k] = 0.0f;
+  for (int64_t e = first; e < e1; e += stride) {
+    float s[K], a[K], da[K], dE[K];
+    load_k<K>(p.S + (int64_t)__ldg(p.col + e) * K, s);
+    load_k<K>(p.alpha + e * K, a);
+#pragma unroll
+    for (int k = 0; k < K; ++k) da[k] = __ldcg(p.dEpre + e * K + k);
+    eb_grad<K>(p, a, da, P, s, dv, dE);
+    store_k<K>(p.dEpre + e * K, dE);
+#pragma unroll
+    for (int k = 0; k < K; ++k) dd[k] += dE[k];
+  }
+}
+
+// Light rows (at most the hub threshold in-edges), one warp per row over the
+// graph's runs of light rows; heavy rows: first pass of each task, one block
+// per task, its eight warps on contiguous parts of the task's edges, the
+// task's P partial to Ppart.  gat_edge_bwd_heavy_kernel finishes them.
 template <int BITS, int K>
-__global__ void __launch_bounds__(kGatThreads) gat_edge_bwd_kernel(const EdgeBwdParams p) {
+__global__ void __launch_bounds__(kGatThreads, K <= 4 ? 4 : 3) gat_edge_bwd_kernel(const EdgeBwdParams p) {
+  constexpr int U = 2;
+  __shared__ float sda_all[kGatWarps][32 * K];
   __shared__ float red[kGatWarps][K];
   const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
-  const int nchunks = p.d >> 3;
+  const bool live = lane < (p.d >> 3);
+  float* sda = sda_all[w];
+  float g[8];
+  float P[K], a[K], da[K], s[K];
+  int32_t x;
   if ((int64_t)blockIdx.x < p.sc.n_tasks) {
     const int4 task = __ldg(reinterpret_cast<const int4*>(p.sc.tasks) + blockIdx.x);
     const int64_t v = task.x;
-    float g[8] = {};
-    if (lane < nchunks) {
-      const float4 a = ldg_f4(p.dOut + v * p.d + lane * 8), b = ldg_f4(p.dOut + v * p.d + lane * 8 + 4);
-      g[0] = a.x; g[1] = a.y; g[2] = a.z; g[3] = a.w; g[4] = b.x; g[5] = b.y; g[6] = b.z; g[7] = b.w;
-    }
-    const float Pw = eb_pass1<BITS, K>(p, task.y, task.z, w, kGatWarps, g);
-    // P per head from each warp's head leaders, summed in warp order
-    if (lane < nchunks && (lane & ((1 << p.gshift) - 1)) == 0) red[w][lane >> p.gshift] = Pw;
-    __syncthreads();
-    float P[K];
 #pragma unroll
-    for (int k = 0; k < K; ++k) {
-      P[k] = 0.0f;
-      for (int ww = 0; ww < kGatWarps; ++ww) P[k] += red[ww][k];
+    for (int i = 0; i < 8; ++i) g[i] = 0.0f;
+    if (live) {
+      const float4 u0 = ldg_f4(p.dOut + v * p.d + lane * 8), u1 = ldg_f4(p.dOut + v * p.d + lane * 8 + 4);
+      g[0] = u0.x; g[1] = u0.y; g[2] = u0.z; g[3] = u0.w; g[4] = u1.x; g[5] = u1.y; g[6] = u1.z; g[7] = u1.w;
     }
-    __syncthreads();
-    int64_t e0 = task.y, e1 = task.z;
-    if (task.w >= 0) {
-      const int4 grp = __ldg(reinterpret_cast<const int4*>(p.sc.groups) + task.w);
-      float* mine = p.sc.partial + (int64_t)(grp.w + ((int)blockIdx.x - grp.y)) * K;
-      if (threadIdx.x < K) mine[threadIdx.x] = P[threadIdx.x];
-      if (!last_of_group(p.sc, task.w, grp.z)) return;
-      const float* base = p.sc.partial + (int64_t)grp.w * K;
-#pragma unroll
-      for (int k = 0; k < K; ++k) {
-        P[k] = 0.0f;
-        for (int t = 0; t < grp.z; ++t) P[k] += __ldcg(base + t * K + k);
-      }
-      e0 = p.rowptr[v];
-      e1 = p.rowptr[v + 1];
-    }
-    float dd[K];
-    eb_pass2<K>(p, v, e0 + threadIdx.x, e1, kGatThreads, P, dd);
-    warp_sum<K>(dd);
+    const int len = task.z - task.y;
+    const int chunk = (len + kGatWarps - 1) / kGatWarps;
+    const int64_t b0 = min(task.y + w * chunk, task.z), b1 = min(b0 + chunk, (int64_t)task.z);
+    eb_pass1<BITS, K, U>(p, b0, b1, g, sda, true, P, x, a, da, s);
+    warp_sum<K>(P);
     if (lane == 0)
 #pragma unroll
-      for (int k = 0; k < K; ++k) red[w][k] = dd[k];
+      for (int k = 0; k < K; ++k) red[w][k] = P[k];
     __syncthreads();
     if (threadIdx.x < K) {
       float t = 0.0f;
       for (int ww = 0; ww < kGatWarps; ++ww) t += red[ww][threadIdx.x];
-      p.dD[v * K + threadIdx.x] = t;
+      p.Ppart[(int64_t)blockIdx.x * K + threadIdx.x] = t;
     }
     return;
   }
   const int64_t gw = ((int64_t)blockIdx.x - p.sc.n_tasks) * kGatWarps + w;
   const int64_t nw = ((int64_t)gridDim.x - p.sc.n_tasks) * kGatWarps;
-  for (int64_t v = gw; v < p.n_rows; v += nw) {
-    const int64_t a = p.rowptr[v], b = p.rowptr[v + 1];
-    if (b - a > p.sc.hub_threshold) continue;
-    float g[8] = {};
-    if (lane < nchunks) {
-      const float4 x = ldg_f4(p.dOut + v * p.d + lane * 8), y = ldg_f4(p.dOut + v * p.d + lane * 8 + 4);
-      g[0] = x.x; g[1] = x.y; g[2] = x.z; g[3] = x.w; g[4] = y.x; g[5] = y.y; g[6] = y.z; g[7] = y.w;
-    }
-    const float Pw = eb_pass1<BITS, K>(p, a, b, 0, 1, g);
-    float P[K];
+  for (int64_t t = gw; t < p.n_light; t += nw) {
+    const int2 run = __ldg(reinterpret_cast<const int2*>(p.light) + t);
+    int64_t b = __ldg(p.rowptr + run.x);
+    for (int64_t v = run.x; v < run.y; ++v) {
+      const int64_t a0 = b;
+      b = __ldg(p.rowptr + v + 1);
+      const bool one = b - a0 <= 32;
 #pragma unroll
-    for (int k = 0; k < K; ++k) P[k] = __shfl_sync(FULL, Pw, k << p.gshift);
-    __syncwarp();
-    float dd[K];
-    eb_pass2<K>(p, v, a + lane, b, 32, P, dd);
-    warp_sum<K>(dd);
-    if (lane < K) {
-      float t = dd[0];
+      for (int i = 0; i < 8; ++i) g[i] = 0.0f;
+      if (live && b > a0) {
+        const float4 u0 = ldg_f4(p.dOut + v * p.d + lane * 8), u1 = ldg_f4(p.dOut + v * p.d + lane * 8 + 4);
+        g[0] = u0.x; g[1] = u0.y; g[2] = u0.z; g[3] = u0.w; g[4] = u1.x; g[5] = u1.y; g[6] = u1.z; g[7] = u1.w;
+      }
+      eb_pass1<BITS, K, U>(p, a0, b, g, sda, !one, P, x, a, da, s);
+      float dv[K];
+      load_k<K>(p.D + v * K, dv);
+      warp_sum<K>(P);
+      float dd[K];
+      if (one) {
+        const bool has = a0 + lane < b;
+        float dE[K];
+        eb_grad<K>(p, a, da, P, s, dv, dE);
+        if (has) store_k<K>(p.dEpre + (a0 + lane) * K, dE);
 #pragma unroll
-      for (int k = 1; k < K; ++k)
-        if (lane == k) t = dd[k];
-      p.dD[v * K + lane] = t;
+        for (int k = 0; k < K; ++k) dd[k] = has ? dE[k] : 0.0f;
+      } else {
+        eb_pass2_mem<K>(p, v, a0 + lane, b, 32, P, dd);
+      }
+      warp_sum<K>(dd);
+      if (lane == 0) store_k<K>(p.dD + v * K, dd);
     }
+  }
+}
+
+// Second pass of the heavy rows, one block per task: P of the row (the
+// row's task partials summed in task order), dE_pre of the task's edges
+// (thread per edge), the task's dD partial; the last block of a split row
+// sums the partials in task order into dD.
+template <int K>
+__global__ void __launch_bounds__(kGatThreads) gat_edge_bwd_heavy_kernel(const EdgeBwdParams p) {
+  __shared__ float red[kGatWarps][K];
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  const int4 task = __ldg(reinterpret_cast<const int4*>(p.sc.tasks) + blockIdx.x);
+  int t0 = blockIdx.x, nt = 1;
+  if (task.w >= 0) {
+    const int4 grp = __ldg(reinterpret_cast<const int4*>(p.sc.groups) + task.w);
+    t0 = grp.y;
+    nt = grp.z;
+  }
+  float P[K];
+#pragma unroll
+  for (int k = 0; k < K; ++k) {
+    P[k] = 0.0f;
+    for (int i = 0; i < nt; ++i) P[k] += __ldcg(p.Ppart + (int64_t)(t0 + i) * K + k);
+  }
+  float dd[K];
+  eb_pass2_mem<K>(p, task.x, task.y + threadIdx.x, task.z, kGatThreads, P, dd);
+  warp_sum<K>(dd);
+  if (lane == 0)
+#pragma unroll
+    for (int k = 0; k < K; ++k) red[w][k] = dd[k];
+  __syncthreads();
+  float t = 0.0f;
+  if (threadIdx.x < K)
+    for (int ww = 0; ww < kGatWarps; ++ww) t += red[ww][threadIdx.x];
+  if (task.w < 0) {
+    if (threadIdx.x < K) p.dD[(int64_t)task.x * K + threadIdx.x] = t;
+    return;
+  }
+  if (threadIdx.x < K) p.dDpart[(int64_t)blockIdx.x * K + threadIdx.x] = t;
+  if (!last_of_group(p.sc, task.w, nt)) return;
+  if (threadIdx.x < K) {
+    float r = 0.0f;
+    for (int i = 0; i < nt; ++i) r += __ldcg(p.dDpart + (int64_t)(t0 + i) * K + threadIdx.x);
+    p.dD[(int64_t)task.x * K + threadIdx.x] = r;
   }
 }
 
@@ -843,9 +912,11 @@ struct NodeBwdParams {
   int64_t ldb;
   float* dHp32;         // optional n x d fp32 copy
   float* dS;            // optional n x K
+  float* dSh;           // n x K: dS of the rows above the hub threshold (gat_node_heavy_kernel)
   float* part;          // [block][2 d] partial da_src | da_dst
   int64_t n_rows;
   int d, fshift;
+  Sched sc;             // the transposed graph's heavy-row tasks
 };
 
 __device__ __forceinline__ uint32_t bf2(float lo, float hi) {
@@ -853,81 +924,186 @@ __device__ __forceinline__ uint32_t bf2(float lo, float hi) {
   return *reinterpret_cast<const uint32_t*>(&h);
 }
 
+// dS[u] = sum over the out-edges of u of dE_pre, for the rows above the hub
+// threshold: one block per task of the transposed schedule, four edges per
+// thread in flight; the tasks of a split row are summed in task order by
+// the last block of the row.
 template <int K>
-__global__ void __launch_bounds__(kGatThreads) gat_node_bwd_kernel(const NodeBwdParams p) {
+__global__ void __launch_bounds__(kGatThreads) gat_node_heavy_kernel(const NodeBwdParams p) {
+  __shared__ float red[kGatWarps][K];
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  const int4 task = __ldg(reinterpret_cast<const int4*>(p.sc.tasks) + blockIdx.x);
+  float ds[K];
+#pragma unroll
+  for (int k = 0; k < K; ++k) ds[k] = 0.0f;
+  for (int64_t e = task.y + threadIdx.x; e < task.z; e += 4 * kGatThreads) {
+    int32_t pe[4];
+#pragma unroll
+    for (int t = 0; t < 4; ++t) pe[t] = e + t * kGatThreads < task.z ? __ldg(p.tr_perm + e + t * kGatThreads) : -1;
+#pragma unroll
+    for (int t = 0; t < 4; ++t) {
+      if (pe[t] >= 0) {
+        float x[K];
+        load_k<K>(p.dEpre + (int64_t)pe[t] * K, x);
+#pragma unroll
+        for (int k = 0; k < K; ++k) ds[k] += x[k];
+      }
+    }
+  }
+  warp_sum<K>(ds);
+  if (lane == 0)
+#pragma unroll
+    for (int k = 0; k < K; ++k) red[w][k] = ds[k];
+  __syncthreads();
+  float t = 0.0f;
+  if (threadIdx.x < K)
+    for (int ww = 0; ww < kGatWarps; ++ww) t += red[ww][threadIdx.x];
+  if (task.w < 0) {
+    if (threadIdx.x < K) p.dSh[(int64_t)task.x * K + threadIdx.x] = t;
+    return;
+  }
+  const int4 grp = __ldg(reinterpret_cast<const int4*>(p.sc.groups) + task.w);
+  if (threadIdx.x < K) p.sc.partial[(int64_t)(grp.w + ((int)blockIdx.x - grp.y)) * K + threadIdx.x] = t;
+  if (!last_of_group(p.sc, task.w, grp.z)) return;
+  if (threadIdx.x < K) {
+    float r = 0.0f;
+    for (int i = 0; i < grp.z; ++i) r += __ldcg(p.sc.partial + (int64_t)(grp.w + i) * K + threadIdx.x);
+    p.dSh[(int64_t)task.x * K + threadIdx.x] = r;
+  }
+}
+
+// One warp per group of 32 consecutive source rows u:
+//   dS[u]  : a row of at most 32 out-edges is one lane's (its edges in order,
+//            four in flight, two for 8 heads); rows up to the hub threshold are the whole
+//            warp's; heavier rows were summed by gat_node_heavy_kernel;
+//   dH'[u] = dM[u] + dS[u,k] a_src + dD[u,k] a_dst, two rows at a time,
+//            lane l owning columns 8l .. 8l+7, with the partial sums of
+//            da_src = sum_u dS[u,k] H'[u] and da_dst = sum_u dD[u,k] H'[u].
+template <int K>
+__global__ void __launch_bounds__(kGatThreads, K == 8 ? 2 : 3) gat_node_bwd_kernel(const NodeBwdParams p) {
+  constexpr int UE = K <= 4 ? 4 : 2;  // out-edges in flight per lane
   extern __shared__ float sm[];  // [kGatWarps][2 d]
+  __shared__ float sds[kGatWarps][32 * K];
+  __shared__ __align__(16) float sa[2][256];  // a_src | a_dst
   const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
   const int nchunks = p.d >> 3;
   const bool live = lane < nchunks;
-  const int head = (lane * 8) >> p.fshift;
-  float as[8] = {}, ad[8] = {};
-  if (live) {
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      as[i] = __ldg(p.a_src + lane * 8 + i);
-      ad[i] = __ldg(p.a_dst + lane * 8 + i);
-    }
+  const int head = live ? (lane * 8) >> p.fshift : 0;
+  for (int j = threadIdx.x; j < p.d; j += blockDim.x) {
+    sa[0][j] = __ldg(p.a_src + j);
+    sa[1][j] = __ldg(p.a_dst + j);
   }
+  __syncthreads();
   float acc_s[8] = {}, acc_d[8] = {};
-  const int64_t gw = (int64_t)blockIdx.x * kGatWarps + w;
-  const int64_t nw = (int64_t)gridDim.x * kGatWarps;
-  for (int64_t u = gw; u < p.n_rows; u += nw) {
-    const int64_t a = p.tr_rowptr[u], b = p.tr_rowptr[u + 1];
-    // the node's rows first: they do not depend on the out-edge sums
-    float4 m0 = make_float4(0.f, 0.f, 0.f, 0.f), m1 = m0, h0 = m0, h1 = m0;
-    float ddh = 0.0f;
-    if (live) {
-      m0 = ldg_f4(p.dM + u * p.d + lane * 8);
-      m1 = ldg_f4(p.dM + u * p.d + lane * 8 + 4);
-      h0 = ldg_f4(p.Hp + u * p.d + lane * 8);
-      h1 = ldg_f4(p.Hp + u * p.d + lane * 8 + 4);
-      ddh = __ldg(p.dD + u * K + head);
+  float* myds = sds[w];
+  const int64_t groups = (p.n_rows + 31) / 32;
+  for (int64_t grp = (int64_t)blockIdx.x * kGatWarps + w; grp < groups; grp += (int64_t)gridDim.x * kGatWarps) {
+    const int64_t u0 = grp * 32;
+    const int rows = (int)min((int64_t)32, p.n_rows - u0);
+    // dS of the group's rows
+    int64_t a = 0, b = 0;
+    if (lane < rows) {
+      a = __ldg(p.tr_rowptr + u0 + lane);
+      b = __ldg(p.tr_rowptr + u0 + lane + 1);
     }
     float ds[K];
 #pragma unroll
     for (int k = 0; k < K; ++k) ds[k] = 0.0f;
-    for (int64_t e = a + lane; e < b; e += 4 * 32) {  // four out-edges per lane at a time
-      int32_t pe[4];
+    if (b - a > p.sc.hub_threshold) {
+      load_k<K>(p.dSh + (u0 + lane) * K, ds);
+    } else if (b - a <= 32) {
+      for (int64_t e = a; e < b; e += UE) {
+        int32_t pe[UE];
 #pragma unroll
-      for (int t = 0; t < 4; ++t) pe[t] = e + 32 * t < b ? __ldg(p.tr_perm + e + 32 * t) : -1;
+        for (int t = 0; t < UE; ++t) pe[t] = e + t < b ? __ldg(p.tr_perm + e + t) : -1;
 #pragma unroll
-      for (int t = 0; t < 4; ++t) {
-        if (pe[t] >= 0) {
-          float x[K];
-          load_k<K>(p.dEpre + (int64_t)pe[t] * K, x);
+        for (int t = 0; t < UE; ++t) {
+          if (pe[t] >= 0) {
+            float x[K];
+            load_k<K>(p.dEpre + (int64_t)pe[t] * K, x);
 #pragma unroll
-          for (int k = 0; k < K; ++k) ds[k] += x[k];
+            for (int k = 0; k < K; ++k) ds[k] += x[k];
+          }
         }
       }
     }
-    warp_sum<K>(ds);
-    float dsh = ds[0];
 #pragma unroll
-    for (int k = 1; k < K; ++k)
-      if (head == k) dsh = ds[k];
-    if (p.dS != nullptr && lane < K) {
-      float t = ds[0];
+    for (int k = 0; k < K; ++k) myds[lane * K + k] = ds[k];
+    __syncwarp();  // lane 0 overwrites the slots of the warp-summed rows below
+    unsigned mid = __ballot_sync(FULL, b - a > 32 && b - a <= p.sc.hub_threshold);
+    while (mid != 0) {
+      const int l0 = __ffs(mid) - 1;
+      mid &= mid - 1;
+      const int64_t va = __shfl_sync(FULL, a, l0), vb = __shfl_sync(FULL, b, l0);
+      float hs[K];
 #pragma unroll
-      for (int k = 1; k < K; ++k)
-        if (lane == k) t = ds[k];
-      p.dS[u * K + lane] = t;
-    }
-    if (!live) continue;
-    const float mv[8] = {m0.x, m0.y, m0.z, m0.w, m1.x, m1.y, m1.z, m1.w};
-    const float hv[8] = {h0.x, h0.y, h0.z, h0.w, h1.x, h1.y, h1.z, h1.w};
-    float o[8];
+      for (int k = 0; k < K; ++k) hs[k] = 0.0f;
+      for (int64_t e = va + lane; e < vb; e += UE * 32) {
+        int32_t pe[UE];
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      o[i] = mv[i] + dsh * as[i] + ddh * ad[i];
-      acc_s[i] = __fmaf_rn(dsh, hv[i], acc_s[i]);
-      acc_d[i] = __fmaf_rn(ddh, hv[i], acc_d[i]);
+        for (int t = 0; t < UE; ++t) pe[t] = e + 32 * t < vb ? __ldg(p.tr_perm + e + 32 * t) : -1;
+#pragma unroll
+        for (int t = 0; t < UE; ++t) {
+          if (pe[t] >= 0) {
+            float x[K];
+            load_k<K>(p.dEpre + (int64_t)pe[t] * K, x);
+#pragma unroll
+            for (int k = 0; k < K; ++k) hs[k] += x[k];
+          }
+        }
+      }
+      warp_sum<K>(hs);
+      if (lane == 0)
+#pragma unroll
+        for (int k = 0; k < K; ++k) myds[l0 * K + k] = hs[k];
     }
-    *reinterpret_cast<uint4*>(p.dHp + u * p.ldb + lane * 8) =
-        make_uint4(bf2(o[0], o[1]), bf2(o[2], o[3]), bf2(o[4], o[5]), bf2(o[6], o[7]));
-    if (p.dHp32 != nullptr) {
-      st_f4(p.dHp32 + u * p.d + lane * 8, o[0], o[1], o[2], o[3]);
-      st_f4(p.dHp32 + u * p.d + lane * 8 + 4, o[4], o[5], o[6], o[7]);
+    __syncwarp();
+    if (p.dS != nullptr)
+      for (int j = lane; j < rows * K; j += 32) p.dS[u0 * K + j] = myds[j];
+    // dH' and the da partials, two rows at a time
+    for (int i = 0; i < rows; i += 2) {
+      float4 m[2][2], h[2][2];
+      float dsh[2], ddh[2];
+#pragma unroll
+      for (int r = 0; r < 2; ++r) {
+        const int64_t u = u0 + i + r;
+        if (live && i + r < rows) {
+          m[r][0] = ldg_f4(p.dM + u * p.d + lane * 8);
+          m[r][1] = ldg_f4(p.dM + u * p.d + lane * 8 + 4);
+          h[r][0] = ldg_f4(p.Hp + u * p.d + lane * 8);
+          h[r][1] = ldg_f4(p.Hp + u * p.d + lane * 8 + 4);
+          ddh[r] = __ldg(p.dD + u * K + head);
+          dsh[r] = myds[(i + r) * K + head];
+        }
+      }
+#pragma unroll
+      for (int r = 0; r < 2; ++r) {
+        const int64_t u = u0 + i + r;
+        if (!live || i + r >= rows) continue;
+        const float mv[8] = {m[r][0].x, m[r][0].y, m[r][0].z, m[r][0].w, m[r][1].x, m[r][1].y, m[r][1].z, m[r][1].w};
+        const float hv[8] = {h[r][0].x, h[r][0].y, h[r][0].z, h[r][0].w, h[r][1].x, h[r][1].y, h[r][1].z, h[r][1].w};
+        const float4 as0 = *reinterpret_cast<const float4*>(&sa[0][lane * 8]);
+        const float4 as1 = *reinterpret_cast<const float4*>(&sa[0][lane * 8 + 4]);
+        const float4 ad0 = *reinterpret_cast<const float4*>(&sa[1][lane * 8]);
+        const float4 ad1 = *reinterpret_cast<const float4*>(&sa[1][lane * 8 + 4]);
+        const float as[8] = {as0.x, as0.y, as0.z, as0.w, as1.x, as1.y, as1.z, as1.w};
+        const float ad[8] = {ad0.x, ad0.y, ad0.z, ad0.w, ad1.x, ad1.y, ad1.z, ad1.w};
+        float o[8];
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+          o[c] = mv[c] + dsh[r] * as[c] + ddh[r] * ad[c];
+          acc_s[c] = __fmaf_rn(dsh[r], hv[c], acc_s[c]);
+          acc_d[c] = __fmaf_rn(ddh[r], hv[c], acc_d[c]);
+        }
+        *reinterpret_cast<uint4*>(p.dHp + u * p.ldb + lane * 8) =
+            make_uint4(bf2(o[0], o[1]), bf2(o[2], o[3]), bf2(o[4], o[5]), bf2(o[6], o[7]));
+        if (p.dHp32 != nullptr) {
+          st_f4(p.dHp32 + u * p.d + lane * 8, o[0], o[1], o[2], o[3]);
+          st_f4(p.dHp32 + u * p.d + lane * 8 + 4, o[4], o[5], o[6], o[7]);
+        }
+      }
     }
+    __syncwarp();  // the group's dS slots are rewritten by the next group
   }
   if (live)
 #pragma unroll
@@ -1024,8 +1200,17 @@ int launch_edge_dequant(const EdgeQuantParams& p, cudaStream_t s) {
 
 template <int BITS, int K>
 int launch_edge_bwd(const EdgeBwdParams& p, cudaStream_t s) {
-  gat_edge_bwd_kernel<BITS, K><<<light_grid(p.n_rows, p.sc.n_tasks), kGatThreads, 0, s>>>(p);
-  return launch_status();
+  int64_t light = (p.n_light + kGatWarps - 1) / kGatWarps;
+  const int64_t cap = (int64_t)sm_count() * (K <= 4 ? 4 : 3);
+  if (light > cap) light = cap;
+  if (light < 1) light = 1;
+  gat_edge_bwd_kernel<BITS, K><<<(unsigned)(light + p.sc.n_tasks), kGatThreads, 0, s>>>(p);
+  GQ_TRY(launch_status());
+  if (p.sc.n_tasks > 0) {
+    gat_edge_bwd_heavy_kernel<K><<<(unsigned)p.sc.n_tasks, kGatThreads, 0, s>>>(p);
+    GQ_TRY(launch_status());
+  }
+  return GQ_OK;
 }
 
 }  // namespace
@@ -1035,7 +1220,12 @@ int launch_edge_bwd(const EdgeBwdParams& p, cudaStream_t s) {
 size_t edge_softmax_workspace(const gq_graph* g, int heads) {
   return ((size_t)g->sched.n_tasks * 2 * heads * sizeof(float) + 255) / 256 * 256;
 }
-size_t edge_bwd_workspace(const gq_graph* g, int heads) { return sched_ws(g->sched, heads); }
+// [task][K] P partials | [task][K] dD partials | tickets of the split rows
+size_t edge_bwd_workspace(const gq_graph* g, int heads) {
+  if (g->sched.n_tasks == 0) return 0;
+  const size_t part = ((size_t)g->sched.n_tasks * heads * sizeof(float) + 255) / 256 * 256;
+  return 2 * part + ((size_t)g->sched.n_groups * sizeof(int) + 255) / 256 * 256;
+}
 
 int edge_softmax(const gq_graph* g, const float* S, const float* D, int heads, float slope, float* Epre,
                  float* alpha, void* ws, size_t ws_bytes, cudaStream_t s) {
@@ -1130,9 +1320,7 @@ int gat_edge_bwd(const gq_graph* g, const float* dOut, const float* Hp, const ui
   if (!(heads == 1 || heads == 2 || heads == 4 || heads == 8)) return GQ_ERR_UNSUPPORTED;
   if (d < 8 || d > 256 || d % heads) return GQ_ERR_UNSUPPORTED;
   const int F = d / heads;
-  int gshift = 0;
-  while ((8 << gshift) < F) ++gshift;
-  if ((8 << gshift) != F) return GQ_ERR_UNSUPPORTED;  // head width: 8 * power of two
+  if (F % 8 || ((F / 8) & (F / 8 - 1))) return GQ_ERR_UNSUPPORTED;  // head width: 8 * power of two
   EdgeBwdParams p{};
   p.rowptr = g->rowptr;
   p.col = g->col;
@@ -1147,11 +1335,19 @@ int gat_edge_bwd(const gq_graph* g, const float* dOut, const float* Hp, const ui
   p.dD = dD;
   p.n_rows = g->n;
   p.d = d;
-  p.gshift = gshift;
+  p.lph = F / 8;
+  p.light = g->sched.light;
+  p.n_light = g->sched.n_light;
   const size_t need = edge_bwd_workspace(g, heads);
   if (need > 0 && (ws == nullptr || ws_bytes < need || !aligned(ws, 256))) return GQ_ERR_WORKSPACE;
-  p.sc = make_sched(g->sched, g->hub_threshold, ws, heads);
-  if (g->sched.n_groups > 0) GQ_TRY_CUDA(cudaMemsetAsync(p.sc.tickets, 0, g->sched.n_groups * sizeof(int), s));
+  p.sc = make_sched(g->sched, g->hub_threshold, nullptr, 0);
+  if (g->sched.n_tasks > 0) {
+    const size_t part = ((size_t)g->sched.n_tasks * heads * sizeof(float) + 255) / 256 * 256;
+    p.Ppart = static_cast<float*>(ws);
+    p.dDpart = reinterpret_cast<float*>(static_cast<char*>(ws) + part);
+    p.sc.tickets = reinterpret_cast<int*>(static_cast<char*>(ws) + 2 * part);
+    if (g->sched.n_groups > 0) GQ_TRY_CUDA(cudaMemsetAsync(p.sc.tickets, 0, g->sched.n_groups * sizeof(int), s));
+  }
 #define GQ_EB(B)                                       \
   switch (heads) {                                     \
     case 1: return launch_edge_bwd<B, 1>(p, s);        \
@@ -1168,19 +1364,29 @@ int gat_edge_bwd(const gq_graph* g, const float* dOut, const float* Hp, const ui
 #undef GQ_EB
 }
 
-int node_bwd_blocks() { return sm_count() * 3; }  // the blocks resident at 80 registers a thread
+// the blocks resident at 85 registers a thread (at most 128 with 8 heads)
+int node_bwd_blocks(int heads = 1) { return sm_count() * (heads == 8 ? 2 : 3); }
 
-size_t node_bwd_workspace(int d) { return (size_t)node_bwd_blocks() * 2 * d * sizeof(float) + 256; }
+// [block][2 d] da partials | [n][K] dS of the heavy rows | their task partials and tickets
+size_t node_bwd_workspace(const gq_graph* g, int heads, int d) {
+  const size_t a = ((size_t)node_bwd_blocks() * 2 * d * sizeof(float) + 255) / 256 * 256;
+  const size_t b = ((size_t)g->n * heads * sizeof(float) + 255) / 256 * 256;
+  return a + b + sched_ws(g->tr_sched, heads) + 256;
+}
 
 int gat_node_bwd(const gq_graph* g, const float* dEpre, const float* dD, const float* dM, const float* Hp,
                  const float* a_src, const float* a_dst, int heads, int d, void* dHp_bf16, int64_t ldb, float* dHp32,
                  float* dS, float* da_src, float* da_dst, void* ws, size_t ws_bytes, cudaStream_t s) {
+  if (g == nullptr) return GQ_ERR_INVALID_ARG;
   if (d < 8 || d > 256 || d % 8 || d % heads) return GQ_ERR_UNSUPPORTED;
+  if (!(heads == 1 || heads == 2 || heads == 4 || heads == 8)) return GQ_ERR_UNSUPPORTED;
   const int F = d / heads;
   int fshift = 0;
   while ((1 << fshift) < F) ++fshift;
   if ((1 << fshift) != F || F < 8) return GQ_ERR_UNSUPPORTED;
-  if (ws == nullptr || ws_bytes < node_bwd_workspace(d)) return GQ_ERR_WORKSPACE;
+  if (ws == nullptr || ws_bytes < node_bwd_workspace(g, heads, d) || !aligned(ws, 256)) return GQ_ERR_WORKSPACE;
+  const int blocks = node_bwd_blocks(heads);
+  char* wp = static_cast<char*>(ws);
   NodeBwdParams p{};
   p.tr_rowptr = g->tr_rowptr;
   p.tr_perm = g->tr_perm;
@@ -1194,19 +1400,31 @@ int gat_node_bwd(const gq_graph* g, const float* dEpre, const float* dD, const f
   p.ldb = ldb;
   p.dHp32 = dHp32;
   p.dS = dS;
-  p.part = static_cast<float*>(ws);
+  p.part = reinterpret_cast<float*>(wp);
+  wp += ((size_t)node_bwd_blocks() * 2 * d * sizeof(float) + 255) / 256 * 256;
+  p.dSh = reinterpret_cast<float*>(wp);
+  wp += ((size_t)g->n * heads * sizeof(float) + 255) / 256 * 256;
   p.n_rows = g->n;
   p.d = d;
   p.fshift = fshift;
-  const int blocks = node_bwd_blocks();
+  p.sc = make_sched(g->tr_sched, g->hub_threshold, wp, heads);
   const size_t smem = sizeof(float) * kGatWarps * 2 * d;
+  if (g->tr_sched.n_groups > 0)
+    GQ_TRY_CUDA(cudaMemsetAsync(p.sc.tickets, 0, g->tr_sched.n_groups * sizeof(int), s));
+#define GQ_NB(KK)                                                                                             \
+  if (p.sc.n_tasks > 0) {                                                                                     \
+    gat_node_heavy_kernel<KK><<<(unsigned)p.sc.n_tasks, kGatThreads, 0, s>>>(p);                              \
+    GQ_TRY(launch_status());                                                                                  \
+  }                                                                                                           \
+  gat_node_bwd_kernel<KK><<<blocks, kGatThreads, smem, s>>>(p);                                               \
+  break;
   switch (heads) {
-    case 1: gat_node_bwd_kernel<1><<<blocks, kGatThreads, smem, s>>>(p); break;
-    case 2: gat_node_bwd_kernel<2><<<blocks, kGatThreads, smem, s>>>(p); break;
-    case 4: gat_node_bwd_kernel<4><<<blocks, kGatThreads, smem, s>>>(p); break;
-    case 8: gat_node_bwd_kernel<8><<<blocks, kGatThreads, smem, s>>>(p); break;
-    default: return GQ_ERR_UNSUPPORTED;
+    case 1: GQ_NB(1)
+    case 2: GQ_NB(2)
+    case 4: GQ_NB(4)
+    default: GQ_NB(8)
   }
+#undef GQ_NB
   GQ_TRY(launch_status());
   sum_blocks_kernel<<<(2 * d + 255) / 256, 256, 0, s>>>(p.part, blocks, 2 * d, da_src, da_dst, d);
   return launch_status();

@@ -62,7 +62,7 @@ namespace gq {
 // GAT edge kernels (gq_gat.cu)
 size_t edge_softmax_workspace(const gq_graph* g, int heads);
 size_t edge_bwd_workspace(const gq_graph* g, int heads);
-size_t node_bwd_workspace(int d);
+size_t node_bwd_workspace(const gq_graph* g, int heads, int d);
 int edge_softmax(const gq_graph* g, const float* S, const float* D, int heads, float slope, float* Epre,
                  float* alpha, void* ws, size_t ws_bytes, cudaStream_t s);
 size_t edge_quant_workspace(const gq_graph* g, int heads);

@@ -214,7 +214,7 @@ Carve carve_gat(const gq_graph* g, void* ws, size_t ws_bytes, int d_in, int head
   w.dD = static_cast<float*>(c.take((size_t)n * heads * sizeof(float)));
   w.dM = static_cast<float*>(c.take((size_t)n * d * sizeof(float)));
   w.dhb = c.take((size_t)n * d * 2);
-  w.nb_bytes = node_bwd_workspace(d);
+  w.nb_bytes = node_bwd_workspace(g, heads, d);
   w.nb = c.take(w.nb_bytes);
   w.wg_bytes = wgrad_workspace(n, d_in, d);
   w.wg = c.take(w.wg_bytes);
