@@ -15,8 +15,10 @@
 //   warp 1  allocates TMEM; one thread issues tcgen05.mma (M=128, N<=256,
 //           K=16 per instruction) into one of two TMEM accumulators and
 //           commits stage releases / accumulator-ready to mbarriers;
-//   warps 2-5  epilogue: tcgen05.ld 16 columns at a time (thread = row),
-//           activation, optional GAT head projections, fp32 stores; then
+//   warps 2-9  epilogue: warp w reads TMEM lanes 32 (w % 4) .. +31 (thread =
+//           row) over one half of the columns, 32 columns per wait,
+//           activation, optional GAT head projections (the head vectors in
+//           shared memory), fp32 stores staged through shared memory; then
 //           release the accumulator, so the next tile's MMAs overlap it.
 // Weight GEMM: grid (M tiles of K1) x (row splits); both operands MN-major
 // (their rows are the contraction), one TMEM accumulator per CTA, fp32
@@ -31,7 +33,8 @@
 namespace gq {
 namespace {
 
-constexpr int kRgThreads = 192;
+constexpr int kRgThreads = 320;  // TMA warp, MMA warp, 8 epilogue warps
+constexpr int kRgEpiWarps = 8;
 constexpr int kTileM = 128;
 constexpr int kChunkK = 64;                       // bf16 elements per 128-byte swizzle row
 constexpr int kATileBytes = kTileM * kChunkK * 2;  // 16 KB
@@ -39,7 +42,8 @@ constexpr int kSmemBudget = 225 * 1024;
 // epilogue staging: per epilogue warp, 32 rows x 16 columns of fp32 at a row
 // pitch of 20 floats (conflict-free 16-byte writes by row)
 constexpr int kStgPitch = 20;
-constexpr int kStgBytes = 4 * 32 * kStgPitch * 4;
+constexpr int kStgBytes = kRgEpiWarps * 32 * kStgPitch * 4;
+constexpr int kVecBytes = 2 * 256 * 4;  // a_src | a_dst of the GAT head projections
 
 // ---------------------------------------------------------------- host ---
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
@@ -85,6 +89,7 @@ struct RowGemmArgs {
   int64_t ldc;
   int act;
   int vec;
+  int half;             // columns [0, half) to epilogue warps 2-5, [half, Npad) to warps 6-9
   const float* a_src;   // optional GAT head projections
   const float* a_dst;
   float* S;
@@ -108,6 +113,7 @@ __global__ void __launch_bounds__(kRgThreads, 1)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tempty + 2);
   volatile int* abort = reinterpret_cast<volatile int*>(tmem_slot + 1);
   float* stg_all = reinterpret_cast<float*>(sA + (size_t)p.stages * kATileBytes + 256);
+  float* svec = stg_all + kStgBytes / 4;  // [2][Npad]
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
@@ -118,7 +124,7 @@ __global__ void __launch_bounds__(kRgThreads, 1)
     mbar_init(bfull, 1);
     for (int a = 0; a < 2; ++a) {
       mbar_init(&tfull[a], 1);
-      mbar_init(&tempty[a], 4);
+      mbar_init(&tempty[a], kRgEpiWarps);
     }
     *abort = 0;
     fence_barrier_init();
@@ -127,6 +133,11 @@ __global__ void __launch_bounds__(kRgThreads, 1)
     tmem_alloc(tmem_slot, p.tmem_cols);
     tmem_relinquish();
   }
+  if (p.S != nullptr)
+    for (int j = threadIdx.x; j < p.Npad; j += kRgThreads) {
+      svec[j] = j < p.N ? __ldg(p.a_src + j) : 0.0f;
+      svec[p.Npad + j] = j < p.N ? __ldg(p.a_dst + j) : 0.0f;
+    }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -192,7 +203,9 @@ __global__ void __launch_bounds__(kRgThreads, 1)
   } else {
     const int q = warp & 3;
     const int row_in_tile = q * 32 + lane;
-    float* stg = stg_all + q * 32 * kStgPitch;
+    const int h = (warp - 2) >> 2;
+    const int cb = h ? p.half : 0, ce = h ? p.Npad : p.half;
+    float* stg = stg_all + (warp - 2) * 32 * kStgPitch;
     int i = 0;
     for (int64_t t = blockIdx.x; t < ntiles; t += gridDim.x, ++i) {
       const int a = i & 1;
@@ -207,40 +220,53 @@ __global__ void __launch_bounds__(kRgThreads, 1)
       const uint32_t taddr = tmem + ((uint32_t)(q * 32) << 16) + a * p.acc_stride;
       float* crow = p.C + row * p.ldc;
       float hs = 0.0f, hd = 0.0f;
-      for (int c0 = 0; c0 < p.Npad; c0 += 16) {
-        uint32_t r[16];
-        tmem_ld16(taddr + c0, r);
+      for (int c1 = cb; c1 < ce; c1 += 32) {
+        const int nc = ce - c1 >= 32 ? 2 : 1;  // 16-column chunks this round
+        uint32_t r[2][16];
+        tmem_ld16(taddr + c1, r[0]);
+        if (nc == 2) tmem_ld16(taddr + c1 + 16, r[1]);
         tmem_ld_wait();
-        float v[16];
 #pragma unroll
-        for (int j = 0; j < 16; ++j) {
-          v[j] = __uint_as_float(r[j]);
-          if (p.act == GQ_ACT_RELU) v[j] = fmaxf(v[j], 0.0f);
-        }
-        if (p.vec && c0 + 16 <= p.N) {
-          // through shared memory, so that each store instruction writes 8
-          // rows x 64 contiguous bytes instead of 32 rows x 16 bytes
+        for (int u = 0; u < 2; ++u) {
+          if (u >= nc) break;
+          const int c0 = c1 + 16 * u;
+          float v[16];
 #pragma unroll
-          for (int j = 0; j < 16; j += 4)
-            *reinterpret_cast<float4*>(stg + lane * kStgPitch + j) = make_float4(v[j], v[j + 1], v[j + 2], v[j + 3]);
-          __syncwarp();
-#pragma unroll
-          for (int k = 0; k < 4; ++k) {
-            const int rr = 8 * k + (lane >> 2), cg = 4 * (lane & 3);
-            const int64_t grow = t * kTileM + q * 32 + rr;
-            const float4 o = *reinterpret_cast<const float4*>(stg + rr * kStgPitch + cg);
-            if (grow < p.M) *reinterpret_cast<float4*>(p.C + grow * p.ldc + c0 + cg) = o;
+          for (int j = 0; j < 16; ++j) {
+            v[j] = __uint_as_float(r[u][j]);
+            if (p.act == GQ_ACT_RELU) v[j] = fmaxf(v[j], 0.0f);
           }
-          __syncwarp();
-        } else if (live) {
-          for (int j = 0; j < 16 && c0 + j < p.N; ++j) crow[c0 + j] = v[j];
-        }
-        if (live) {
-          if (p.S != nullptr && c0 < p.N) {
+          if (p.vec && c0 + 16 <= p.N) {
+            // through shared memory, so that each store instruction writes 8
+            // rows x 64 contiguous bytes instead of 32 rows x 16 bytes
 #pragma unroll
-            for (int j = 0; j < 16; ++j) {
-              hs = __fmaf_rn(v[j], __ldg(p.a_src + c0 + j), hs);
-              hd = __fmaf_rn(v[j], __ldg(p.a_dst + c0 + j), hd);
+            for (int j = 0; j < 16; j += 4)
+              *reinterpret_cast<float4*>(stg + lane * kStgPitch + j) = make_float4(v[j], v[j + 1], v[j + 2], v[j + 3]);
+            __syncwarp();
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+              const int rr = 8 * k + (lane >> 2), cg = 4 * (lane & 3);
+              const int64_t grow = t * kTileM + q * 32 + rr;
+              const float4 o = *reinterpret_cast<const float4*>(stg + rr * kStgPitch + cg);
+              if (grow < p.M) *reinterpret_cast<float4*>(p.C + grow * p.ldc + c0 + cg) = o;
+            }
+            __syncwarp();
+          } else if (live) {
+            for (int j = 0; j < 16 && c0 + j < p.N; ++j) crow[c0 + j] = v[j];
+          }
+          if (live && p.S != nullptr && c0 < p.N) {
+#pragma unroll
+            for (int j = 0; j < 16; j += 4) {
+              const float4 as = *reinterpret_cast<const float4*>(svec + c0 + j);
+              const float4 ad = *reinterpret_cast<const float4*>(svec + p.Npad + c0 + j);
+              hs = __fmaf_rn(v[j], as.x, hs);
+              hs = __fmaf_rn(v[j + 1], as.y, hs);
+              hs = __fmaf_rn(v[j + 2], as.z, hs);
+              hs = __fmaf_rn(v[j + 3], as.w, hs);
+              hd = __fmaf_rn(v[j], ad.x, hd);
+              hd = __fmaf_rn(v[j + 1], ad.y, hd);
+              hd = __fmaf_rn(v[j + 2], ad.z, hd);
+              hd = __fmaf_rn(v[j + 3], ad.w, hd);
             }
             if (((c0 + 16) >> p.fshift) != (c0 >> p.fshift) || c0 + 16 >= p.N) {
               const int head = c0 >> p.fshift;
@@ -486,7 +512,7 @@ int row_gemm(const void* A, int64_t M, int K, int64_t lda, const void* B, int N,
   p.K = K;
   p.kch = (K + kChunkK - 1) / kChunkK;
   const int b_bytes = p.kch * p.Npad * 128;
-  p.stages = (kSmemBudget - 2048 - b_bytes - kStgBytes) / kATileBytes;
+  p.stages = (kSmemBudget - 2048 - b_bytes - kStgBytes - kVecBytes) / kATileBytes;
   if (p.stages > 8) p.stages = 8;
   if (p.stages < 2) return GQ_ERR_UNSUPPORTED;
   p.tmem_cols = pow2_at_least(2 * (uint32_t)p.Npad);
@@ -495,6 +521,10 @@ int row_gemm(const void* A, int64_t M, int K, int64_t lda, const void* B, int N,
   p.ldc = ldc;
   p.act = act;
   p.vec = (ldc % 4 == 0) && aligned(C, 16);
+  // the two epilogue column halves, 16-aligned; with head projections a
+  // half holds whole heads, else every column goes to the first half
+  p.half = (p.Npad / 2 + 15) / 16 * 16;
+  if (S != nullptr && p.half % (1 << fshift) != 0) p.half = p.Npad;
   p.a_src = a_src;
   p.a_dst = a_dst;
   p.S = S;
@@ -505,7 +535,7 @@ int row_gemm(const void* A, int64_t M, int K, int64_t lda, const void* B, int N,
   CUtensorMap tmA, tmB;
   GQ_TRY(make_tmap(&tmA, A, (uint64_t)K, (uint64_t)M, (uint64_t)lda, kChunkK, kTileM));
   GQ_TRY(make_tmap(&tmB, B, (uint64_t)K, (uint64_t)N, (uint64_t)ldb, kChunkK, (uint32_t)p.Npad));
-  const size_t smem = 1024 + (size_t)b_bytes + (size_t)p.stages * kATileBytes + 256 + kStgBytes;
+  const size_t smem = 1024 + (size_t)b_bytes + (size_t)p.stages * kATileBytes + 256 + kStgBytes + kVecBytes;
   GQ_TRY_CUDA(cudaFuncSetAttribute(row_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem));
   const int64_t ntiles = (M + kTileM - 1) / kTileM;
   const int grid = (int)(ntiles < sm_count() ? ntiles : sm_count());
