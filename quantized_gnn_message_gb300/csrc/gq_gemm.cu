@@ -18,13 +18,18 @@
 //   warps 2-9  epilogue: warp w reads TMEM lanes 32 (w % 4) .. +31 (thread =
 //           row) over one half of the columns, 32 columns per wait,
 //           activation, optional GAT head projections (the head vectors in
-//           shared memory), fp32 stores staged through shared memory; then
-//           release the accumulator, so the next tile's MMAs overlap it.
+//           shared memory), fp32 rows staged in shared memory and written
+//           by TMA stores, 32 rows x 16 columns each, two in flight per
+//           warp; then release the accumulator, so the next tile's MMAs
+//           overlap it.
 // Weight GEMM: grid (M tiles of K1) x (row splits); both operands MN-major
 // (their rows are the contraction), one TMEM accumulator per CTA, fp32
 // partials to a workspace, then a fixed-order reduction over splits.
 #include <cuda_bf16.h>
 #include <cudaTypedefs.h>
+
+#include <cstdint>
+#include <cstring>
 
 #include "gq_common.cuh"
 #include "gq_internal.cuh"
@@ -39,10 +44,13 @@ constexpr int kTileM = 128;
 constexpr int kChunkK = 64;                       // bf16 elements per 128-byte swizzle row
 constexpr int kATileBytes = kTileM * kChunkK * 2;  // 16 KB
 constexpr int kSmemBudget = 225 * 1024;
-// epilogue staging: per epilogue warp, 32 rows x 16 columns of fp32 at a row
-// pitch of 20 floats (conflict-free 16-byte writes by row)
+// epilogue staging, 4 KB per epilogue warp: two 32-row x 16-column fp32
+// boxes for TMA stores (64-byte rows, 64-byte swizzle: conflict-free 16-byte
+// writes by row), or one 32 x 16 block at a row pitch of 20 floats for
+// plain stores
 constexpr int kStgPitch = 20;
-constexpr int kStgBytes = kRgEpiWarps * 32 * kStgPitch * 4;
+constexpr int kStgWarpBytes = 4096;
+constexpr int kStgBytes = kRgEpiWarps * kStgWarpBytes;
 constexpr int kVecBytes = 2 * 256 * 4;  // a_src | a_dst of the GAT head projections
 
 // ---------------------------------------------------------------- host ---
@@ -60,6 +68,20 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 
 // 2-D bf16 tensor [outer][inner] with row pitch ld (elements); box of
 // box_inner x box_outer, 128-byte swizzle, zero fill out of bounds.
+// 2-D fp32 tensor [outer][inner] with row pitch ld (elements); box of
+// 16 x 32, 64-byte swizzle: the output boxes of the row GEMM's TMA stores.
+int make_tmap_f32_out(CUtensorMap* m, void* base, uint64_t inner, uint64_t outer, uint64_t ld) {
+  auto fn = encode_fn();
+  if (fn == nullptr) return GQ_ERR_CUDA;
+  const cuuint64_t dims[2] = {inner, outer};
+  const cuuint64_t strides[1] = {ld * 4};
+  const cuuint32_t box[2] = {16, 32};
+  const cuuint32_t estr[2] = {1, 1};
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, base, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                  CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? GQ_OK : GQ_ERR_INVALID_ARG;
+}
+
 int make_tmap(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer, uint64_t ld, uint32_t box_inner,
               uint32_t box_outer) {
   auto fn = encode_fn();
@@ -89,6 +111,7 @@ struct RowGemmArgs {
   int64_t ldc;
   int act;
   int vec;
+  int tma;              // C written by TMA stores (tmC)
   int half;             // columns [0, half) to epilogue warps 2-5, [half, Npad) to warps 6-9
   const float* a_src;   // optional GAT head projections
   const float* a_dst;
@@ -100,20 +123,20 @@ struct RowGemmArgs {
 
 __global__ void __launch_bounds__(kRgThreads, 1)
     row_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                    const RowGemmArgs p) {
+                    const __grid_constant__ CUtensorMap tmC, const RowGemmArgs p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
   uint8_t* sB = smem;
   uint8_t* sA = sB + (size_t)p.kch * p.Npad * 128;
-  uint64_t* full = reinterpret_cast<uint64_t*>(sA + (size_t)p.stages * kATileBytes);
+  float* stg_all = reinterpret_cast<float*>(sA + (size_t)p.stages * kATileBytes);  // 1024-byte aligned
+  float* svec = stg_all + kStgBytes / 4;                                              // [2][Npad]
+  uint64_t* full = reinterpret_cast<uint64_t*>(svec + kVecBytes / 4);
   uint64_t* empty = full + p.stages;
   uint64_t* bfull = empty + p.stages;
   uint64_t* tfull = bfull + 1;
   uint64_t* tempty = tfull + 2;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tempty + 2);
   volatile int* abort = reinterpret_cast<volatile int*>(tmem_slot + 1);
-  float* stg_all = reinterpret_cast<float*>(sA + (size_t)p.stages * kATileBytes + 256);
-  float* svec = stg_all + kStgBytes / 4;  // [2][Npad]
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
@@ -148,6 +171,7 @@ __global__ void __launch_bounds__(kRgThreads, 1)
     if (lane == 0) {
       prefetch_tmap(&tmA);
       prefetch_tmap(&tmB);
+      if (p.tma) prefetch_tmap(&tmC);
       mbar_expect_tx(bfull, (uint32_t)(p.kch * p.Npad * 128));
       for (int kc = 0; kc < p.kch; ++kc) tma_load_2d(sB + (size_t)kc * p.Npad * 128, &tmB, kc * kChunkK, 0, bfull);
       int stage = 0;
@@ -205,7 +229,8 @@ __global__ void __launch_bounds__(kRgThreads, 1)
     const int row_in_tile = q * 32 + lane;
     const int h = (warp - 2) >> 2;
     const int cb = h ? p.half : 0, ce = h ? p.Npad : p.half;
-    float* stg = stg_all + (warp - 2) * 32 * kStgPitch;
+    float* stg = stg_all + (warp - 2) * (kStgWarpBytes / 4);
+    int nbox = 0;  // boxes this warp has stored
     int i = 0;
     for (int64_t t = blockIdx.x; t < ntiles; t += gridDim.x, ++i) {
       const int a = i & 1;
@@ -236,7 +261,24 @@ __global__ void __launch_bounds__(kRgThreads, 1)
             v[j] = __uint_as_float(r[u][j]);
             if (p.act == GQ_ACT_RELU) v[j] = fmaxf(v[j], 0.0f);
           }
-          if (p.vec && c0 + 16 <= p.N) {
+          if (p.tma && c0 < p.N) {
+            // row `lane` of the box; 16-byte piece j at piece j ^ ((lane >> 1) & 3)
+            float* box = stg + (nbox & 1) * 512;
+            if (lane == 0) bulk_wait_read<1>();  // the store of two boxes ago has read this buffer
+            __syncwarp();
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+              *reinterpret_cast<float4*>(box + lane * 16 + 4 * (j ^ ((lane >> 1) & 3))) =
+                  make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+            fence_proxy_async_smem();
+            __syncwarp();
+            const int64_t y = t * kTileM + q * 32;
+            if (lane == 0) {
+              if (y < p.M) tma_store_2d(&tmC, box, c0, (int)y);
+              bulk_commit();
+            }
+            ++nbox;
+          } else if (p.vec && c0 + 16 <= p.N) {
             // through shared memory, so that each store instruction writes 8
             // rows x 64 contiguous bytes instead of 32 rows x 16 bytes
 #pragma unroll
@@ -281,6 +323,7 @@ __global__ void __launch_bounds__(kRgThreads, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(&tempty[a]);
     }
+    if (lane == 0) bulk_wait<0>();  // every TMA store of this warp done
   }
   __syncthreads();
   if (warp == 1) {
@@ -521,6 +564,7 @@ int row_gemm(const void* A, int64_t M, int K, int64_t lda, const void* B, int N,
   p.ldc = ldc;
   p.act = act;
   p.vec = (ldc % 4 == 0) && aligned(C, 16);
+  p.tma = p.vec && M <= INT32_MAX - kTileM;
   // the two epilogue column halves, 16-aligned; with head projections a
   // half holds whole heads, else every column goes to the first half
   p.half = (p.Npad / 2 + 15) / 16 * 16;
@@ -532,14 +576,16 @@ int row_gemm(const void* A, int64_t M, int K, int64_t lda, const void* B, int N,
   p.heads = heads;
   p.fshift = fshift;
   p.err = err;
-  CUtensorMap tmA, tmB;
+  CUtensorMap tmA, tmB, tmC;
   GQ_TRY(make_tmap(&tmA, A, (uint64_t)K, (uint64_t)M, (uint64_t)lda, kChunkK, kTileM));
   GQ_TRY(make_tmap(&tmB, B, (uint64_t)K, (uint64_t)N, (uint64_t)ldb, kChunkK, (uint32_t)p.Npad));
-  const size_t smem = 1024 + (size_t)b_bytes + (size_t)p.stages * kATileBytes + 256 + kStgBytes + kVecBytes;
+  memset(&tmC, 0, sizeof(tmC));
+  if (p.tma) GQ_TRY(make_tmap_f32_out(&tmC, C, (uint64_t)N, (uint64_t)M, (uint64_t)ldc));
+  const size_t smem = 1024 + (size_t)b_bytes + (size_t)p.stages * kATileBytes + kStgBytes + kVecBytes + 256;
   GQ_TRY_CUDA(cudaFuncSetAttribute(row_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem));
   const int64_t ntiles = (M + kTileM - 1) / kTileM;
   const int grid = (int)(ntiles < sm_count() ? ntiles : sm_count());
-  row_gemm_kernel<<<grid, kRgThreads, smem, s>>>(tmA, tmB, p);
+  row_gemm_kernel<<<grid, kRgThreads, smem, s>>>(tmA, tmB, tmC, p);
   return launch_status();
 }
 
