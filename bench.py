@@ -163,13 +163,14 @@ def seeds_for(base, L, b):
     return f, bw
 
 
-def spmm_bytes(n, nnz, d, bits, n_marg, rows_gathered_marg, out_elem_bytes, q):
+def spmm_bytes(n, nnz, d, bits, n_marg, rows_gathered_marg, out_elem_bytes, q, gated=False):
     """Algorithmic bytes of one de-quantizing aggregation.
     compulsory: every array once (each gathered message row read once);
-    streaming: every edge's gathered row counted."""
+    streaming: every edge's gathered row counted.  gated: the output goes
+    through a ReLU gate read as an fp32 n x d array."""
     pitch = q.packed_pitch(d, bits) if bits < 32 else 0
     meta = (n + 1) * 4 + nnz * 4 + 2 * n * 4 + (n if bits < 32 else 0)
-    out = n * d * out_elem_bytes
+    out = n * d * out_elem_bytes + (n * d * 4 if gated else 0)
     comp = meta + n_marg * pitch + (n - n_marg) * d * 4 + out
     stream = (n + 1) * 4 + nnz * 4 * 2 + (nnz if bits < 32 else 0) + n * 4 + out \
         + rows_gathered_marg * pitch + (nnz - rows_gathered_marg) * d * 4
@@ -450,7 +451,11 @@ def run_ours(args, w):
             continue
         d = w.widths[l]
         fwd = name == "aggregate"
-        c, s_ = spmm_bytes(g.n, g.nnz, d, b, n_marg, marg_out if fwd else marg_in, 2 if fwd else 4, q)
+        # the transposed aggregation of layer l > 0 writes layer l-1's dZ:
+        # bf16, through the ReLU gate of layer l-1's output
+        fused = not fwd and model.fuse_dz and l > 0
+        c, s_ = spmm_bytes(g.n, g.nnz, d, b, n_marg, marg_out if fwd else marg_in, 2 if fwd or fused else 4, q,
+                           gated=fused)
         agg_bytes_c += c * len(times)
         agg_bytes_s += s_ * len(times)
         agg_ms += sum(times)

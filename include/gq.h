@@ -376,6 +376,10 @@ GQ_API int gq_to_bf16(const float* src, int64_t rows, int cols, int64_t lds, uin
  *   packed = quantize_pack(H_in rows with mask != 0, bits, seed)   (bits<32)
  *   A      = sum_{u->v} a_{u,v} m_u   -> A_save, bf16, n x d_in (lda)
  *   H_out  = act(A W)                 -> fp32, n x d_out (ldo)
+ *   relu_bits (nullable): the derivative of act as bits, bit c % 32 of
+ *           word relu_bits[r * ldrb + c / 32] = [H_out[r][c] > 0]
+ *           (ldrb >= ceil(d_out / 32); words 4-byte aligned) -- the gate
+ *           the layer above's backward applies to this layer's dZ.
  *   W is d_in x d_out fp32 row-major.  d_in % 4 == 0, lda % 8 == 0,
  *   d_in, d_out <= 256.  A_save is what the backward pass needs.
  *
@@ -391,11 +395,12 @@ GQ_API int gq_to_bf16(const float* src, int64_t rows, int cols, int64_t lds, uin
  *     packed= quantize_pack(dA rows with mask != 0, bits, seed)
  *     dH_in = A^T-aggregation of the mixed messages -> n x d_in (ldi)
  *     or, when dZ_prev is non-NULL, the layer below's dZ in its place:
- *     dZ_prev = bf16(dH_in * [gate_in > 0]) -> n x d_in (ldzp >= d_in,
- *     ldzp % 8 == 0; columns d_in .. ldzp are not written), with gate_in
- *     the layer's input H_in (the layer below's ReLU output, n x d_in,
- *     ldgi; NULL: no gate) -- the row flush of the aggregation applies the
- *     gate and the rounding, so no fp32 dH_in is written.
+ *     dZ_prev = bf16(dH_in * g) -> n x d_in (ldzp >= d_in, ldzp % 8 == 0;
+ *     columns d_in .. ldzp are not written), with g[r][c] = bit c % 32 of
+ *     gate_in[r * ldgi + c / 32]: the relu_bits the layer below's forward
+ *     wrote for its output, this layer's input (ldgi >= ceil(d_in / 32);
+ *     NULL: no gate) -- the row flush of the aggregation applies the gate
+ *     and the rounding, so no fp32 dH_in is written.
  * Both take a workspace of gq_gcn_layer_workspace_bytes(g, d_in, d_out,
  * bits) bytes (256-byte aligned) and a nullable device error word (see
  * the GEMMs).  Errors: GQ_ERR_INVALID_ARG, GQ_ERR_UNSUPPORTED,
@@ -409,13 +414,14 @@ GQ_API int gq_to_bf16(const float* src, int64_t rows, int cols, int64_t lds, uin
 GQ_API size_t gq_gcn_layer_workspace_bytes(const gq_graph* g, int d_in, int d_out, int bits);
 GQ_API int gq_gcn_layer_fwd(const gq_graph* g, int coef, const float* H_in, int64_t ldh, int d_in,
                      const float* W, int d_out, const uint8_t* mask, int bits, uint64_t seed, int act,
-                     uint16_t* A_save, int64_t lda, float* H_out, int64_t ldo, void* ws,
-                     size_t ws_bytes, int* dev_err, void* const* stage_events, gq_stream stream);
+                     uint16_t* A_save, int64_t lda, float* H_out, int64_t ldo, uint32_t* relu_bits,
+                     int64_t ldrb, void* ws, size_t ws_bytes, int* dev_err, void* const* stage_events,
+                     gq_stream stream);
 GQ_API int gq_gcn_layer_bwd(const gq_graph* g, int coef, const float* dH_out, int64_t ldd,
                      const uint16_t* dZ_in, int64_t ldzi, const uint16_t* A_save, int64_t lda,
                      const float* H_out, int64_t ldo, const float* W, int d_in, int d_out,
                      const uint8_t* mask, int bits, uint64_t seed, int act, int need_dinput, float* dW,
-                     float* dH_in, int64_t ldi, const float* gate_in, int64_t ldgi, uint16_t* dZ_prev,
+                     float* dH_in, int64_t ldi, const uint32_t* gate_in, int64_t ldgi, uint16_t* dZ_prev,
                      int64_t ldzp, float* dA_save, void* ws, size_t ws_bytes, int* dev_err,
                      void* const* stage_events, gq_stream stream);
 

@@ -108,7 +108,7 @@ def _SIGNATURES(P, I64, I, U64, F, S):
         ("gq_gat_layer_fwd", [GP, P, I64, I, P, P, P, I, I, F, P, I, U64, I, P, P, P, P, P, P, P, P, P, S, P, P], I),
         ("gq_gat_layer_bwd", [GP, P, P, I64, P, P, P, P, P, P, P, P, P, P, I, I, I, F, P, I, U64, P, P, P, P, P, P,
                               P, S, P, P], I),
-        ("gq_gcn_layer_fwd", [GP, I, P, I64, I, P, I, P, I, U64, I, P, I64, P, I64, P, S, P, P, P], I),
+        ("gq_gcn_layer_fwd", [GP, I, P, I64, I, P, I, P, I, U64, I, P, I64, P, I64, P, I64, P, S, P, P, P], I),
         ("gq_gcn_layer_bwd",
          [GP, I, P, I64, P, I64, P, I64, P, I64, P, I, I, P, I, U64, I, I, P, P, I64, P, I64, P, I64, P, P, S, P,
           P, P], I),
@@ -540,10 +540,14 @@ def _events(evs):
 
 def gcn_layer_fwd(g: Graph, H_in: torch.Tensor, W: torch.Tensor, mask, bits: int, seed: int, act: int,
                   coef: int = COEF_GCN, ws: Workspace | None = None, A_save=None, H_out=None,
-                  dev_err: torch.Tensor | None = None, events=None):
-    """Returns (A_save bf16 [n x d_in] view, H_out fp32 [n x d_out])."""
+                  dev_err: torch.Tensor | None = None, events=None, relu_bits: torch.Tensor | None = None):
+    """Returns (A_save bf16 [n x d_in] view, H_out fp32 [n x d_out]).
+    relu_bits (int32 [n x ceil(d_out / 32)] words, optional): receives
+    [H_out > 0] as bits, the gate of this layer's dZ in the layer above's
+    backward."""
     _cuda(H_in, torch.float32, "H_in")
     _cuda(W, torch.float32, "W")
+    _cuda(relu_bits, torch.int32, "relu_bits")
     n, d_in = H_in.shape
     d_out = W.shape[1]
     dev = H_in.device
@@ -558,7 +562,8 @@ def gcn_layer_fwd(g: Graph, H_in: torch.Tensor, W: torch.Tensor, mask, bits: int
     W = W.contiguous()  # held until the call has been enqueued
     _check(L.gq_gcn_layer_fwd(g.ref, coef, _ptr(H_in), _rows(H_in), d_in, _ptr(W), d_out, _ptr(mask),
                               bits, seed & 0xFFFFFFFFFFFFFFFF, act, _ptr(A_save), _rows(A_save), _ptr(H_out),
-                              _rows(H_out), _ptr(buf), buf.numel(), _ptr(dev_err), _events(events), _stream()),
+                              _rows(H_out), _ptr(relu_bits), _rows(relu_bits) if relu_bits is not None else 0,
+                              _ptr(buf), buf.numel(), _ptr(dev_err), _events(events), _stream()),
            "gq_gcn_layer_fwd")
     return A_save[:, :d_in], H_out
 
@@ -570,13 +575,14 @@ def gcn_layer_bwd(g: Graph, dH_out: torch.Tensor | None, A_save: torch.Tensor, H
                   gate_in: torch.Tensor | None = None, dZ_prev: torch.Tensor | None = None):
     """Returns (dW [d_in x d_out], dH_in [n x d_in] or None).  dZ_in: the
     layer's bf16 dZ made by the layer above (dH_out, H_out unused); dZ_prev:
-    write the layer below's bf16 dZ = dH_in * [gate_in > 0] instead of an
-    fp32 dH_in (then None is returned for dH_in)."""
+    write the layer below's bf16 dZ = dH_in * gate instead of an fp32 dH_in
+    (then None is returned for dH_in), the gate being gate_in, the
+    relu_bits of the layer below's forward."""
     _cuda(dH_out, torch.float32, "dH_out")
     _cuda(A_save, torch.bfloat16, "A_save")
     _cuda(dZ_in, torch.bfloat16, "dZ_in")
     _cuda(dZ_prev, torch.bfloat16, "dZ_prev")
-    _cuda(gate_in, torch.float32, "gate_in")
+    _cuda(gate_in, torch.int32, "gate_in")
     n = A_save.shape[0]
     d_in, d_out = W.shape
     dev = A_save.device

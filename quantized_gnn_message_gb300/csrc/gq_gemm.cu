@@ -113,6 +113,8 @@ struct RowGemmArgs {
   int vec;
   int tma;              // C written by TMA stores (tmC)
   int half;             // columns [0, half) to epilogue warps 2-5, [half, Npad) to warps 6-9
+  uint32_t* rbits;      // optional [C > 0] bits: bit c % 32 of rbits[r * ldrb + c / 32]
+  int64_t ldrb;
   const float* a_src;   // optional GAT head projections
   const float* a_dst;
   float* S;
@@ -247,6 +249,7 @@ __global__ void __launch_bounds__(kRgThreads, 1)
       float hs = 0.0f, hd = 0.0f;
       for (int c1 = cb; c1 < ce; c1 += 32) {
         const int nc = ce - c1 >= 32 ? 2 : 1;  // 16-column chunks this round
+        uint32_t rb = 0;                       // [value > 0] of the round's columns
         uint32_t r[2][16];
         tmem_ld16(taddr + c1, r[0]);
         if (nc == 2) tmem_ld16(taddr + c1 + 16, r[1]);
@@ -260,6 +263,7 @@ __global__ void __launch_bounds__(kRgThreads, 1)
           for (int j = 0; j < 16; ++j) {
             v[j] = __uint_as_float(r[u][j]);
             if (p.act == GQ_ACT_RELU) v[j] = fmaxf(v[j], 0.0f);
+            rb |= (v[j] > 0.0f ? 1u : 0u) << (16 * u + j);
           }
           if (p.tma && c0 < p.N) {
             // row `lane` of the box; 16-byte piece j at piece j ^ ((lane >> 1) & 3)
@@ -318,6 +322,7 @@ __global__ void __launch_bounds__(kRgThreads, 1)
             }
           }
         }
+        if (p.rbits != nullptr && live && c1 < p.N) p.rbits[row * p.ldrb + (c1 >> 5)] = rb;
       }
       tc_fence_before();
       __syncwarp();
@@ -534,7 +539,7 @@ __global__ void transpose_bf16_kernel(const float* __restrict__ W, int K, int N,
 // ------------------------------------------------------------------ API ---
 int row_gemm(const void* A, int64_t M, int K, int64_t lda, const void* B, int N, int64_t ldb, int act, float* C,
              int64_t ldc, const float* a_src, const float* a_dst, float* S, float* D, int heads, int* err,
-             cudaStream_t s) {
+             cudaStream_t s, uint32_t* rbits, int64_t ldrb) {
   if (A == nullptr || B == nullptr || C == nullptr || M < 0 || K < 1 || N < 1) return GQ_ERR_INVALID_ARG;
   if (K > 256 || N > 256) return GQ_ERR_UNSUPPORTED;
   if (lda < K || ldb < K || ldc < N || lda % 8 || ldb % 8 || !aligned(A, 16) || !aligned(B, 16))
@@ -569,6 +574,13 @@ int row_gemm(const void* A, int64_t M, int K, int64_t lda, const void* B, int N,
   // half holds whole heads, else every column goes to the first half
   p.half = (p.Npad / 2 + 15) / 16 * 16;
   if (S != nullptr && p.half % (1 << fshift) != 0) p.half = p.Npad;
+  if (rbits != nullptr) {  // a word of bits is one 32-column round of one half
+    if (ldrb < (N + 31) / 32 || !aligned(rbits, 4)) return GQ_ERR_INVALID_ARG;
+    p.half = min((p.Npad / 2 + 31) / 32 * 32, p.Npad);
+    if (S != nullptr && p.half % (1 << fshift) != 0) p.half = p.Npad;
+  }
+  p.rbits = rbits;
+  p.ldrb = ldrb;
   p.a_src = a_src;
   p.a_dst = a_dst;
   p.S = S;

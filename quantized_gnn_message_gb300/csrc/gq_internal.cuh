@@ -13,13 +13,14 @@ int quantize_pack(const float* X, int64_t n, int d, int64_t ldx, const uint8_t* 
                   uint8_t* packed, cudaStream_t s);
 
 // Aggregation; Yb != nullptr writes the output in bf16 (leading dim ldy);
-// gate != nullptr zeroes every output element whose gate element is not > 0.
+// gate != nullptr zeroes every output element (r, c) whose bit c % 32 of
+// gate[r * ldg + c / 32] is clear.
 size_t spmm_workspace(const gq_graph* g, int transpose, int d);
 int spmm_check(const gq_graph* g, const float* X, int64_t ldx, const uint8_t* packed, const uint8_t* mask, int d,
                int bits, const float* Y, int64_t ldy, const void* Yb);
 int dequant_spmm(const gq_graph* g, int transpose, int coef, const float* X, int64_t ldx, const uint8_t* packed,
                  const uint8_t* mask, int d, int bits, float* Y, int64_t ldy, void* ws, size_t ws_bytes,
-                 cudaStream_t s, void* Yb, const float* gate = nullptr, int64_t ldg = 0);
+                 cudaStream_t s, void* Yb, const uint32_t* gate = nullptr, int64_t ldg = 0);
 int edge_spmm(const gq_graph* g, int transpose, const float* alpha, int heads, const float* X, int64_t ldx,
               const uint8_t* packed, const uint8_t* mask, int d, int bits, float* Y, int64_t ldy, void* ws,
               size_t ws_bytes, cudaStream_t s);
@@ -27,9 +28,10 @@ int edge_spmm_alpha8(const gq_graph* g, const uint8_t* acode, const float* ahdr,
                      int64_t ldx, const uint8_t* packed, const uint8_t* mask, int d, int bits, float* Y,
                      int64_t ldy, void* ws, size_t ws_bytes, cudaStream_t s);
 
+// rbits != nullptr: bit c % 32 of rbits[r * ldrb + c / 32] = [C[r][c] > 0]
 int row_gemm(const void* A, int64_t M, int K, int64_t lda, const void* B, int N, int64_t ldb, int act, float* C,
              int64_t ldc, const float* a_src, const float* a_dst, float* S, float* D, int heads, int* err,
-             cudaStream_t s);
+             cudaStream_t s, uint32_t* rbits = nullptr, int64_t ldrb = 0);
 size_t wgrad_workspace(int64_t R, int K1, int N1);
 int wgrad_gemm(const void* X, int64_t R, int K1, int64_t ldx, const void* Y, int N1, int64_t ldy, float* C,
                int64_t ldc, int accumulate, void* ws, size_t ws_bytes, int* err, cudaStream_t s);

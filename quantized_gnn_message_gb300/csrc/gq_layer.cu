@@ -79,12 +79,14 @@ extern "C" size_t gq_gcn_layer_workspace_bytes(const gq_graph* g, int d_in, int 
 
 extern "C" int gq_gcn_layer_fwd(const gq_graph* g, int coef, const float* H_in, int64_t ldh, int d_in,
                                 const float* W, int d_out, const uint8_t* mask, int bits, uint64_t seed, int act,
-                                uint16_t* A_save, int64_t lda, float* H_out, int64_t ldo, void* ws,
-                                size_t ws_bytes, int* dev_err, void* const* stage_events, gq_stream stream) {
+                                uint16_t* A_save, int64_t lda, float* H_out, int64_t ldo, uint32_t* relu_bits,
+                                int64_t ldrb, void* ws, size_t ws_bytes, int* dev_err, void* const* stage_events,
+                                gq_stream stream) {
   using namespace gq;
   cudaStream_t s = (cudaStream_t)stream;
   if (g == nullptr || H_in == nullptr || W == nullptr || A_save == nullptr || H_out == nullptr)
     return GQ_ERR_INVALID_ARG;
+  if (relu_bits != nullptr && ldrb < (d_out + 31) / 32) return GQ_ERR_INVALID_ARG;
   if (d_in < 1 || d_out < 1 || d_in % 4 || lda < d_in || lda % 8 || ldo < d_out || ldh < d_in)
     return GQ_ERR_INVALID_ARG;
   if (!(bits == 32 || valid_bits(bits))) return GQ_ERR_INVALID_ARG;
@@ -101,7 +103,7 @@ extern "C" int gq_gcn_layer_fwd(const gq_graph* g, int coef, const float* H_in, 
   GQ_TRY(tr.begin(2));
   GQ_TRY(transpose_bf16(W, d_in, d_out, d_out, w.wt, round8(d_in), (int)round8(d_in), s));
   GQ_TRY(row_gemm(A_save, g->n, d_in, lda, w.wt, d_out, round8(d_in), act, H_out, ldo, nullptr, nullptr, nullptr,
-                  nullptr, 0, dev_err, s));
+                  nullptr, 0, dev_err, s, relu_bits, ldrb));
   return tr.end(2);
 }
 
@@ -109,7 +111,7 @@ extern "C" int gq_gcn_layer_bwd(const gq_graph* g, int coef, const float* dH_out
                                 const uint16_t* dZ_in, int64_t ldzi, const uint16_t* A_save, int64_t lda,
                                 const float* H_out, int64_t ldo, const float* W, int d_in, int d_out,
                                 const uint8_t* mask, int bits, uint64_t seed, int act, int need_dinput, float* dW,
-                                float* dH_in, int64_t ldi, const float* gate_in, int64_t ldgi, uint16_t* dZ_prev,
+                                float* dH_in, int64_t ldi, const uint32_t* gate_in, int64_t ldgi, uint16_t* dZ_prev,
                                 int64_t ldzp, float* dA_save, void* ws, size_t ws_bytes, int* dev_err,
                                 void* const* stage_events, gq_stream stream) {
   using namespace gq;
@@ -125,7 +127,7 @@ extern "C" int gq_gcn_layer_bwd(const gq_graph* g, int coef, const float* dH_out
   if (need_dinput) {
     if (dZ_prev != nullptr) {
       if (ldzp < d_in || ldzp % 8 || !aligned(dZ_prev, 16)) return GQ_ERR_INVALID_ARG;
-      if (gate_in != nullptr && (ldgi < d_in || ldgi % 4 || !aligned(gate_in, 16))) return GQ_ERR_INVALID_ARG;
+      if (gate_in != nullptr && (ldgi < (d_in + 31) / 32 || !aligned(gate_in, 4))) return GQ_ERR_INVALID_ARG;
     } else if (dH_in == nullptr || ldi < d_in) {
       return GQ_ERR_INVALID_ARG;
     }
@@ -156,7 +158,7 @@ extern "C" int gq_gcn_layer_bwd(const gq_graph* g, int coef, const float* dH_out
                   0, dev_err, s));
   GQ_TRY(tr.end(2));
   // 4-5. quantize the marginal rows of dA, aggregate over the transpose: fp32
-  // dH_in, or the previous layer's dZ = bf16(dH_in * [gate_in > 0])
+  // dH_in, or the previous layer's dZ = bf16(dH_in * relu'), relu' as the gate_in bits
   GQ_TRY(tr.begin(3));
   if (bits < 32) GQ_TRY(quantize_pack(dA, g->n, d_in, d_in, mask, bits, seed, w.packed, s));
   GQ_TRY(tr.end(3));

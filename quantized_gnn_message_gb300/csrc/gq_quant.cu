@@ -142,6 +142,72 @@ __global__ void __launch_bounds__(kQuantThreads) quantize_pack_kernel(
   }
 }
 
+// The same quantization, rows of d <= 8 G (one chunk per lane), one mask
+// (or none): a warp takes the rows in blocks of 32, reads the block's mask
+// bytes at once (one per lane), lists its marginal rows in shared memory and
+// quantizes them 32 / G at a time, loading the next step's rows before the
+// current ones are reduced and packed.  Central rows cost nothing but their
+// mask byte.  The packed bytes are those of quantize_pack_kernel.
+template <int BITS, int G>
+__global__ void __launch_bounds__(kQuantThreads) quantize_rows_kernel(
+    const float* __restrict__ X, int64_t n, int d, int64_t ldx, const uint8_t* __restrict__ mask,
+    uint32_t seed_key, uint8_t* __restrict__ packed, int64_t pitch, int hoff, bool vec) {
+  constexpr float L = (float)((1 << BITS) - 1);
+  constexpr int NGR = 32 / G;
+  __shared__ uint8_t list_all[kQuantThreads / 32][32];
+  const int lane = threadIdx.x & 31;
+  const int gl = lane % G, k = lane / G;
+  uint8_t* list = list_all[threadIdx.x >> 5];
+  const int64_t warp = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
+  const int nchunks = (d + 7) >> 3;
+  const int p8 = nchunks * BITS;
+  const bool live = gl < nchunks;
+  const float nan = __int_as_float(0x7fc00000);  // fill of columns >= d: ignored by fminf / fmaxf
+  for (int64_t rb = warp * 32; rb < n; rb += nwarps * 32) {  // warp-uniform
+    const bool on = rb + lane < n && (mask == nullptr || mask[rb + lane] != 0);
+    const unsigned act = __ballot_sync(FULL, on);
+    const int na = __popc(act);
+    if (on) list[__popc(act & ((1u << lane) - 1u))] = (uint8_t)lane;
+    __syncwarp();
+    int64_t r = k < na ? rb + list[k] : -1;
+    float v[8];
+    if (r >= 0 && live) load_chunk(X + r * ldx, gl, d, vec, nan, v);
+    for (int s0 = 0; s0 < na; s0 += NGR) {
+      const int jn = s0 + NGR + k;
+      const int64_t rn = jn < na ? rb + list[jn] : -1;
+      float vn[8];
+      if (rn >= 0 && live) load_chunk(X + rn * ldx, gl, d, vec, nan, vn);
+      float mn = __int_as_float(0x7f800000), mx = -__int_as_float(0x7f800000);
+      if (r >= 0 && live) {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) { mn = fminf(mn, v[i]); mx = fmaxf(mx, v[i]); }
+      }
+#pragma unroll
+      for (int o = G / 2; o > 0; o >>= 1) {
+        mn = fminf(mn, __shfl_xor_sync(FULL, mn, o));
+        mx = fmaxf(mx, __shfl_xor_sync(FULL, mx, o));
+      }
+      if (r >= 0) {
+        // Eqn 4: Z = min, S = (max - min) / (2^b - 1)
+        const float S = __fdiv_rn(__fsub_rn(mx, mn), L);
+        const bool constant = !(S >= 1.17549435e-38f);  // S below FLT_MIN: code as constant
+        const float inv = constant ? 0.0f : __frcp_rn(S);
+        const uint32_t kr = row_key(seed_key, (uint32_t)r);
+        uint8_t* row = packed + r * pitch;
+        if (live) store_word<BITS>(row + (int64_t)gl * BITS, quantize_chunk<BITS>(v, gl * 8, d, mn, inv, constant, kr));
+        if (gl == 0) *reinterpret_cast<float2*>(row + hoff) = make_float2(S, mn);
+        for (int b = p8 + gl; b < hoff; b += G) row[b] = 0;
+        for (int b = hoff + 8 + gl; b < pitch; b += G) row[b] = 0;
+      }
+      r = rn;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) v[i] = vn[i];
+    }
+    __syncwarp();  // the list is rewritten by the next block
+  }
+}
+
 template <int BITS>
 __global__ void __launch_bounds__(kQuantThreads) dequant_unpack_kernel(
     const uint8_t* __restrict__ packed, int64_t n, int d, int64_t pitch, int hoff,
@@ -196,6 +262,18 @@ int launch_quantize_t(const float* X, int64_t n, int d, int64_t ldx, const uint8
   const int nch = (d + 7) / 8;
   const int G = nch <= 1 ? 1 : nch <= 2 ? 2 : nch <= 4 ? 4 : nch <= 8 ? 8 : nch <= 16 ? 16 : 32;
   const int grid = grid_for_rows((n + 32 / G - 1) / (32 / G));
+  if (!MIX && d <= 8 * G) {  // one chunk per lane: the block-listing kernel
+    const int gridb = grid_for_rows((n + 31) / 32);
+    switch (G) {
+      case 1: quantize_rows_kernel<BITS, 1><<<gridb, kQuantThreads, 0, s>>>(X, n, d, ldx, mask, h, packed, pitch, hoff, vec); break;
+      case 2: quantize_rows_kernel<BITS, 2><<<gridb, kQuantThreads, 0, s>>>(X, n, d, ldx, mask, h, packed, pitch, hoff, vec); break;
+      case 4: quantize_rows_kernel<BITS, 4><<<gridb, kQuantThreads, 0, s>>>(X, n, d, ldx, mask, h, packed, pitch, hoff, vec); break;
+      case 8: quantize_rows_kernel<BITS, 8><<<gridb, kQuantThreads, 0, s>>>(X, n, d, ldx, mask, h, packed, pitch, hoff, vec); break;
+      case 16: quantize_rows_kernel<BITS, 16><<<gridb, kQuantThreads, 0, s>>>(X, n, d, ldx, mask, h, packed, pitch, hoff, vec); break;
+      default: quantize_rows_kernel<BITS, 32><<<gridb, kQuantThreads, 0, s>>>(X, n, d, ldx, mask, h, packed, pitch, hoff, vec); break;
+    }
+    return launch_status();
+  }
   switch (G) {
     case 1: quantize_pack_kernel<BITS, 1, 1, MIX><<<grid, kQuantThreads, 0, s>>>(X, n, d, ldx, mask, h, packed, pitch, hoff, vec, roff); break;
     case 2: quantize_pack_kernel<BITS, 1, 2, MIX><<<grid, kQuantThreads, 0, s>>>(X, n, d, ldx, mask, h, packed, pitch, hoff, vec, roff); break;

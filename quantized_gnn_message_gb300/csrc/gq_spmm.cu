@@ -65,8 +65,8 @@ struct SpmmParams {
   float* Y;
   __nv_bfloat16* Yb;        // if set, the output is written in bf16 here instead
   int64_t ldy;
-  const float* gate;        // if set, an output element whose gate[r][c] is not > 0 is written as 0
-  int64_t ldg;
+  const uint32_t* gate;     // if set, output element (r, c) is written as 0 unless bit c % 32 of
+  int64_t ldg;              // word gate[r * ldg + c / 32] is set (a ReLU derivative as bits)
   int64_t n_rows;
   int d;
   const int32_t* tasks;     // heavy-row schedule (see gq_sched)
@@ -239,17 +239,19 @@ __device__ __forceinline__ void group_reduce(float (&acc)[CPL][8]) {
 }
 
 // The output value of row r, column c after the optional ReLU gate (the
-// derivative of the activation of the layer whose input this output is).
+// derivative of the activation of the layer whose input this output is, one
+// bit per element).
 __device__ __forceinline__ float gated(const SpmmParams& p, int64_t r, int c, float v) {
-  return (p.gate != nullptr && !(__ldg(p.gate + r * p.ldg + c) > 0.0f)) ? 0.0f : v;
+  return (p.gate != nullptr && !((__ldg(p.gate + r * p.ldg + (c >> 5)) >> (c & 31)) & 1u)) ? 0.0f : v;
 }
+// columns c .. c+3 (c a multiple of 4)
 __device__ __forceinline__ float4 gated4(const SpmmParams& p, int64_t r, int c, float4 v) {
   if (p.gate != nullptr) {
-    const float4 g = __ldg(reinterpret_cast<const float4*>(p.gate + r * p.ldg + c));
-    if (!(g.x > 0.0f)) v.x = 0.0f;
-    if (!(g.y > 0.0f)) v.y = 0.0f;
-    if (!(g.z > 0.0f)) v.z = 0.0f;
-    if (!(g.w > 0.0f)) v.w = 0.0f;
+    const uint32_t b = __ldg(p.gate + r * p.ldg + (c >> 5)) >> (c & 31);
+    if (!(b & 1u)) v.x = 0.0f;
+    if (!(b & 2u)) v.y = 0.0f;
+    if (!(b & 4u)) v.z = 0.0f;
+    if (!(b & 8u)) v.w = 0.0f;
   }
   return v;
 }
@@ -752,8 +754,10 @@ __device__ __forceinline__ void a_consume(const SpmmParams& p, const ALane<LG>& 
   }
 }
 
-// Write the lane's columns of row r: (acc + accz) * rs.
-template <int BITS, int LG>
+// Write the lane's columns of row r: (acc + accz) * rs, through the ReLU
+// gate when GATE (a separate instantiation: the gate's code changes the
+// register allocation of the whole streaming loop).
+template <int BITS, int LG, bool GATE>
 __device__ __forceinline__ void a_flush(const SpmmParams& p, const ALane<LG>& L, int64_t r, float rs,
                                         const f32x2 (&acc)[8], float accz) {
   float o[16];
@@ -767,7 +771,7 @@ __device__ __forceinline__ void a_flush(const SpmmParams& p, const ALane<LG>& L,
   for (int k = 0; k < 4; ++k) {
     const int col = a_col<BITS, LG>(L, 4 * k);
     if (col < p.d) {
-      if (p.gate != nullptr) {
+      if (GATE) {
         const float4 g = gated4(p, r, col, make_float4(o[4 * k], o[4 * k + 1], o[4 * k + 2], o[4 * k + 3]));
         o[4 * k] = g.x; o[4 * k + 1] = g.y; o[4 * k + 2] = g.z; o[4 * k + 3] = g.w;
       }
@@ -783,7 +787,7 @@ __device__ __forceinline__ void a_flush(const SpmmParams& p, const ALane<LG>& L,
 // Stream the edges [eb, eb + n) through the group's ring.  LIGHT: they are
 // the edges of rows [row0, row1) and each row is written once its last edge
 // has been consumed; otherwise the sums are left in acc / accz.
-template <int BITS, int LG, int U, bool LIGHT, bool MX>
+template <int BITS, int LG, int U, bool LIGHT, bool MX, bool GATE>
 __device__ __forceinline__ void a_stream(const SpmmParams& p, const ALane<LG>& L, f32x2 bias, int eb, int n,
                                          int row0, int row1, f32x2 (&acc)[8], float& accz) {
   const float* __restrict__ colscale = p.colscale;
@@ -887,7 +891,7 @@ __device__ __forceinline__ void a_stream(const SpmmParams& p, const ALane<LG>& L
           if (U == 1 || e < n) {
             if (LIGHT) {
               while (e >= rend) {
-                if (L.on) a_flush<BITS, LG>(p, L, row, rs, acc, accz);
+                if (L.on) a_flush<BITS, LG, GATE>(p, L, row, rs, acc, accz);
 #pragma unroll
                 for (int i = 0; i < 8; ++i) acc[i] = 0ull;
                 accz = 0.0f;
@@ -908,7 +912,7 @@ __device__ __forceinline__ void a_stream(const SpmmParams& p, const ALane<LG>& L
   }
   if (LIGHT) {
     for (; row < row1; ++row) {
-      if (L.on) a_flush<BITS, LG>(p, L, row, p.rowscale ? __ldg(p.rowscale + row) : 1.0f, acc, accz);
+      if (L.on) a_flush<BITS, LG, GATE>(p, L, row, p.rowscale ? __ldg(p.rowscale + row) : 1.0f, acc, accz);
 #pragma unroll
       for (int i = 0; i < 8; ++i) acc[i] = 0ull;
       accz = 0.0f;
@@ -916,7 +920,7 @@ __device__ __forceinline__ void a_stream(const SpmmParams& p, const ALane<LG>& L
   }
 }
 
-template <int BITS, int LG, int U, bool MX>
+template <int BITS, int LG, int U, bool MX, bool GATE>
 __global__ void __launch_bounds__(kSpmmThreads) spmm_async_kernel(const SpmmParams p) {
   extern __shared__ __align__(16) uint8_t asm_[];
   constexpr int NG = 32 / LG;
@@ -977,7 +981,7 @@ __global__ void __launch_bounds__(kSpmmThreads) spmm_async_kernel(const SpmmPara
     chunk = (chunk + U - 1) / U * U;
     const int b0 = task.y + sid * chunk;
     const int b1 = min(b0 + chunk, task.z);
-    if (b0 < b1) a_stream<BITS, LG, U, false, MX>(p, L, bias, b0, b1 - b0, 0, 0, acc, accz);
+    if (b0 < b1) a_stream<BITS, LG, U, false, MX, GATE>(p, L, bias, b0, b1 - b0, 0, 0, acc, accz);
     float o[16];
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
@@ -1006,12 +1010,12 @@ __global__ void __launch_bounds__(kSpmmThreads) spmm_async_kernel(const SpmmPara
   for (int64_t t = gid; t < p.n_light; t += ngroups) {
     const int2 run = __ldg(reinterpret_cast<const int2*>(p.light) + t);
     const int eb = __ldg(p.rowptr + run.x), ee = __ldg(p.rowptr + run.y);
-    a_stream<BITS, LG, U, true, MX>(p, L, bias, eb, ee - eb, run.x, run.y, acc, accz);
+    a_stream<BITS, LG, U, true, MX, GATE>(p, L, bias, eb, ee - eb, run.x, run.y, acc, accz);
   }
 }
 
-template <int BITS, int LG, int U, bool MX>
-int launch_async(const SpmmParams& p, cudaStream_t s) {
+template <int BITS, int LG, int U, bool MX, bool GATE>
+int launch_async_g(const SpmmParams& p, cudaStream_t s) {
   constexpr int NG = 32 / LG;
   constexpr int SLOT = kSlot<BITS, LG, MX>;
   static_assert(BITS == 32 || BITS == 0 || kSlot<BITS, LG, false> / 16 <= kPiecesPerLane<BITS> * LG,
@@ -1023,7 +1027,7 @@ int launch_async(const SpmmParams& p, cudaStream_t s) {
   size_t smem = (size_t)kSpmmWarps * NG * kAS * U * SLOT;
   const size_t part = sizeof(float) * kSpmmWarps * p.d;
   if (smem < part) smem = part;
-  auto kern = spmm_async_kernel<BITS, LG, U, MX>;
+  auto kern = spmm_async_kernel<BITS, LG, U, MX, GATE>;
   // (the kernel also holds a few bytes of static shared memory)
   if (smem > 32 * 1024) GQ_TRY_CUDA(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem));
   int per_sm = 0;
@@ -1037,6 +1041,11 @@ int launch_async(const SpmmParams& p, cudaStream_t s) {
   if (grid > 0x7fffffff) return GQ_ERR_UNSUPPORTED;
   kern<<<(unsigned)grid, kSpmmThreads, smem, s>>>(p);
   return launch_status();
+}
+
+template <int BITS, int LG, int U, bool MX>
+int launch_async(const SpmmParams& p, cudaStream_t s) {
+  return p.gate != nullptr ? launch_async_g<BITS, LG, U, MX, true>(p, s) : launch_async_g<BITS, LG, U, MX, false>(p, s);
 }
 
 template <int BITS, int U, bool MX>
@@ -1602,18 +1611,21 @@ __device__ __forceinline__ void w_consume(const WSlot<BITS, MX, C>& s, bool pack
 
 // The lane's columns of (acc + accz) * rs to row r of Y / Yb, or to the
 // fp32 partial row `part`.
-template <int C>
+template <int C, bool GATE>
 __device__ __forceinline__ void w_flush(const SpmmParams& p, const WLane<C>& L, int64_t r, float rs, float* part,
-                                        const f32x2 (&acc)[C / 2], float accz) {
+                                        const f32x2 (&acc)[C / 2], float accz, uint32_t gw = 0u) {
 #pragma unroll
   for (int k = 0; k < C / 4; ++k) {
     if (4 * k < L.nv) {
       const float2 u = f2_unpack(acc[2 * k]), v = f2_unpack(acc[2 * k + 1]);
       float o0 = (u.x + accz) * rs, o1 = (u.y + accz) * rs, o2 = (v.x + accz) * rs, o3 = (v.y + accz) * rs;
       const int col = L.c0 + 4 * k;
-      if (part == nullptr && p.gate != nullptr) {
-        const float4 g = gated4(p, r, col, make_float4(o0, o1, o2, o3));
-        o0 = g.x; o1 = g.y; o2 = g.z; o3 = g.w;
+      if (GATE && part == nullptr) {  // gw: the gate word of the lane's columns
+        const uint32_t b = gw >> (col & 31);
+        if (!(b & 1u)) o0 = 0.0f;
+        if (!(b & 2u)) o1 = 0.0f;
+        if (!(b & 4u)) o2 = 0.0f;
+        if (!(b & 8u)) o3 = 0.0f;
       }
       if (part != nullptr)
         st_f4(part + col, o0, o1, o2, o3);
@@ -1625,12 +1637,12 @@ __device__ __forceinline__ void w_flush(const SpmmParams& p, const WLane<C>& L, 
   }
 }
 
-// Ask L2 for the lane's part of row r's gate when the row becomes current, so
-// that the gate load of its flush, many edges later, does not wait on DRAM.
+// The gate word holding the lane's columns of row r (C <= 8 columns, inside
+// one 32-column word), loaded when the row becomes current so that its
+// flush, many edges later, does not wait on it.
 template <int C>
-__device__ __forceinline__ void w_gate_prefetch(const SpmmParams& p, const WLane<C>& L, int64_t r) {
-  if (p.gate != nullptr && L.nv > 0)
-    asm volatile("prefetch.global.L2 [%0];" ::"l"(p.gate + r * p.ldg + L.c0));
+__device__ __forceinline__ uint32_t w_gate_word(const SpmmParams& p, const WLane<C>& L, int64_t r) {
+  return L.nv > 0 ? __ldg(p.gate + r * p.ldg + (L.c0 >> 5)) : 0u;
 }
 
 // The coefficient of gathered row x with the row's kind in its sign bit
@@ -1647,7 +1659,7 @@ __device__ __forceinline__ float w_coef(float cfk) { return __uint_as_float(__fl
 // Stream the edges [eb, ee).  LIGHT: the edges of rows [row0, row1), each
 // row written once its last edge is consumed; otherwise the sums are left
 // in acc / accz.
-template <int BITS, bool MX, int C, int U, bool LIGHT, int EW>
+template <int BITS, bool MX, int C, int U, bool LIGHT, int EW, bool GATE>
 __device__ __forceinline__ void w_stream(const SpmmParams& p, const WLane<C>& L, int eb, int ee, int row0, int row1,
                                          f32x2 (&acc)[C / 2], float& accz) {
   const int lane = threadIdx.x & 31;
@@ -1660,8 +1672,9 @@ __device__ __forceinline__ void w_stream(const SpmmParams& p, const WLane<C>& L,
   uint32_t xn = eb + lane < ee ? (uint32_t)__ldg(col + eb + lane) : 0u;  // column ids of the next batch
   int row = row0, rend = 0x7fffffff, rnext = 0x7fffffff;
   float rs = 1.0f, rsn = 1.0f;
+  uint32_t gw = 0u;  // GATE: the gate word of the current row
   if (LIGHT) {
-    w_gate_prefetch(p, L, row0);
+    if (GATE) gw = w_gate_word(p, L, row0);
     rend = __ldg(p.rowptr + row0 + 1);
     rnext = row0 + 1 < row1 ? __ldg(p.rowptr + row0 + 2) : 0x7fffffff;
     if (p.rowscale) {
@@ -1700,12 +1713,12 @@ __device__ __forceinline__ void w_stream(const SpmmParams& p, const WLane<C>& L,
         if (t0 + t < cnt) {
           if (LIGHT) {
             while (base + t0 + t >= rend) {
-              if (L.nv > 0) w_flush<C>(p, L, row, rs, nullptr, acc, accz);
+              if (L.nv > 0) w_flush<C, GATE>(p, L, row, rs, nullptr, acc, accz, gw);
 #pragma unroll
               for (int i = 0; i < C / 2; ++i) acc[i] = 0ull;
               accz = 0.0f;
               ++row;
-              if (row < row1) w_gate_prefetch(p, L, row);
+              if (GATE && row < row1) gw = w_gate_word(p, L, row);
               rend = rnext;
               rnext = row + 1 < row1 ? __ldg(p.rowptr + row + 2) : 0x7fffffff;
               rs = rsn;
@@ -1722,7 +1735,8 @@ __device__ __forceinline__ void w_stream(const SpmmParams& p, const WLane<C>& L,
   }
   if (LIGHT) {
     for (; row < row1; ++row) {
-      if (L.nv > 0) w_flush<C>(p, L, row, p.rowscale ? __ldg(p.rowscale + row) : 1.0f, nullptr, acc, accz);
+      if (L.nv > 0) w_flush<C, GATE>(p, L, row, p.rowscale ? __ldg(p.rowscale + row) : 1.0f, nullptr, acc, accz,
+                                     GATE ? w_gate_word(p, L, row) : 0u);
 #pragma unroll
       for (int i = 0; i < C / 2; ++i) acc[i] = 0ull;
       accz = 0.0f;
@@ -1730,7 +1744,7 @@ __device__ __forceinline__ void w_stream(const SpmmParams& p, const WLane<C>& L,
   }
 }
 
-template <int BITS, bool MX, int C, int U, int MINB, int EW>
+template <int BITS, bool MX, int C, int U, int MINB, int EW, bool GATE>
 __global__ void __launch_bounds__(kSpmmThreads, MINB) spmm_warp_kernel(const SpmmParams p) {
   extern __shared__ __align__(16) float wpart[];  // [kSpmmWarps][d] for heavy rows
   const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
@@ -1747,8 +1761,8 @@ __global__ void __launch_bounds__(kSpmmThreads, MINB) spmm_warp_kernel(const Spm
     const int chunk = (len + kSpmmWarps - 1) / kSpmmWarps;
     const int b0 = min(task.y + w * chunk, task.z);
     const int b1 = min(b0 + chunk, task.z);
-    if (b0 < b1) w_stream<BITS, MX, C, U, false, EW>(p, L, b0, b1, task.x, task.x + 1, acc, accz);
-    if (L.nv > 0) w_flush<C>(p, L, 0, 1.0f, wpart + w * p.d, acc, accz);
+    if (b0 < b1) w_stream<BITS, MX, C, U, false, EW, GATE>(p, L, b0, b1, task.x, task.x + 1, acc, accz);
+    if (L.nv > 0) w_flush<C, GATE>(p, L, 0, 1.0f, wpart + w * p.d, acc, accz);
     __syncthreads();
     finish_heavy(p, task, wpart);
     return;
@@ -1758,15 +1772,15 @@ __global__ void __launch_bounds__(kSpmmThreads, MINB) spmm_warp_kernel(const Spm
   for (int64_t t = gw; t < p.n_light; t += nw) {
     const int2 run = __ldg(reinterpret_cast<const int2*>(p.light) + t);
     const int eb = __ldg(p.rowptr + run.x), ee = __ldg(p.rowptr + run.y);
-    w_stream<BITS, MX, C, U, true, EW>(p, L, eb, ee, run.x, run.y, acc, accz);
+    w_stream<BITS, MX, C, U, true, EW, GATE>(p, L, eb, ee, run.x, run.y, acc, accz);
   }
 }
 
-template <int BITS, bool MX, int C, int U, int MINB, int EW = 0>
-int launch_warp(const SpmmParams& p, cudaStream_t s) {
+template <int BITS, bool MX, int C, int U, int MINB, int EW, bool GATE>
+int launch_warp_g(const SpmmParams& p, cudaStream_t s) {
   if (p.d > 32 * C || p.d % 4 != 0) return GQ_ERR_UNSUPPORTED;
   const size_t smem = sizeof(float) * kSpmmWarps * p.d;
-  auto kern = spmm_warp_kernel<BITS, MX, C, U, MINB, EW>;
+  auto kern = spmm_warp_kernel<BITS, MX, C, U, MINB, EW, GATE>;
   int per_sm = 0;
   if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kSpmmThreads, smem) != cudaSuccess || per_sm < 1)
     return GQ_ERR_UNSUPPORTED;
@@ -1778,6 +1792,16 @@ int launch_warp(const SpmmParams& p, cudaStream_t s) {
   if (grid > 0x7fffffff) return GQ_ERR_UNSUPPORTED;
   kern<<<(unsigned)grid, kSpmmThreads, smem, s>>>(p);
   return launch_status();
+}
+
+// The gate (coefficient mode only) is its own instantiation: its code in the
+// row flush changes the register allocation of the whole edge loop.
+template <int BITS, bool MX, int C, int U, int MINB, int EW = 0>
+int launch_warp(const SpmmParams& p, cudaStream_t s) {
+  if constexpr (EW == 0) {
+    if (p.gate != nullptr) return launch_warp_g<BITS, MX, C, U, MINB, 0, true>(p, s);
+  }
+  return launch_warp_g<BITS, MX, C, U, MINB, EW, false>(p, s);
 }
 
 // 64 < d <= 256 on the warp-per-edge register kernel: 4 columns per lane and
@@ -1871,8 +1895,8 @@ size_t spmm_workspace(const gq_graph* g, int transpose, int d) {
 
 int dequant_spmm(const gq_graph* g, int transpose, int coef, const float* X, int64_t ldx, const uint8_t* packed,
                  const uint8_t* mask, int d, int bits, float* Y, int64_t ldy, void* ws, size_t ws_bytes,
-                 cudaStream_t s, void* Yb, const float* gate, int64_t ldg) {
-  if (gate != nullptr && (ldg < d || ldg % 4 != 0 || !aligned(gate, 16))) return GQ_ERR_INVALID_ARG;
+                 cudaStream_t s, void* Yb, const uint32_t* gate, int64_t ldg) {
+  if (gate != nullptr && (ldg < (d + 31) / 32 || !aligned(gate, 4))) return GQ_ERR_INVALID_ARG;
   SpmmParams p;
   GQ_TRY(spmm_setup(g, transpose, X, ldx, packed, mask, d, bits, Y, ldy, ws, ws_bytes, s, p, Yb));
   p.gate = gate;

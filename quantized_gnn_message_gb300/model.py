@@ -55,6 +55,10 @@ class GCNStack:
         self.fuse_dz = fuse_dz
         self.dZ = [torch.empty(n, r8(widths[l + 1]), dtype=torch.bfloat16, device=device)
                    if fuse_dz and l < self.L - 1 else None for l in range(self.L)]
+        # with fuse_dz: [H[l] > 0] as bits (written by layer l's forward GEMM),
+        # the gate layer l+1's transposed aggregation applies to dZ[l]
+        self.Rb = [torch.empty(n, (widths[l + 1] + 31) // 32, dtype=torch.int32, device=device)
+                   if fuse_dz and l < self.L - 1 else None for l in range(self.L)]
         self.err = torch.zeros(1, dtype=torch.int32, device=device)
         L = lib()
         self.ws.get(max(int(L.gq_gcn_layer_workspace_bytes(g.ref, widths[l], widths[l + 1], 2))
@@ -68,7 +72,7 @@ class GCNStack:
         for l in range(self.L):
             ev = None if events is None else events[l]
             gcn_layer_fwd(self.g, h, Ws[l], self.mask, bits, seeds[l], self.act(l), coef=self.coef, ws=self.ws,
-                          A_save=self.A[l], H_out=self.H[l], dev_err=self.err, events=ev)
+                          A_save=self.A[l], H_out=self.H[l], dev_err=self.err, events=ev, relu_bits=self.Rb[l])
             h = self.H[l]
         return h
 
@@ -84,7 +88,7 @@ class GCNStack:
                           self.act(l), need, coef=self.coef, ws=self.ws, dW=self.dW[l],
                           dH_in=self.dH[l] if need and not fuse else None,
                           dA_save=self.dA[l] if need else None, dev_err=self.err, events=ev, dZ_in=dz_in,
-                          gate_in=self.H[l - 1] if fuse else None, dZ_prev=self.dZ[l - 1] if fuse else None)
+                          gate_in=self.Rb[l - 1] if fuse else None, dZ_prev=self.dZ[l - 1] if fuse else None)
             g = self.dH[l]
         return self.dW
 

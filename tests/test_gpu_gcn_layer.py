@@ -86,9 +86,10 @@ def test_gcn_layer_all_central_and_all_marginal(orc):
 @pytest.mark.parametrize("bits", [2, 8, 32])
 def test_gcn_layer_fused_dz_handoff(orc, bits):
     """The transposed aggregation writes the layer below's dZ = bf16(dH_in *
-    [H_in > 0]) (the ReLU gate of the layer below), and the layer below takes
-    it as its dZ: dZ within the bf16 bar of the oracle's gated dH_in, and the
-    layer below's dW from it at the GEMM bars."""
+    [H_in > 0]) (the ReLU gate of the layer below, as the bits its forward
+    wrote), and the layer below takes it as its dZ: dZ within the bf16 bar of
+    the oracle's gated dH_in, and the layer below's dW from it at the GEMM
+    bars."""
     q = gq()
     g = rmat_small()
     G = q.graph_prepare(g.rowptr.cuda(), g.col.cuda())
@@ -101,12 +102,13 @@ def test_gcn_layer_fused_dz_handoff(orc, bits):
     dY = synth.normal_matrix(g.n, d2, seed=35, tag=synth.TAG_GRAD)
     err = torch.zeros(1, dtype=torch.int32, device="cuda")
     md = mask.cuda()
-    A0, H0 = q.gcn_layer_fwd(G, X.cuda(), W0.cuda(), md, bits, 1, q.ACT_RELU, dev_err=err)
+    R0 = torch.empty(g.n, (d1 + 31) // 32, dtype=torch.int32, device="cuda")
+    A0, H0 = q.gcn_layer_fwd(G, X.cuda(), W0.cuda(), md, bits, 1, q.ACT_RELU, dev_err=err, relu_bits=R0)
     A1, H1 = q.gcn_layer_fwd(G, H0, W1.cuda(), md, bits, 2, q.ACT_NONE, dev_err=err)
     dA1 = torch.empty(g.n, d1, device="cuda")
     dZ0 = torch.full((g.n, d1), float("nan"), dtype=torch.bfloat16, device="cuda")
     dW1, none = q.gcn_layer_bwd(G, dY.cuda(), A1, H1, W1.cuda(), md, bits, 3, q.ACT_NONE, True, dA_save=dA1,
-                                dev_err=err, gate_in=H0, dZ_prev=dZ0)
+                                dev_err=err, gate_in=R0, dZ_prev=dZ0)
     assert none is None
     dW0, _ = q.gcn_layer_bwd(G, None, A0, None, W0.cuda(), md, bits, 4, q.ACT_RELU, False, dev_err=err,
                              dZ_in=dZ0)
@@ -123,3 +125,33 @@ def test_gcn_layer_fused_dz_handoff(orc, bits):
     dW0_ref = orc.gemm(A0[:, :d0].float().cpu().numpy().T, dZg, bf16=True)
     close(dW0.cpu().numpy(), dW0_ref, rtol=2e-2, what="dW from the fused dZ bar")
     close(dW0.cpu().numpy(), dW0_ref, rtol=1e-3, what="dW from the fused dZ")
+
+
+def _unpack_bits(words, d):
+    """[n x d] bool from int32 words, bit c % 32 of word c // 32."""
+    w = words.cpu().numpy().view(np.uint32)
+    cols = np.arange(d)
+    return ((w[:, cols // 32] >> (cols % 32).astype(np.uint32)) & 1).astype(bool)
+
+
+@pytest.mark.parametrize("d_out", [16, 47, 100, 256])
+@pytest.mark.parametrize("act", [0, 1])
+def test_gcn_layer_relu_bits(d_out, act):
+    """The forward's relu_bits are exactly [H_out > 0], bit c % 32 of word
+    c // 32, with the bits past d_out clear."""
+    q = gq()
+    g = rmat_small()
+    G = q.graph_prepare(g.rowptr.cuda(), g.col.cuda())
+    d_in = 64
+    X = synth.normal_matrix(g.n, d_in, seed=41).cuda()
+    W = synth.glorot(d_in, d_out, seed=42).cuda()
+    nw = (d_out + 31) // 32
+    R = torch.full((g.n, nw + 1), -1, dtype=torch.int32, device="cuda")  # one word of padding per row
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    _, H = q.gcn_layer_fwd(G, X, W, None, 32, 1, act, dev_err=err, relu_bits=R)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    got = _unpack_bits(R[:, :nw], 32 * nw)
+    np.testing.assert_array_equal(got[:, :d_out], H.cpu().numpy() > 0)
+    assert not got[:, d_out:].any()
+    assert bool((R[:, nw] == -1).all())  # words past ceil(d_out / 32) untouched
