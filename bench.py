@@ -167,10 +167,10 @@ def spmm_bytes(n, nnz, d, bits, n_marg, rows_gathered_marg, out_elem_bytes, q, g
     """Algorithmic bytes of one de-quantizing aggregation.
     compulsory: every array once (each gathered message row read once);
     streaming: every edge's gathered row counted.  gated: the output goes
-    through a ReLU gate read as an fp32 n x d array."""
+    through a ReLU gate read as bits (ceil(d / 32) words per row)."""
     pitch = q.packed_pitch(d, bits) if bits < 32 else 0
     meta = (n + 1) * 4 + nnz * 4 + 2 * n * 4 + (n if bits < 32 else 0)
-    out = n * d * out_elem_bytes + (n * d * 4 if gated else 0)
+    out = n * d * out_elem_bytes + (n * ((d + 31) // 32) * 4 if gated else 0)
     comp = meta + n_marg * pitch + (n - n_marg) * d * 4 + out
     stream = (n + 1) * 4 + nnz * 4 * 2 + (nnz if bits < 32 else 0) + n * 4 + out \
         + rows_gathered_marg * pitch + (nnz - rows_gathered_marg) * d * 4
@@ -195,7 +195,7 @@ def spmm_bytes(n, nnz, d, bits, n_marg, rows_gathered_marg, out_elem_bytes, q, g
 #     for the quantizer, rows for the GEMMs and the element-wise steps.
 # The value is 3 layers x E over the scaled step time.
 
-ORACLE_ROWS = 2000      # destination rows drawn per sampled step
+ORACLE_ROWS = 8000      # destination rows drawn per sampled step
 
 
 class OracleSample:
