@@ -1805,11 +1805,11 @@ int launch_warp(const SpmmParams& p, cudaStream_t s) {
 }
 
 // 64 < d <= 256 on the warp-per-edge register kernel: 4 columns per lane and
-// 4 edges in flight up to d = 128, 8 columns and 2 edges above; 4 blocks
+// 4 edges in flight up to d = 128, 8 columns and 3 edges above; 4 blocks
 // per SM (each measured the fastest of its range on the large GCN graph).
 template <int BITS, bool MX, int EW>
 int launch_warp_d(const SpmmParams& p, cudaStream_t s) {
-  return p.d <= 128 ? launch_warp<BITS, MX, 4, 4, 4, EW>(p, s) : launch_warp<BITS, MX, 8, 2, 4, EW>(p, s);
+  return p.d <= 128 ? launch_warp<BITS, MX, 4, 4, 4, EW>(p, s) : launch_warp<BITS, MX, 8, 3, 4, EW>(p, s);
 }
 
 // EW = 1: per-edge, per-head attention weights (fp32) instead of the
