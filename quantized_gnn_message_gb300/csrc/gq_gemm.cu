@@ -16,7 +16,7 @@
 //           K=16 per instruction) into one of two TMEM accumulators and
 //           commits stage releases / accumulator-ready to mbarriers;
 //   warps 2-9  epilogue: warp w reads TMEM lanes 32 (w % 4) .. +31 (thread =
-//           row) over one half of the columns, 32 columns per wait,
+//           row) over one half of the columns, 64 columns per wait,
 //           activation, optional GAT head projections (the head vectors in
 //           shared memory), fp32 rows staged in shared memory and written
 //           by TMA stores, 32 rows x 16 columns each, two in flight per
@@ -247,15 +247,17 @@ __global__ void __launch_bounds__(kRgThreads, 1)
       const uint32_t taddr = tmem + ((uint32_t)(q * 32) << 16) + a * p.acc_stride;
       float* crow = p.C + row * p.ldc;
       float hs = 0.0f, hd = 0.0f;
-      for (int c1 = cb; c1 < ce; c1 += 32) {
-        const int nc = ce - c1 >= 32 ? 2 : 1;  // 16-column chunks this round
-        uint32_t rb = 0;                       // [value > 0] of the round's columns
-        uint32_t r[2][16];
+      for (int c1 = cb; c1 < ce; c1 += 64) {
+        const int nc = min(4, (ce - c1) >> 4);  // 16-column chunks this round
+        uint64_t rb = 0;                         // [value > 0] of the round's columns
+        uint32_t r[4][16];
         tmem_ld16(taddr + c1, r[0]);
-        if (nc == 2) tmem_ld16(taddr + c1 + 16, r[1]);
+        if (nc > 1) tmem_ld16(taddr + c1 + 16, r[1]);
+        if (nc > 2) tmem_ld16(taddr + c1 + 32, r[2]);
+        if (nc > 3) tmem_ld16(taddr + c1 + 48, r[3]);
         tmem_ld_wait();
 #pragma unroll
-        for (int u = 0; u < 2; ++u) {
+        for (int u = 0; u < 4; ++u) {
           if (u >= nc) break;
           const int c0 = c1 + 16 * u;
           float v[16];
@@ -263,7 +265,7 @@ __global__ void __launch_bounds__(kRgThreads, 1)
           for (int j = 0; j < 16; ++j) {
             v[j] = __uint_as_float(r[u][j]);
             if (p.act == GQ_ACT_RELU) v[j] = fmaxf(v[j], 0.0f);
-            rb |= (v[j] > 0.0f ? 1u : 0u) << (16 * u + j);
+            rb |= (uint64_t)(v[j] > 0.0f ? 1u : 0u) << (16 * u + j);
           }
           if (p.tma && c0 < p.N) {
             // row `lane` of the box; 16-byte piece j at piece j ^ ((lane >> 1) & 3)
@@ -322,7 +324,10 @@ __global__ void __launch_bounds__(kRgThreads, 1)
             }
           }
         }
-        if (p.rbits != nullptr && live && c1 < p.N) p.rbits[row * p.ldrb + (c1 >> 5)] = rb;
+        if (p.rbits != nullptr && live) {
+          if (c1 < p.N) p.rbits[row * p.ldrb + (c1 >> 5)] = (uint32_t)rb;
+          if (nc > 2 && c1 + 32 < p.N) p.rbits[row * p.ldrb + (c1 >> 5) + 1] = (uint32_t)(rb >> 32);
+        }
       }
       tc_fence_before();
       __syncwarp();
