@@ -167,9 +167,10 @@ typedef struct gq_sched {
   int64_t n_groups;
   int64_t n_slots;          /* partial-row slots over all groups          */
   const int32_t* light;     /* n_light x {row_begin, row_end}: runs of
-                               consecutive light rows with at most
-                               light_edges edges in all (heavy rows never
-                               inside), covering every light row once     */
+                               consecutive light rows with at most 256
+                               edges in all, or one light row (heavy rows
+                               never inside), covering every light row
+                               once                                       */
   int64_t n_light;
 } gq_sched;
 
