@@ -15,9 +15,10 @@
 // writes one partial row per task to the workspace and the last task to
 // finish (arrival ticket) adds them in task order.  Four kernels share it:
 //   - spmm_warp_kernel (packed and fp32 rows mixed by a mask, or fp32 rows
-//     alone, 64 < d <= 256).  One warp per edge; lane l owns 4 or 8
-//     columns and loads its part of the message row straight into
-//     registers, a few edges in flight per warp and many warps per SM.
+//     alone, with coefficients or with per-edge, per-head attention weights,
+//     fp32 or 8-bit codes; 64 < d <= 256).  One warp per edge; lane l owns
+//     4 or 8 columns and loads its part of the message row straight into
+//     registers, 3-4 edges in flight per warp and 32 warps per SM.
 //   - spmm_async_kernel (d <= 512: rows of one kind, all packed or all fp32;
 //     packed and fp32 rows mixed by a mask; or rows of mixed widths for
 //     d <= 128).  A group of LG lanes walks a stream of edges (a slice of a
@@ -29,7 +30,7 @@
 //     edge: the lane holding an edge's metadata copies the whole message row
 //     into a slot of the warp's shared-memory ring with one bulk copy onto
 //     the slot's mbarrier, and all 32 lanes consume it.
-//   - spmm_kernel (attention weights, fp32 or 8-bit, or d > 512).  A light
+//   - spmm_kernel (attention weights outside 64 < d <= 256, or d > 512).  A light
 //     row is one warp's job: lane groups of G lanes take one edge at a time,
 //     each lane owning 8 consecutive columns (CPL chunks of 8 for d > 256);
 //     edge metadata is loaded 32 edges at a time and broadcast with
@@ -37,6 +38,10 @@
 //     A heavy task's 8 warps split its edges into contiguous streams
 //     (stream_row) whose partial rows are summed in shared memory in warp
 //     order.
+// An optional ReLU gate (one bit per output element) zeroes output elements
+// as rows are written; in the warp and ring kernels it is a template
+// parameter, since its code in the row flush changes the register
+// allocation of their edge loops.
 // Every sum runs in a fixed order, so results are identical run to run.
 #include <cuda_bf16.h>
 
