@@ -106,20 +106,29 @@ def test_three_layer_stack_error_shrinks_with_bits(orc):
     assert err[8] < 2e-2 and err[2] < 1.0, err
 
 
-def test_stack_fused_dz_is_bit_identical(orc):
+# (widths, marginal fraction or None for every row packed, bits): the gated
+# transposed aggregation on the warp-per-edge kernel (64 < d <= 256 with a
+# mask or fp32 rows) and on the ring kernel (d <= 64, or every row packed)
+FUSED_CASES = [((100, 128, 128, 47), 0.6, 2), ((64, 64, 32), 0.6, 8), ((64, 256, 32), None, 4),
+               ((48, 64, 16), 0.5, 32), ((64, 200, 24), 0.3, 32)]
+
+
+@pytest.mark.parametrize("widths,mask_frac,bits", FUSED_CASES)
+def test_stack_fused_dz_is_bit_identical(orc, widths, mask_frac, bits):
     """The stack's fused backward (each transposed aggregation writes the
-    layer below's gated bf16 dZ) gives exactly the weight gradients of the
-    unfused one (fp32 gradient, then a separate gate-and-round pass)."""
+    layer below's bf16 dZ through its ReLU bits) gives exactly the weight
+    gradients of the unfused one (fp32 gradient, then a separate
+    gate-and-round pass)."""
     from quantized_gnn_message_gb300.model import GCNStack
-    widths = (100, 128, 128, 47)
     L = len(widths) - 1
-    q, g, G, X, Ws, mask, dY = _setup(widths, 0.6, seed=7)
+    q, g, G, X, Ws, mask, dY = _setup(widths, 0.6 if mask_frac is None else mask_frac, seed=7)
+    md = None if mask_frac is None else mask.cuda()
     Wd = [w.cuda() for w in Ws]
     out = []
     for fuse in (True, False):
-        model = GCNStack(G, widths, mask.cuda(), fuse_dz=fuse)
-        model.forward(X.cuda(), Wd, 2, _seeds(9, L, False))
-        model.backward(dY.cuda(), Wd, 2, _seeds(9, L, True), need_input_grad=True)
+        model = GCNStack(G, widths, md, fuse_dz=fuse)
+        model.forward(X.cuda(), Wd, bits, _seeds(9, L, False))
+        model.backward(dY.cuda(), Wd, bits, _seeds(9, L, True), need_input_grad=True)
         torch.cuda.synchronize()
         assert int(model.err.item()) == 0
         out.append([w.clone() for w in model.dW] + [model.dH[0].clone()])
