@@ -8,7 +8,9 @@
 //   a row of at most 32 edges is one thread's, rows up to the hub threshold
 //   a warp's, heavier rows are cut into tasks of one warp each, whose
 //   (max, sum) partials are merged in task order before their second pass.
-// gat_edge_bwd_kernel  (Fig. 1b), per destination row v:
+// gat_edge_bwd_kernel + gat_edge_bwd_heavy_kernel  (Fig. 1b), per
+// destination row v (light rows one warp each over the graph's light-row
+// runs; heavy rows as block tasks, their P and dD merged in task order):
 //     dalpha[e,k] = sum_f dOut[v,kF+f] m_u[kF+f]          (SDDMM dot)
 //     P[v,k]      = sum_e alpha[e,k] dalpha[e,k]
 //     dE_pre[e,k] = alpha (dalpha - P) * (E_pre > 0 ? 1 : slope)
@@ -24,8 +26,9 @@
 //   vector per (destination, head) segment, and their de-quantized values.
 // Heavy rows follow the graph's static schedule: the softmax and the
 // quantizer cut them into warp tasks whose partials a second kernel merges;
-// the edge backward uses block tasks that combine per-task partials in task
-// order in the last block to finish.  The softmax and the quantizer check
+// the edge and node backward use block tasks whose per-task partials are
+// combined in task order (by a second kernel, or by the last block of the
+// row to finish).  The softmax and the quantizer check
 // each range and index they read against the graph and record an invalid
 // one in the graph status word.
 // Scores, attention and their gradients stay fp32 (Tango Sec. 3.2: full
