@@ -13,7 +13,7 @@ import pytest
 import torch
 
 import synth
-from gpu_helpers import close, gq, rmat_small
+from gpu_helpers import close, gq, hub_graph, rmat_small
 
 pytestmark = pytest.mark.gpu
 
@@ -131,6 +131,34 @@ def test_stack_fused_dz_is_bit_identical(orc, widths, mask_frac, bits):
         model.backward(dY.cuda(), Wd, bits, _seeds(9, L, True), need_input_grad=True)
         torch.cuda.synchronize()
         assert int(model.err.item()) == 0
+        out.append([w.clone() for w in model.dW] + [model.dH[0].clone()])
+    for a, b in zip(*out):
+        assert torch.equal(a, b)
+
+
+@pytest.mark.parametrize("widths,bits", [((64, 128, 128, 16), 2), ((64, 64, 16), 8)])
+def test_stack_fused_dz_heavy_splits(orc, widths, bits):
+    """The fused hand-off on a graph whose heavy rows are cut into several
+    tasks (the gate applied where the last task of a row adds the partial
+    rows), on the warp-per-edge kernel (d = 128) and the ring kernel
+    (d = 64): bit-identical to the unfused stack."""
+    from quantized_gnn_message_gb300.model import GCNStack
+    q = gq()
+    g = hub_graph()
+    G = q.graph_prepare(g.rowptr.cuda(), g.col.cuda(), hub_threshold=32, split_edges=256)
+    assert G.c.tr_sched.n_groups > 0 and G.c.sched.n_groups > 0
+    L = len(widths) - 1
+    X = synth.normal_matrix(g.n, widths[0], seed=51).cuda()
+    Wd = [synth.glorot(widths[l], widths[l + 1], seed=52 + l).cuda() for l in range(L)]
+    mask = synth.bernoulli_mask(g.n, 0.5, seed=55).cuda()
+    dY = synth.normal_matrix(g.n, widths[-1], seed=56, tag=synth.TAG_GRAD).cuda()
+    out = []
+    for fuse in (True, False):
+        model = GCNStack(G, widths, mask, fuse_dz=fuse)
+        model.forward(X, Wd, bits, _seeds(3, L, False))
+        model.backward(dY, Wd, bits, _seeds(3, L, True), need_input_grad=True)
+        torch.cuda.synchronize()
+        assert int(model.err.item()) == 0 and int(G.status.cpu()[0]) == 0
         out.append([w.clone() for w in model.dW] + [model.dH[0].clone()])
     for a, b in zip(*out):
         assert torch.equal(a, b)
