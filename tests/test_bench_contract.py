@@ -44,3 +44,27 @@ def test_single_gpu_workloads_other_ranks_are_silent():
         out = _run(["--workload", wl, "--steps", "1", "--warmup", "0"], {"RANK": "1", "WORLD_SIZE": "2",
                                                                          "LOCAL_RANK": "1"})
         assert out.strip() == ""
+
+
+def test_aggregation_bytes_by_hand():
+    """The roofline numerator: compulsory bytes of one aggregation, worked by
+    hand for a small case (n = 10 rows, 30 edges, d = 64, b = 2, 4 marginal
+    rows): row pointers, column ids, the two degree norms, the mask, each
+    packed row once, each fp32 row once, the output; a gated launch adds the
+    gate bits (ceil(64 / 32) words per row)."""
+    import sys
+    sys.path.insert(0, ROOT)
+    import bench
+    import quantized_gnn_message_gb300 as q
+    from quantized_gnn_message_gb300 import build
+    build.build()  # the host-side pitch query of libgq (no GPU needed)
+    pitch = q.packed_pitch(64, 2)
+    assert pitch == 32  # 8-byte header after 16 payload bytes, padded to 16
+    meta = 11 * 4 + 30 * 4 + 2 * 10 * 4 + 10
+    comp, stream = bench.spmm_bytes(10, 30, 64, 2, 4, 12, 2, q)
+    assert comp == meta + 4 * pitch + 6 * 64 * 4 + 10 * 64 * 2
+    # streaming: metadata read per edge (column id and coefficient), the mask
+    # byte per edge, every gathered row
+    assert stream == 11 * 4 + 30 * 8 + 30 + 10 * 4 + 10 * 64 * 2 + 12 * pitch + 18 * 64 * 4
+    comp_g, _ = bench.spmm_bytes(10, 30, 64, 2, 4, 12, 2, q, gated=True)
+    assert comp_g - comp == 10 * 2 * 4
